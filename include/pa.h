@@ -1,0 +1,291 @@
+/*
+ * pa.h - C ABI of the paged KV-cache library (paged decode attention,
+ * cache write, block copy, host block allocator) for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions for every entry point:
+ *  - Plain C types only.  "Device" pointers are CUDA global-memory addresses
+ *    owned by the caller (the library never frees or keeps them); "host"
+ *    pointers are ordinary CPU memory.  No entry point allocates device
+ *    memory: scratch space for split-KV comes from a caller-provided
+ *    workspace.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream of the current device).  Device entry points enqueue work on it
+ *    and return after launch, without synchronising.
+ *  - Shapes and arguments are validated on the host before any launch;
+ *    invalid ones return PA_ERR_INVALID and launch nothing.  Combinations of
+ *    (head_dim, block_size, G) that are not compiled in return
+ *    PA_ERR_UNSUPPORTED.  Launch failures return PA_ERR_CUDA.
+ *  - Index values read on the device (block-table entries, slots, copy
+ *    pairs, sequence lengths) are range-checked inside the kernels: a bad
+ *    value is never dereferenced; the kernel records PA_ERR_BAD_INDEX in a
+ *    per-device error word and skips or clamps the access.  Bounded waits
+ *    that run out record PA_ERR_DEVICE_TIMEOUT.  pa_check_error reads the
+ *    word.  Kernels never trap.
+ *  - Element type of K/V/q/out is given by pa_dtype (16-bit IEEE half or
+ *    bfloat16); arithmetic is fp32 with fp32 accumulation; outputs are
+ *    rounded to nearest even.
+ *
+ * Memory layout (all dense, row-major, no padding):
+ *    K / V pool       [num_blocks][num_kv_heads][block_size][head_dim]
+ *    q, out           [num_seqs][num_q_heads][head_dim]
+ *    block_tables     int32 [num_seqs][max_blocks_per_seq]
+ *    seq_lens         int32 [num_seqs]
+ *    k_new, v_new     [num_tokens][num_kv_heads][head_dim]
+ *    slot_mapping     int64 [num_tokens]   (slot = block * block_size + offset)
+ *    block_mapping    int64 [num_pairs][2] (src, dst)
+ *
+ * Sources for the operations (page title, section):
+ *  [P1] "PagedAttention: Treating KV Memory Like Virtual Memory"
+ *       (lenatriestounderstand.com)
+ *  [P2] "Why AI servers waste memory, and how paging fixes it" (spicyshark.co)
+ *  [P3] "PagedAttention and Virtual Memory Management: Mathematical
+ *       Foundations of Non-Contiguous KV-Cache Allocation, Dynamic Block
+ *       Translation, and Copy-on-Write Forking Mechanics" (llms.blog)
+ *  [P4] "2.1 PagedAttention" (infra-guide)
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,       /* bad argument or shape; nothing changed / launched */
+    PA_ERR_OUT_OF_BLOCKS = 2, /* allocator: not enough free blocks; nothing changed */
+    PA_ERR_UNSUPPORTED = 3,   /* shape combination not compiled in */
+    PA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    PA_ERR_DEVICE_TIMEOUT = 5,/* a bounded device wait ran out (reported by pa_check_error) */
+    PA_ERR_BAD_INDEX = 6,     /* an out-of-range index was met on the device (pa_check_error) */
+    PA_ERR_NOT_FOUND = 7      /* allocator: unknown sequence id, or id already in use */
+} pa_status;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int pa_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *pa_status_string(pa_status s);
+
+/* ------------------------------------------------------------------------
+ * pa_cache_write (reshape_and_cache)
+ *
+ * For every new token t and KV head h:
+ *   K_pool[slot/B][h][slot%B][:] = k_new[t][h][:]   (same for V)
+ * with slot = slot_mapping[t] and B = block_size.  A negative slot means
+ * "skip this token".  A slot >= num_blocks*block_size is a bad index: it is
+ * not written and PA_ERR_BAD_INDEX is recorded.  Pure copy, bit-exact.
+ *   [P2] "The real implementation" (append writes k, v at the offset of the
+ *   last block); [P3] section 5, case 1 (write into slot o = t mod B of block
+ *   p); [P4] section 5 (physical_block_number, physical_block_offset).
+ * Arguments: k_new, v_new, slot_mapping, k_pool, v_pool are device pointers;
+ * num_tokens >= 0 (0 launches nothing); head_dim in {64, 128};
+ * block_size > 0.  Pools are updated in place.
+ * ---------------------------------------------------------------------- */
+pa_status pa_cache_write(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                         int num_tokens, void *k_pool, void *v_pool, int num_blocks,
+                         int num_kv_heads, int head_dim, int block_size, pa_dtype dtype,
+                         void *stream);
+
+/* ------------------------------------------------------------------------
+ * pa_copy_blocks (copy-on-write block duplication)
+ *
+ * For each pair (src, dst) of block_mapping, in every layer l < num_layers,
+ * for both pools:  pool_l[dst][:] = pool_l[src][:]  (the whole block:
+ * num_kv_heads*block_size*head_dim elements = block_bytes bytes).
+ *   [P2] "The real implementation", the copy-on-write branch of append (the
+ *   whole block is copied); [P3] section 5 case 2 step 2 (copies the first o
+ *   token vectors: the extra slots copied here are never read).
+ * Pairs are independent: a dst must not also appear as a src or as another
+ * pair's dst in the same call (the allocator never produces that).  An index
+ * outside [0, num_blocks) is a bad index (pair skipped, PA_ERR_BAD_INDEX).
+ * Arguments: k_pools, v_pools are HOST arrays of num_layers DEVICE pointers
+ * (1 <= num_layers <= 1024); block_mapping is a DEVICE int64 array
+ * [num_pairs][2]; num_pairs >= 0 (0 launches nothing); block_bytes > 0 and a
+ * multiple of 16; every pool pointer 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+pa_status pa_copy_blocks(void *const *k_pools, void *const *v_pools, int num_layers,
+                         const int64_t *block_mapping, int num_pairs, int num_blocks,
+                         size_t block_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * pa_decode (single-query paged decode attention with grouped-query heads)
+ *
+ * For sequence i (L_i = seq_lens[i] tokens), query head h, G =
+ * num_q_heads/num_kv_heads, kv = h / G, T_i = block_tables[i]:
+ *   K_i[p] = K_pool[T_i[p / B]][kv][p % B][:],  p < L_i   (same for V)
+ *   s_p    = scale * dot(q[i][h], K_i[p])
+ *   out[i][h][:] = sum_p softmax(s)_p * V_i[p][:]
+ * L_i = 0 gives a zero row.  Slots past L_i are never read into the result,
+ * whatever they hold (NaN included).
+ *   [P1] "How the kernel reads a block table" (tiles, running max and sum,
+ *   address = block_table[i / B] * block stride + (i mod B) * slot stride);
+ *   [P3] section 4 (Vectorized Address Computation; Fused PagedAttention
+ *   Algorithm with online softmax; Parallel Partitioning, steps 1-3);
+ *   [P2] "Reading through the table".
+ *
+ * Long sequences are split into partitions of P tokens (split-KV: P3 section
+ * 4, Parallel Partitioning, step 2), each producing (m_k, l_k, O_k), then
+ * combined by the cross-partition reduce (step 3).  partition_tokens:
+ *   -1  single pass (one work unit per (sequence, KV head); no workspace)
+ *    0  automatic choice from the shapes and the GPU's SM count
+ *   >0  P = partition_tokens (must be a multiple of block_size)
+ * With P > 0 or automatic, workspace must hold at least
+ * pa_decode_workspace_size(...) bytes (device memory, 256-byte aligned); it
+ * is scratch, overwritten on every call, and may be NULL when the size is 0.
+ *
+ * Arguments (device pointers unless stated):
+ *   out, q                 [num_seqs][num_q_heads][head_dim]
+ *   k_pool, v_pool         [num_blocks][num_kv_heads][block_size][head_dim]
+ *   block_tables           int32 [num_seqs][max_blocks_per_seq]; entries
+ *                          must lie in [0, num_blocks) for the blocks a
+ *                          sequence uses (checked: PA_ERR_BAD_INDEX)
+ *   seq_lens               int32 [num_seqs]; 0 <= L_i <= max_seq_len and
+ *                          L_i <= max_blocks_per_seq*block_size (checked)
+ *   max_seq_len            host int, an upper bound of every L_i (sizes the
+ *                          launch); 0 is allowed
+ *   head_dim in {64,128}; block_size in {16,32}; 1 <= G <= 8; scale finite.
+ *   q, out, pools and workspace 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_pool,
+                    int num_blocks, const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *seq_lens, int max_seq_len, int num_seqs, int num_q_heads,
+                    int num_kv_heads, int head_dim, int block_size, float scale,
+                    int partition_tokens, void *workspace, size_t workspace_bytes,
+                    pa_dtype dtype, void *stream);
+
+/* Partition size pa_decode uses for these shapes when partition_tokens = 0
+ * (-1 means it will run single pass).  Needs the current CUDA device. */
+int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
+                             int block_size, int group_size, pa_dtype dtype);
+
+/* Bytes of workspace pa_decode / pa_decode_partitions need for these
+ * shapes; 0 for single pass.  partition_tokens as in pa_decode (0 = auto,
+ * resolved as pa_decode would with the same arguments). */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_seq_len, int partition_tokens,
+                                pa_dtype dtype);
+
+/* ------------------------------------------------------------------------
+ * pa_decode_partitions (split-KV step 2 on its own)
+ *
+ * Computes, for every sequence i, query head h and partition k <
+ * NP = ceil(max_seq_len / P), over positions [k*P, min((k+1)*P, L_i)):
+ *   m[i][h][k] = max_p s_p * log2(e)       (fp32, base-2 units)
+ *   l[i][h][k] = sum_p 2^(s_p*log2(e) - m)  (fp32)
+ *   O[i][h][k][:] = sum_p 2^(s_p*log2(e) - m) V_i[p] / l   (fp32)
+ * Partitions that start at or past L_i hold m = -inf, l = 0, O = 0.
+ * Workspace layout (from its start, each array 256-byte aligned):
+ *   m  float [num_seqs][num_q_heads][NP]
+ *   l  float [num_seqs][num_q_heads][NP]
+ *   O  float [num_seqs][num_q_heads][NP][head_dim]
+ *   [P3] section 4, "Parallel Partitioning Across GPU Warps", step 2.
+ * partition_tokens must be > 0 here.  Other arguments as pa_decode.
+ * ---------------------------------------------------------------------- */
+pa_status pa_decode_partitions(const void *q, const void *k_pool, const void *v_pool,
+                               int num_blocks, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *seq_lens, int max_seq_len,
+                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, float scale, int partition_tokens,
+                               void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                               void *stream);
+
+/* ------------------------------------------------------------------------
+ * pa_split_kv_reduce (split-KV step 3 on its own)
+ *
+ * Reads the partials that pa_decode_partitions wrote (same workspace
+ * layout, same partition_tokens and max_seq_len) and writes, per (i, h):
+ *   M = max_k m_k ;  w_k = l_k * 2^(m_k - M) ;  out = sum_k w_k O_k / sum_k w_k
+ * over the partitions k < ceil(L_i / P); L_i = 0 gives zeros.
+ *   [P3] section 4, "Parallel Partitioning Across GPU Warps", step 3
+ *   (m_global = max m_k, l_global = sum l_k e^(m_k - m_global),
+ *    O = sum_k l_k e^(m_k - m_global) / l_global * O_k), in base 2.
+ * ---------------------------------------------------------------------- */
+pa_status pa_split_kv_reduce(void *out, const void *workspace, size_t workspace_bytes,
+                             const int32_t *seq_lens, int max_seq_len, int num_seqs,
+                             int num_q_heads, int head_dim, int partition_tokens, pa_dtype dtype,
+                             void *stream);
+
+/* ------------------------------------------------------------------------
+ * pa_check_error: synchronises `stream`, then reads and clears the current
+ * device's error word.  Returns PA_OK, PA_ERR_BAD_INDEX,
+ * PA_ERR_DEVICE_TIMEOUT, or PA_ERR_CUDA if the synchronisation failed.
+ * ---------------------------------------------------------------------- */
+pa_status pa_check_error(void *stream);
+
+/* ========================================================================
+ * Host block allocator (CPU only; no device calls).
+ *
+ * Semantics ([P2] "The idea: a block table", "A hand-worked example", "The
+ * real implementation", "Sharing a prefix with copy-on-write"; [P3]
+ * section 5; [P4] sections 3, 6 and 9.3):
+ *  - num_blocks blocks of block_size slots; a FIFO free list (take from the
+ *    front, freed blocks join the back, in table order); freed blocks are
+ *    not cleared.  The initial order is 0..num_blocks-1 unless given.
+ *  - each sequence has a block table and a token count; position p is slot
+ *    p % B of block table[p / B]; flat slot = block * B + offset.
+ *  - append: when the count is a multiple of B (incl. 0) a block is taken
+ *    and appended; else if the last block is shared (refcount > 1) a block
+ *    is taken, the old block's count drops by one, the table points at the
+ *    new block and the pair (old, new) is reported for pa_copy_blocks
+ *    (copy-on-write).  Multi-token appends are all or nothing.
+ *  - fork: child gets the parent's table and count; each block gains a
+ *    reference.  free: each block loses one; at zero it joins the free list.
+ * Every failing call returns an error and leaves the state unchanged.  An
+ * allocator object is not thread-safe: one thread at a time.
+ * ===================================================================== */
+typedef struct pa_alloc pa_alloc;
+
+/* free_order: NULL, or a host array holding a permutation of
+ * 0..num_blocks-1 that sets the initial free-list order. */
+pa_status pa_alloc_create(int num_blocks, int block_size, const int32_t *free_order,
+                          pa_alloc **out);
+void pa_alloc_destroy(pa_alloc *a);
+
+/* New empty sequence (PA_ERR_NOT_FOUND if the id is in use). */
+pa_status pa_seq_add(pa_alloc *a, int64_t seq_id);
+
+/* Append n_tokens >= 0 tokens.  slots_out (host, may be NULL if n_tokens
+ * is 0) receives each token's flat slot.  cow_pair_out (host, 2 entries)
+ * receives (src, dst) when a copy-on-write happened; *n_cow_out (host) is
+ * set to 0 or 1.  PA_ERR_OUT_OF_BLOCKS when the blocks needed exceed the
+ * free list (nothing changes). */
+pa_status pa_seq_append(pa_alloc *a, int64_t seq_id, int n_tokens, int64_t *slots_out,
+                        int64_t *cow_pair_out, int *n_cow_out);
+
+pa_status pa_seq_fork(pa_alloc *a, int64_t parent, int64_t child);
+pa_status pa_seq_free(pa_alloc *a, int64_t seq_id);
+
+/* Token count of a sequence. */
+pa_status pa_seq_len(const pa_alloc *a, int64_t seq_id, int64_t *len_out);
+
+/* Copy a sequence's block table into out (host, cap entries).  *n_out gets
+ * the table length; PA_ERR_INVALID if cap is too small (nothing written). */
+pa_status pa_seq_block_table(const pa_alloc *a, int64_t seq_id, int32_t *out, int cap,
+                             int *n_out);
+
+/* Export tables and lengths of n sequences into a dense int32
+ * [n][max_blocks_per_seq] array (host; unused entries set to 0) and an
+ * int32 [n] length array (host).  PA_ERR_INVALID if a table is longer than
+ * max_blocks_per_seq or a length does not fit in int32. */
+pa_status pa_alloc_export(const pa_alloc *a, const int64_t *seq_ids, int n,
+                          int32_t *tables_out, int max_blocks_per_seq, int32_t *lens_out);
+
+int pa_alloc_num_free(const pa_alloc *a);
+
+/* Free list, front first (host, cap entries); *n_out gets its length. */
+pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n_out);
+
+/* Reference count of a block (-1 if out of range). */
+int pa_block_refcount(const pa_alloc *a, int block);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

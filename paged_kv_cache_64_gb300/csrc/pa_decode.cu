@@ -1,0 +1,857 @@
+// Paged decode attention for GB300 (sm_103a): pa_decode, pa_decode_partitions,
+// pa_split_kv_reduce.
+//
+// What is computed (the pages' definition): for sequence i, query head h,
+// KV head kv = h / G, positions p < L_i gathered through the block table,
+//   out = softmax(scale * q K^T) V
+// walked in tiles with a running maximum and sum ("PagedAttention: Treating
+// KV Memory Like Virtual Memory", "How the kernel reads a block table";
+// "PagedAttention and Virtual Memory Management ..." (llms.blog) section 4,
+// "Fused PagedAttention Algorithm"), optionally split into partitions whose
+// (m, l, O) partials are combined by a second kernel (same section,
+// "Parallel Partitioning Across GPU Warps", steps 2 and 3).
+//
+// Design (GB300-first, HBM-bound: about G flops per byte of K/V):
+//  * One CTA per (partition, KV head, sequence): 4 consumer warps + 1
+//    producer warp.  Every query head of the KV head's group is served from
+//    the same K/V bytes, so each K/V tile is read from HBM exactly once.
+//  * Pipeline stage = 16 consecutive positions of one (block, KV head): a
+//    contiguous 16*d*2-byte run in the [block][head][slot][dim] pool, moved
+//    by one 1-D bulk copy (TMA engine) for K and one for V into a ring of
+//    shared-memory stages, completion tracked by mbarrier transaction bytes.
+//    The producer warp reads the block table 32 entries at a time
+//    (coalesced) and translates each stage's position: physical block =
+//    table[pos >> log2(B)], slot offset = pos & (B - 1).
+//  * Consumer warp w takes stages w, w+4, ...  Inside a warp, LT lanes share
+//    one token (LT = 8, or 16 when G*d is large); a lane owns d/LT dims in
+//    whole 16-byte pieces, so each group of 8 lanes reads one 128-byte
+//    row segment: bank-conflict-free LDS.128.
+//  * q (pre-scaled by scale*log2 e) lives in registers; dot products use
+//    packed fp32x2 FMA (FFMA2); partial sums are combined with a butterfly of
+//    warp shuffles; the softmax is base 2 (ex2.approx).
+//  * Online softmax with a lazy rescale: the running max m only moves when a
+//    new tile's max exceeds it by more than 8 (base-2 units), so the
+//    accumulator is rescaled rarely; exp2(s - m) <= 256 keeps fp32 far from
+//    overflow.  The true max is tracked separately for the partial outputs.
+//  * Masked positions (past L_i in a partial last stage) get score -inf and
+//    their V values are replaced by zero with a select, never multiplied
+//    by a zero weight, so NaN/Inf in stale slots cannot leak.
+//  * Each warp keeps its own (m, l, acc); at the end warps are merged through
+//    shared memory with the same rescaling as the cross-partition combine.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kUnit = 16;                // positions per pipeline stage
+constexpr float kLazyRescale = 8.0f;     // base-2 units
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kSinglePassTokens = 1 << 30;  // "partition" covering any sequence
+
+template <int D, int GP>
+struct DecodeShape {
+    static constexpr int LT = (GP * D / 64 > 8) ? 16 : 8;  // lanes per token
+    static constexpr int DPL = D / LT;                     // dims per lane
+    static constexpr int NPC = DPL / 8;                    // 16-byte pieces per lane
+    static constexpr int TPR = 32 / LT;                    // tokens per warp row
+    static constexpr int R = 4;                            // rows per chunk
+    static constexpr int CHUNKS = kUnit / (R * TPR);       // chunks per stage
+    static constexpr int TILE_BYTES = kUnit * D * 2;       // one of K or V
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int NS = (D == 128) ? 8 : 16;         // 64 KiB ring
+    static constexpr int RING_BYTES = NS * STAGE_BYTES;
+    static constexpr int SMEM_BYTES = RING_BYTES + 2 * NS * 8 + 16;
+    static_assert(NS % kConsumerWarps == 0, "stages are dealt to warps round robin");
+    static_assert(CHUNKS >= 1 && kUnit % (R * TPR) == 0, "chunking");
+    static_assert(kConsumerWarps * GP * D * 4 + 3 * kConsumerWarps * GP * 4 <= RING_BYTES,
+                  "merge scratch must fit in the ring");
+};
+
+struct DecodeParams {
+    void *out;                   // [S][Hq][D] (mode 0) or nullptr
+    const uint16_t *q;           // [S][Hq][D]
+    const uint16_t *k_pool;      // [NB][Hkv][B][D]
+    const uint16_t *v_pool;
+    const int32_t *block_tables; // [S][max_blocks_per_seq]
+    const int32_t *seq_lens;     // [S]
+    float *part_m;               // [S][Hq][NP]
+    float *part_l;               // [S][Hq][NP]
+    float *part_o;               // [S][Hq][NP][D]
+    int *err;
+    int num_blocks;
+    int max_blocks_per_seq;
+    int max_seq_len;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                   // G
+    int block_size;
+    int log2_block;
+    int partition_tokens;        // P, multiple of kUnit
+    int num_partitions;          // NP (grid.x)
+    float scale_log2;            // scale * log2(e)
+    int mode;                    // 0: decode (direct output when 1 partition), 1: partials only
+};
+
+// Length of sequence i, clamped to what the launch covers; a value out of
+// range is a bad index.
+__device__ __forceinline__ int checked_len(const int32_t *seq_lens, int i, int max_seq_len,
+                                           int table_cap, int *err, bool report) {
+    int L = seq_lens[i];
+    const int cap = max_seq_len < table_cap ? max_seq_len : table_cap;
+    if (L < 0 || L > cap) {
+        if (report) record_error(err, PA_ERR_BAD_INDEX);
+        L = L < 0 ? 0 : cap;
+    }
+    return L;
+}
+
+template <bool BF16, int D, int GP>
+__global__ void __launch_bounds__(kDecodeThreads)
+    paged_decode_kernel(const DecodeParams p) {
+    using S = DecodeShape<D, GP>;
+    constexpr int LT = S::LT, DPL = S::DPL, NPC = S::NPC, TPR = S::TPR, R = S::R;
+    constexpr int NS = S::NS;
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t *ring = smem;
+    uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + S::RING_BYTES);
+    uint64_t *empty_bar = full_bar + NS;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty_bar + NS);
+
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int seq = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = p.group;
+    const int P = p.partition_tokens;
+
+    const int L = checked_len(p.seq_lens, seq, p.max_seq_len,
+                              p.max_blocks_per_seq * p.block_size, p.err,
+                              threadIdx.x == 0 && part == 0 && kvh == 0);
+    const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
+    const int start = part * P;
+
+    if (start >= L) {
+        // Empty partition.  Mode 0: the zero-length sequence's output row is
+        // zeros (written by partition 0); nothing else is ever read.  Mode 1:
+        // write the empty partial (m = -inf, l = 0, O = 0).
+        if (p.mode == 0) {
+            if (part == 0) {
+                uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
+                const int64_t base = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * D / 2;
+                for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) o[base + i] = 0u;
+            }
+        } else {
+            for (int g = 0; g < G; ++g) {
+                const int64_t row = ((int64_t)seq * p.num_q_heads + kvh * G + g) * p.num_partitions + part;
+                if (threadIdx.x == 0) {
+                    p.part_m[row] = -INFINITY;
+                    p.part_l[row] = 0.f;
+                }
+                for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
+            }
+        }
+        return;
+    }
+    const int end = (start + P < L) ? start + P : L;
+    const int nunits = (end - start + kUnit - 1) / kUnit;
+    const bool direct = (p.mode == 0) && (nparts_seq <= 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    // Per-warp softmax state (consumers) kept across the final barrier.
+    float m_run[GP], m_true[GP], l_run[GP];
+    float2 acc[GP][DPL / 2];
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        const int64_t tile_elems = (int64_t)kUnit * D;
+        const int64_t head_elems = (int64_t)p.block_size * D;
+        const int64_t block_elems = (int64_t)p.num_kv_heads * head_elems;
+        const int32_t *table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
+        bool ok = true;
+        for (int u0 = 0; u0 < nunits && ok; u0 += 32) {
+            const int u = u0 + lane;
+            int phys = 0;
+            if (u < nunits) {
+                const int pos = start + u * kUnit;
+                phys = table[pos >> p.log2_block];
+                if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                    record_error(p.err, PA_ERR_BAD_INDEX);
+                    phys = 0;
+                }
+            }
+            const int cnt = (nunits - u0 < 32) ? nunits - u0 : 32;
+            for (int j = 0; j < cnt; ++j) {
+                const int uu = u0 + j;
+                const int ph = __shfl_sync(kFullMask, phys, j);
+                const int stage = uu % NS;
+                if (uu >= NS) {
+                    if (!mbar_wait(&empty_bar[stage], ((uu / NS) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (lane == 0) {
+                    const int pos = start + uu * kUnit;
+                    const int off = pos & (p.block_size - 1);
+                    const int64_t elem = (int64_t)ph * block_elems + (int64_t)kvh * head_elems +
+                                         (int64_t)off * D;
+                    uint8_t *dst = ring + stage * S::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full_bar[stage], 2 * S::TILE_BYTES);
+                    bulk_copy_g2s(dst, p.k_pool + elem, S::TILE_BYTES, &full_bar[stage]);
+                    bulk_copy_g2s(dst + S::TILE_BYTES, p.v_pool + elem, S::TILE_BYTES,
+                                  &full_bar[stage]);
+                }
+                __syncwarp();
+            }
+            (void)tile_elems;
+        }
+        if (!ok && lane == 0) {
+            record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else {
+        // ------------------------------------------------------ consumers
+        const int tg = lane / LT;  // token slot within a warp row
+        const int c = lane % LT;   // lane within the token group
+
+        // q for every head of the group, pre-scaled to base-2 units.
+        float2 q2[GP][DPL / 2];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            if (g < G) {
+                const uint16_t *qrow =
+                    p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D;
+#pragma unroll
+                for (int i = 0; i < NPC; ++i) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + (c + LT * i) * 8);
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float2 f = widen2<BF16>(w[k]);
+                        q2[g][i * 4 + k] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < DPL / 2; ++j) q2[g][j] = make_float2(0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+            m_run[g] = -INFINITY;
+            m_true[g] = -INFINITY;
+            l_run[g] = 0.f;
+#pragma unroll
+            for (int j = 0; j < DPL / 2; ++j) acc[g][j] = make_float2(0.f, 0.f);
+        }
+
+        for (int u = warp; u < nunits; u += kConsumerWarps) {
+            const int stage = u % NS;
+            if (!mbar_wait(&full_bar[stage], (u / NS) & 1)) {
+                if (lane == 0) {
+                    record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            const uint8_t *kt = ring + stage * S::STAGE_BYTES;
+            const uint8_t *vt = kt + S::TILE_BYTES;
+            const int nvalid = end - (start + u * kUnit);  // >= 1
+            const bool partial = nvalid < kUnit;
+
+#pragma unroll
+            for (int ch = 0; ch < S::CHUNKS; ++ch) {
+                // ---- scores for R tokens of this lane group
+                float s[R][GP];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int t = (ch * R + r) * TPR + tg;
+                    float2 k2[DPL / 2];
+#pragma unroll
+                    for (int i = 0; i < NPC; ++i) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(
+                            kt + t * D * 2 + (c + LT * i) * 16);
+                        k2[i * 4 + 0] = widen2<BF16>(raw.x);
+                        k2[i * 4 + 1] = widen2<BF16>(raw.y);
+                        k2[i * 4 + 2] = widen2<BF16>(raw.z);
+                        k2[i * 4 + 3] = widen2<BF16>(raw.w);
+                    }
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int j = 0; j < DPL / 2; ++j) a = __ffma2_rn(q2[g][j], k2[j], a);
+                        s[r][g] = a.x + a.y;
+                    }
+                }
+#pragma unroll
+                for (int off = LT / 2; off >= 1; off >>= 1) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+#pragma unroll
+                        for (int g = 0; g < GP; ++g)
+                            s[r][g] += __shfl_xor_sync(kFullMask, s[r][g], off);
+                }
+                if (partial) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const int t = (ch * R + r) * TPR + tg;
+                        if (t >= nvalid) {
+#pragma unroll
+                            for (int g = 0; g < GP; ++g) s[r][g] = -INFINITY;
+                        }
+                    }
+                }
+                // ---- tile max per head across the warp; lazy rescale
+                float mx[GP];
+                bool need = false;
+#pragma unroll
+                for (int g = 0; g < GP; ++g) {
+                    float v = s[0][g];
+#pragma unroll
+                    for (int r = 1; r < R; ++r) v = fmaxf(v, s[r][g]);
+#pragma unroll
+                    for (int off = LT; off < 32; off <<= 1)
+                        v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
+                    mx[g] = v;
+                    m_true[g] = fmaxf(m_true[g], v);
+                    need |= v > m_run[g] + kLazyRescale;
+                }
+                if (need) {  // warp-uniform: every lane holds the same mx and m_run
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        const float mn = fmaxf(m_run[g], mx[g]);
+                        const float alpha = fast_exp2(m_run[g] - mn);
+                        m_run[g] = mn;
+                        l_run[g] *= alpha;
+                        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                        for (int j = 0; j < DPL / 2; ++j) acc[g][j] = __fmul2_rn(acc[g][j], a2);
+                    }
+                }
+                // ---- probabilities and P.V
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int t = (ch * R + r) * TPR + tg;
+                    float pr[GP];
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        pr[g] = fast_exp2(s[r][g] - m_run[g]);
+                        l_run[g] += pr[g];
+                    }
+                    float2 v2[DPL / 2];
+#pragma unroll
+                    for (int i = 0; i < NPC; ++i) {
+                        uint4 raw =
+                            *reinterpret_cast<const uint4 *>(vt + t * D * 2 + (c + LT * i) * 16);
+                        if (partial && t >= nvalid) raw = make_uint4(0u, 0u, 0u, 0u);
+                        v2[i * 4 + 0] = widen2<BF16>(raw.x);
+                        v2[i * 4 + 1] = widen2<BF16>(raw.y);
+                        v2[i * 4 + 2] = widen2<BF16>(raw.z);
+                        v2[i * 4 + 3] = widen2<BF16>(raw.w);
+                    }
+#pragma unroll
+                    for (int g = 0; g < GP; ++g) {
+                        const float2 pp = make_float2(pr[g], pr[g]);
+#pragma unroll
+                        for (int j = 0; j < DPL / 2; ++j) acc[g][j] = __ffma2_rn(pp, v2[j], acc[g][j]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        }
+
+        // Sum the token groups of the warp (they share m_run).
+#pragma unroll
+        for (int off = LT; off < 32; off <<= 1) {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                l_run[g] += __shfl_xor_sync(kFullMask, l_run[g], off);
+#pragma unroll
+                for (int j = 0; j < DPL / 2; ++j) {
+                    acc[g][j].x += __shfl_xor_sync(kFullMask, acc[g][j].x, off);
+                    acc[g][j].y += __shfl_xor_sync(kFullMask, acc[g][j].y, off);
+                }
+            }
+        }
+    }
+
+    __syncthreads();  // ring drained: every issued copy was waited on by a consumer
+    if (*abort_flag) {
+        // A bounded wait ran out.  Let any copy still in flight land before
+        // the CTA's shared memory is released, then stop.
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < NS; ++s) {
+                const int issued = (nunits - s + NS - 1) / NS;  // upper bound of phases
+                if (issued > 0) (void)mbar_wait(&full_bar[s], (issued - 1) & 1);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- warp merge
+    float *red_acc = reinterpret_cast<float *>(ring);                  // [W][GP][D]
+    float *red_m = red_acc + kConsumerWarps * GP * D;                  // [W][GP]
+    float *red_l = red_m + kConsumerWarps * GP;
+    float *red_t = red_l + kConsumerWarps * GP;
+    if (warp < kConsumerWarps) {
+        const int tg = lane / LT, c = lane % LT;
+        if (tg == 0) {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+#pragma unroll
+                for (int i = 0; i < NPC; ++i) {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        red_acc + ((warp * GP + g) * D) + (c + LT * i) * 8);
+                    dst[0] = make_float4(acc[g][i * 4 + 0].x, acc[g][i * 4 + 0].y,
+                                         acc[g][i * 4 + 1].x, acc[g][i * 4 + 1].y);
+                    dst[1] = make_float4(acc[g][i * 4 + 2].x, acc[g][i * 4 + 2].y,
+                                         acc[g][i * 4 + 3].x, acc[g][i * 4 + 3].y);
+                }
+            }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+                red_m[warp * GP + g] = m_run[g];
+                red_l[warp * GP + g] = l_run[g];
+                red_t[warp * GP + g] = m_true[g];
+            }
+        }
+    }
+    __syncthreads();
+
+    constexpr int kPer = 8;  // outputs per thread
+    for (int item = threadIdx.x; item < G * (D / kPer); item += blockDim.x) {
+        const int g = item / (D / kPer);
+        const int x0 = (item % (D / kPer)) * kPer;
+        float M = -INFINITY, MT = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            M = fmaxf(M, red_m[w * GP + g]);
+            MT = fmaxf(MT, red_t[w * GP + g]);
+        }
+        float f[kConsumerWarps];
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            f[w] = fast_exp2(red_m[w * GP + g] - M);  // empty warp: exp2(-inf) = 0
+            lsum += f[w] * red_l[w * GP + g];
+        }
+        const float inv = 1.0f / lsum;
+        float o[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) a += f[w] * red_acc[(w * GP + g) * D + x0 + k];
+            o[k] = a * inv;
+        }
+        const int h = kvh * G + g;
+        if (direct) {
+            uint4 packed = make_uint4(narrow2<BF16>(o[0], o[1]), narrow2<BF16>(o[2], o[3]),
+                                      narrow2<BF16>(o[4], o[5]), narrow2<BF16>(o[6], o[7]));
+            uint16_t *out = static_cast<uint16_t *>(p.out);
+            *reinterpret_cast<uint4 *>(out + ((int64_t)seq * p.num_q_heads + h) * D + x0) = packed;
+        } else {
+            const int64_t row = ((int64_t)seq * p.num_q_heads + h) * p.num_partitions + part;
+            if (x0 == 0) {
+                p.part_m[row] = MT;
+                p.part_l[row] = lsum * fast_exp2(M - MT);
+            }
+            float4 *dst = reinterpret_cast<float4 *>(p.part_o + row * D + x0);
+            dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ reduce
+struct ReduceParams {
+    void *out;
+    const float *part_m;
+    const float *part_l;
+    const float *part_o;
+    const int32_t *seq_lens;
+    int *err;
+    int num_seqs;
+    int num_q_heads;
+    int max_seq_len;
+    int partition_tokens;
+    int num_partitions;
+    int skip_single;  // 1: rows of single-partition sequences were written directly
+};
+
+constexpr int kReduceWarps = 4;
+
+// One warp per (sequence, query head); lane owns D/32 consecutive dims.
+template <bool BF16, int D>
+__global__ void __launch_bounds__(kReduceWarps * 32) split_reduce_kernel(const ReduceParams p) {
+    constexpr int V = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * kReduceWarps + warp;
+    if (row >= (int64_t)p.num_seqs * p.num_q_heads) return;
+    const int seq = (int)(row / p.num_q_heads);
+    const int L = checked_len(p.seq_lens, seq, p.max_seq_len, p.max_seq_len, p.err, false);
+    const int np = L == 0 ? 0 : (L - 1) / p.partition_tokens + 1;
+    if (p.skip_single && np <= 1) return;
+    uint16_t *out = static_cast<uint16_t *>(p.out) + row * D + lane * V;
+    if (np == 0) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) out[k] = 0;
+        return;
+    }
+    const float *m = p.part_m + row * p.num_partitions;
+    const float *l = p.part_l + row * p.num_partitions;
+    const float *o = p.part_o + row * p.num_partitions * D + lane * V;
+    float M = -INFINITY;
+    for (int k = lane; k < np; k += 32) M = fmaxf(M, m[k]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
+    float acc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) acc[k] = 0.f;
+    float lsum = 0.f;
+    for (int k = 0; k < np; ++k) {
+        const float mk = m[k];
+        const float w = (mk == -INFINITY) ? 0.f : l[k] * fast_exp2(mk - M);
+        lsum += w;
+        const float *ok = o + (int64_t)k * D;
+        if constexpr (V == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(ok);
+            acc[0] += w * v.x;
+            acc[1] += w * v.y;
+            acc[2] += w * v.z;
+            acc[3] += w * v.w;
+        } else {
+            const float2 v = *reinterpret_cast<const float2 *>(ok);
+            acc[0] += w * v.x;
+            acc[1] += w * v.y;
+        }
+    }
+    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+    if constexpr (V == 4) {
+        uint2 packed = make_uint2(narrow2<BF16>(acc[0] * inv, acc[1] * inv),
+                                  narrow2<BF16>(acc[2] * inv, acc[3] * inv));
+        *reinterpret_cast<uint2 *>(out) = packed;
+    } else {
+        *reinterpret_cast<uint32_t *>(out) = narrow2<BF16>(acc[0] * inv, acc[1] * inv);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+using DecodeKernel = void (*)(const DecodeParams);
+using ReduceKernel = void (*)(const ReduceParams);
+
+struct DecodeEntry {
+    DecodeKernel fn;
+    int smem;
+};
+
+template <bool BF16, int D, int GP>
+DecodeEntry decode_entry() {
+    return {paged_decode_kernel<BF16, D, GP>, DecodeShape<D, GP>::SMEM_BYTES};
+}
+
+static int group_pad(int G) { return G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8; }
+
+static bool pick_decode(pa_dtype dt, int D, int GP, DecodeEntry *e) {
+    const bool bf = dt == PA_BF16;
+#define PA_CASE(BFV, DV, GV)                          \
+    if (bf == BFV && D == DV && GP == GV) {            \
+        *e = decode_entry<BFV, DV, GV>();              \
+        return true;                                   \
+    }
+    PA_CASE(false, 64, 1) PA_CASE(false, 64, 2) PA_CASE(false, 64, 4) PA_CASE(false, 64, 8)
+    PA_CASE(false, 128, 1) PA_CASE(false, 128, 2) PA_CASE(false, 128, 4) PA_CASE(false, 128, 8)
+    PA_CASE(true, 64, 1) PA_CASE(true, 64, 2) PA_CASE(true, 64, 4) PA_CASE(true, 64, 8)
+    PA_CASE(true, 128, 1) PA_CASE(true, 128, 2) PA_CASE(true, 128, 4) PA_CASE(true, 128, 8)
+#undef PA_CASE
+    return false;
+}
+
+static ReduceKernel pick_reduce(pa_dtype dt, int D) {
+    if (dt == PA_BF16) return D == 64 ? split_reduce_kernel<true, 64> : split_reduce_kernel<true, 128>;
+    return D == 64 ? split_reduce_kernel<false, 64> : split_reduce_kernel<false, 128>;
+}
+
+static int ilog2_exact(int x) {
+    int k = 0;
+    while ((1 << k) < x) ++k;
+    return (1 << k) == x ? k : -1;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WorkspaceLayout {
+    size_t m_off, l_off, o_off, bytes;
+};
+
+static WorkspaceLayout workspace_layout(int S, int Hq, int D, int NP) {
+    const size_t rows = (size_t)S * Hq * NP;
+    WorkspaceLayout w;
+    w.m_off = 0;
+    w.l_off = align256(rows * sizeof(float));
+    w.o_off = w.l_off + align256(rows * sizeof(float));
+    w.bytes = w.o_off + align256(rows * D * sizeof(float));
+    return w;
+}
+
+// Occupancy of a decode instantiation (CTAs per SM), cached per kernel/device.
+static int decode_ctas_per_sm(const DecodeEntry &e) {
+    int n = 0;
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(e.fn), e.smem)) return 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, e.fn, kDecodeThreads, e.smem) !=
+        cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+// Automatic partition size: aim for the largest work item to be at most
+// 1/32 of one CTA slot's share of the whole job (taking the average length
+// as half the maximum), in multiples of 256 positions, and run single pass
+// when that would not split anything.
+static int auto_partition(int S, int Hkv, int max_seq_len, const DecodeEntry &e, int block_size) {
+    if (max_seq_len <= 0) return -1;
+    const int slots = sm_count() * decode_ctas_per_sm(e);
+    const double units = (double)S * Hkv;
+    double target = (double)max_seq_len * units / (32.0 * (slots > 0 ? slots : 1));
+    int P = (int)std::ceil(target / 256.0) * 256;
+    if (P < 256) P = 256;
+    if (P % block_size) P = (P / block_size + 1) * block_size;
+    if (P >= max_seq_len) return -1;
+    return P;
+}
+
+struct ResolvedDecode {
+    DecodeEntry entry;
+    int P;   // -1 single pass, else partition size
+    int NP;  // partitions in the grid
+};
+
+static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int max_seq_len, int partition_tokens, pa_dtype dtype,
+                         ResolvedDecode *r) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0)
+        return PA_ERR_INVALID;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID;
+    if (num_q_heads % num_kv_heads) return PA_ERR_INVALID;
+    const int G = num_q_heads / num_kv_heads;
+    if (G > 8 || (head_dim != 64 && head_dim != 128) || (block_size != 16 && block_size != 32))
+        return PA_ERR_UNSUPPORTED;
+    if (!pick_decode(dtype, head_dim, group_pad(G), &r->entry)) return PA_ERR_UNSUPPORTED;
+    int P = partition_tokens;
+    if (P == 0) P = auto_partition(num_seqs, num_kv_heads, max_seq_len, r->entry, block_size);
+    if (P < -1) return PA_ERR_INVALID;
+    if (P > 0 && (P % block_size != 0 || P % kUnit != 0)) return PA_ERR_INVALID;
+    r->P = P;
+    r->NP = (P > 0) ? (max_seq_len + P - 1) / P : 1;
+    if (r->NP < 1) r->NP = 1;
+    return PA_OK;
+}
+
+static pa_status launch_decode(const ResolvedDecode &r, DecodeParams prm, int num_seqs,
+                               int num_kv_heads, cudaStream_t stream) {
+    if (num_seqs == 0) return PA_OK;
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(r.entry.fn), r.entry.smem))
+        return PA_ERR_CUDA;
+    if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_INVALID;
+    dim3 grid((unsigned)r.NP, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    r.entry.fn<<<grid, kDecodeThreads, r.entry.smem, stream>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+static pa_status fill_common(DecodeParams *prm, const void *q, const void *k_pool,
+                             const void *v_pool, int num_blocks, const int32_t *block_tables,
+                             int max_blocks_per_seq, const int32_t *seq_lens, int max_seq_len,
+                             int num_seqs, int num_q_heads, int num_kv_heads, int block_size,
+                             float scale) {
+    if (num_blocks <= 0 || max_blocks_per_seq < 0 || !std::isfinite(scale)) return PA_ERR_INVALID;
+    if (num_seqs > 0 && (!q || !k_pool || !v_pool || !block_tables || !seq_lens))
+        return PA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_INVALID;
+    std::memset(prm, 0, sizeof *prm);
+    prm->q = static_cast<const uint16_t *>(q);
+    prm->k_pool = static_cast<const uint16_t *>(k_pool);
+    prm->v_pool = static_cast<const uint16_t *>(v_pool);
+    prm->block_tables = block_tables;
+    prm->seq_lens = seq_lens;
+    prm->num_blocks = num_blocks;
+    prm->max_blocks_per_seq = max_blocks_per_seq;
+    prm->max_seq_len = max_seq_len;
+    prm->num_q_heads = num_q_heads;
+    prm->num_kv_heads = num_kv_heads;
+    prm->group = num_q_heads / num_kv_heads;
+    prm->block_size = block_size;
+    prm->log2_block = ilog2_exact(block_size);
+    prm->scale_log2 = scale * kLog2e;
+    prm->err = error_word();
+    return prm->err ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
+                             int block_size, int group_size, pa_dtype dtype) {
+    DecodeEntry e;
+    if (!pick_decode(dtype, head_dim, group_pad(group_size), &e)) return -1;
+    return auto_partition(num_seqs, num_kv_heads, max_seq_len, e, block_size);
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_seq_len, int partition_tokens,
+                                pa_dtype dtype) {
+    ResolvedDecode r;
+    if (resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                partition_tokens, dtype, &r) != PA_OK)
+        return 0;
+    if (r.P <= 0) return 0;
+    return workspace_layout(num_seqs, num_q_heads, head_dim, r.NP).bytes;
+}
+
+pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_pool,
+                    int num_blocks, const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *seq_lens, int max_seq_len, int num_seqs, int num_q_heads,
+                    int num_kv_heads, int head_dim, int block_size, float scale,
+                    int partition_tokens, void *workspace, size_t workspace_bytes,
+                    pa_dtype dtype, void *stream) {
+    ResolvedDecode r;
+    pa_status st = resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_seq_len, partition_tokens, dtype, &r);
+    if (st != PA_OK) return st;
+    if (num_seqs > 0 && (!out || !aligned16(out))) return PA_ERR_INVALID;
+    DecodeParams prm;
+    st = fill_common(&prm, q, k_pool, v_pool, num_blocks, block_tables, max_blocks_per_seq,
+                     seq_lens, max_seq_len, num_seqs, num_q_heads, num_kv_heads, block_size,
+                     scale);
+    if (st != PA_OK) return st;
+    prm.out = out;
+    prm.mode = 0;
+    cudaStream_t s = as_stream(stream);
+    if (r.P <= 0) {
+        prm.partition_tokens = kSinglePassTokens;
+        prm.num_partitions = 1;
+        return launch_decode(r, prm, num_seqs, num_kv_heads, s);
+    }
+    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, r.NP);
+    if (!workspace || workspace_bytes < w.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return PA_ERR_INVALID;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    prm.part_m = reinterpret_cast<float *>(ws + w.m_off);
+    prm.part_l = reinterpret_cast<float *>(ws + w.l_off);
+    prm.part_o = reinterpret_cast<float *>(ws + w.o_off);
+    prm.partition_tokens = r.P;
+    prm.num_partitions = r.NP;
+    st = launch_decode(r, prm, num_seqs, num_kv_heads, s);
+    if (st != PA_OK || num_seqs == 0) return st;
+    ReduceParams rp;
+    rp.out = out;
+    rp.part_m = prm.part_m;
+    rp.part_l = prm.part_l;
+    rp.part_o = prm.part_o;
+    rp.seq_lens = seq_lens;
+    rp.err = prm.err;
+    rp.num_seqs = num_seqs;
+    rp.num_q_heads = num_q_heads;
+    rp.max_seq_len = max_seq_len < max_blocks_per_seq * block_size
+                         ? max_seq_len
+                         : max_blocks_per_seq * block_size;
+    rp.partition_tokens = r.P;
+    rp.num_partitions = r.NP;
+    rp.skip_single = 1;
+    const int64_t rows = (int64_t)num_seqs * num_q_heads;
+    const unsigned blocks = (unsigned)((rows + kReduceWarps - 1) / kReduceWarps);
+    pick_reduce(dtype, head_dim)<<<blocks, kReduceWarps * 32, 0, s>>>(rp);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_partitions(const void *q, const void *k_pool, const void *v_pool,
+                               int num_blocks, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *seq_lens, int max_seq_len,
+                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, float scale, int partition_tokens,
+                               void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                               void *stream) {
+    if (partition_tokens <= 0) return PA_ERR_INVALID;
+    ResolvedDecode r;
+    pa_status st = resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_seq_len, partition_tokens, dtype, &r);
+    if (st != PA_OK) return st;
+    DecodeParams prm;
+    st = fill_common(&prm, q, k_pool, v_pool, num_blocks, block_tables, max_blocks_per_seq,
+                     seq_lens, max_seq_len, num_seqs, num_q_heads, num_kv_heads, block_size,
+                     scale);
+    if (st != PA_OK) return st;
+    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, r.NP);
+    if (num_seqs > 0 &&
+        (!workspace || workspace_bytes < w.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255)))
+        return PA_ERR_INVALID;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    prm.part_m = reinterpret_cast<float *>(ws + w.m_off);
+    prm.part_l = reinterpret_cast<float *>(ws + w.l_off);
+    prm.part_o = reinterpret_cast<float *>(ws + w.o_off);
+    prm.partition_tokens = r.P;
+    prm.num_partitions = r.NP;
+    prm.mode = 1;
+    return launch_decode(r, prm, num_seqs, num_kv_heads, as_stream(stream));
+}
+
+pa_status pa_split_kv_reduce(void *out, const void *workspace, size_t workspace_bytes,
+                             const int32_t *seq_lens, int max_seq_len, int num_seqs,
+                             int num_q_heads, int head_dim, int partition_tokens, pa_dtype dtype,
+                             void *stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || max_seq_len < 0 || partition_tokens <= 0 ||
+        partition_tokens % kUnit)
+        return PA_ERR_INVALID;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    const int NP = max_seq_len > 0 ? (max_seq_len + partition_tokens - 1) / partition_tokens : 1;
+    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, NP);
+    if (!out || !seq_lens || !workspace || workspace_bytes < w.bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255) || !aligned16(out))
+        return PA_ERR_INVALID;
+    ReduceParams rp;
+    const uint8_t *ws = static_cast<const uint8_t *>(workspace);
+    rp.out = out;
+    rp.part_m = reinterpret_cast<const float *>(ws + w.m_off);
+    rp.part_l = reinterpret_cast<const float *>(ws + w.l_off);
+    rp.part_o = reinterpret_cast<const float *>(ws + w.o_off);
+    rp.seq_lens = seq_lens;
+    rp.err = error_word();
+    if (!rp.err) return PA_ERR_CUDA;
+    rp.num_seqs = num_seqs;
+    rp.num_q_heads = num_q_heads;
+    rp.max_seq_len = max_seq_len;
+    rp.partition_tokens = partition_tokens;
+    rp.num_partitions = NP;
+    rp.skip_single = 0;
+    const int64_t rows = (int64_t)num_seqs * num_q_heads;
+    const unsigned blocks = (unsigned)((rows + kReduceWarps - 1) / kReduceWarps);
+    pick_reduce(dtype, head_dim)<<<blocks, kReduceWarps * 32, 0, as_stream(stream)>>>(rp);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // extern "C"
