@@ -1,0 +1,494 @@
+"""Benchmark of the paged decode step on GB300.
+
+One step = the whole hot path over one batch: (copy-on-write block copies,)
+the cache write of every sequence's new token, and paged decode attention
+(split-KV partition kernel + reduce) -- for every layer of the workload.
+
+Default workload: the Llama-3-8B-shaped decode batch (256 sequences, lengths
+U[512, 8192], 32 q / 8 KV heads, d 128, bf16, B 16), whose K/V (~4.6 GB per
+step) is far larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, same metric
+
+Prints one JSON line (rank 0).  Multi-GPU: one process per GPU under
+torch.distributed.run; every rank decodes its own batch (weak scaling, no
+collective on the data path); value = bytes of all ranks / max time.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention achieved HBM GB/s (% of GB300 peak); decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------- helpers
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def reduce_over_ranks(seconds, units, device=None):
+    """(max seconds, summed units) over all ranks; identity when not
+    distributed.  Works with gloo (CPU tensors) and nccl (CUDA tensors)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return seconds, units
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_digest():
+    """Hash of the decode kernel source, to tell whether a stored ncu traffic
+    figure still describes the kernel being timed."""
+    h = hashlib.sha256()
+    for f in ("pa_decode.cu", "pa_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_64_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    workload, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"pa_decode_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_digest():
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------- oracle arm
+def oracle_sample(plan, budget_s, rng_seed=0):
+    """Time the fp64 oracle on as many of the workload's sequences as fit in
+    about budget_s seconds of host time.  Inputs are drawn on the host for
+    the sampled sequences only.  Returns (seconds, algorithmic bytes, tokens,
+    number of sequences, threads)."""
+    import torch
+
+    import oracle
+    from oracle.allocator import BlockAllocatorModel
+    from paged_kv_cache_64_gb300 import workloads
+
+    spec = plan.spec
+    lay = workloads.layout(plan, BlockAllocatorModel)
+    B = spec.block_size
+    shape = (plan.num_blocks, spec.num_kv_heads, B, spec.head_dim)
+    k = np.zeros(shape, dtype=np.uint16)  # pages are only touched where filled
+    v = np.zeros(shape, dtype=np.uint16)
+    dt = workloads.torch_dtype(spec.dtype)
+    gen = torch.Generator().manual_seed(spec.seed + rng_seed)
+    q = torch.randn((spec.num_seqs, spec.num_q_heads, spec.head_dim), generator=gen,
+                    dtype=dt).view(torch.int16).numpy().view(np.uint16)
+
+    def fill(seqs):
+        for s in seqs:
+            nb = -(-int(lay.seq_lens[s]) // B)
+            ids = lay.block_tables[s, :nb]
+            for pool in (k, v):
+                vals = torch.randn((nb,) + shape[1:], generator=gen, dtype=dt)
+                pool[ids] = vals.view(torch.int16).numpy().view(np.uint16)
+
+    order = list(range(spec.num_seqs))
+    done, seconds, nbytes, tokens = [], 0.0, 0, 0
+    batch = 1
+    filled = set()
+    while order and seconds < budget_s:
+        take, order = order[:batch], order[batch:]
+        fill([s for s in take if s not in filled])
+        filled.update(take)
+        if not order and seconds < 0.6 * budget_s:
+            order = list(range(spec.num_seqs))  # go round the batch again
+        t0 = time.perf_counter()
+        oracle.decode(q, k, v, lay.block_tables, lay.seq_lens, plan.scale, spec.dtype, seqs=take)
+        dt_s = time.perf_counter() - t0
+        seconds += dt_s
+        done += take
+        nbytes += workloads.algorithmic_bytes(spec, lay.seq_lens[take])
+        tokens += len(take)
+        per_seq = dt_s / len(take)
+        batch = max(1, min(len(order), int((budget_s - seconds) / max(per_seq, 1e-6) / 2) or 1))
+    return seconds, nbytes, tokens, len(done), oracle.num_threads()
+
+
+def sample_text(nseq, total):
+    if nseq <= total:
+        return f"{nseq} of {total} sequences"
+    return f"all {total} sequences, {nseq / total:.1f} passes"
+
+
+
+def run_reference(args, rank, world):
+    from paged_kv_cache_64_gb300 import workloads
+    if rank != 0:
+        return
+    plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs)
+    per_step = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        budget = args.ref_step_seconds
+        secs, nbytes, toks, nseq, threads = oracle_sample(plan, budget, rng_seed=i)
+        if i >= args.warmup:
+            per_step.append((secs, nbytes, toks, nseq))
+        info = threads
+    secs = sum(s for s, _, _, _ in per_step)
+    nbytes = sum(b for _, b, _, _ in per_step)
+    toks = sum(t for _, _, t, _ in per_step)
+    gbs = nbytes / secs / 1e9
+    layers = plan.spec.num_layers
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / len(per_step), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": plan.spec.dtype, "data": "synthetic",
+        "config": {"workload": plan.spec.name + ": " + plan.spec.describe,
+                   "layers_in_step": layers,
+                   "sample": "each step decodes as many of the batch's sequences as fit in "
+                             f"~{args.ref_step_seconds:.0f} s (all heads of each)"},
+        "tokens_per_s": toks / secs / layers,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": info, "kind": "oracle",
+                         "sample": sample_text(per_step[0][3], plan.spec.num_seqs) + " per step"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- GPU arm
+class GpuStep:
+    """Device state of one workload and the calls of one decode step."""
+
+    def __init__(self, plan, device):
+        import torch
+        from paged_kv_cache_64_gb300 import api, workloads
+
+        self.api, self.torch = api, torch
+        self.plan, self.spec = plan, plan.spec
+        self.device = device
+        self.lay = workloads.layout(plan, api.BlockAllocator)
+        self.vals = workloads.make_values(plan, self.lay, device)
+        t = lambda a: torch.as_tensor(a, device=device)
+        self.tables, self.lens = t(self.lay.block_tables), t(self.lay.seq_lens)
+        self.slots, self.copies = t(self.lay.slot_mapping), t(self.lay.pre_copies)
+        self.max_seq_len = int(self.lay.max_seq_len)
+        spec = self.spec
+        self.P = spec.partition_tokens
+        self.resolved_P = self.P if self.P else api.auto_partition(
+            spec.num_seqs, spec.num_kv_heads, self.max_seq_len, spec.head_dim, spec.block_size,
+            spec.num_q_heads // spec.num_kv_heads, self.vals.q.dtype)
+        size = api.workspace_size(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads,
+                                  spec.head_dim, spec.block_size, self.max_seq_len, self.P,
+                                  self.vals.q.dtype)
+        self.ws = api.alloc_workspace(size, device) if size else None
+        self.out = [torch.empty_like(self.vals.q) for _ in range(spec.num_layers)]
+        self.decode_bytes = workloads.algorithmic_bytes(spec, self.lay.seq_lens)
+        self.write_bytes = workloads.cache_write_bytes(spec, spec.num_seqs)
+        self.copy_bytes = 2 * 2 * len(self.lay.pre_copies) * spec.num_kv_heads * \
+            spec.block_size * spec.head_dim * workloads.DTYPE_BYTES[spec.dtype]
+        per_layer = 2 + (1 if self.resolved_P and self.resolved_P > 0 else 0) + \
+            (1 if len(self.lay.pre_copies) else 0)
+        self.launches_per_step = per_layer * spec.num_layers
+
+    def step_bytes(self):
+        return self.spec.num_layers * (self.decode_bytes + self.write_bytes + self.copy_bytes)
+
+    def run(self, ev=None, q=None, k_new=None, v_new=None, stream=None):
+        """One step.  ev: optional list collecting (start, end) events around
+        each decode call."""
+        api, v = self.api, self.vals
+        q = v.q if q is None else q
+        for layer in range(self.spec.num_layers):
+            kp, vp = v.k_pools[layer], v.v_pools[layer]
+            if self.copies.numel():
+                api.copy_blocks([kp], [vp], self.copies, stream=stream)
+            api.cache_write(v.k_new[layer] if k_new is None else k_new[layer],
+                            v.v_new[layer] if v_new is None else v_new[layer],
+                            self.slots, kp, vp, stream=stream)
+            if ev is not None:
+                a = self.torch.cuda.Event(enable_timing=True)
+                b = self.torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            api.decode(self.out[layer], q, kp, vp, self.tables, self.lens, self.max_seq_len,
+                       self.plan.scale, partition_tokens=self.P, workspace=self.ws, stream=stream)
+            if ev is not None:
+                b.record(stream)
+                ev.append((a, b))
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    from paged_kv_cache_64_gb300 import api, workloads
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    base = workloads.SPECS[args.workload]
+    plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs,
+                               seed=base.seed + 1000 * rank if rank else None)
+    st = GpuStep(plan, device)
+    stream = torch.cuda.current_stream()
+    spec = st.spec
+    flush = None
+    if st.step_bytes() < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+
+    for _ in range(args.warmup):
+        st.run()
+    api.check_error()
+
+    # ------------------------------------------------ timed region (device)
+    ev = []
+    step_ms = []
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        if flush is None:
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for _ in range(args.steps):
+                st.run(ev)
+            t1.record()
+            torch.cuda.synchronize()
+            total_ms = t0.elapsed_time(t1)
+        else:
+            for _ in range(args.steps):
+                flush.fill_(1)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                st.run(ev)
+                b.record()
+                step_ms.append((a, b))
+            torch.cuda.synchronize()
+            total_ms = sum(a.elapsed_time(b) for a, b in step_ms)
+    barrier()
+    api.check_error()
+    secs, all_bytes = reduce_over_ranks(total_ms / 1e3, st.step_bytes() * args.steps, device)
+    value = all_bytes / secs / 1e9
+    decode_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_avg_ms = statistics.mean(decode_ms)
+    peak, peak_kind = measured_peaks()
+    achieved = st.decode_bytes / (dec_avg_ms / 1e3) / 1e9
+    traffic = stored_traffic(args.workload)
+
+    # ------------------------------------------------ end to end (host buffers)
+    pin = lambda t: t.cpu().pin_memory()
+    h_q = pin(st.vals.q)
+    h_kn = [pin(t) for t in st.vals.k_new]
+    h_vn = [pin(t) for t in st.vals.v_new]
+    h_tab, h_len, h_slot = pin(st.tables), pin(st.lens), pin(st.slots)
+    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.out]
+    d_q = torch.empty_like(st.vals.q)
+    d_kn = [torch.empty_like(t) for t in st.vals.k_new]
+    d_vn = [torch.empty_like(t) for t in st.vals.v_new]
+    h2d = (h_q.nbytes + sum(t.nbytes for t in h_kn + h_vn) + h_tab.nbytes + h_len.nbytes +
+           h_slot.nbytes)
+    d2h = sum(t.nbytes for t in h_out)
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        for d, h in zip(d_kn + d_vn, h_kn + h_vn):
+            d.copy_(h, non_blocking=True)
+        st.tables.copy_(h_tab, non_blocking=True)
+        st.lens.copy_(h_len, non_blocking=True)
+        st.slots.copy_(h_slot, non_blocking=True)
+        st.run(q=d_q, k_new=d_kn, v_new=d_vn)
+        for h, o in zip(h_out, st.out):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, args.steps // 2)
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    t1.record()
+    torch.cuda.synchronize()
+    e2e_s, e2e_bytes = reduce_over_ranks(t0.elapsed_time(t1) / 1e3,
+                                         st.step_bytes() * e2e_steps, device)
+    api.check_error()
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": spec.dtype, "data": "synthetic",
+        "config": {
+            "workload": f"{spec.name}: {spec.describe}",
+            "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
+            "kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+            "block_size": spec.block_size, "layers": spec.num_layers,
+            "mean_seq_len": float(np.mean(st.lay.seq_lens)),
+            "partition_tokens": st.resolved_P,
+            "decode_ctas_per_sm": api.ctas_per_sm(spec.head_dim,
+                                                  spec.num_q_heads // spec.num_kv_heads,
+                                                  st.vals.q.dtype),
+            "step": "copy_blocks (if any) + cache_write + paged decode, every layer",
+            "l2": ("inputs larger than L2 (%.2f GB per step)" % (st.step_bytes() / 1e9))
+            if flush is None else "L2 flushed (256 MiB write) before every step",
+        },
+        "pct_of_peak": 100.0 * value / peak,
+        "tokens_per_s": spec.num_seqs * world / (secs / args.steps),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "pa_decode call (split-KV partition kernel + reduce)",
+                     "bytes_per_launch": st.decode_bytes, "avg_launch_ms": dec_avg_ms,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "e2e": {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": 1e3 * e2e_s / e2e_steps},
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        secs_c, nbytes_c, toks_c, nseq_c, threads = oracle_sample(plan, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": nbytes_c / secs_c / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle decode of {sample_text(nseq_c, spec.num_seqs)} (all "
+                      f"heads), {secs_c:.1f} s on host cores"}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama",
+                    choices=["tiny", "qwen", "llama", "prefix", "long"])
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="shrink the batch (profiling of small cases only)")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

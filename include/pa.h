@@ -164,6 +164,10 @@ pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_
 int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
                              int block_size, int group_size, pa_dtype dtype);
 
+/* Resident CTAs per SM of the decode kernel that these shapes select
+ * (occupancy query on the current device; 0 if unsupported). */
+int pa_decode_ctas_per_sm(int head_dim, int group_size, pa_dtype dtype);
+
 /* Bytes of workspace pa_decode / pa_decode_partitions need for these
  * shapes; 0 for single pass.  partition_tokens as in pa_decode (0 = auto,
  * resolved as pa_decode would with the same arguments). */
@@ -217,6 +221,17 @@ pa_status pa_split_kv_reduce(void *out, const void *workspace, size_t workspace_
  * PA_ERR_DEVICE_TIMEOUT, or PA_ERR_CUDA if the synchronisation failed.
  * ---------------------------------------------------------------------- */
 pa_status pa_check_error(void *stream);
+
+/* ------------------------------------------------------------------------
+ * pa_selftest_wait_timeout: exercises the bounded-wait error path.  Launches
+ * one CTA that waits on a shared-memory mbarrier no thread ever arrives on,
+ * with the same bounded wait the decode pipeline uses; after the library's
+ * wait limit (about one second) the kernel gives up, records
+ * PA_ERR_DEVICE_TIMEOUT in the error word and returns.  The GPU context
+ * stays usable.  Read the result with pa_check_error.  (Diagnostic entry
+ * point; the pages have no counterpart.)
+ * ---------------------------------------------------------------------- */
+pa_status pa_selftest_wait_timeout(void *stream);
 
 /* ========================================================================
  * Host block allocator (CPU only; no device calls).

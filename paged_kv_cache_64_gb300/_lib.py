@@ -39,6 +39,7 @@ SIGNATURES = {
                            _c_int, _c_int, _c_int, _c_f, _c_int, _vp, _c_sz, _c_int, _vp]),
     "pa_decode_auto_partition": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           _c_int]),
+    "pa_decode_ctas_per_sm": (_c_int, [_c_int, _c_int, _c_int]),
     "pa_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                          _c_int]),
     "pa_decode_partitions": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _c_int, _vp, _c_int, _c_int,
@@ -47,6 +48,7 @@ SIGNATURES = {
     "pa_split_kv_reduce": (_c_int, [_vp, _vp, _c_sz, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                     _c_int, _vp]),
     "pa_check_error": (_c_int, [_vp]),
+    "pa_selftest_wait_timeout": (_c_int, [_vp]),
     "pa_alloc_create": (_c_int, [_c_int, _c_int, _i32p, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_seq_add": (_c_int, [_vp, _c_i64]),

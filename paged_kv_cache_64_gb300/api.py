@@ -50,6 +50,12 @@ def check_error(stream=None):
     _lib.check("pa_check_error", _lib.load().pa_check_error(_stream_handle(stream)))
 
 
+def selftest_wait_timeout(stream=None):
+    """Launch the bounded-wait self-test kernel (see pa.h)."""
+    _lib.check("pa_selftest_wait_timeout",
+               _lib.load().pa_selftest_wait_timeout(_stream_handle(stream)))
+
+
 def cache_write(k_new, v_new, slot_mapping, k_pool, v_pool, stream=None):
     """reshape_and_cache: k_new/v_new [T, Hkv, d] into pools [NB, Hkv, B, d]
     at slot_mapping (int64 [T]; slot = block * B + offset, < 0 skips)."""
@@ -108,6 +114,10 @@ def _decode_dims(q, k_pool, block_tables, seq_lens):
 def auto_partition(num_seqs, num_kv_heads, max_seq_len, head_dim, block_size, group, dtype):
     return _lib.load().pa_decode_auto_partition(num_seqs, num_kv_heads, max_seq_len, head_dim,
                                                 block_size, group, _DTYPES[dtype])
+
+
+def ctas_per_sm(head_dim, group, dtype):
+    return _lib.load().pa_decode_ctas_per_sm(head_dim, group, _DTYPES[dtype])
 
 
 def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,

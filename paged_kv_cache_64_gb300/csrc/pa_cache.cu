@@ -124,6 +124,17 @@ __global__ void copy_blocks_kernel(const PoolPtrs pools, const int64_t *__restri
         d[i] = s[i];
 }
 
+// Waits on a barrier that never completes; the bounded wait must give up.
+__global__ void wait_timeout_kernel(int *err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) record_error(err, PA_ERR_DEVICE_TIMEOUT);
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -205,6 +216,13 @@ pa_status pa_copy_blocks(void *const *k_pools, void *const *v_pools, int num_lay
         if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
+}
+
+pa_status pa_selftest_wait_timeout(void *stream) {
+    int *err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, as_stream(stream)>>>(err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_check_error(void *stream) {

@@ -60,7 +60,7 @@ struct DecodeShape {
     static constexpr int DPL = D / LT;                     // dims per lane
     static constexpr int NPC = DPL / 8;                    // 16-byte pieces per lane
     static constexpr int TPR = 32 / LT;                    // tokens per warp row
-    static constexpr int R = 4;                            // rows per chunk
+    static constexpr int R = (GP >= 8) ? 2 : 4;            // rows per chunk
     static constexpr int CHUNKS = kUnit / (R * TPR);       // chunks per stage
     static constexpr int TILE_BYTES = kUnit * D * 2;       // one of K or V
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
@@ -202,7 +202,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 const int ph = __shfl_sync(kFullMask, phys, j);
                 const int stage = uu % NS;
                 if (uu >= NS) {
-                    if (!mbar_wait(&empty_bar[stage], ((uu / NS) - 1) & 1)) {
+                    // every lane waits; the outcome is made warp-uniform
+                    const bool done = mbar_wait(&empty_bar[stage], ((uu / NS) - 1) & 1);
+                    if (!__all_sync(kFullMask, done)) {
                         ok = false;
                         break;
                     }
@@ -264,7 +266,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
 
         for (int u = warp; u < nunits; u += kConsumerWarps) {
             const int stage = u % NS;
-            if (!mbar_wait(&full_bar[stage], (u / NS) & 1)) {
+            const bool landed = mbar_wait(&full_bar[stage], (u / NS) & 1);
+            if (!__all_sync(kFullMask, landed)) {
                 if (lane == 0) {
                     record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
                     *abort_flag = 1;
@@ -718,6 +721,13 @@ int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, in
     DecodeEntry e;
     if (!pick_decode(dtype, head_dim, group_pad(group_size), &e)) return -1;
     return auto_partition(num_seqs, num_kv_heads, max_seq_len, e, block_size);
+}
+
+int pa_decode_ctas_per_sm(int head_dim, int group_size, pa_dtype dtype) {
+    DecodeEntry e;
+    if (group_size < 1 || group_size > 8 || !pick_decode(dtype, head_dim, group_pad(group_size), &e))
+        return 0;
+    return decode_ctas_per_sm(e);
 }
 
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,

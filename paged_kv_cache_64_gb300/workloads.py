@@ -234,8 +234,8 @@ def algorithmic_bytes(spec, seq_lens):
     L = np.asarray(seq_lens, dtype=np.int64)
     kv = 2 * L.sum() * spec.num_kv_heads * spec.head_dim * b
     table = 4 * sum(_blocks(x, spec.block_size) for x in L)
-    qo = 2 * spec.num_seqs * spec.num_q_heads * spec.head_dim * b
-    return int(kv + table + qo + 4 * spec.num_seqs)
+    qo = 2 * len(L) * spec.num_q_heads * spec.head_dim * b
+    return int(kv + table + qo + 4 * len(L))
 
 
 def cache_write_bytes(spec, num_tokens):

@@ -1,0 +1,66 @@
+"""Host logic of bench.py's multi-rank path on CPU: two gloo ranks, max of the
+times and sum of the work across ranks (the only cross-rank step; there is no
+collective on the data path)."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        assert bench.dist_env() == (rank, world, rank)
+        secs, units = bench.reduce_over_ranks(1.0 + rank, 100.0 * (rank + 1))
+        bench.barrier()
+        q.put((rank, secs, units))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, secs, units in got:
+        assert secs == 2.0 and units == 300.0
+
+
+def test_single_process_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_over_ranks(1.5, 7.0) == (1.5, 7.0)
+
+
+def test_reference_arm_runs_on_cpu(capsys):
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3",
+                "--ref-step-seconds", "0.2"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0

@@ -1,0 +1,398 @@
+"""GPU parity: the CUDA kernels, called through the C ABI, against the fp64
+CPU oracle on the same seeded inputs.
+
+Decode outputs must satisfy |gpu - ref| <= 2e-3 + 1e-2 |ref| element by
+element; cache writes and block copies must be bit-exact over the whole pool.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_64_gb300 import _lib, api, workloads
+
+from _parity import Case, assert_close, bits
+
+pytestmark = pytest.mark.gpu
+
+LOG2E = 1.0 / math.log(2.0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+    _lib.load()  # fails loudly when the library was not built
+    yield
+    api.check_error()
+
+
+def full_step_parity(case, layer=0, partition=None, seqs=None):
+    blocks = None if seqs is None else case.blocks_of(seqs)
+    if case.lay.pre_copies.size:
+        blocks = None  # copies read blocks outside the sample: take whole pools
+    hk, hv = case.snapshot(layer, blocks)
+    case.gpu_writes(layer)
+    out = case.gpu_decode(layer, partition)
+    ref = case.oracle_step(layer, hk, hv, seqs)
+    api.check_error()
+    rows = None if seqs is None else np.asarray(seqs)
+    return assert_close(out, ref, case.spec.name, mask_rows=rows)
+
+
+# -------------------------------------------------------------- cache write
+@pytest.mark.parametrize("name", ["tiny", "qwen", "llama", "long"])
+def test_cache_write_bit_exact(name):
+    kw = {"tiny": {}, "qwen": {"num_seqs": 64}, "llama": {"num_seqs": 16, "len_range": (512, 1024)},
+          "long": {"num_seqs": 2, "len_range": (2000, 3000)}}[name]
+    case = Case(workloads.make_plan(name, **kw))
+    hk, hv = case.snapshot(0)
+    slots = case.slots.clone()
+    slots[::3] = -1  # negative slot: skip
+    kp, vp = case.vals.k_pools[0], case.vals.v_pools[0]
+    api.cache_write(case.vals.k_new[0], case.vals.v_new[0], slots, kp, vp)
+    oracle.cache_write(hk, hv, bits(case.vals.k_new[0]), bits(case.vals.v_new[0]),
+                       slots.cpu().numpy())
+    api.check_error()
+    assert np.array_equal(bits(kp), hk)
+    assert np.array_equal(bits(vp), hv)
+
+
+def test_cache_write_many_tokens_bit_exact():
+    """The prefix workload writes ~9k tail tokens in one call."""
+    case = Case(workloads.make_plan("prefix", cow=True))
+    hk, hv = case.snapshot(0)
+    kp, vp = case.vals.k_pools[0], case.vals.v_pools[0]
+    api.copy_blocks([kp], [vp], case.pre_copies)
+    api.cache_write(case.vals.k_pre[0], case.vals.v_pre[0], case.pre_slots, kp, vp)
+    oracle.copy_blocks([hk, hv], case.ref_lay.pre_copies)
+    oracle.cache_write(hk, hv, bits(case.vals.k_pre[0]), bits(case.vals.v_pre[0]),
+                       case.ref_lay.pre_slots)
+    api.check_error()
+    assert np.array_equal(bits(kp), hk) and np.array_equal(bits(vp), hv)
+
+
+# -------------------------------------------------------------- copy blocks
+def test_copy_blocks_cow_pairs_bit_exact():
+    case = Case(workloads.make_plan("prefix", cow=True))
+    assert case.pre_copies.shape == (63, 2)
+    hk, hv = case.snapshot(0)
+    kp, vp = case.vals.k_pools[0], case.vals.v_pools[0]
+    api.copy_blocks([kp], [vp], case.pre_copies)
+    oracle.copy_blocks([hk, hv], case.ref_lay.pre_copies)
+    api.check_error()
+    assert np.array_equal(bits(kp), hk) and np.array_equal(bits(vp), hv)
+
+
+def test_copy_blocks_multi_layer_bit_exact():
+    """Three layers of the Qwen-shaped pool, 40 random disjoint pairs."""
+    plan = workloads.make_plan("qwen", num_seqs=8)
+    case = Case(plan, layers=3)
+    rng = np.random.default_rng(7)
+    ids = rng.choice(plan.num_blocks, 80, replace=False)
+    pairs = np.stack([ids[:40], ids[40:]], axis=1).astype(np.int64)
+    hosts = [case.snapshot(l) for l in range(3)]
+    api.copy_blocks(case.vals.k_pools, case.vals.v_pools, torch.as_tensor(pairs, device="cuda"))
+    for hk, hv in hosts:
+        oracle.copy_blocks([hk, hv], pairs)
+    api.check_error()
+    for l, (hk, hv) in enumerate(hosts):
+        assert np.array_equal(bits(case.vals.k_pools[l]), hk)
+        assert np.array_equal(bits(case.vals.v_pools[l]), hv)
+
+
+def test_copy_blocks_empty_is_noop():
+    case = Case(workloads.make_plan("prefix"))
+    assert case.pre_copies.numel() == 0  # full shared blocks are never copied
+    before = bits(case.vals.k_pools[0])
+    api.copy_blocks([case.vals.k_pools[0]], [case.vals.v_pools[0]], case.pre_copies)
+    api.check_error()
+    assert np.array_equal(bits(case.vals.k_pools[0]), before)
+
+
+# ---------------------------------------------------------------- decode
+@pytest.mark.parametrize("partition", [None, -1, 16, 32])
+def test_decode_tiny_full(partition):
+    """Tiny workload: every output compared; single pass and split-KV with
+    partitions of one and two blocks."""
+    full_step_parity(Case(workloads.make_plan("tiny")), partition=partition)
+
+
+@pytest.mark.parametrize("name,kw,partition", [
+    ("qwen", {"num_seqs": 24}, None),
+    ("qwen", {"num_seqs": 24}, -1),
+    ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, None),
+    ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, -1),
+    ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, 256),
+    ("prefix", {"num_seqs": 6}, None),
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, None),
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, -1),
+])
+def test_decode_small_every_output(name, kw, partition):
+    """Reduced workloads (same heads, d, B, dtype) where the oracle checks
+    every output: many tiles, ragged last blocks, several partitions."""
+    full_step_parity(Case(workloads.make_plan(name, **kw)), partition=partition)
+
+
+def test_decode_prefix_cow_small():
+    full_step_parity(Case(workloads.make_plan("prefix", num_seqs=6, cow=True)))
+
+
+@pytest.mark.parametrize("name,cow,nsample", [("llama", False, 12), ("long", False, 3),
+                                             ("prefix", True, 8), ("qwen", False, 16)])
+def test_decode_full_size_sampled(name, cow, nsample):
+    """Full-size workloads in the launch configuration the benchmark times;
+    the oracle checks every head of a sample of sequences (always including
+    the longest and the shortest)."""
+    case = Case(workloads.make_plan(name, cow=cow))
+    lens = case.lay.seq_lens
+    rng = np.random.default_rng(11)
+    seqs = {int(np.argmax(lens)), int(np.argmin(lens))}
+    seqs.update(rng.choice(len(lens), nsample, replace=False).tolist())
+    full_step_parity(case, seqs=sorted(seqs)[:nsample + 2])
+
+
+def test_decode_qwen_layers_sampled():
+    """Several layers of the 24-layer Qwen-shaped step, each with its own pools."""
+    case = Case(workloads.make_plan("qwen"), layers=3)
+    seqs = [0, 5, int(np.argmax(case.lay.seq_lens))]
+    for layer in range(3):
+        full_step_parity(case, layer=layer, seqs=seqs)
+
+
+# ------------------------------------------------------------- edge cases
+def test_zero_and_one_token_sequences():
+    case = Case(workloads.make_plan("tiny"))
+    case.gpu_writes(0)
+    lens = case.lay.seq_lens.copy()
+    lens[0], lens[1] = 0, 1
+    lens_t = torch.as_tensor(lens, device="cuda")
+    for P in (-1, 16, 0):
+        out = torch.full_like(case.vals.q, float("nan"))
+        api.decode(out, case.vals.q, case.vals.k_pools[0], case.vals.v_pools[0], case.tables,
+                   lens_t, case.max_seq_len, case.plan.scale, partition_tokens=P)
+        hk, hv = bits(case.vals.k_pools[0]), bits(case.vals.v_pools[0])
+        ref = oracle.decode(bits(case.vals.q), hk, hv, case.ref_lay.block_tables, lens,
+                            case.plan.scale, "f16")
+        assert torch.all(out[0] == 0)
+        # one token: the output is that token's value vector (rounded once)
+        v0 = oracle.widen(hv[case.ref_lay.block_tables[1, 0], :, 0, :], "f16")
+        assert np.allclose(ref[1], np.repeat(v0, 2, axis=0), atol=0)
+        assert_close(out, ref, f"edge P={P}")
+    api.check_error()
+
+
+def test_all_zero_lengths():
+    case = Case(workloads.make_plan("tiny"))
+    lens_t = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out = torch.full_like(case.vals.q, float("nan"))
+    api.decode(out, case.vals.q, case.vals.k_pools[0], case.vals.v_pools[0], case.tables,
+               lens_t, 0, case.plan.scale, partition_tokens=0)
+    api.check_error()
+    assert torch.all(out == 0)
+
+
+@pytest.mark.parametrize("name,kw", [("llama", {"num_seqs": 4, "len_range": (600, 1500)}),
+                                     ("qwen", {"num_seqs": 16})])
+def test_stale_slots_poisoned_with_nan(name, kw):
+    """NaN in every unreferenced block and in every slot past a sequence's
+    length: the output stays finite and equal to the oracle's (which ignores
+    those slots by definition)."""
+    case = Case(workloads.make_plan(name, **kw))
+    case.gpu_writes(0)
+    kp, vp = case.vals.k_pools[0], case.vals.v_pools[0]
+    B = case.spec.block_size
+    used = np.zeros(case.plan.num_blocks, dtype=bool)
+    for s, L in enumerate(case.lay.seq_lens):
+        nb = -(-int(L) // B)
+        used[case.lay.block_tables[s, :nb]] = True
+        last = case.lay.block_tables[s, nb - 1]
+        for p in range(int(L), nb * B):
+            kp[last, :, p % B, :] = float("nan")
+            vp[last, :, p % B, :] = float("nan")
+    unused = torch.as_tensor(np.flatnonzero(~used), device="cuda")
+    kp[unused] = float("nan")
+    vp[unused] = float("nan")
+    out = case.gpu_decode(0)
+    assert torch.isfinite(out).all()
+    hk, hv = bits(kp), bits(vp)
+    ref = oracle.decode(bits(case.vals.q), hk, hv, case.ref_lay.block_tables,
+                        case.ref_lay.seq_lens, case.plan.scale, case.spec.dtype)
+    assert_close(out, ref, "poison")
+    api.check_error()
+
+
+def test_paging_invariance_bitwise():
+    """The same logical cache under a different physical permutation of the
+    blocks gives bitwise the same output (only the addressing changes)."""
+    case = Case(workloads.make_plan("llama", num_seqs=5, len_range=(700, 1800)))
+    case.gpu_writes(0)
+    kp, vp = case.vals.k_pools[0], case.vals.v_pools[0]
+    nb = case.plan.num_blocks
+    perm = torch.as_tensor(np.random.default_rng(3).permutation(nb), device="cuda")
+    kp2 = torch.empty_like(kp)
+    vp2 = torch.empty_like(vp)
+    kp2[perm] = kp
+    vp2[perm] = vp
+    tables2 = perm.to(torch.int32)[case.tables.long()]
+    for P in (-1, 0, 512):
+        a = torch.empty_like(case.vals.q)
+        b = torch.empty_like(case.vals.q)
+        api.decode(a, case.vals.q, kp, vp, case.tables, case.lens, case.max_seq_len,
+                   case.plan.scale, partition_tokens=P)
+        api.decode(b, case.vals.q, kp2, vp2, tables2, case.lens, case.max_seq_len,
+                   case.plan.scale, partition_tokens=P)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), P
+    api.check_error()
+
+
+def test_uniform_keys_give_mean_values_on_gpu():
+    """All keys of a sequence equal -> output = mean of its values."""
+    case = Case(workloads.make_plan("llama", num_seqs=3, len_range=(513, 900)))
+    kp, vp = case.vals.k_pools[0], case.vals.v_pools[0]
+    kp.copy_(kp[0:1, :, 0:1, :].expand_as(kp))
+    out = case.gpu_decode(0, partition=256)
+    hk, hv = bits(kp), bits(vp)
+    ref = oracle.decode(bits(case.vals.q), hk, hv, case.ref_lay.block_tables,
+                        case.ref_lay.seq_lens, case.plan.scale, "bf16")
+    assert_close(out, ref, "uniform keys")
+    api.check_error()
+
+
+def test_decode_on_side_stream_and_repeat_deterministic():
+    case = Case(workloads.make_plan("llama", num_seqs=8, len_range=(512, 3000)))
+    case.gpu_writes(0)
+    a = case.gpu_decode(0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = case.gpu_decode(0)
+    s.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    api.check_error()
+
+
+# -------------------------------------------------------- split-KV steps
+@pytest.mark.parametrize("name,kw,P", [("long", {"num_seqs": 2, "len_range": (1500, 2600)}, 512),
+                                       ("tiny", {}, 16),
+                                       ("qwen", {"num_seqs": 8}, 64)])
+def test_partitions_match_oracle(name, kw, P):
+    """Split-KV step 2 on its own: (m, l, O) per partition against the
+    oracle's partials; empty partitions hold (-inf, 0, 0)."""
+    case = Case(workloads.make_plan(name, **kw))
+    case.gpu_writes(0)
+    spec = case.spec
+    size = api.workspace_size(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                              spec.block_size, case.max_seq_len, P, case.dtype)
+    ws = api.alloc_workspace(size, "cuda")
+    ws.fill_(0xAB)
+    api.decode_partitions(case.vals.q, case.vals.k_pools[0], case.vals.v_pools[0], case.tables,
+                          case.lens, case.max_seq_len, case.plan.scale, P, ws)
+    m, l, o = api.partials_view(ws, spec.num_seqs, spec.num_q_heads, spec.head_dim,
+                                case.max_seq_len, P)
+    hk, hv = bits(case.vals.k_pools[0]), bits(case.vals.v_pools[0])
+    NP = api.partition_count(case.max_seq_len, P)
+    rm, rl, ro = oracle.partitions(bits(case.vals.q), hk, hv, case.ref_lay.block_tables,
+                                   case.ref_lay.seq_lens, case.plan.scale, spec.dtype, P, NP)
+    gm = m.double().cpu().numpy() / LOG2E   # base-2 units -> natural
+    gl = l.double().cpu().numpy()
+    go = o.double().cpu().numpy()
+    empty = np.isinf(rm)
+    assert np.array_equal(np.isinf(gm), empty)
+    assert (gl[empty] == 0).all() and (go[empty] == 0).all()
+    ok = ~empty
+    # fp32 intermediates: m to 1e-4 absolute, l to 1e-4 relative, O within
+    # the output tolerance (it is rounded once more before use)
+    assert np.max(np.abs(gm[ok] - rm[ok])) <= 1e-4 * (1 + np.max(np.abs(rm[ok])))
+    assert np.max(np.abs(gl[ok] - rl[ok]) / rl[ok]) <= 1e-4
+    err = np.abs(go[ok] - ro[ok])
+    assert (err <= 2e-3 + 1e-2 * np.abs(ro[ok])).all(), float(err.max())
+    api.check_error()
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_split_reduce_matches_oracle(dtype):
+    """Split-KV step 3 on its own: oracle partials (converted to the
+    workspace's fp32 base-2 layout) combined by the kernel against the
+    oracle's combine."""
+    rng = np.random.default_rng(5)
+    S, Hq, d, P = 7, 6, 128, 64
+    lens = np.array([0, 1, 64, 65, 200, 448, 129], dtype=np.int32)
+    max_len = int(lens.max())
+    NP = api.partition_count(max_len, P)
+    m = rng.normal(0, 3, (S, Hq, NP))
+    l = rng.uniform(0.5, 40, (S, Hq, NP))
+    o = rng.normal(0, 1, (S, Hq, NP, d))
+    for i, L in enumerate(lens):
+        k = -(-int(L) // P)
+        m[i, :, k:], l[i, :, k:], o[i, :, k:] = -np.inf, 0, 0
+    tdt = workloads.torch_dtype(dtype)
+    size = api.workspace_size(S, Hq, 1, d, 16, max_len, P, tdt)
+    ws = api.alloc_workspace(size, "cuda")
+    gm, gl, go = api.partials_view(ws, S, Hq, d, max_len, P)
+    gm.copy_(torch.as_tensor(m * LOG2E, dtype=torch.float32))
+    gl.copy_(torch.as_tensor(l, dtype=torch.float32))
+    go.copy_(torch.as_tensor(o, dtype=torch.float32))
+    out = torch.full((S, Hq, d), float("nan"), dtype=tdt, device="cuda")
+    api.split_kv_reduce(out, ws, torch.as_tensor(lens, device="cuda"), max_len, P)
+    # oracle on the fp32-rounded partials the kernel actually read
+    ref = oracle.reduce(gm.double().cpu().numpy() / LOG2E, gl.double().cpu().numpy(),
+                        go.double().cpu().numpy())
+    assert torch.all(out[0] == 0)
+    assert_close(out, ref, "reduce")
+    api.check_error()
+
+
+# ------------------------------------------------------------- error word
+def test_bad_indices_are_reported_not_dereferenced():
+    case = Case(workloads.make_plan("tiny"))
+    api.check_error()
+    kp, vp = case.vals.k_pools[0], case.vals.v_pools[0]
+    nb = case.plan.num_blocks
+    # cache write: one slot past the pool
+    bad = case.slots.clone()
+    bad[1] = nb * case.spec.block_size + 5
+    before = bits(kp)
+    api.cache_write(case.vals.k_new[0], case.vals.v_new[0], bad, kp, vp)
+    with pytest.raises(_lib.PagedAttentionError) as e:
+        api.check_error()
+    assert e.value.code == 6
+    after = bits(kp)
+    hk = before.copy()
+    hv = bits(vp)  # only K compared below
+    good = bad.cpu().numpy().copy()
+    good[1] = -1
+    oracle.cache_write(hk, hv.copy(), bits(case.vals.k_new[0]), bits(case.vals.v_new[0]), good)
+    assert np.array_equal(after, hk)
+    # decode: a block-table entry past the pool and a negative one
+    tables = case.tables.clone()
+    tables[0, 0] = nb + 100
+    tables[2, 1] = -7
+    out = torch.empty_like(case.vals.q)
+    api.decode(out, case.vals.q, kp, vp, tables, case.lens, case.max_seq_len, case.plan.scale)
+    with pytest.raises(_lib.PagedAttentionError) as e:
+        api.check_error()
+    assert e.value.code == 6
+    # a length beyond max_seq_len
+    lens = case.lens.clone()
+    lens[3] = case.max_seq_len + 50
+    api.decode(out, case.vals.q, kp, vp, case.tables, lens, case.max_seq_len, case.plan.scale)
+    with pytest.raises(_lib.PagedAttentionError) as e:
+        api.check_error()
+    assert e.value.code == 6
+    # copy pair with a bad block id
+    pairs = torch.tensor([[0, nb + 3]], dtype=torch.int64, device="cuda")
+    api.copy_blocks([kp], [vp], pairs)
+    with pytest.raises(_lib.PagedAttentionError) as e:
+        api.check_error()
+    assert e.value.code == 6
+    api.check_error()  # cleared
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    api.selftest_wait_timeout()
+    with pytest.raises(_lib.PagedAttentionError) as e:
+        api.check_error()
+    assert e.value.code == 5
+    # the context is still usable
+    full_step_parity(Case(workloads.make_plan("tiny")))
