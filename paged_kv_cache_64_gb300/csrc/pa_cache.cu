@@ -57,6 +57,10 @@ bool ensure_smem_attr(const void *kernel, int bytes) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)
         return false;
+    // Prefer the largest shared-memory carveout so several CTAs fit per SM.
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return false;
     done.insert({kernel, dev});
     return true;
 }

@@ -54,21 +54,32 @@ constexpr float kLazyRescale = 8.0f;     // base-2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kSinglePassTokens = 1 << 30;  // "partition" covering any sequence
 
+constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x / 2); }
+
 template <int D, int GP>
 struct DecodeShape {
-    static constexpr int LT = (GP * D / 64 > 8) ? 16 : 8;  // lanes per token
-    static constexpr int DPL = D / LT;                     // dims per lane
-    static constexpr int NPC = DPL / 8;                    // 16-byte pieces per lane
-    static constexpr int TPR = 32 / LT;                    // tokens per warp row
-    static constexpr int R = (GP >= 8) ? 2 : 4;            // rows per chunk
-    static constexpr int CHUNKS = kUnit / (R * TPR);       // chunks per stage
-    static constexpr int TILE_BYTES = kUnit * D * 2;       // one of K or V
+    static constexpr int LT = D / 8;                        // lanes per token: 8 dims each
+    static constexpr int TPR = 32 / LT;                     // tokens per warp row
+    static constexpr int ROWS = kUnit / TPR;                // rows per stage
+    static constexpr int R0 = (GP >= 8) ? 1 : 16 / GP;     // rows per chunk: ~16 scores
+    static constexpr int R = (R0 < 1) ? 1 : (R0 > ROWS ? ROWS : R0);
+    static constexpr int CHUNKS = ROWS / R;
+    static constexpr int NV = R * GP;                       // partial scores per lane
+    static constexpr int L2LT = ilog2c(LT), L2NV = ilog2c(NV), L2GP = ilog2c(GP);
+    static constexpr int LEVELS = L2LT < L2NV ? L2LT : L2NV;  // reduce-scatter levels
+    static constexpr int K = NV >> LEVELS;                  // complete sums kept per lane
+    static constexpr int L2K = ilog2c(K);
+    static constexpr int SHIFT = L2LT - LEVELS;             // low lane bits: butterfly copies
+    static constexpr int TILE_BYTES = kUnit * D * 2;        // one of K or V
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int NS = (D == 128) ? 8 : 16;         // 64 KiB ring
+    // Ring of stages: 96 KiB when two CTAs share an SM, 192 KiB when the
+    // register budget of G = 8 leaves one CTA per SM.
+    static constexpr int NS = ((GP >= 8) ? 192 * 1024 : 96 * 1024) / STAGE_BYTES;
     static constexpr int RING_BYTES = NS * STAGE_BYTES;
     static constexpr int SMEM_BYTES = RING_BYTES + 2 * NS * 8 + 16;
     static_assert(NS % kConsumerWarps == 0, "stages are dealt to warps round robin");
-    static_assert(CHUNKS >= 1 && kUnit % (R * TPR) == 0, "chunking");
+    static_assert(ROWS % R == 0, "chunking");
+    static_assert(K <= GP, "a lane's sums belong to one row");
     static_assert(kConsumerWarps * GP * D * 4 + 3 * kConsumerWarps * GP * 4 <= RING_BYTES,
                   "merge scratch must fit in the ring");
 };
@@ -111,11 +122,42 @@ __device__ __forceinline__ int checked_len(const int32_t *seq_lens, int i, int m
     return L;
 }
 
+// Reduce-scatter of NV partial sums over an LT-lane group (lane c in the
+// group): after the call, v[0 .. NV >> LEVELS) of lane c hold the complete
+// sums of indices ((c >> (log2 LT - LEVELS)) << log2 K) + j.  Each level
+// halves the values a lane keeps, trading half with its partner; when NV < LT
+// the last levels are a plain butterfly (lanes end with copies).
+template <int NV, int LT, int LEVELS>
+__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int c) {
+#pragma unroll
+    for (int lvl = 0; lvl < LEVELS; ++lvl) {
+        const int o = LT >> (lvl + 1);
+        const int half = NV >> (lvl + 1);
+        const bool up = (c & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFullMask, send, o);
+        }
+    }
+#pragma unroll
+    for (int o = LT >> (LEVELS + 1); o >= 1; o >>= 1) {
+#pragma unroll
+        for (int j = 0; j < (NV >> LEVELS); ++j) v[j] += __shfl_xor_sync(kFullMask, v[j], o);
+    }
+}
+
+// Register cap: <= 168 per thread lets two 5-warp CTAs share an SM (a warp's
+// registers come from one of the four 16K-register sub-partitions).
+template <int GP>
+constexpr int decode_max_regs() { return GP >= 8 ? 255 : 168; }
+
 template <bool BF16, int D, int GP>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP>())
     paged_decode_kernel(const DecodeParams p) {
     using S = DecodeShape<D, GP>;
-    constexpr int LT = S::LT, DPL = S::DPL, NPC = S::NPC, TPR = S::TPR, R = S::R;
+    constexpr int LT = S::LT, TPR = S::TPR, R = S::R;
     constexpr int NS = S::NS;
 
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -174,9 +216,19 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     __syncthreads();
 
-    // Per-warp softmax state (consumers) kept across the final barrier.
-    float m_run[GP], m_true[GP], l_run[GP];
-    float2 acc[GP][DPL / 2];
+    // Consumer lanes' softmax state, kept across the final barrier.  After
+    // the reduce-scatter a lane owns K complete scores per chunk: heads
+    // h0 .. h0+K-1 of one row; slot j of m_run / m_true / l_run is head h0+j.
+    constexpr int K = S::K, L2K = S::L2K, SHIFT = S::SHIFT, NV = S::NV;
+    constexpr int L2LT = S::L2LT, L2GP = S::L2GP;
+    constexpr int ROWBIT0 = SHIFT + L2GP - L2K;  // first lane bit that changes the row
+    float m_run[K], m_true[K], l_run[K];
+    float2 acc[GP][4];  // the lane's 8 dims, every head of the group
+    const int tg = lane / LT;                    // token group within a warp row
+    const int c = lane % LT;                     // lane in the group: dims [8c, 8c+8)
+    const int vbase = (c >> SHIFT) << L2K;       // first score index v = row*GP + head
+    const int my_row = vbase / GP;
+    const int h0 = vbase % GP;
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer
@@ -230,38 +282,32 @@ __global__ void __launch_bounds__(kDecodeThreads)
         }
     } else {
         // ------------------------------------------------------ consumers
-        const int tg = lane / LT;  // token slot within a warp row
-        const int c = lane % LT;   // lane within the token group
-
-        // q for every head of the group, pre-scaled to base-2 units.
-        float2 q2[GP][DPL / 2];
+        const int gbase = tg * LT;
+        float2 q2[GP][4];  // q of every head of the group, scaled to base 2
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
             if (g < G) {
                 const uint16_t *qrow =
                     p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D;
+                const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + c * 8);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-                for (int i = 0; i < NPC; ++i) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(qrow + (c + LT * i) * 8);
-                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float2 f = widen2<BF16>(w[k]);
-                        q2[g][i * 4 + k] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
-                    }
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = widen2<BF16>(w[k]);
+                    q2[g][k] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < DPL / 2; ++j) q2[g][j] = make_float2(0.f, 0.f);
+                for (int k = 0; k < 4; ++k) q2[g][k] = make_float2(0.f, 0.f);
             }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[g][k] = make_float2(0.f, 0.f);
         }
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
-            m_run[g] = -INFINITY;
-            m_true[g] = -INFINITY;
-            l_run[g] = 0.f;
-#pragma unroll
-            for (int j = 0; j < DPL / 2; ++j) acc[g][j] = make_float2(0.f, 0.f);
+        for (int j = 0; j < K; ++j) {
+            m_run[j] = -INFINITY;
+            m_true[j] = -INFINITY;
+            l_run[j] = 0.f;
         }
 
         for (int u = warp; u < nunits; u += kConsumerWarps) {
@@ -281,100 +327,84 @@ __global__ void __launch_bounds__(kDecodeThreads)
 
 #pragma unroll
             for (int ch = 0; ch < S::CHUNKS; ++ch) {
-                // ---- scores for R tokens of this lane group
-                float s[R][GP];
+                // ---- partial dot products over the lane's 8 dims
+                float sv[NV];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const int t = (ch * R + r) * TPR + tg;
-                    float2 k2[DPL / 2];
-#pragma unroll
-                    for (int i = 0; i < NPC; ++i) {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(
-                            kt + t * D * 2 + (c + LT * i) * 16);
-                        k2[i * 4 + 0] = widen2<BF16>(raw.x);
-                        k2[i * 4 + 1] = widen2<BF16>(raw.y);
-                        k2[i * 4 + 2] = widen2<BF16>(raw.z);
-                        k2[i * 4 + 3] = widen2<BF16>(raw.w);
-                    }
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(kt + t * D * 2 + c * 16);
+                    const float2 k2[4] = {widen2<BF16>(raw.x), widen2<BF16>(raw.y),
+                                          widen2<BF16>(raw.z), widen2<BF16>(raw.w)};
 #pragma unroll
                     for (int g = 0; g < GP; ++g) {
-                        float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int j = 0; j < DPL / 2; ++j) a = __ffma2_rn(q2[g][j], k2[j], a);
-                        s[r][g] = a.x + a.y;
+                        float2 a = __fmul2_rn(q2[g][0], k2[0]);
+                        a = __ffma2_rn(q2[g][1], k2[1], a);
+                        a = __ffma2_rn(q2[g][2], k2[2], a);
+                        a = __ffma2_rn(q2[g][3], k2[3], a);
+                        sv[r * GP + g] = a.x + a.y;
                     }
                 }
+                // ---- complete sums: lane keeps scores vbase .. vbase+K-1
+                reduce_scatter<NV, LT, S::LEVELS>(sv, c);
+                if (partial && (ch * R + my_row) * TPR + tg >= nvalid) {
 #pragma unroll
-                for (int off = LT / 2; off >= 1; off >>= 1) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-#pragma unroll
-                        for (int g = 0; g < GP; ++g)
-                            s[r][g] += __shfl_xor_sync(kFullMask, s[r][g], off);
+                    for (int j = 0; j < K; ++j) sv[j] = -INFINITY;
                 }
-                if (partial) {
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const int t = (ch * R + r) * TPR + tg;
-                        if (t >= nvalid) {
-#pragma unroll
-                            for (int g = 0; g < GP; ++g) s[r][g] = -INFINITY;
-                        }
-                    }
-                }
-                // ---- tile max per head across the warp; lazy rescale
-                float mx[GP];
+                // ---- tile max of each head over the warp; lazy rescale
+                float mx[K];
                 bool need = false;
 #pragma unroll
-                for (int g = 0; g < GP; ++g) {
-                    float v = s[0][g];
+                for (int j = 0; j < K; ++j) {
+                    float v = sv[j];
 #pragma unroll
-                    for (int r = 1; r < R; ++r) v = fmaxf(v, s[r][g]);
+                    for (int b = ROWBIT0; b < L2LT; ++b)
+                        v = fmaxf(v, __shfl_xor_sync(kFullMask, v, 1 << b));
 #pragma unroll
-                    for (int off = LT; off < 32; off <<= 1)
-                        v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
-                    mx[g] = v;
-                    m_true[g] = fmaxf(m_true[g], v);
-                    need |= v > m_run[g] + kLazyRescale;
+                    for (int o = LT; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+                    mx[j] = v;
+                    m_true[j] = fmaxf(m_true[j], v);
+                    need |= v > m_run[j] + kLazyRescale;
                 }
-                if (need) {  // warp-uniform: every lane holds the same mx and m_run
+                if (__any_sync(kFullMask, need)) {
+                    float al[K];
+#pragma unroll
+                    for (int j = 0; j < K; ++j) {
+                        const float mn = fmaxf(m_run[j], mx[j]);
+                        al[j] = fast_exp2(m_run[j] - mn);
+                        m_run[j] = mn;
+                        l_run[j] *= al[j];
+                    }
 #pragma unroll
                     for (int g = 0; g < GP; ++g) {
-                        const float mn = fmaxf(m_run[g], mx[g]);
-                        const float alpha = fast_exp2(m_run[g] - mn);
-                        m_run[g] = mn;
-                        l_run[g] *= alpha;
-                        const float2 a2 = make_float2(alpha, alpha);
+                        // lane (g >> L2K) << SHIFT holds head g in slot g % K
+                        const float a = __shfl_sync(kFullMask, al[g & (K - 1)], (g >> L2K) << SHIFT);
+                        const float2 a2 = make_float2(a, a);
 #pragma unroll
-                        for (int j = 0; j < DPL / 2; ++j) acc[g][j] = __fmul2_rn(acc[g][j], a2);
+                        for (int k = 0; k < 4; ++k) acc[g][k] = __fmul2_rn(acc[g][k], a2);
                     }
                 }
-                // ---- probabilities and P.V
+                float pj[K];
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    pj[j] = fast_exp2(sv[j] - m_run[j]);  // masked: 2^-inf = 0
+                    l_run[j] += pj[j];
+                }
+                // ---- P.V: every lane gathers the weights of its token group
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const int t = (ch * R + r) * TPR + tg;
-                    float pr[GP];
+                    uint4 raw = *reinterpret_cast<const uint4 *>(vt + t * D * 2 + c * 16);
+                    if (partial && t >= nvalid) raw = make_uint4(0u, 0u, 0u, 0u);
+                    const float2 v2[4] = {widen2<BF16>(raw.x), widen2<BF16>(raw.y),
+                                          widen2<BF16>(raw.z), widen2<BF16>(raw.w)};
 #pragma unroll
                     for (int g = 0; g < GP; ++g) {
-                        pr[g] = fast_exp2(s[r][g] - m_run[g]);
-                        l_run[g] += pr[g];
-                    }
-                    float2 v2[DPL / 2];
+                        const int v = r * GP + g;
+                        const float pr =
+                            __shfl_sync(kFullMask, pj[v & (K - 1)], gbase + ((v >> L2K) << SHIFT));
+                        const float2 pp = make_float2(pr, pr);
 #pragma unroll
-                    for (int i = 0; i < NPC; ++i) {
-                        uint4 raw =
-                            *reinterpret_cast<const uint4 *>(vt + t * D * 2 + (c + LT * i) * 16);
-                        if (partial && t >= nvalid) raw = make_uint4(0u, 0u, 0u, 0u);
-                        v2[i * 4 + 0] = widen2<BF16>(raw.x);
-                        v2[i * 4 + 1] = widen2<BF16>(raw.y);
-                        v2[i * 4 + 2] = widen2<BF16>(raw.z);
-                        v2[i * 4 + 3] = widen2<BF16>(raw.w);
-                    }
-#pragma unroll
-                    for (int g = 0; g < GP; ++g) {
-                        const float2 pp = make_float2(pr[g], pr[g]);
-#pragma unroll
-                        for (int j = 0; j < DPL / 2; ++j) acc[g][j] = __ffma2_rn(pp, v2[j], acc[g][j]);
+                        for (int k = 0; k < 4; ++k) acc[g][k] = __ffma2_rn(pp, v2[k], acc[g][k]);
                     }
                 }
             }
@@ -382,18 +412,25 @@ __global__ void __launch_bounds__(kDecodeThreads)
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
         }
 
-        // Sum the token groups of the warp (they share m_run).
+        // Sum the token groups' accumulators (they share m_run), and each
+        // head's l over the lanes that hold it.
 #pragma unroll
-        for (int off = LT; off < 32; off <<= 1) {
+        for (int o = LT; o < 32; o <<= 1) {
 #pragma unroll
-            for (int g = 0; g < GP; ++g) {
-                l_run[g] += __shfl_xor_sync(kFullMask, l_run[g], off);
+            for (int g = 0; g < GP; ++g)
 #pragma unroll
-                for (int j = 0; j < DPL / 2; ++j) {
-                    acc[g][j].x += __shfl_xor_sync(kFullMask, acc[g][j].x, off);
-                    acc[g][j].y += __shfl_xor_sync(kFullMask, acc[g][j].y, off);
+                for (int k = 0; k < 4; ++k) {
+                    acc[g][k].x += __shfl_xor_sync(kFullMask, acc[g][k].x, o);
+                    acc[g][k].y += __shfl_xor_sync(kFullMask, acc[g][k].y, o);
                 }
-            }
+        }
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+#pragma unroll
+            for (int b = ROWBIT0; b < L2LT; ++b)
+                l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 1 << b);
+#pragma unroll
+            for (int o = LT; o < 32; o <<= 1) l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], o);
         }
     }
 
@@ -416,27 +453,20 @@ __global__ void __launch_bounds__(kDecodeThreads)
     float *red_l = red_m + kConsumerWarps * GP;
     float *red_t = red_l + kConsumerWarps * GP;
     if (warp < kConsumerWarps) {
-        const int tg = lane / LT, c = lane % LT;
         if (tg == 0) {
 #pragma unroll
             for (int g = 0; g < GP; ++g) {
-#pragma unroll
-                for (int i = 0; i < NPC; ++i) {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        red_acc + ((warp * GP + g) * D) + (c + LT * i) * 8);
-                    dst[0] = make_float4(acc[g][i * 4 + 0].x, acc[g][i * 4 + 0].y,
-                                         acc[g][i * 4 + 1].x, acc[g][i * 4 + 1].y);
-                    dst[1] = make_float4(acc[g][i * 4 + 2].x, acc[g][i * 4 + 2].y,
-                                         acc[g][i * 4 + 3].x, acc[g][i * 4 + 3].y);
-                }
+                float4 *dst = reinterpret_cast<float4 *>(red_acc + (warp * GP + g) * D + c * 8);
+                dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+                dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
             }
-        }
-        if (lane == 0) {
+            if (my_row == 0 && (c & ((1 << SHIFT) - 1)) == 0) {
 #pragma unroll
-            for (int g = 0; g < GP; ++g) {
-                red_m[warp * GP + g] = m_run[g];
-                red_l[warp * GP + g] = l_run[g];
-                red_t[warp * GP + g] = m_true[g];
+                for (int j = 0; j < K; ++j) {
+                    red_m[warp * GP + h0 + j] = m_run[j];
+                    red_l[warp * GP + h0 + j] = l_run[j];
+                    red_t[warp * GP + h0 + j] = m_true[j];
+                }
             }
         }
     }
