@@ -61,7 +61,8 @@ typedef enum {
     PA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
     PA_ERR_DEVICE_TIMEOUT = 5,/* a bounded device wait ran out (reported by pa_check_error) */
     PA_ERR_BAD_INDEX = 6,     /* an out-of-range index was met on the device (pa_check_error) */
-    PA_ERR_NOT_FOUND = 7      /* allocator: unknown sequence id, or id already in use */
+    PA_ERR_NOT_FOUND = 7,     /* allocator: unknown sequence id, or id already in use */
+    PA_ERR_TOO_LARGE = 8      /* pa_decode_static_scratch: partials exceed the fixed scratch */
 } pa_status;
 
 typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
@@ -214,6 +215,43 @@ pa_status pa_split_kv_reduce(void *out, const void *workspace, size_t workspace_
                              const int32_t *seq_lens, int max_seq_len, int num_seqs,
                              int num_q_heads, int head_dim, int partition_tokens, pa_dtype dtype,
                              void *stream);
+
+/* ------------------------------------------------------------------------
+ * pa_decode_static_scratch: pa_decode for callers that cannot allocate.
+ *
+ * Some callers of this library cannot hand it a workspace: an inference
+ * engine that has already given (nearly) all device memory to its KV-cache
+ * pool and its weights, or a latency-critical decode loop that must not
+ * call cudaMalloc (it can synchronise the device and can fail under memory
+ * pressure), or a foreign-language host that reaches the library only
+ * through this C ABI with no allocator of its own.  This entry point
+ * computes exactly what pa_decode computes, with the same arguments minus
+ * the workspace, and allocates nothing: its split-KV partials live in one
+ * file-scope device array of PA_STATIC_SCRATCH_BYTES bytes that every GPU
+ * holds from the moment the library is loaded until the process exits.
+ * The pages have no counterpart to this entry point.
+ *  - A request whose partials need more than PA_STATIC_SCRATCH_BYTES
+ *    (pa_decode_workspace_size with the same arguments) is rejected with
+ *    PA_ERR_TOO_LARGE before anything is launched; pick a larger
+ *    partition_tokens (fewer partials) or -1 (single pass, no scratch).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array, and it keeps whatever the
+ *    last call left there.  Nothing in it needs to start at zero: every
+ *    partial the combine step reads is written earlier in the same call.
+ *    Calls whose kernels overlap on the GPU (different streams, no ordering
+ *    between them) race on the array and give wrong results; order them.
+ * ---------------------------------------------------------------------- */
+#define PA_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+pa_status pa_decode_static_scratch(void *out, const void *q, const void *k_pool,
+                                   const void *v_pool, int num_blocks,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *seq_lens, int max_seq_len, int num_seqs,
+                                   int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float scale, int partition_tokens,
+                                   pa_dtype dtype, void *stream);
 
 /* ------------------------------------------------------------------------
  * pa_check_error: synchronises `stream`, then reads and clears the current

@@ -18,7 +18,10 @@ STATUS = {
     5: "PA_ERR_DEVICE_TIMEOUT",
     6: "PA_ERR_BAD_INDEX",
     7: "PA_ERR_NOT_FOUND",
+    8: "PA_ERR_TOO_LARGE",
 }
+# Size of the fixed device scratch behind pa_decode_static_scratch (pa.h).
+STATIC_SCRATCH_BYTES = 16 << 20
 PA_F16, PA_BF16 = 0, 1
 
 # Every symbol pa.h declares, with (restype, argtypes).
@@ -47,6 +50,9 @@ SIGNATURES = {
                                       _c_int, _vp]),
     "pa_split_kv_reduce": (_c_int, [_vp, _vp, _c_sz, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                     _c_int, _vp]),
+    "pa_decode_static_scratch": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _vp, _c_int,
+                                          _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int,
+                                          _c_int, _vp]),
     "pa_check_error": (_c_int, [_vp]),
     "pa_selftest_wait_timeout": (_c_int, [_vp]),
     "pa_alloc_create": (_c_int, [_c_int, _c_int, _i32p, ctypes.POINTER(_vp)]),

@@ -153,6 +153,24 @@ def decode(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale,
     return workspace
 
 
+def decode_static_scratch(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale,
+                          partition_tokens=0, stream=None):
+    """Same result as decode(), for callers that cannot allocate device
+    memory: split-KV partials go to the library's fixed device array
+    (_lib.STATIC_SCRATCH_BYTES per GPU) instead of a workspace.  Raises
+    PagedAttentionError (PA_ERR_TOO_LARGE) when they would not fit; calls on
+    one device share that array, so they must not overlap on the GPU."""
+    S, hq, hkv, d, nb, bs = _decode_dims(q, k_pool, block_tables, seq_lens)
+    if out.shape != q.shape or out.dtype != q.dtype or k_pool.dtype != q.dtype:
+        raise ValueError("out/q/pool shapes or types differ")
+    rc = _lib.load().pa_decode_static_scratch(
+        _cuda(out, "out"), _cuda(q, "q"), _cuda(k_pool, "k_pool"), _cuda(v_pool, "v_pool"), nb,
+        _cuda(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _cuda(seq_lens, "seq_lens", torch.int32), int(max_seq_len), S, hq, hkv, d, bs,
+        float(scale), int(partition_tokens), _dt(q), _stream_handle(stream))
+    _lib.check("pa_decode_static_scratch", rc)
+
+
 def partition_count(max_seq_len, partition_tokens):
     return max(1, -(-int(max_seq_len) // int(partition_tokens)))
 

@@ -157,6 +157,7 @@ const char *pa_status_string(pa_status s) {
         case PA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
         case PA_ERR_BAD_INDEX: return "out-of-range index met on the device";
         case PA_ERR_NOT_FOUND: return "unknown or duplicate sequence id";
+        case PA_ERR_TOO_LARGE: return "split-KV partials exceed the fixed static scratch";
     }
     return "unknown status";
 }

@@ -41,6 +41,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -740,6 +741,26 @@ static pa_status fill_common(DecodeParams *prm, const void *q, const void *k_poo
     return prm->err ? PA_OK : PA_ERR_CUDA;
 }
 
+// Fixed scratch of pa_decode_static_scratch, for callers that cannot
+// allocate.  Every GPU that loads the library holds it until exit.
+static __device__ __align__(256) unsigned char g_static_scratch[PA_STATIC_SCRATCH_BYTES];
+
+// Device address of this device's copy of g_static_scratch, looked up once
+// per device (with that device current); nullptr if the lookup fails.
+static void *static_scratch_address() {
+    static std::mutex mu;
+    static void *addr[128] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress((void **)&ptr, g_static_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = ptr;
+    }
+    return addr[dev];
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -892,6 +913,33 @@ pa_status pa_split_kv_reduce(void *out, const void *workspace, size_t workspace_
     const unsigned blocks = (unsigned)((rows + kReduceWarps - 1) / kReduceWarps);
     pick_reduce(dtype, head_dim)<<<blocks, kReduceWarps * 32, 0, as_stream(stream)>>>(rp);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Same computation as pa_decode; the split-KV partials go to the library's
+// fixed device array instead of a caller workspace (see pa.h).
+pa_status pa_decode_static_scratch(void *out, const void *q, const void *k_pool,
+                                   const void *v_pool, int num_blocks,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *seq_lens, int max_seq_len, int num_seqs,
+                                   int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float scale, int partition_tokens,
+                                   pa_dtype dtype, void *stream) {
+    ResolvedDecode r;
+    pa_status st = resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_seq_len, partition_tokens, dtype, &r);
+    if (st != PA_OK) return st;
+    const size_t need =
+        r.P > 0 ? workspace_layout(num_seqs, num_q_heads, head_dim, r.NP).bytes : 0;
+    if (need > PA_STATIC_SCRATCH_BYTES) return PA_ERR_TOO_LARGE;
+    void *scratch = nullptr;
+    if (need > 0) {
+        scratch = static_scratch_address();
+        if (!scratch) return PA_ERR_CUDA;
+    }
+    return pa_decode(out, q, k_pool, v_pool, num_blocks, block_tables, max_blocks_per_seq,
+                     seq_lens, max_seq_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     block_size, scale, r.P > 0 ? r.P : -1, scratch,
+                     need > 0 ? (size_t)PA_STATIC_SCRATCH_BYTES : 0, dtype, stream);
 }
 
 }  // extern "C"
