@@ -333,65 +333,89 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(args.warmup):
         st.run()
     api.check_error()
+    use_graph = args.graph == "on" or (args.graph == "auto" and spec.num_layers > 1)
+    graph = None
+    if use_graph:
+        # The step's library calls, captured once and replayed (launch-bound
+        # multi-layer steps); the captured kernels are the same launches.
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            st.run()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            st.run()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        api.check_error()
+
+    def one_step(ev=None):
+        if graph is not None:
+            graph.replay()
+        else:
+            st.run(ev)
 
     # ------------------------------------------------ timed region (device)
     ev = []
-    step_ms = []
+    step_ev = []
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clocks:
-        if flush is None:
+        if flush is None and graph is None:
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record()
             for _ in range(args.steps):
-                st.run(ev)
+                one_step(ev)
             t1.record()
             torch.cuda.synchronize()
             total_ms = t0.elapsed_time(t1)
         else:
             for _ in range(args.steps):
-                flush.fill_(1)
+                if flush is not None:
+                    flush.fill_(1)
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record()
-                st.run(ev)
+                one_step(ev)
                 b.record()
-                step_ms.append((a, b))
+                step_ev.append((a, b))
             torch.cuda.synchronize()
-            total_ms = sum(a.elapsed_time(b) for a, b in step_ms)
+            total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     barrier()
     api.check_error()
     secs, all_bytes = reduce_over_ranks(total_ms / 1e3, st.step_bytes() * args.steps, device)
     value = all_bytes / secs / 1e9
-    decode_ms = [a.elapsed_time(b) for a, b in ev]
-    dec_avg_ms = statistics.mean(decode_ms)
+    if ev:
+        dec_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        kernel_note = "pa_decode call (split-KV partition kernel + reduce), CUDA events"
+    else:
+        # graph replay: a step's time spread over its layers (cache write included)
+        dec_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in step_ev) / spec.num_layers
+        kernel_note = ("pa_decode + cache write per layer: graph-replayed step time / layers "
+                       "(CUDA events around each replay)")
     peak, peak_kind = measured_peaks()
     achieved = st.decode_bytes / (dec_avg_ms / 1e3) / 1e9
     traffic = stored_traffic(args.workload)
 
     # ------------------------------------------------ end to end (host buffers)
+    # Every step copies its inputs from pinned host memory into the step's
+    # device input tensors, runs the step, and reads every layer's output back.
     pin = lambda t: t.cpu().pin_memory()
-    h_q = pin(st.vals.q)
-    h_kn = [pin(t) for t in st.vals.k_new]
-    h_vn = [pin(t) for t in st.vals.v_new]
-    h_tab, h_len, h_slot = pin(st.tables), pin(st.lens), pin(st.slots)
+    h_in = [pin(st.vals.q)] + [pin(t) for t in st.vals.k_new + st.vals.v_new] + \
+        [pin(st.tables), pin(st.lens), pin(st.slots)]
+    d_in = [st.vals.q] + list(st.vals.k_new) + list(st.vals.v_new) + \
+        [st.tables, st.lens, st.slots]
     h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.out]
-    d_q = torch.empty_like(st.vals.q)
-    d_kn = [torch.empty_like(t) for t in st.vals.k_new]
-    d_vn = [torch.empty_like(t) for t in st.vals.v_new]
-    h2d = (h_q.nbytes + sum(t.nbytes for t in h_kn + h_vn) + h_tab.nbytes + h_len.nbytes +
-           h_slot.nbytes)
+    h2d = sum(t.nbytes for t in h_in)
     d2h = sum(t.nbytes for t in h_out)
 
     def e2e_step():
-        d_q.copy_(h_q, non_blocking=True)
-        for d, h in zip(d_kn + d_vn, h_kn + h_vn):
+        for d, h in zip(d_in, h_in):
             d.copy_(h, non_blocking=True)
-        st.tables.copy_(h_tab, non_blocking=True)
-        st.lens.copy_(h_len, non_blocking=True)
-        st.slots.copy_(h_slot, non_blocking=True)
-        st.run(q=d_q, k_new=d_kn, v_new=d_vn)
+        one_step()
         for h, o in zip(h_out, st.out):
             h.copy_(o, non_blocking=True)
 
@@ -429,6 +453,7 @@ def run_gpu(args, rank, world, local_rank):
                                                   spec.num_q_heads // spec.num_kv_heads,
                                                   st.vals.q.dtype),
             "step": "copy_blocks (if any) + cache_write + paged decode, every layer",
+            "launch": "CUDA graph replay" if graph is not None else "eager",
             "l2": ("inputs larger than L2 (%.2f GB per step)" % (st.step_bytes() / 1e9))
             if flush is None else "L2 flushed (256 MiB write) before every step",
         },
@@ -436,7 +461,7 @@ def run_gpu(args, rank, world, local_rank):
         "tokens_per_s": spec.num_seqs * world / (secs / args.steps),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "pa_decode call (split-KV partition kernel + reduce)",
+                     "kernel": kernel_note,
                      "bytes_per_launch": st.decode_bytes, "avg_launch_ms": dec_avg_ms,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
@@ -465,6 +490,8 @@ def main(argv=None):
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="shrink the batch (profiling of small cases only)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
+                    help="replay the step as a CUDA graph (auto: when the step has >1 layer)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

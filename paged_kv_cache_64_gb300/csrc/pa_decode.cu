@@ -57,12 +57,32 @@ constexpr int kSinglePassTokens = 1 << 30;  // "partition" covering any sequence
 
 constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x / 2); }
 
+// Tuning of the G = 8 instantiations (compile-time; defaults measured on
+// GB300): heads whose q stays in registers, register cap, rows per chunk,
+// ring size.  Other G: q in registers, 168-register cap, 96 KiB ring.
+#ifndef PA_G8_QREG
+#define PA_G8_QREG 4
+#endif
+#ifndef PA_G8_MAXREGS
+#define PA_G8_MAXREGS 168
+#endif
+#ifndef PA_G8_ROWS
+#define PA_G8_ROWS 1
+#endif
+#ifndef PA_G8_RING_KB
+#define PA_G8_RING_KB 96
+#endif
+#ifndef PA_RING_KB
+#define PA_RING_KB 96
+#endif
+constexpr int QREG8 = PA_G8_QREG;  // heads whose q stays in registers when G = 8
+
 template <int D, int GP>
 struct DecodeShape {
     static constexpr int LT = D / 8;                        // lanes per token: 8 dims each
     static constexpr int TPR = 32 / LT;                     // tokens per warp row
     static constexpr int ROWS = kUnit / TPR;                // rows per stage
-    static constexpr int R0 = (GP >= 8) ? 1 : 16 / GP;     // rows per chunk: ~16 scores
+    static constexpr int R0 = (GP >= 8) ? PA_G8_ROWS : 16 / GP;  // rows per chunk
     static constexpr int R = (R0 < 1) ? 1 : (R0 > ROWS ? ROWS : R0);
     static constexpr int CHUNKS = ROWS / R;
     static constexpr int NV = R * GP;                       // partial scores per lane
@@ -73,11 +93,15 @@ struct DecodeShape {
     static constexpr int SHIFT = L2LT - LEVELS;             // low lane bits: butterfly copies
     static constexpr int TILE_BYTES = kUnit * D * 2;        // one of K or V
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    // Ring of stages: 96 KiB when two CTAs share an SM, 192 KiB when the
-    // register budget of G = 8 leaves one CTA per SM.
-    static constexpr int NS = ((GP >= 8) ? 192 * 1024 : 96 * 1024) / STAGE_BYTES;
+    // Ring of stages: 96 KiB, so that two CTAs share an SM.
+    static constexpr int NS = ((GP >= 8) ? PA_G8_RING_KB : PA_RING_KB) * 1024 / STAGE_BYTES;
     static constexpr int RING_BYTES = NS * STAGE_BYTES;
-    static constexpr int SMEM_BYTES = RING_BYTES + 2 * NS * 8 + 16;
+    // q of heads QREG.. lives in shared memory (fp32, pre-scaled) instead of
+    // registers, to keep G = 8 under the register cap.
+    static constexpr int QREG = (GP >= 8) ? QREG8 : GP;
+    static constexpr int QS_OFF = (RING_BYTES + 2 * NS * 8 + 16 + 15) / 16 * 16;
+    static constexpr int QS_BYTES = (GP - QREG) * D * 4;
+    static constexpr int SMEM_BYTES = QS_OFF + QS_BYTES;
     static_assert(NS % kConsumerWarps == 0, "stages are dealt to warps round robin");
     static_assert(ROWS % R == 0, "chunking");
     static_assert(K <= GP, "a lane's sums belong to one row");
@@ -149,10 +173,20 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int c) {
     }
 }
 
+// Shared-memory load the compiler may not hoist out of the token loop (a
+// hoisted copy would put the q of every head back into registers).
+__device__ __forceinline__ float4 lds_f4(const float *p) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
 // Register cap: <= 168 per thread lets two 5-warp CTAs share an SM (a warp's
 // registers come from one of the four 16K-register sub-partitions).
 template <int GP>
-constexpr int decode_max_regs() { return GP >= 8 ? 255 : 168; }
+constexpr int decode_max_regs() { return GP >= 8 ? PA_G8_MAXREGS : 168; }
 
 template <bool BF16, int D, int GP>
 __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP>())
@@ -284,9 +318,34 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
     } else {
         // ------------------------------------------------------ consumers
         const int gbase = tg * LT;
-        float2 q2[GP][4];  // q of every head of the group, scaled to base 2
+        constexpr int QREG = S::QREG;
+        // q of heads >= QREG: fp32 copy in shared memory, filled once
+        float *qs = reinterpret_cast<float *>(smem + S::QS_OFF);
+        if constexpr (QREG < GP) {
+            for (int i = threadIdx.x; i < (GP - QREG) * (D / 8); i += kConsumerWarps * 32) {
+                const int g = QREG + i / (D / 8);
+                const int x0 = (i % (D / 8)) * 8;
+                float f8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (g < G) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(
+                        p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + x0);
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 f = widen2<BF16>(w[k]);
+                        f8[2 * k] = f.x * p.scale_log2;
+                        f8[2 * k + 1] = f.y * p.scale_log2;
+                    }
+                }
+                float4 *dst = reinterpret_cast<float4 *>(qs + (g - QREG) * D + x0);
+                dst[0] = make_float4(f8[0], f8[1], f8[2], f8[3]);
+                dst[1] = make_float4(f8[4], f8[5], f8[6], f8[7]);
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        }
+        float2 q2[QREG > 0 ? QREG : 1][4];  // q of heads < QREG, scaled to base 2
+#pragma unroll
+        for (int g = 0; g < QREG; ++g) {
             if (g < G) {
                 const uint16_t *qrow =
                     p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D;
@@ -301,9 +360,11 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
 #pragma unroll
                 for (int k = 0; k < 4; ++k) q2[g][k] = make_float2(0.f, 0.f);
             }
+        }
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[g][k] = make_float2(0.f, 0.f);
-        }
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             m_run[j] = -INFINITY;
@@ -338,10 +399,22 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
                                           widen2<BF16>(raw.z), widen2<BF16>(raw.w)};
 #pragma unroll
                     for (int g = 0; g < GP; ++g) {
-                        float2 a = __fmul2_rn(q2[g][0], k2[0]);
-                        a = __ffma2_rn(q2[g][1], k2[1], a);
-                        a = __ffma2_rn(q2[g][2], k2[2], a);
-                        a = __ffma2_rn(q2[g][3], k2[3], a);
+                        float2 qg[4];
+                        if (g < QREG) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) qg[k] = q2[g < QREG ? g : 0][k];
+                        } else {
+                            const float4 a0 = lds_f4(qs + (g - QREG) * D + c * 8);
+                            const float4 a1 = lds_f4(qs + (g - QREG) * D + c * 8 + 4);
+                            qg[0] = make_float2(a0.x, a0.y);
+                            qg[1] = make_float2(a0.z, a0.w);
+                            qg[2] = make_float2(a1.x, a1.y);
+                            qg[3] = make_float2(a1.z, a1.w);
+                        }
+                        float2 a = __fmul2_rn(qg[0], k2[0]);
+                        a = __ffma2_rn(qg[1], k2[1], a);
+                        a = __ffma2_rn(qg[2], k2[2], a);
+                        a = __ffma2_rn(qg[3], k2[3], a);
                         sv[r * GP + g] = a.x + a.y;
                     }
                 }
