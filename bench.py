@@ -320,6 +320,7 @@ def run_gpu(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
+    api.set_decode_impl(args.decode_impl)
     base = workloads.SPECS[args.workload]
     plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs,
                                seed=base.seed + 1000 * rank if rank else None)
@@ -454,6 +455,10 @@ def run_gpu(args, rank, world, local_rank):
                                                   st.vals.q.dtype),
             "step": "copy_blocks (if any) + cache_write + paged decode, every layer",
             "launch": "CUDA graph replay" if graph is not None else "eager",
+            "decode_kernel": ("tensor cores (tcgen05)" if (
+                args.decode_impl == "tensor_cores" or (args.decode_impl == "auto" and
+                                                       spec.num_q_heads // spec.num_kv_heads >= 5))
+                else "CUDA cores"),
             "l2": ("inputs larger than L2 (%.2f GB per step)" % (st.step_bytes() / 1e9))
             if flush is None else "L2 flushed (256 MiB write) before every step",
         },
@@ -492,6 +497,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
                     help="replay the step as a CUDA graph (auto: when the step has >1 layer)")
+    ap.add_argument("--decode-impl", default="auto",
+                    choices=["auto", "cuda_cores", "tensor_cores"],
+                    help="decode kernel (default: the library's automatic choice)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

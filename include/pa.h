@@ -165,6 +165,17 @@ pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_
 int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
                              int block_size, int group_size, pa_dtype dtype);
 
+/* Decode kernel selection, process-wide, for every later call:
+ *   0 automatic (default): the tensor-core kernel (tcgen05 MMAs, TMA tensor
+ *     copies) for groups of 5..8 query heads per KV head, the CUDA-core
+ *     kernel (packed fp32 FMAs) for smaller groups;
+ *   1 always the CUDA-core kernel;  2 always the tensor-core kernel.
+ * Both compute the same result to within the output tolerance.  Returns the
+ * previous setting, or -1 (nothing changed) for an invalid value.  Not
+ * synchronised with decode calls running on other host threads. */
+int pa_set_decode_impl(int impl);
+int pa_get_decode_impl(void);
+
 /* Resident CTAs per SM of the decode kernel that these shapes select
  * (occupancy query on the current device; 0 if unsupported). */
 int pa_decode_ctas_per_sm(int head_dim, int group_size, pa_dtype dtype);

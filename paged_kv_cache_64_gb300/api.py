@@ -116,6 +116,22 @@ def auto_partition(num_seqs, num_kv_heads, max_seq_len, head_dim, block_size, gr
                                                 block_size, group, _DTYPES[dtype])
 
 
+DECODE_IMPLS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
+
+
+def set_decode_impl(name):
+    """Select the decode kernel for later calls ("auto", "cuda_cores",
+    "tensor_cores"); returns the previous name."""
+    prev = _lib.load().pa_set_decode_impl(DECODE_IMPLS[name])
+    if prev < 0:
+        raise ValueError(name)
+    return {v: k for k, v in DECODE_IMPLS.items()}[prev]
+
+
+def get_decode_impl():
+    return {v: k for k, v in DECODE_IMPLS.items()}[_lib.load().pa_get_decode_impl()]
+
+
 def ctas_per_sm(head_dim, group, dtype):
     return _lib.load().pa_decode_ctas_per_sm(head_dim, group, _DTYPES[dtype])
 

@@ -41,19 +41,17 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "pa_common.cuh"
+#include "pa_decode.cuh"
 #include "pa_internal.h"
 
 namespace pa {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-constexpr int kUnit = 16;                // positions per pipeline stage
-constexpr float kLazyRescale = 8.0f;     // base-2 units
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kSinglePassTokens = 1 << 30;  // "partition" covering any sequence
 
 constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x / 2); }
 
@@ -109,43 +107,6 @@ struct DecodeShape {
                   "merge scratch must fit in the ring");
 };
 
-struct DecodeParams {
-    void *out;                   // [S][Hq][D] (mode 0) or nullptr
-    const uint16_t *q;           // [S][Hq][D]
-    const uint16_t *k_pool;      // [NB][Hkv][B][D]
-    const uint16_t *v_pool;
-    const int32_t *block_tables; // [S][max_blocks_per_seq]
-    const int32_t *seq_lens;     // [S]
-    float *part_m;               // [S][Hq][NP]
-    float *part_l;               // [S][Hq][NP]
-    float *part_o;               // [S][Hq][NP][D]
-    int *err;
-    int num_blocks;
-    int max_blocks_per_seq;
-    int max_seq_len;
-    int num_q_heads;
-    int num_kv_heads;
-    int group;                   // G
-    int block_size;
-    int log2_block;
-    int partition_tokens;        // P, multiple of kUnit
-    int num_partitions;          // NP (grid.x)
-    float scale_log2;            // scale * log2(e)
-    int mode;                    // 0: decode (direct output when 1 partition), 1: partials only
-};
-
-// Length of sequence i, clamped to what the launch covers; a value out of
-// range is a bad index.
-__device__ __forceinline__ int checked_len(const int32_t *seq_lens, int i, int max_seq_len,
-                                           int table_cap, int *err, bool report) {
-    int L = seq_lens[i];
-    const int cap = max_seq_len < table_cap ? max_seq_len : table_cap;
-    if (L < 0 || L > cap) {
-        if (report) record_error(err, PA_ERR_BAD_INDEX);
-        L = L < 0 ? 0 : cap;
-    }
-    return L;
-}
 
 // Reduce-scatter of NV partial sums over an LT-lane group (lane c in the
 // group): after the call, v[0 .. NV >> LEVELS) of lane c hold the complete
@@ -736,9 +697,9 @@ static int decode_ctas_per_sm(const DecodeEntry &e) {
 // 1/32 of one CTA slot's share of the whole job (taking the average length
 // as half the maximum), in multiples of 256 positions, and run single pass
 // when that would not split anything.
-static int auto_partition(int S, int Hkv, int max_seq_len, const DecodeEntry &e, int block_size) {
+static int auto_partition(int S, int Hkv, int max_seq_len, int ctas_per_sm, int block_size) {
     if (max_seq_len <= 0) return -1;
-    const int slots = sm_count() * decode_ctas_per_sm(e);
+    const int slots = sm_count() * ctas_per_sm;
     const double units = (double)S * Hkv;
     double target = (double)max_seq_len * units / (32.0 * (slots > 0 ? slots : 1));
     int P = (int)std::ceil(target / 256.0) * 256;
@@ -750,9 +711,25 @@ static int auto_partition(int S, int Hkv, int max_seq_len, const DecodeEntry &e,
 
 struct ResolvedDecode {
     DecodeEntry entry;
-    int P;   // -1 single pass, else partition size
-    int NP;  // partitions in the grid
+    bool tc;  // tensor-core kernel (pa_decode_tc.cu) instead of the CUDA-core one
+    bool bf16;
+    int head_dim;
+    int P;    // -1 single pass, else partition size
+    int NP;   // partitions in the grid
 };
+
+// Process-wide choice of decode kernel: 0 automatic, 1 CUDA cores, 2 tensor cores.
+static std::atomic<int> g_decode_impl{0};
+
+// Automatic choice: the tensor-core kernel for groups of 5..8 query heads,
+// where the CUDA-core kernel is bound by instruction issue; CUDA cores below.
+static bool use_tensor_cores(int head_dim, int group) {
+    const int impl = g_decode_impl.load(std::memory_order_relaxed);
+    if (!tc_supported(head_dim, group)) return false;
+    if (impl == 2) return true;
+    if (impl == 1) return false;
+    return group >= 5;
+}
 
 static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                          int block_size, int max_seq_len, int partition_tokens, pa_dtype dtype,
@@ -765,8 +742,15 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
     if (G > 8 || (head_dim != 64 && head_dim != 128) || (block_size != 16 && block_size != 32))
         return PA_ERR_UNSUPPORTED;
     if (!pick_decode(dtype, head_dim, group_pad(G), &r->entry)) return PA_ERR_UNSUPPORTED;
+    r->tc = use_tensor_cores(head_dim, G);
+    r->bf16 = dtype == PA_BF16;
+    r->head_dim = head_dim;
     int P = partition_tokens;
-    if (P == 0) P = auto_partition(num_seqs, num_kv_heads, max_seq_len, r->entry, block_size);
+    if (P == 0) {
+        const int per_sm =
+            r->tc ? tc_ctas_per_sm(dtype == PA_BF16, head_dim) : decode_ctas_per_sm(r->entry);
+        P = auto_partition(num_seqs, num_kv_heads, max_seq_len, per_sm, block_size);
+    }
     if (P < -1) return PA_ERR_INVALID;
     if (P > 0 && (P % block_size != 0 || P % kUnit != 0)) return PA_ERR_INVALID;
     r->P = P;
@@ -778,6 +762,9 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
 static pa_status launch_decode(const ResolvedDecode &r, DecodeParams prm, int num_seqs,
                                int num_kv_heads, cudaStream_t stream) {
     if (num_seqs == 0) return PA_OK;
+    if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_INVALID;
+    if (r.tc)
+        return launch_decode_tc(prm, r.bf16, r.head_dim, r.NP, num_kv_heads, num_seqs, stream);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(r.entry.fn), r.entry.smem))
         return PA_ERR_CUDA;
     if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_INVALID;
@@ -842,15 +829,25 @@ extern "C" {
 
 int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
                              int block_size, int group_size, pa_dtype dtype) {
-    DecodeEntry e;
-    if (!pick_decode(dtype, head_dim, group_pad(group_size), &e)) return -1;
-    return auto_partition(num_seqs, num_kv_heads, max_seq_len, e, block_size);
+    ResolvedDecode r;
+    if (group_size < 1 || resolve(num_seqs, num_kv_heads * group_size, num_kv_heads, head_dim,
+                                  block_size, max_seq_len, 0, dtype, &r) != PA_OK)
+        return -1;
+    return r.P;
 }
+
+int pa_set_decode_impl(int impl) {
+    if (impl < 0 || impl > 2) return -1;
+    return g_decode_impl.exchange(impl);
+}
+
+int pa_get_decode_impl(void) { return g_decode_impl.load(); }
 
 int pa_decode_ctas_per_sm(int head_dim, int group_size, pa_dtype dtype) {
     DecodeEntry e;
     if (group_size < 1 || group_size > 8 || !pick_decode(dtype, head_dim, group_pad(group_size), &e))
         return 0;
+    if (use_tensor_cores(head_dim, group_size)) return tc_ctas_per_sm(dtype == PA_BF16, head_dim);
     return decode_ctas_per_sm(e);
 }
 

@@ -1,0 +1,613 @@
+// Tensor-core paged decode for GB300 (sm_103a): the head-group products
+// q.K^T and P.V on the 5th-generation tensor cores (tcgen05.mma, fp32
+// accumulators in TMEM), K/V tiles moved by 2-D TMA tensor copies with
+// 128-byte swizzle.
+//
+// Same computation as the CUDA-core kernel in pa_decode.cu (see the header
+// comment there and the sources cited in pa.h): for each (partition, KV head,
+// sequence) the positions [start, end) are gathered through the block table
+// and attended by the G query heads of the KV head with an online softmax.
+// What changes is who does the arithmetic.  Per tile of 128 positions:
+//
+//   S^T[128 pos x 16]  = K_tile[128 x d]  . Q^T[d x 16]          (M=128, N=16, K=d)
+//   O^T[d(128) x 16]   = V_tile^T[128 x 128 pos] . P^T[128 x 16] (M=128, N=16, K=128)
+//
+// with the G <= 8 heads of the group in the N columns (zero-padded to 16).
+// Tokens on M is the layout that makes both operands of q.K^T and P.V come
+// straight from the swizzled K/V tiles (K as a K-major A operand, V as an
+// MN-major A operand); the softmax warps read S^T and O^T out of TMEM one
+// row (position, or dimension) per thread.
+//
+// Roles (6 warps):
+//   warp 0      producer: block-table lookups and TMA tensor copies of 16-row
+//               boxes (one per 16 positions and 64 dims) into the K and V tiles;
+//   warp 1      allocates the 64 TMEM columns; lane 0 issues every MMA and
+//               commits its completion to mbarriers;
+//   warps 2..5  softmax / epilogue: thread r owns TMEM lane r (position r of a
+//               tile for S, dimension r for O); they also write q and P^T into
+//               shared memory in the operand layout (K-major, 128-byte swizzle).
+// Online softmax with the same lazy rescale as the CUDA-core kernel; the
+// accumulator lives in registers (thread = dimension) and takes each tile's
+// O^T from a double-buffered TMEM slot.
+#include <cuda.h>  // CUtensorMap and its enums only; the encoder comes from the driver at run time
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr int kTcTile = 128;       // positions per tile (MMA M of q.K^T)
+constexpr int kTcN = 16;           // MMA N: the query heads of a group, zero-padded
+constexpr int kTcG = 8;            // largest group the kernel serves
+constexpr int kTcWarps = 6;
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcCols = 64;        // TMEM columns: S x2 and O x2, 16 fp32 columns each
+constexpr int kSCol0 = 0, kOCol0 = 32;
+
+enum TcBar {
+    kKFull = 0, kVFull, kKEmpty, kVEmpty, kQReady,
+    kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kOFull0, kOFull1, kOEmpty0, kOEmpty1,
+    kNumTcBars
+};
+
+template <int D>
+struct TcShape {
+    static constexpr int KH = D / 64;                 // 64-dim (128-byte) slabs of K along d
+    static constexpr int SLAB = kTcTile * 128;        // one slab of a tile: 16 KiB
+    static constexpr int K_BYTES = KH * SLAB;
+    static constexpr int V_BYTES = 2 * SLAB;          // V^T is M = 128 dims; d = 64 pads with zeros
+    static constexpr int Q_BYTES = KH * kTcN * 128;   // q as a 16-row K-major operand
+    static constexpr int P_BYTES = 2 * kTcN * 128;    // P^T: 16 rows x 128 positions (two atoms)
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + K_BYTES;
+    static constexpr int OFF_Q = OFF_V + V_BYTES;
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;     // two buffers
+    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;
+    static constexpr int RED_BYTES = 3 * 4 * kTcN * 4;  // two tile-max buffers + the final sums
+    static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+    static constexpr int OFF_MISC = OFF_BAR + kNumTcBars * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
+    static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] . B[smem desc], kind::f16 (f16 or bf16 in, f32 accumulate)
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive (once) on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+// 32 lanes x 16 columns of 32-bit TMEM cells: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 2-D TMA tensor copy (tile mode) global -> shared, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+        "[%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void softmax_bar() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 layout):
+// start >> 4 at [0,14), leading byte offset >> 4 at [16,30), stride byte
+// offset >> 4 at [32,46), version 1 at [46,48), layout SWIZZLE_128B (2) at [61,64).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: f32 accumulator, A/B format
+// (0 = f16, 1 = bf16), A/B major (0 = K, 1 = MN), N >> 3, M >> 4.
+__host__ __device__ constexpr uint32_t f16_idesc(bool bf16, bool a_mn, bool b_mn, int M, int N) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// Byte offset of element (row, col) of a K-major operand stored as
+// 128-byte-swizzled atoms of 8 rows x 64 columns (16-bit elements): atoms
+// along the columns are `atom_stride` bytes apart, 8-row groups 1024 bytes.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int col, int atom_stride) {
+    const int chunk = (col & 63) >> 3;
+    return (uint32_t)((col >> 6) * atom_stride + (row >> 3) * 1024 + (row & 7) * 128 +
+                      ((chunk ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t narrow1(float x) {
+    if constexpr (BF16) {
+        __nv_bfloat16 h = __float2bfloat16_rn(x);
+        uint16_t u;
+        memcpy(&u, &h, 2);
+        return u;
+    } else {
+        __half h = __float2half_rn(x);
+        uint16_t u;
+        memcpy(&u, &h, 2);
+        return u;
+    }
+}
+
+template <bool BF16, int D>
+__global__ void __launch_bounds__(kTcThreads)
+    paged_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
+                           const __grid_constant__ CUtensorMap tmap_v) {
+    using S = TcShape<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::OFF_MISC + 8);
+    float *red = reinterpret_cast<float *>(smem + S::OFF_RED);
+
+    const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.group;
+    const int P = p.partition_tokens;
+    const int L = checked_len(p.seq_lens, seq, p.max_seq_len, p.max_blocks_per_seq * p.block_size,
+                              p.err, threadIdx.x == 0 && part == 0 && kvh == 0);
+    const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
+    const int start = part * P;
+    if (start >= L) {  // empty partition: as in the CUDA-core kernel
+        if (p.mode == 0) {
+            if (part == 0) {
+                uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
+                const int64_t base = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * D / 2;
+                for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) o[base + i] = 0u;
+            }
+        } else {
+            for (int g = 0; g < G; ++g) {
+                const int64_t row =
+                    ((int64_t)seq * p.num_q_heads + kvh * G + g) * p.num_partitions + part;
+                if (threadIdx.x == 0) {
+                    p.part_m[row] = -INFINITY;
+                    p.part_l[row] = 0.f;
+                }
+                for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
+            }
+        }
+        return;
+    }
+    const int end = (start + P < L) ? start + P : L;
+    const int nunits = (end - start + kUnit - 1) / kUnit;
+    const int ntiles = (end - start + kTcTile - 1) / kTcTile;
+    const bool direct = (p.mode == 0) && (nparts_seq <= 1);
+
+    if (threadIdx.x == 0) {
+        const int counts[kNumTcBars] = {1, 1, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4};
+        for (int b = 0; b < kNumTcBars; ++b) mbar_init(&bar[b], counts[b]);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTcCols);
+        tmem_relinquish();
+    }
+    if constexpr (D == 64) {
+        // rows 64..127 of the V^T operand: zero once, never loaded
+        uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_V + S::SLAB);
+        for (int i = threadIdx.x; i < S::SLAB / 16; i += kTcThreads) z[i] = make_uint4(0, 0, 0, 0);
+        fence_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        const int32_t *table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
+        const int rows_per_block = p.block_size;
+        bool ok = true;
+        for (int u0 = 0; u0 < nunits && ok; u0 += 32) {  // 32 units = 4 tiles
+            const int u = u0 + lane;
+            int row0 = 0;  // first row of the unit in the 2-D view [NB*Hkv*B, d]
+            if (u < nunits) {
+                const int pos = start + u * kUnit;
+                int phys = table[pos >> p.log2_block];
+                if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                    record_error(p.err, PA_ERR_BAD_INDEX);
+                    phys = 0;
+                }
+                row0 = (phys * p.num_kv_heads + kvh) * rows_per_block + (pos & (p.block_size - 1));
+            }
+            for (int t = u0 / 8; t < ntiles && t < (u0 + 32) / 8 && ok; ++t) {
+                const int nu = (nunits - 8 * t < 8) ? nunits - 8 * t : 8;
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    if (t >= 1) {
+                        const bool done = mbar_wait(&bar[kv ? kVEmpty : kKEmpty], (t - 1) & 1);
+                        if (!__all_sync(kFullMask, done)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    const int base_off = kv ? S::OFF_V : S::OFF_K;
+                    const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
+                    uint64_t *full = &bar[kv ? kVFull : kKFull];
+                    if (lane == 0) mbar_arrive_expect_tx(full, nu * S::KH * 2048);
+                    for (int j = 0; j < nu; ++j) {
+                        const int r0 = __shfl_sync(kFullMask, row0, 8 * t + j - u0);
+                        if (lane == 0) {
+#pragma unroll
+                            for (int h = 0; h < S::KH; ++h)
+                                tma_load_2d(smem + base_off + h * S::SLAB + j * 2048, map, 64 * h,
+                                            r0, full);
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = f16_idesc(BF16, false, false, kTcTile, kTcN);
+            constexpr uint32_t idesc_pv = f16_idesc(BF16, true, false, 128, kTcN);
+            const uint32_t sbase = smem_addr(smem);
+            bool ok = mbar_wait(&bar[kQReady], 0);
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int b = i & 1;
+                ok = mbar_wait(&bar[kKFull], i & 1) &&
+                     (i < 2 || mbar_wait(&bar[kSEmpty0 + b], ((i >> 1) - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
+                    const uint32_t qoff = (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
+                    tc_mma(tmem + kSCol0 + 16 * b, sw128_desc(sbase + S::OFF_K + koff, 16, 1024),
+                           sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
+                }
+                tc_commit(&bar[kSFull0 + b]);
+                tc_commit(&bar[kKEmpty]);
+                ok = mbar_wait(&bar[kVFull], i & 1) && mbar_wait(&bar[kPFull0 + b], (i >> 1) & 1) &&
+                     (i < 2 || mbar_wait(&bar[kOEmpty0 + b], ((i >> 1) - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kTcTile / 16; ++ks) {
+                    const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
+                    const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
+                    tc_mma(tmem + kOCol0 + 16 * b,
+                           sw128_desc(sbase + S::OFF_V + voff, S::SLAB, 1024),
+                           sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
+                }
+                tc_commit(&bar[kOFull0 + b]);
+                tc_commit(&bar[kVEmpty]);
+            }
+            if (!ok) {
+                record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- softmax / epilogue
+        const int sw = warp - 2;                 // softmax warp 0..3
+        const int quad = warp & 3;               // TMEM lane quadrant this warp may access
+        const int r = quad * 32 + lane;          // TMEM lane: position (S) or dimension (O)
+        const int st = threadIdx.x - 64;         // 0..127
+        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+
+        // q of the group as the K-major B operand (16 rows, 128-byte swizzle),
+        // rows >= G zero.  Unscaled: the scale is applied to S in fp32.
+        for (int ci = st; ci < kTcN * (D / 8); ci += 128) {
+            const int g = ci / (D / 8), c = ci % (D / 8);
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (g < G)
+                v = *reinterpret_cast<const uint4 *>(
+                    p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * 8);
+            *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(g, c * 8, kTcN * 128)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kQReady]);
+
+        float m_run[kTcG], m_true[kTcG], l_part[kTcG], acc[kTcG], alpha_prev[kTcG];
+#pragma unroll
+        for (int g = 0; g < kTcG; ++g) {
+            m_run[g] = -INFINITY;
+            m_true[g] = -INFINITY;
+            l_part[g] = 0.f;
+            acc[g] = 0.f;
+            alpha_prev[g] = 1.f;
+        }
+        bool failed = false;
+        auto accumulate = [&](int k) -> bool {
+            const int b = k & 1;
+            const bool landed = mbar_wait(&bar[kOFull0 + b], (k >> 1) & 1);
+            if (!__all_sync(kFullMask, landed)) return false;
+            tc_fence_after();
+            float o[16];
+            tmem_load16(tmem + lane_addr + kOCol0 + 16 * b, o);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kOEmpty0 + b]);
+#pragma unroll
+            for (int g = 0; g < kTcG; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
+            return true;
+        };
+
+        for (int i = 0; i < ntiles; ++i) {
+            const int b = i & 1;
+            const bool landed = !failed && mbar_wait(&bar[kSFull0 + b], (i >> 1) & 1);
+            const bool ok = __all_sync(kFullMask, landed);
+            float s[16];
+            if (ok) {
+                tc_fence_after();
+                tmem_load16(tmem + lane_addr + kSCol0 + 16 * b, s);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kSEmpty0 + b]);
+            } else {
+#pragma unroll
+                for (int g = 0; g < 16; ++g) s[g] = 0.f;
+            }
+            const int tile0 = start + i * kTcTile;
+            const int nvalid = (end - tile0 < kTcTile) ? end - tile0 : kTcTile;
+            const bool valid = r < nvalid;
+            // tile max of each head over the 128 positions
+            float *tmax = red + b * (4 * kTcN);
+#pragma unroll
+            for (int g = 0; g < kTcG; ++g) {
+                s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
+                float v = s[g];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
+                if (lane == 0) tmax[sw * kTcN + g] = v;
+            }
+            if (lane == 0) tmax[sw * kTcN + kTcN - 1] = ok ? 1.f : 0.f;  // column 15: health flag
+            softmax_bar();
+            bool all_ok = true;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) all_ok &= tmax[w * kTcN + kTcN - 1] != 0.f;
+            if (!all_ok) {
+                failed = true;
+                break;
+            }
+            bool need = false;
+            float mx[kTcG];
+#pragma unroll
+            for (int g = 0; g < kTcG; ++g) {
+                mx[g] = fmaxf(fmaxf(tmax[g], tmax[kTcN + g]),
+                              fmaxf(tmax[2 * kTcN + g], tmax[3 * kTcN + g]));
+                need |= (g < G) && (mx[g] > m_run[g] + kLazyRescale);
+            }
+            float alpha[kTcG];
+#pragma unroll
+            for (int g = 0; g < kTcG; ++g) {
+                alpha[g] = 1.f;
+                if (need) {  // block-uniform
+                    const float mn = fmaxf(m_run[g], mx[g]);
+                    alpha[g] = fast_exp2(m_run[g] - mn);
+                    m_run[g] = mn;
+                    l_part[g] *= alpha[g];
+                }
+                m_true[g] = fmaxf(m_true[g], mx[g]);
+            }
+            // P^T (16 rows = heads, 128 positions) in the operand layout
+            uint8_t *pbuf = smem + S::OFF_P + b * S::P_BYTES;
+#pragma unroll
+            for (int g = 0; g < kTcN; ++g) {
+                float pv = 0.f;
+                if (g < kTcG && g < G) {
+                    pv = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
+                    l_part[g] += pv;
+                }
+                *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kTcN * 128)) =
+                    narrow1<BF16>(pv);
+            }
+            if (!valid) {
+                // Stale rows of the last tile: V must be finite there (0 * NaN
+                // would poison the product), so zero the row once it has landed.
+                if (mbar_wait(&bar[kVFull], i & 1)) {
+#pragma unroll
+                    for (int h = 0; h < S::KH; ++h) {
+                        uint4 *row = reinterpret_cast<uint4 *>(smem + S::OFF_V + h * S::SLAB + r * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                    }
+                } else {
+                    failed = true;
+                }
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kPFull0 + b]);
+            if (i >= 1 && !accumulate(i - 1)) failed = true;
+#pragma unroll
+            for (int g = 0; g < kTcG; ++g) alpha_prev[g] = alpha[g];
+        }
+        if (!failed && !accumulate(ntiles - 1)) failed = true;
+
+        // l over the 128 position-threads, per head
+        float *lsum = red + 2 * (4 * kTcN);
+#pragma unroll
+        for (int g = 0; g < kTcG; ++g) {
+            float v = l_part[g];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
+            if (lane == 0) lsum[sw * kTcN + g] = v;
+        }
+        softmax_bar();
+        if (failed) {
+            if (st == 0) {
+                record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+        } else if (r < D) {
+#pragma unroll
+            for (int g = 0; g < kTcG; ++g) {
+                if (g >= G) break;
+                const float lt =
+                    lsum[g] + lsum[kTcN + g] + lsum[2 * kTcN + g] + lsum[3 * kTcN + g];
+                const float o = acc[g] / lt;
+                const int h = kvh * G + g;
+                if (direct) {
+                    uint16_t *out = static_cast<uint16_t *>(p.out);
+                    out[((int64_t)seq * p.num_q_heads + h) * D + r] = narrow1<BF16>(o);
+                } else {
+                    const int64_t row = ((int64_t)seq * p.num_q_heads + h) * p.num_partitions + part;
+                    p.part_o[row * D + r] = o;
+                    if (r == 0) {
+                        p.part_m[row] = m_true[g];
+                        p.part_l[row] = lt * fast_exp2(m_run[g] - m_true[g]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // let copies and MMAs still in flight finish before shared memory and
+        // TMEM are released (each wait is bounded)
+        (void)mbar_wait(&bar[kKFull], (ntiles - 1) & 1);
+        (void)mbar_wait(&bar[kVFull], (ntiles - 1) & 1);
+        (void)mbar_wait(&bar[kVEmpty], (ntiles - 1) & 1);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTcCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn tensor_map_encoder() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// The pool [NB][Hkv][B][d] viewed as a 2-D tensor of NB*Hkv*B rows of d
+// elements; boxes of 16 rows x 64 columns, 128-byte swizzle.
+static bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, bool bf16) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kUnit};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+               const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+using TcKernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
+
+static TcKernel pick_tc(bool bf16, int D, int *smem) {
+    if (D == 128) {
+        *smem = TcShape<128>::SMEM_BYTES;
+        return bf16 ? paged_decode_tc_kernel<true, 128> : paged_decode_tc_kernel<false, 128>;
+    }
+    *smem = TcShape<64>::SMEM_BYTES;
+    return bf16 ? paged_decode_tc_kernel<true, 64> : paged_decode_tc_kernel<false, 64>;
+}
+
+bool tc_supported(int head_dim, int group) {
+    return (head_dim == 64 || head_dim == 128) && group >= 1 && group <= kTcG;
+}
+
+int tc_ctas_per_sm(bool bf16, int head_dim) {
+    int smem = 0;
+    TcKernel k = pick_tc(bf16, head_dim, &smem);
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kTcThreads, smem) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+pa_status launch_decode_tc(const DecodeParams &prm, bool bf16, int head_dim, int num_partitions,
+                           int num_kv_heads, int num_seqs, cudaStream_t stream) {
+    if (num_seqs == 0) return PA_OK;
+    int smem = 0;
+    TcKernel k = pick_tc(bf16, head_dim, &smem);
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return PA_ERR_CUDA;
+    const int64_t rows = (int64_t)prm.num_blocks * num_kv_heads * prm.block_size;
+    CUtensorMap mk, mv;
+    if (!pool_tensor_map(&mk, prm.k_pool, rows, head_dim, bf16) ||
+        !pool_tensor_map(&mv, prm.v_pool, rows, head_dim, bf16))
+        return PA_ERR_CUDA;
+    dim3 grid((unsigned)num_partitions, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    k<<<grid, kTcThreads, smem, stream>>>(prm, mk, mv);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa
