@@ -257,7 +257,7 @@ def run_reference(args, rank, world):
 class GpuStep:
     """Device state of one workload and the calls of one decode step."""
 
-    def __init__(self, plan, device):
+    def __init__(self, plan, device, partition_tokens=None):
         import torch
         from paged_kv_cache_64_gb300 import api, workloads
 
@@ -271,7 +271,7 @@ class GpuStep:
         self.slots, self.copies = t(self.lay.slot_mapping), t(self.lay.pre_copies)
         self.max_seq_len = int(self.lay.max_seq_len)
         spec = self.spec
-        self.P = spec.partition_tokens
+        self.P = spec.partition_tokens if partition_tokens is None else partition_tokens
         self.resolved_P = self.P if self.P else api.auto_partition(
             spec.num_seqs, spec.num_kv_heads, self.max_seq_len, spec.head_dim, spec.block_size,
             spec.num_q_heads // spec.num_kv_heads, self.vals.q.dtype)
@@ -284,8 +284,10 @@ class GpuStep:
         self.write_bytes = workloads.cache_write_bytes(spec, spec.num_seqs)
         self.copy_bytes = 2 * 2 * len(self.lay.pre_copies) * spec.num_kv_heads * \
             spec.block_size * spec.head_dim * workloads.DTYPE_BYTES[spec.dtype]
-        per_layer = 2 + (1 if self.resolved_P and self.resolved_P > 0 else 0) + \
-            (1 if len(self.lay.pre_copies) else 0)
+        NP = -(-self.max_seq_len // self.resolved_P) if self.resolved_P and self.resolved_P > 0 else 1
+        # fused write + decode (+ combine) launch, a separate combine above 8
+        # partitions, and the copy-on-write copies when there are any
+        per_layer = 1 + (1 if NP > 8 else 0) + (1 if len(self.lay.pre_copies) else 0)
         self.launches_per_step = per_layer * spec.num_layers
 
     def step_bytes(self):
@@ -300,15 +302,15 @@ class GpuStep:
             kp, vp = v.k_pools[layer], v.v_pools[layer]
             if self.copies.numel():
                 api.copy_blocks([kp], [vp], self.copies, stream=stream)
-            api.cache_write(v.k_new[layer] if k_new is None else k_new[layer],
-                            v.v_new[layer] if v_new is None else v_new[layer],
-                            self.slots, kp, vp, stream=stream)
             if ev is not None:
                 a = self.torch.cuda.Event(enable_timing=True)
                 b = self.torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-            api.decode(self.out[layer], q, kp, vp, self.tables, self.lens, self.max_seq_len,
-                       self.plan.scale, partition_tokens=self.P, workspace=self.ws, stream=stream)
+            # the new token's cache write and the decode, one launch
+            api.decode_step(self.out[layer], q, v.k_new[layer] if k_new is None else k_new[layer],
+                            v.v_new[layer] if v_new is None else v_new[layer], self.slots, kp, vp,
+                            self.tables, self.lens, self.max_seq_len, self.plan.scale,
+                            partition_tokens=self.P, workspace=self.ws, stream=stream)
             if ev is not None:
                 b.record(stream)
                 ev.append((a, b))
@@ -324,7 +326,7 @@ def run_gpu(args, rank, world, local_rank):
     base = workloads.SPECS[args.workload]
     plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs,
                                seed=base.seed + 1000 * rank if rank else None)
-    st = GpuStep(plan, device)
+    st = GpuStep(plan, device, args.partition_tokens)
     stream = torch.cuda.current_stream()
     spec = st.spec
     flush = None
@@ -391,14 +393,16 @@ def run_gpu(args, rank, world, local_rank):
     value = all_bytes / secs / 1e9
     if ev:
         dec_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-        kernel_note = "pa_decode call (split-KV partition kernel + reduce), CUDA events"
+        kernel_note = ("pa_decode_step launch (new-token cache write + split-KV decode + combine), "
+                       "CUDA events")
     else:
         # graph replay: a step's time spread over its layers (cache write included)
         dec_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in step_ev) / spec.num_layers
-        kernel_note = ("pa_decode + cache write per layer: graph-replayed step time / layers "
+        kernel_note = ("pa_decode_step per layer: graph-replayed step time / layers "
                        "(CUDA events around each replay)")
     peak, peak_kind = measured_peaks()
-    achieved = st.decode_bytes / (dec_avg_ms / 1e3) / 1e9
+    launch_bytes = st.decode_bytes + st.write_bytes  # what one decode_step launch must move
+    achieved = launch_bytes / (dec_avg_ms / 1e3) / 1e9
     traffic = stored_traffic(args.workload)
 
     # ------------------------------------------------ end to end (host buffers)
@@ -453,12 +457,10 @@ def run_gpu(args, rank, world, local_rank):
             "decode_ctas_per_sm": api.ctas_per_sm(spec.head_dim,
                                                   spec.num_q_heads // spec.num_kv_heads,
                                                   st.vals.q.dtype),
-            "step": "copy_blocks (if any) + cache_write + paged decode, every layer",
+            "step": "copy_blocks (if any) + pa_decode_step (cache write + decode), every layer",
             "launch": "CUDA graph replay" if graph is not None else "eager",
-            "decode_kernel": ("tensor cores (tcgen05)" if (
-                args.decode_impl == "tensor_cores" or (args.decode_impl == "auto" and
-                                                       spec.num_q_heads // spec.num_kv_heads >= 5))
-                else "CUDA cores"),
+            "decode_kernel": ("CUDA cores" if args.decode_impl == "cuda_cores"
+                              else "tensor cores (tcgen05)"),
             "l2": ("inputs larger than L2 (%.2f GB per step)" % (st.step_bytes() / 1e9))
             if flush is None else "L2 flushed (256 MiB write) before every step",
         },
@@ -467,7 +469,7 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": kernel_note,
-                     "bytes_per_launch": st.decode_bytes, "avg_launch_ms": dec_avg_ms,
+                     "bytes_per_launch": launch_bytes, "avg_launch_ms": dec_avg_ms,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s",
@@ -497,6 +499,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
                     help="replay the step as a CUDA graph (auto: when the step has >1 layer)")
+    ap.add_argument("--partition-tokens", type=int, default=None,
+                    help="override the workload's split-KV partition size (0 auto, -1 single pass)")
     ap.add_argument("--decode-impl", default="auto",
                     choices=["auto", "cuda_cores", "tensor_cores"],
                     help="decode kernel (default: the library's automatic choice)")

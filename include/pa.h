@@ -139,6 +139,12 @@ pa_status pa_copy_blocks(void *const *k_pools, void *const *v_pools, int num_lay
  * With P > 0 or automatic, workspace must hold at least
  * pa_decode_workspace_size(...) bytes (device memory, 256-byte aligned); it
  * is scratch, overwritten on every call, and may be NULL when the size is 0.
+ * It needs no initialisation: besides the partials it holds one arrival
+ * counter per (sequence, KV head), tagged with a per-call epoch so that
+ * stale contents read as zero; when a sequence has at most 8 partitions the
+ * last CTA to finish combines them (one launch), otherwise a separate
+ * combine kernel runs.  Launches use programmatic dependent launch: each
+ * kernel waits for the previous work on the stream before reading memory.
  *
  * Arguments (device pointers unless stated):
  *   out, q                 [num_seqs][num_q_heads][head_dim]
@@ -160,6 +166,27 @@ pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_
                     int partition_tokens, void *workspace, size_t workspace_bytes,
                     pa_dtype dtype, void *stream);
 
+/* ------------------------------------------------------------------------
+ * pa_decode_step: one decode step, fused.  For every sequence i its newest
+ * token (position seq_lens[i]-1) is first written into the cache exactly as
+ * pa_cache_write would write k_new[i], v_new[i] at slot_mapping[i]; then
+ * pa_decode runs over seq_lens[i] positions, new token included.  Both happen
+ * inside one kernel: the CTA that reads position seq_lens[i]-1 writes it
+ * first.  slot_mapping[i] must be the slot the block table gives for that
+ * position (block_tables[i][(L-1)/B]*B + (L-1)%B); a different slot is
+ * reported as PA_ERR_BAD_INDEX and that token is not written.  Sequences
+ * with seq_lens[i] = 0 write nothing.  The pools are updated in place.
+ *   k_new, v_new: [num_seqs][num_kv_heads][head_dim] (device); slot_mapping:
+ *   int64 [num_seqs] (device).  Other arguments as pa_decode.
+ * ---------------------------------------------------------------------- */
+pa_status pa_decode_step(void *out, const void *q, const void *k_new, const void *v_new,
+                         const int64_t *slot_mapping, void *k_pool, void *v_pool, int num_blocks,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *seq_lens, int max_seq_len, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, float scale,
+                         int partition_tokens, void *workspace, size_t workspace_bytes,
+                         pa_dtype dtype, void *stream);
+
 /* Partition size pa_decode uses for these shapes when partition_tokens = 0
  * (-1 means it will run single pass).  Needs the current CUDA device. */
 int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
@@ -167,8 +194,8 @@ int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, in
 
 /* Decode kernel selection, process-wide, for every later call:
  *   0 automatic (default): the tensor-core kernel (tcgen05 MMAs, TMA tensor
- *     copies) for groups of 5..8 query heads per KV head, the CUDA-core
- *     kernel (packed fp32 FMAs) for smaller groups;
+ *     copies) wherever it applies (head_dim 64/128, G <= 8), else the
+ *     CUDA-core kernel (packed fp32 FMAs);
  *   1 always the CUDA-core kernel;  2 always the tensor-core kernel.
  * Both compute the same result to within the output tolerance.  Returns the
  * previous setting, or -1 (nothing changed) for an invalid value.  Not
@@ -200,6 +227,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  *   m  float [num_seqs][num_q_heads][NP]
  *   l  float [num_seqs][num_q_heads][NP]
  *   O  float [num_seqs][num_q_heads][NP][head_dim]
+ *   arrival counters  uint64 [num_seqs][num_kv_heads]  (pa_decode only)
  *   [P3] section 4, "Parallel Partitioning Across GPU Warps", step 2.
  * partition_tokens must be > 0 here.  Other arguments as pa_decode.
  * ---------------------------------------------------------------------- */

@@ -40,6 +40,9 @@ SIGNATURES = {
                                 _c_int, _c_sz, _vp]),
     "pa_decode": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _c_f, _c_int, _vp, _c_sz, _c_int, _vp]),
+    "pa_decode_step": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _vp,
+                                _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int, _vp,
+                                _c_sz, _c_int, _vp]),
     "pa_decode_auto_partition": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           _c_int]),
     "pa_decode_ctas_per_sm": (_c_int, [_c_int, _c_int, _c_int]),

@@ -169,6 +169,32 @@ def decode(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale,
     return workspace
 
 
+def decode_step(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables, seq_lens,
+                max_seq_len, scale, partition_tokens=0, workspace=None, stream=None):
+    """One fused decode step: write each sequence's newest token (k_new /
+    v_new [S, Hkv, d] at slot_mapping [S], the slot of position seq_lens-1)
+    and attend over seq_lens positions, in one launch."""
+    S, hq, hkv, d, nb, bs = _decode_dims(q, k_pool, block_tables, seq_lens)
+    if out.shape != q.shape or out.dtype != q.dtype or k_pool.dtype != q.dtype:
+        raise ValueError("out/q/pool shapes or types differ")
+    if k_new.shape != (S, hkv, d) or v_new.shape != k_new.shape or slot_mapping.shape != (S,):
+        raise ValueError("k_new/v_new must be [S, Hkv, d] and slot_mapping [S]")
+    need = workspace_size(S, hq, hkv, d, bs, max_seq_len, partition_tokens, q.dtype)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = alloc_workspace(need, q.device)
+    ws = _cuda(workspace, "workspace") if workspace is not None else ctypes.c_void_p(0)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = _lib.load().pa_decode_step(
+        _cuda(out, "out"), _cuda(q, "q"), _cuda(k_new, "k_new"), _cuda(v_new, "v_new"),
+        _cuda(slot_mapping, "slot_mapping", torch.int64), _cuda(k_pool, "k_pool"),
+        _cuda(v_pool, "v_pool"), nb, _cuda(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _cuda(seq_lens, "seq_lens", torch.int32), int(max_seq_len), S, hq,
+        hkv, d, bs, float(scale), int(partition_tokens), ws, wbytes, _dt(q),
+        _stream_handle(stream))
+    _lib.check("pa_decode_step", rc)
+    return workspace
+
+
 def decode_static_scratch(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale,
                           partition_tokens=0, stream=None):
     """Same result as decode(), for callers that cannot allocate device

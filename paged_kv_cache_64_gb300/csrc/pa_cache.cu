@@ -73,6 +73,7 @@ __global__ void cache_write_kernel(const uint4 *__restrict__ k_new, const uint4 
                                    uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool,
                                    int64_t num_slots, int num_kv_heads, int pieces, int block_size,
                                    int *err) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
     const int64_t per_token = 2ll * num_kv_heads * pieces;
     const int64_t total = per_token * num_tokens;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;

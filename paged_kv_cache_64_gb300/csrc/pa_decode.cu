@@ -43,6 +43,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <utility>
 
 #include "pa_common.cuh"
 #include "pa_decode.cuh"
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
     const int G = p.group;
     const int P = p.partition_tokens;
 
+    pdl_wait();  // inputs may come from the previous kernel on the stream
     const int L = checked_len(p.seq_lens, seq, p.max_seq_len,
                               p.max_blocks_per_seq * p.block_size, p.err,
                               threadIdx.x == 0 && part == 0 && kvh == 0);
@@ -202,6 +204,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
     const int nunits = (end - start + kUnit - 1) / kUnit;
     const bool direct = (p.mode == 0) && (nparts_seq <= 1);
 
+    if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write<D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full_bar[s], 1);
@@ -469,6 +472,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
         }
     }
 
+    pdl_trigger();
     __syncthreads();  // ring drained: every issued copy was waited on by a consumer
     if (*abort_flag) {
         // A bounded wait ran out.  Let any copy still in flight land before
@@ -550,6 +554,20 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
             dst[1] = make_float4(o[4], o[5], o[6], o[7]);
         }
     }
+    if (!direct && p.counters != nullptr) {
+        __shared__ int last_flag;
+        __shared__ float wsm[8 * kFuseMaxParts];
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0)
+            last_flag = arrive_last(p.counters + (int64_t)seq * p.num_kv_heads + kvh, p.epoch,
+                                    nparts_seq, p.err);
+        __syncthreads();
+        if (last_flag) {
+            __threadfence();
+            fused_combine<BF16, D>(p, seq, kvh, nparts_seq, wsm, blockDim.x);
+        }
+    }
 }
 
 // ------------------------------------------------------------------ reduce
@@ -574,6 +592,7 @@ constexpr int kReduceWarps = 4;
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kReduceWarps * 32) split_reduce_kernel(const ReduceParams p) {
     constexpr int V = D / 32;
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * kReduceWarps + warp;
     if (row >= (int64_t)p.num_seqs * p.num_q_heads) return;
@@ -670,18 +689,29 @@ static int ilog2_exact(int x) {
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WorkspaceLayout {
-    size_t m_off, l_off, o_off, bytes;
+    size_t m_off, l_off, o_off, c_off, bytes;
 };
 
-static WorkspaceLayout workspace_layout(int S, int Hq, int D, int NP) {
+// m, l, O partials, then one 64-bit arrival counter per (sequence, KV head)
+// for the fused combine.
+static WorkspaceLayout workspace_layout(int S, int Hq, int D, int NP, int Hkv) {
     const size_t rows = (size_t)S * Hq * NP;
     WorkspaceLayout w;
     w.m_off = 0;
     w.l_off = align256(rows * sizeof(float));
     w.o_off = w.l_off + align256(rows * sizeof(float));
-    w.bytes = w.o_off + align256(rows * D * sizeof(float));
+    w.c_off = w.o_off + align256(rows * D * sizeof(float));
+    w.bytes = w.c_off + align256((size_t)S * Hkv * sizeof(unsigned long long));
     return w;
 }
+
+// Tag of a decode call in the fused-combine counters (never 0 twice in a row).
+static unsigned int next_epoch() {
+    static std::atomic<unsigned int> epoch{0x9e3779b9u};
+    unsigned int e = epoch.fetch_add(1) + 1;
+    return e ? e : epoch.fetch_add(1) + 1;
+}
+
 
 // Occupancy of a decode instantiation (CTAs per SM), cached per kernel/device.
 static int decode_ctas_per_sm(const DecodeEntry &e) {
@@ -721,14 +751,13 @@ struct ResolvedDecode {
 // Process-wide choice of decode kernel: 0 automatic, 1 CUDA cores, 2 tensor cores.
 static std::atomic<int> g_decode_impl{0};
 
-// Automatic choice: the tensor-core kernel for groups of 5..8 query heads,
-// where the CUDA-core kernel is bound by instruction issue; CUDA cores below.
+// Automatic choice: the tensor-core kernel wherever it applies (measured
+// faster on every workload shape here; the CUDA-core kernel is bound by
+// instruction issue at 5..8 heads per KV head).
 static bool use_tensor_cores(int head_dim, int group) {
     const int impl = g_decode_impl.load(std::memory_order_relaxed);
     if (!tc_supported(head_dim, group)) return false;
-    if (impl == 2) return true;
-    if (impl == 1) return false;
-    return group >= 5;
+    return impl != 1;
 }
 
 static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -769,7 +798,9 @@ static pa_status launch_decode(const ResolvedDecode &r, DecodeParams prm, int nu
         return PA_ERR_CUDA;
     if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_INVALID;
     dim3 grid((unsigned)r.NP, (unsigned)num_kv_heads, (unsigned)num_seqs);
-    r.entry.fn<<<grid, kDecodeThreads, r.entry.smem, stream>>>(prm);
+    if (launch_pdl(r.entry.fn, grid, dim3(kDecodeThreads), (size_t)r.entry.smem, stream, prm) !=
+        cudaSuccess)
+        return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -821,6 +852,79 @@ static void *static_scratch_address() {
     return addr[dev];
 }
 
+// Shared body of pa_decode and pa_decode_step (k_new == nullptr: no fused write).
+static pa_status decode_impl(void *out, const void *q, const void *k_new, const void *v_new,
+                             const int64_t *slot_mapping, const void *k_pool, const void *v_pool,
+                             int num_blocks, const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *seq_lens, int max_seq_len, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             float scale, int partition_tokens, void *workspace,
+                             size_t workspace_bytes, pa_dtype dtype, void *stream) {
+    ResolvedDecode r;
+    pa_status st = resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_seq_len, partition_tokens, dtype, &r);
+    if (st != PA_OK) return st;
+    if (num_seqs > 0 && (!out || !aligned16(out))) return PA_ERR_INVALID;
+    DecodeParams prm;
+    st = fill_common(&prm, q, k_pool, v_pool, num_blocks, block_tables, max_blocks_per_seq,
+                     seq_lens, max_seq_len, num_seqs, num_q_heads, num_kv_heads, block_size,
+                     scale);
+    if (st != PA_OK) return st;
+    prm.out = out;
+    prm.mode = 0;
+    if (k_new) {
+        if (num_seqs > 0 && (!v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)))
+            return PA_ERR_INVALID;
+        prm.k_new = static_cast<const uint16_t *>(k_new);
+        prm.v_new = static_cast<const uint16_t *>(v_new);
+        prm.slot_mapping = slot_mapping;
+    }
+    cudaStream_t s = as_stream(stream);
+    if (r.P <= 0) {
+        prm.partition_tokens = kSinglePassTokens;
+        prm.num_partitions = 1;
+        return launch_decode(r, prm, num_seqs, num_kv_heads, s);
+    }
+    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, r.NP, num_kv_heads);
+    if (!workspace || workspace_bytes < w.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return PA_ERR_INVALID;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    prm.part_m = reinterpret_cast<float *>(ws + w.m_off);
+    prm.part_l = reinterpret_cast<float *>(ws + w.l_off);
+    prm.part_o = reinterpret_cast<float *>(ws + w.o_off);
+    prm.partition_tokens = r.P;
+    prm.num_partitions = r.NP;
+    const bool fuse = r.NP <= kFuseMaxParts;
+    if (fuse) {
+        // the last CTA of each (sequence, KV head) combines its partials
+        prm.counters = reinterpret_cast<unsigned long long *>(ws + w.c_off);
+        prm.epoch = next_epoch();
+    }
+    st = launch_decode(r, prm, num_seqs, num_kv_heads, s);
+    if (st != PA_OK || num_seqs == 0 || fuse) return st;
+    ReduceParams rp;
+    rp.out = out;
+    rp.part_m = prm.part_m;
+    rp.part_l = prm.part_l;
+    rp.part_o = prm.part_o;
+    rp.seq_lens = seq_lens;
+    rp.err = prm.err;
+    rp.num_seqs = num_seqs;
+    rp.num_q_heads = num_q_heads;
+    rp.max_seq_len = max_seq_len < max_blocks_per_seq * block_size
+                         ? max_seq_len
+                         : max_blocks_per_seq * block_size;
+    rp.partition_tokens = r.P;
+    rp.num_partitions = r.NP;
+    rp.skip_single = 1;
+    const int64_t rows = (int64_t)num_seqs * num_q_heads;
+    const unsigned blocks = (unsigned)((rows + kReduceWarps - 1) / kReduceWarps);
+    if (launch_pdl(pick_reduce(dtype, head_dim), dim3(blocks), dim3(kReduceWarps * 32), 0, s,
+                   rp) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -859,7 +963,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                 partition_tokens, dtype, &r) != PA_OK)
         return 0;
     if (r.P <= 0) return 0;
-    return workspace_layout(num_seqs, num_q_heads, head_dim, r.NP).bytes;
+    return workspace_layout(num_seqs, num_q_heads, head_dim, r.NP, num_kv_heads).bytes;
 }
 
 pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_pool,
@@ -868,54 +972,24 @@ pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_
                     int num_kv_heads, int head_dim, int block_size, float scale,
                     int partition_tokens, void *workspace, size_t workspace_bytes,
                     pa_dtype dtype, void *stream) {
-    ResolvedDecode r;
-    pa_status st = resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                           max_seq_len, partition_tokens, dtype, &r);
-    if (st != PA_OK) return st;
-    if (num_seqs > 0 && (!out || !aligned16(out))) return PA_ERR_INVALID;
-    DecodeParams prm;
-    st = fill_common(&prm, q, k_pool, v_pool, num_blocks, block_tables, max_blocks_per_seq,
-                     seq_lens, max_seq_len, num_seqs, num_q_heads, num_kv_heads, block_size,
-                     scale);
-    if (st != PA_OK) return st;
-    prm.out = out;
-    prm.mode = 0;
-    cudaStream_t s = as_stream(stream);
-    if (r.P <= 0) {
-        prm.partition_tokens = kSinglePassTokens;
-        prm.num_partitions = 1;
-        return launch_decode(r, prm, num_seqs, num_kv_heads, s);
-    }
-    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, r.NP);
-    if (!workspace || workspace_bytes < w.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
-        return PA_ERR_INVALID;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    prm.part_m = reinterpret_cast<float *>(ws + w.m_off);
-    prm.part_l = reinterpret_cast<float *>(ws + w.l_off);
-    prm.part_o = reinterpret_cast<float *>(ws + w.o_off);
-    prm.partition_tokens = r.P;
-    prm.num_partitions = r.NP;
-    st = launch_decode(r, prm, num_seqs, num_kv_heads, s);
-    if (st != PA_OK || num_seqs == 0) return st;
-    ReduceParams rp;
-    rp.out = out;
-    rp.part_m = prm.part_m;
-    rp.part_l = prm.part_l;
-    rp.part_o = prm.part_o;
-    rp.seq_lens = seq_lens;
-    rp.err = prm.err;
-    rp.num_seqs = num_seqs;
-    rp.num_q_heads = num_q_heads;
-    rp.max_seq_len = max_seq_len < max_blocks_per_seq * block_size
-                         ? max_seq_len
-                         : max_blocks_per_seq * block_size;
-    rp.partition_tokens = r.P;
-    rp.num_partitions = r.NP;
-    rp.skip_single = 1;
-    const int64_t rows = (int64_t)num_seqs * num_q_heads;
-    const unsigned blocks = (unsigned)((rows + kReduceWarps - 1) / kReduceWarps);
-    pick_reduce(dtype, head_dim)<<<blocks, kReduceWarps * 32, 0, s>>>(rp);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return decode_impl(out, q, nullptr, nullptr, nullptr, k_pool, v_pool, num_blocks,
+                       block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_tokens,
+                       workspace, workspace_bytes, dtype, stream);
+}
+
+pa_status pa_decode_step(void *out, const void *q, const void *k_new, const void *v_new,
+                         const int64_t *slot_mapping, void *k_pool, void *v_pool, int num_blocks,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *seq_lens, int max_seq_len, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, float scale,
+                         int partition_tokens, void *workspace, size_t workspace_bytes,
+                         pa_dtype dtype, void *stream) {
+    if (num_seqs > 0 && !k_new) return PA_ERR_INVALID;
+    return decode_impl(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, num_blocks,
+                       block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_tokens,
+                       workspace, workspace_bytes, dtype, stream);
 }
 
 pa_status pa_decode_partitions(const void *q, const void *k_pool, const void *v_pool,
@@ -935,7 +1009,7 @@ pa_status pa_decode_partitions(const void *q, const void *k_pool, const void *v_
                      seq_lens, max_seq_len, num_seqs, num_q_heads, num_kv_heads, block_size,
                      scale);
     if (st != PA_OK) return st;
-    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, r.NP);
+    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, r.NP, num_kv_heads);
     if (num_seqs > 0 &&
         (!workspace || workspace_bytes < w.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255)))
         return PA_ERR_INVALID;
@@ -960,7 +1034,7 @@ pa_status pa_split_kv_reduce(void *out, const void *workspace, size_t workspace_
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     const int NP = max_seq_len > 0 ? (max_seq_len + partition_tokens - 1) / partition_tokens : 1;
-    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, NP);
+    const WorkspaceLayout w = workspace_layout(num_seqs, num_q_heads, head_dim, NP, 0);
     if (!out || !seq_lens || !workspace || workspace_bytes < w.bytes ||
         (reinterpret_cast<uintptr_t>(workspace) & 255) || !aligned16(out))
         return PA_ERR_INVALID;
@@ -999,7 +1073,7 @@ pa_status pa_decode_static_scratch(void *out, const void *q, const void *k_pool,
                            max_seq_len, partition_tokens, dtype, &r);
     if (st != PA_OK) return st;
     const size_t need =
-        r.P > 0 ? workspace_layout(num_seqs, num_q_heads, head_dim, r.NP).bytes : 0;
+        r.P > 0 ? workspace_layout(num_seqs, num_q_heads, head_dim, r.NP, num_kv_heads).bytes : 0;
     if (need > PA_STATIC_SCRATCH_BYTES) return PA_ERR_TOO_LARGE;
     void *scratch = nullptr;
     if (need > 0) {

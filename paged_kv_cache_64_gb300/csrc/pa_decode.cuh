@@ -4,6 +4,8 @@
 
 #include <stdint.h>
 
+#include <utility>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -36,6 +38,13 @@ struct DecodeParams {
     int num_partitions;          // NP (grid.x)
     float scale_log2;            // scale * log2(e)
     int mode;                    // 0: decode (direct output when 1 partition), 1: partials only
+    // Fused cache write of each sequence's newest token (pa_decode_step), or nullptr.
+    const uint16_t *k_new;       // [S][Hkv][D]
+    const uint16_t *v_new;
+    const int64_t *slot_mapping; // [S]
+    // Fused split-KV combine: one arrival counter per (sequence, KV head), or nullptr.
+    unsigned long long *counters;
+    unsigned int epoch;          // tag of this call in the counters
 };
 
 // Length of sequence i, clamped to what the launch covers; a value out of
@@ -49,6 +58,134 @@ __device__ __forceinline__ int checked_len(const int32_t *seq_lens, int i, int m
         L = L < 0 ? 0 : cap;
     }
     return L;
+}
+
+// Programmatic dependent launch: wait for the previous kernel on the stream
+// (and its memory) before touching global memory; let the next one start its
+// prologue once this one is past its main loop.  No-ops without the launch
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Fused cache write (pa_decode_step): the CTA that owns the newest position
+// L-1 of (seq, kvh) first writes that token's K and V into its slot, so the
+// copies it issues afterwards read it.  The slot must be the one the block
+// table gives for position L-1; otherwise nothing is written and a bad index
+// is recorded.  Threads [0, D/4) take one 16-byte piece each; the caller
+// synchronises the CTA before its copies start.
+template <int D>
+__device__ __forceinline__ void fused_cache_write(const DecodeParams &p, int seq, int kvh, int L) {
+    constexpr int pieces = D / 8;
+    const int t = threadIdx.x;
+    if (t >= 2 * pieces) return;
+    const int pos = L - 1;
+    const int phys = p.block_tables[(int64_t)seq * p.max_blocks_per_seq + (pos >> p.log2_block)];
+    const int off = pos & (p.block_size - 1);
+    const int64_t slot = p.slot_mapping[seq];
+    if ((unsigned)phys >= (unsigned)p.num_blocks || slot != (int64_t)phys * p.block_size + off) {
+        if (t == 0) record_error(p.err, PA_ERR_BAD_INDEX);
+        return;
+    }
+    const bool is_v = t >= pieces;
+    const int c = t % pieces;
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+                           (is_v ? p.v_new : p.k_new) + ((int64_t)seq * p.num_kv_heads + kvh) * D) +
+                       c;
+    uint4 *dst = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(is_v ? p.v_pool : p.k_pool) +
+                                           (((int64_t)phys * p.num_kv_heads + kvh) * p.block_size +
+                                            off) * D) +
+                 c;
+    *dst = *src;
+    // make the generic-proxy store visible to the bulk-copy (async) proxy
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+constexpr int kFuseMaxParts = 8;  // combine inside the decode kernel up to this many partitions
+
+// Epoch-tagged arrival counter of the fused combine: true in exactly one CTA,
+// the last of `expected` to arrive in this call.  The count is kept under the
+// call's epoch (a stale or garbage word reads as zero) and is reset by the
+// last arrival, so graph replays of one call start from zero again.
+__device__ __forceinline__ bool arrive_last(unsigned long long *ctr, unsigned int epoch,
+                                            int expected, int *err) {
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(ctr);
+    for (int it = 0; it < (1 << 16); ++it) {
+        const unsigned long long cnt = ((old >> 32) == epoch) ? (old & 0xffffffffull) : 0ull;
+        const unsigned long long nv = ((unsigned long long)epoch << 32) | (cnt + 1);
+        const unsigned long long prev = atomicCAS(ctr, old, nv);
+        if (prev == old) {
+            if (cnt + 1 == (unsigned long long)expected) {
+                atomicExch(ctr, (unsigned long long)epoch << 32);
+                return true;
+            }
+            return false;
+        }
+        old = prev;
+    }
+    record_error(err, PA_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+
+// Split-KV step 3 inside the last CTA of (seq, kvh): for its G heads,
+// M = max_k m_k, w_k = l_k 2^(m_k - M) / sum, out = sum_k w_k O_k.  All
+// `nthreads` threads of the CTA call it; wsm holds 8 * kFuseMaxParts floats
+// of shared memory.
+template <bool BF16, int D>
+__device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, float *wsm,
+                              int nthreads) {
+    const int G = p.group;
+    const int tid = threadIdx.x;
+    if (tid < G) {
+        const int64_t row = ((int64_t)seq * p.num_q_heads + kvh * G + tid) * p.num_partitions;
+        float M = -INFINITY;
+        for (int k = 0; k < np; ++k) M = fmaxf(M, __ldcg(p.part_m + row + k));
+        float tot = 0.f;
+        for (int k = 0; k < np; ++k) {
+            const float mk = __ldcg(p.part_m + row + k);
+            const float w = (mk == -INFINITY) ? 0.f : __ldcg(p.part_l + row + k) * fast_exp2(mk - M);
+            wsm[tid * kFuseMaxParts + k] = w;
+            tot += w;
+        }
+        const float inv = tot > 0.f ? 1.0f / tot : 0.f;
+        for (int k = 0; k < np; ++k) wsm[tid * kFuseMaxParts + k] *= inv;
+    }
+    __syncthreads();
+    for (int item = tid; item < G * (D / 8); item += nthreads) {
+        const int g = item / (D / 8);
+        const int x0 = (item % (D / 8)) * 8;
+        const int64_t row = ((int64_t)seq * p.num_q_heads + kvh * G + g) * p.num_partitions;
+        float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < np; ++k) {
+            const float w = wsm[g * kFuseMaxParts + k];
+            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (row + k) * D + x0);
+            const float4 a = __ldcg(src), b = __ldcg(src + 1);
+            o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
+            o[4] += w * b.x; o[5] += w * b.y; o[6] += w * b.z; o[7] += w * b.w;
+        }
+        uint16_t *out = static_cast<uint16_t *>(p.out) +
+                        ((int64_t)seq * p.num_q_heads + kvh * G + g) * D + x0;
+        *reinterpret_cast<uint4 *>(out) = make_uint4(narrow2<BF16>(o[0], o[1]), narrow2<BF16>(o[2], o[3]),
+                                                     narrow2<BF16>(o[4], o[5]), narrow2<BF16>(o[6], o[7]));
+    }
+}
+
+// Kernel launch with programmatic stream serialization allowed (PDL).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Tensor-core decode (pa_decode_tc.cu).

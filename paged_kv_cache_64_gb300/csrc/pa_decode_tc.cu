@@ -201,6 +201,7 @@ __global__ void __launch_bounds__(kTcThreads)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
     const int P = p.partition_tokens;
+    pdl_wait();  // inputs may come from the previous kernel on the stream
     const int L = checked_len(p.seq_lens, seq, p.max_seq_len, p.max_blocks_per_seq * p.block_size,
                               p.err, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
@@ -230,6 +231,7 @@ __global__ void __launch_bounds__(kTcThreads)
     const int ntiles = (end - start + kTcTile - 1) / kTcTile;
     const bool direct = (p.mode == 0) && (nparts_seq <= 1);
 
+    if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write<D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
         const int counts[kNumTcBars] = {1, 1, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4};
         for (int b = 0; b < kNumTcBars; ++b) mbar_init(&bar[b], counts[b]);
@@ -518,6 +520,7 @@ __global__ void __launch_bounds__(kTcThreads)
         }
     }
 
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) {
@@ -531,6 +534,20 @@ __global__ void __launch_bounds__(kTcThreads)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTcCols);
+    }
+    if (!direct && p.counters != nullptr && !*abort_flag) {
+        __shared__ int last_flag;
+        __shared__ float wsm[8 * kFuseMaxParts];
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0)
+            last_flag = arrive_last(p.counters + (int64_t)seq * p.num_kv_heads + kvh, p.epoch,
+                                    nparts_seq, p.err);
+        __syncthreads();
+        if (last_flag) {
+            __threadfence();
+            fused_combine<BF16, D>(p, seq, kvh, nparts_seq, wsm, blockDim.x);
+        }
     }
 }
 
@@ -584,13 +601,31 @@ bool tc_supported(int head_dim, int group) {
     return (head_dim == 64 || head_dim == 128) && group >= 1 && group <= kTcG;
 }
 
+// Resident CTAs per SM, from the kernel's own footprint: the runtime's
+// occupancy query answers 1 for kernels that allocate TMEM, while the
+// hardware co-schedules as many as registers and shared memory allow (the 64
+// TMEM columns of a CTA are 1/8 of an SM's).  A warp's registers come from one
+// of the 4 sub-partitions (16K registers each).
 int tc_ctas_per_sm(bool bf16, int head_dim) {
     int smem = 0;
     TcKernel k = pick_tc(bf16, head_dim, &smem);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kTcThreads, smem) != cudaSuccess)
+    int dev = 0, smem_sm = 0, reserved = 0;
+    cudaFuncAttributes a;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess ||
+        cudaFuncGetAttributes(&a, k) != cudaSuccess)
         return 1;
+    const int by_smem = smem_sm / (smem + reserved);
+    const int regs = (a.numRegs + 7) / 8 * 8;
+    const int warps_per_subpartition = 16384 / (regs * 32);
+    const int by_regs = 4 * warps_per_subpartition / kTcWarps;
+    const int by_tmem = 512 / kTcCols;
+    int n = by_smem < by_regs ? by_smem : by_regs;
+    n = n < by_tmem ? n : by_tmem;
     return n > 0 ? n : 1;
 }
 
@@ -606,7 +641,8 @@ pa_status launch_decode_tc(const DecodeParams &prm, bool bf16, int head_dim, int
         !pool_tensor_map(&mv, prm.v_pool, rows, head_dim, bf16))
         return PA_ERR_CUDA;
     dim3 grid((unsigned)num_partitions, (unsigned)num_kv_heads, (unsigned)num_seqs);
-    k<<<grid, kTcThreads, smem, stream>>>(prm, mk, mv);
+    if (launch_pdl(k, grid, dim3(kTcThreads), (size_t)smem, stream, prm, mk, mv) != cudaSuccess)
+        return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

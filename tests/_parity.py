@@ -103,6 +103,24 @@ class Case:
             api.cache_write(self.vals.k_pre[layer], self.vals.v_pre[layer], self.pre_slots, kp, vp)
         api.cache_write(self.vals.k_new[layer], self.vals.v_new[layer], self.slots, kp, vp)
 
+    def gpu_pre_writes(self, layer):
+        kp, vp = self.vals.k_pools[layer], self.vals.v_pools[layer]
+        if self.pre_copies.numel():
+            api.copy_blocks([kp], [vp], self.pre_copies)
+        if self.pre_slots.numel():
+            api.cache_write(self.vals.k_pre[layer], self.vals.v_pre[layer], self.pre_slots, kp, vp)
+
+    def gpu_step_fused(self, layer, partition=None, workspace=None):
+        """Copies and earlier writes, then the fused write + decode launch."""
+        P = self.spec.partition_tokens if partition is None else partition
+        self.gpu_pre_writes(layer)
+        out = torch.empty_like(self.vals.q)
+        api.decode_step(out, self.vals.q, self.vals.k_new[layer], self.vals.v_new[layer],
+                        self.slots, self.vals.k_pools[layer], self.vals.v_pools[layer],
+                        self.tables, self.lens, self.max_seq_len, self.plan.scale,
+                        partition_tokens=P, workspace=workspace)
+        return out
+
     def gpu_decode(self, layer, partition=None, workspace=None):
         P = self.spec.partition_tokens if partition is None else partition
         out = torch.empty_like(self.vals.q)

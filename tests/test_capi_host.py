@@ -81,12 +81,12 @@ def test_validation_before_launch(lib):
 
 def test_workspace_size_layout(lib):
     # explicit partition: m, l (256-aligned) then O
-    S, hq, d, maxlen, P = 3, 8, 128, 1000, 256
+    S, hq, hkv, d, maxlen, P = 3, 8, 2, 128, 1000, 256
     NP = 4
     rows = S * hq * NP
     a = lambda x: (x + 255) // 256 * 256
-    want = a(rows * 4) * 2 + a(rows * d * 4)
-    assert lib.pa_decode_workspace_size(S, hq, 2, d, 16, maxlen, P, 1) == want
+    want = a(rows * 4) * 2 + a(rows * d * 4) + a(S * hkv * 8)  # + one counter per (seq, kv head)
+    assert lib.pa_decode_workspace_size(S, hq, hkv, d, 16, maxlen, P, 1) == want
     assert lib.pa_decode_workspace_size(S, hq, 2, d, 16, maxlen, -1, 1) == 0
 
 

@@ -272,6 +272,77 @@ def test_decode_on_side_stream_and_repeat_deterministic():
     api.check_error()
 
 
+# ------------------------------------------------ fused write + decode
+@pytest.mark.parametrize("name,kw,partition", [
+    ("tiny", {}, None), ("tiny", {}, 16),
+    ("qwen", {"num_seqs": 24}, None),
+    ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, 512),
+    ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, 128),
+    ("prefix", {"num_seqs": 6, "cow": True}, None),
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, None),
+])
+def test_decode_step_fused_matches_oracle(name, kw, partition):
+    """pa_decode_step (new token written inside the decode launch, and the
+    split-KV combine inside it when a sequence has <= 8 partitions) against
+    the oracle's cache write + decode; the pools afterwards are bit-exact."""
+    case = Case(workloads.make_plan(name, **kw))
+    hk, hv = case.snapshot(0)
+    out = case.gpu_step_fused(0, partition)
+    ref = case.oracle_step(0, hk, hv)
+    api.check_error()
+    assert_close(out, ref, f"fused step {name}")
+    assert np.array_equal(bits(case.vals.k_pools[0]), hk)
+    assert np.array_equal(bits(case.vals.v_pools[0]), hv)
+
+
+def test_fused_combine_garbage_workspace_and_graph_replay():
+    """The fused combine's counters need no initialisation (garbage
+    workspace), and a CUDA graph of the step replays correctly (each replay
+    reuses the captured epoch; the last CTA resets the count)."""
+    case = Case(workloads.make_plan("llama", num_seqs=6, len_range=(900, 2100)))
+    spec, P = case.spec, 512
+    size = api.workspace_size(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                              spec.block_size, case.max_seq_len, P, case.dtype)
+    ws = api.alloc_workspace(size, "cuda")
+    ws.fill_(0xFF)
+    hk, hv = case.snapshot(0)
+    case.gpu_writes(0)
+    ref = case.oracle_step(0, hk, hv)
+    out = torch.empty_like(case.vals.q)
+    api.decode(out, case.vals.q, case.vals.k_pools[0], case.vals.v_pools[0], case.tables,
+               case.lens, case.max_seq_len, case.plan.scale, partition_tokens=P, workspace=ws)
+    api.check_error()
+    assert_close(out, ref, "garbage workspace")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g):
+            api.decode(out, case.vals.q, case.vals.k_pools[0], case.vals.v_pools[0],
+                       case.tables, case.lens, case.max_seq_len, case.plan.scale,
+                       partition_tokens=P, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(out, ref, "graph replay")
+    api.check_error()
+
+
+def test_decode_step_rejects_a_slot_off_the_table():
+    case = Case(workloads.make_plan("tiny"))
+    bad = case.slots.clone()
+    bad[2] += 1  # not the slot of position L-1
+    out = torch.empty_like(case.vals.q)
+    api.decode_step(out, case.vals.q, case.vals.k_new[0], case.vals.v_new[0], bad,
+                    case.vals.k_pools[0], case.vals.v_pools[0], case.tables, case.lens,
+                    case.max_seq_len, case.plan.scale)
+    with pytest.raises(_lib.PagedAttentionError) as e:
+        api.check_error()
+    assert e.value.code == 6
+
+
 # -------------------------------------------------------- split-KV steps
 @pytest.mark.parametrize("name,kw,P", [("long", {"num_seqs": 2, "len_range": (1500, 2600)}, 512),
                                        ("tiny", {}, 16),

@@ -143,6 +143,22 @@ def test_tc_partitions_match_oracle():
     assert (err <= 2e-3 + 1e-2 * np.abs(ro[ok])).all(), float(err.max())
 
 
+@pytest.mark.parametrize("name,kw,partition", [
+    ("qwen", {"num_seqs": 24}, None),
+    ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, 512),
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, None),
+    ("tiny", {}, 16),
+])
+def test_tc_decode_step_fused(name, kw, partition):
+    case = Case(workloads.make_plan(name, **kw))
+    hk, hv = case.snapshot(0)
+    out = case.gpu_step_fused(0, partition)
+    ref = case.oracle_step(0, hk, hv)
+    api.check_error()
+    assert_close(out, ref, f"tc fused step {name}")
+    assert np.array_equal(bits(case.vals.k_pools[0]), hk)
+
+
 def test_tc_matches_cuda_core_kernel():
     """Both kernels on the same inputs agree within the output tolerance."""
     case = Case(workloads.make_plan("long", num_seqs=4, len_range=(2000, 9000)))
