@@ -138,7 +138,7 @@ def source_digest():
     """Hash of the decode kernel source, to tell whether a stored ncu traffic
     figure still describes the kernel being timed."""
     h = hashlib.sha256()
-    for f in ("pa_decode.cu", "pa_common.cuh"):
+    for f in ("pa_decode.cu", "pa_decode_tc.cu", "pa_decode.cuh", "pa_common.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_64_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

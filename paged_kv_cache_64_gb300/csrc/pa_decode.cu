@@ -725,7 +725,7 @@ static int decode_ctas_per_sm(const DecodeEntry &e) {
 
 // Automatic partition size: aim for the largest work item to be at most
 // 1/32 of one CTA slot's share of the whole job (taking the average length
-// as half the maximum), in multiples of 256 positions, and run single pass
+// as half the maximum), in multiples of 256 positions and at least 512, and run single pass
 // when that would not split anything.
 static int auto_partition(int S, int Hkv, int max_seq_len, int ctas_per_sm, int block_size) {
     if (max_seq_len <= 0) return -1;
@@ -733,7 +733,7 @@ static int auto_partition(int S, int Hkv, int max_seq_len, int ctas_per_sm, int 
     const double units = (double)S * Hkv;
     double target = (double)max_seq_len * units / (32.0 * (slots > 0 ? slots : 1));
     int P = (int)std::ceil(target / 256.0) * 256;
-    if (P < 256) P = 256;
+    if (P < 512) P = 512;
     if (P % block_size) P = (P / block_size + 1) * block_size;
     if (P >= max_seq_len) return -1;
     return P;
@@ -819,6 +819,7 @@ static pa_status fill_common(DecodeParams *prm, const void *q, const void *k_poo
     prm->v_pool = static_cast<const uint16_t *>(v_pool);
     prm->block_tables = block_tables;
     prm->seq_lens = seq_lens;
+    prm->num_seqs = num_seqs;
     prm->num_blocks = num_blocks;
     prm->max_blocks_per_seq = max_blocks_per_seq;
     prm->max_seq_len = max_seq_len;

@@ -26,6 +26,7 @@ struct DecodeParams {
     float *part_l;               // [S][Hq][NP]
     float *part_o;               // [S][Hq][NP][D]
     int *err;
+    int num_seqs;
     int num_blocks;
     int max_blocks_per_seq;
     int max_seq_len;
