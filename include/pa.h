@@ -187,6 +187,53 @@ pa_status pa_decode_step(void *out, const void *q, const void *k_new, const void
                          int partition_tokens, void *workspace, size_t workspace_bytes,
                          pa_dtype dtype, void *stream);
 
+/* ------------------------------------------------------------------------
+ * pa_decode_cascade: pa_decode (or, with k_new != NULL, pa_decode_step) for
+ * a batch whose sequences share a prefix, computed as a cascade.  The result
+ * is the same attention as pa_decode's (within the output tolerance).
+ *
+ * Sequences forked from one prompt point the first entries of their block
+ * tables at the same physical blocks ([P1] "The same trick for the cache";
+ * [P2] "Sharing a prefix with copy-on-write"; [P3] section 5, page-table
+ * duplication on a fork).  With P = prefix_len positions (a whole number of
+ * blocks) shared by every sequence of the batch:
+ *   1. prefix pass: for each KV head, the q rows of ALL sequences of its
+ *      group attend to positions [0, P) once, as dense products on the
+ *      tensor cores (tcgen05), reading the shared blocks through sequence
+ *      0's table; the positions are cut into chunks, each leaving a partial
+ *      (m, l, O) per (sequence, query head) in the workspace;
+ *   2. tail pass: each sequence attends to its own positions [P, L_i)
+ *      (through table entries P/B onwards), as pa_decode does, writes that
+ *      partial next to the prefix's, and combines all of them with the
+ *      split-KV log-sum-exp merge ([P3] section 4, Parallel Partitioning,
+ *      step 3).  softmax over [0, L_i) equals that merge of the two ranges.
+ * Requirements (checked on the device, PA_ERR_BAD_INDEX when violated, the
+ * output then being unspecified): for every sequence i, seq_lens[i] >= P and
+ * block_tables[i][b] == block_tables[0][b] for b < P / block_size.
+ * prefix_len must be a multiple of block_size, <= max_seq_len and
+ * <= max_blocks_per_seq*block_size (else PA_ERR_INVALID); prefix_len = 0
+ * is plain pa_decode / pa_decode_step with partition_tokens = 0.
+ * k_new, v_new, slot_mapping: NULL for a plain decode, or the newest tokens
+ * as in pa_decode_step (their positions lie in the tails).
+ * workspace: pa_decode_cascade_workspace_size(...) bytes of device memory,
+ * 256-byte aligned, scratch (no initialisation needed).  Other arguments as
+ * pa_decode.
+ * ---------------------------------------------------------------------- */
+pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, const void *v_new,
+                            const int64_t *slot_mapping, void *k_pool, void *v_pool,
+                            int num_blocks, const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *seq_lens, int max_seq_len, int num_seqs,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            float scale, int prefix_len, void *workspace, size_t workspace_bytes,
+                            pa_dtype dtype, void *stream);
+
+/* Bytes of workspace pa_decode_cascade needs for these shapes on the current
+ * CUDA device (the prefix chunking follows its SM count); 0 for invalid
+ * arguments. */
+size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int max_seq_len,
+                                        int prefix_len, pa_dtype dtype);
+
 /* Partition size pa_decode uses for these shapes when partition_tokens = 0
  * (-1 means it will run single pass).  Needs the current CUDA device. */
 int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,

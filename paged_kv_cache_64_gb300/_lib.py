@@ -43,6 +43,11 @@ SIGNATURES = {
     "pa_decode_step": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _vp,
                                 _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int, _vp,
                                 _c_sz, _c_int, _vp]),
+    "pa_decode_cascade": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int,
+                                   _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f,
+                                   _c_int, _vp, _c_sz, _c_int, _vp]),
+    "pa_decode_cascade_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                                 _c_int, _c_int]),
     "pa_decode_auto_partition": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           _c_int]),
     "pa_decode_ctas_per_sm": (_c_int, [_c_int, _c_int, _c_int]),

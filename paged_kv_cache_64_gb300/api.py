@@ -195,6 +195,47 @@ def decode_step(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables
     return workspace
 
 
+def cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_seq_len, prefix_len, dtype):
+    return _lib.load().pa_decode_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads,
+                                                        head_dim, block_size, max_seq_len,
+                                                        prefix_len, _DTYPES[dtype])
+
+
+def decode_cascade(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale,
+                   prefix_len, k_new=None, v_new=None, slot_mapping=None, workspace=None,
+                   stream=None):
+    """Decode of a batch whose sequences share their first prefix_len
+    positions (the same first prefix_len / block_size block-table entries):
+    the prefix is attended once per KV head for every sequence's queries,
+    each tail separately, and the two merged.  With k_new / v_new /
+    slot_mapping, each sequence's newest token is written first, as in
+    decode_step."""
+    S, hq, hkv, d, nb, bs = _decode_dims(q, k_pool, block_tables, seq_lens)
+    if out.shape != q.shape or out.dtype != q.dtype or k_pool.dtype != q.dtype:
+        raise ValueError("out/q/pool shapes or types differ")
+    step = k_new is not None
+    if step and (k_new.shape != (S, hkv, d) or v_new is None or v_new.shape != k_new.shape
+                 or slot_mapping is None or slot_mapping.shape != (S,)):
+        raise ValueError("k_new/v_new must be [S, Hkv, d] and slot_mapping [S]")
+    need = cascade_workspace_size(S, hq, hkv, d, bs, max_seq_len, prefix_len, q.dtype)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = alloc_workspace(need, q.device)
+    ws = _cuda(workspace, "workspace") if workspace is not None else ctypes.c_void_p(0)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    null = ctypes.c_void_p(0)
+    rc = _lib.load().pa_decode_cascade(
+        _cuda(out, "out"), _cuda(q, "q"), _cuda(k_new, "k_new") if step else null,
+        _cuda(v_new, "v_new") if step else null,
+        _cuda(slot_mapping, "slot_mapping", torch.int64) if step else null,
+        _cuda(k_pool, "k_pool"), _cuda(v_pool, "v_pool"), nb,
+        _cuda(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _cuda(seq_lens, "seq_lens", torch.int32), int(max_seq_len), S, hq, hkv, d, bs,
+        float(scale), int(prefix_len), ws, wbytes, _dt(q), _stream_handle(stream))
+    _lib.check("pa_decode_cascade", rc)
+    return workspace
+
+
 def decode_static_scratch(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale,
                           partition_tokens=0, stream=None):
     """Same result as decode(), for callers that cannot allocate device

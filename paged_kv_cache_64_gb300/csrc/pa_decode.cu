@@ -172,9 +172,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
     const int P = p.partition_tokens;
 
     pdl_wait();  // inputs may come from the previous kernel on the stream
-    const int L = checked_len(p.seq_lens, seq, p.max_seq_len,
-                              p.max_blocks_per_seq * p.block_size, p.err,
-                              threadIdx.x == 0 && part == 0 && kvh == 0);
+    const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
     const int start = part * P;
 
@@ -190,13 +188,16 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
             }
         } else {
             for (int g = 0; g < G; ++g) {
-                const int64_t row = ((int64_t)seq * p.num_q_heads + kvh * G + g) * p.num_partitions + part;
+                const int64_t row = part_row(p, seq, kvh * G + g, part);
                 if (threadIdx.x == 0) {
                     p.part_m[row] = -INFINITY;
                     p.part_l[row] = 0.f;
                 }
                 for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
             }
+            // empty cascade tail: the output is the prefix's partials combined
+            if (p.prefix_parts > 0 && nparts_seq == 0 && part == 0)
+                finish_item<BF16, D>(p, seq, kvh, 0);
         }
         return;
     }
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
         const int64_t tile_elems = (int64_t)kUnit * D;
         const int64_t head_elems = (int64_t)p.block_size * D;
         const int64_t block_elems = (int64_t)p.num_kv_heads * head_elems;
-        const int32_t *table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
+        const int32_t *table = seq_table(p, seq);
         bool ok = true;
         for (int u0 = 0; u0 < nunits && ok; u0 += 32) {
             const int u = u0 + lane;
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
             uint16_t *out = static_cast<uint16_t *>(p.out);
             *reinterpret_cast<uint4 *>(out + ((int64_t)seq * p.num_q_heads + h) * D + x0) = packed;
         } else {
-            const int64_t row = ((int64_t)seq * p.num_q_heads + h) * p.num_partitions + part;
+            const int64_t row = part_row(p, seq, h, part);
             if (x0 == 0) {
                 p.part_m[row] = MT;
                 p.part_l[row] = lsum * fast_exp2(M - MT);
@@ -554,20 +555,8 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
             dst[1] = make_float4(o[4], o[5], o[6], o[7]);
         }
     }
-    if (!direct && p.counters != nullptr) {
-        __shared__ int last_flag;
-        __shared__ float wsm[8 * kFuseMaxParts];
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0)
-            last_flag = arrive_last(p.counters + (int64_t)seq * p.num_kv_heads + kvh, p.epoch,
-                                    nparts_seq, p.err);
-        __syncthreads();
-        if (last_flag) {
-            __threadfence();
-            fused_combine<BF16, D>(p, seq, kvh, nparts_seq, wsm, blockDim.x);
-        }
-    }
+    if (!direct && (p.counters != nullptr || p.prefix_parts > 0))
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq);
 }
 
 // ------------------------------------------------------------------ reduce
@@ -792,11 +781,12 @@ static pa_status launch_decode(const ResolvedDecode &r, DecodeParams prm, int nu
                                int num_kv_heads, cudaStream_t stream) {
     if (num_seqs == 0) return PA_OK;
     if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_INVALID;
+    if (prm.ws_parts == 0) prm.ws_parts = prm.num_partitions;  // plain launch: own workspace
+    if (!prm.out && (prm.mode == 0 || prm.counters || prm.prefix_parts)) return PA_ERR_INVALID;
     if (r.tc)
         return launch_decode_tc(prm, r.bf16, r.head_dim, r.NP, num_kv_heads, num_seqs, stream);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(r.entry.fn), r.entry.smem))
         return PA_ERR_CUDA;
-    if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_INVALID;
     dim3 grid((unsigned)r.NP, (unsigned)num_kv_heads, (unsigned)num_seqs);
     if (launch_pdl(r.entry.fn, grid, dim3(kDecodeThreads), (size_t)r.entry.smem, stream, prm) !=
         cudaSuccess)
@@ -926,6 +916,30 @@ static pa_status decode_impl(void *out, const void *q, const void *k_new, const 
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// Shared-prefix (cascade) decode: chunking of the prefix pass and the tail
+// launch (positions [prefix_len, L) of each sequence).
+struct CascadePlan {
+    ResolvedDecode tail;   // the tail launch (positions [prefix_len, L))
+    int chunk_tokens;
+    int num_chunks;
+    int ws_parts;          // num_chunks prefix slots + the tail's partitions
+};
+static pa_status cascade_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_seq_len, int prefix_len, pa_dtype dtype,
+                              CascadePlan *c) {
+    if (prefix_len <= 0 || max_seq_len < prefix_len || block_size <= 0 ||
+        prefix_len % block_size)
+        return PA_ERR_INVALID;
+    pa_status st = resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_seq_len - prefix_len, 0, dtype, &c->tail);
+    if (st != PA_OK) return st;
+    const int G = num_q_heads / num_kv_heads;
+    c->chunk_tokens = cascade_chunk_tokens(prefix_len, num_seqs * G, num_kv_heads);
+    c->num_chunks = (prefix_len + c->chunk_tokens - 1) / c->chunk_tokens;
+    c->ws_parts = c->num_chunks + c->tail.NP;
+    return PA_OK;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -991,6 +1005,102 @@ pa_status pa_decode_step(void *out, const void *q, const void *k_new, const void
                        block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
                        num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_tokens,
                        workspace, workspace_bytes, dtype, stream);
+}
+
+
+size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int max_seq_len,
+                                        int prefix_len, pa_dtype dtype) {
+    if (prefix_len == 0)
+        return pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                        block_size, max_seq_len, 0, dtype);
+    CascadePlan c;
+    if (cascade_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                     prefix_len, dtype, &c) != PA_OK)
+        return 0;
+    return workspace_layout(num_seqs, num_q_heads, head_dim, c.ws_parts, num_kv_heads).bytes;
+}
+
+pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, const void *v_new,
+                            const int64_t *slot_mapping, void *k_pool, void *v_pool,
+                            int num_blocks, const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *seq_lens, int max_seq_len, int num_seqs,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            float scale, int prefix_len, void *workspace, size_t workspace_bytes,
+                            pa_dtype dtype, void *stream) {
+    if (prefix_len == 0)
+        return decode_impl(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, num_blocks,
+                           block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
+                           num_q_heads, num_kv_heads, head_dim, block_size, scale, 0, workspace,
+                           workspace_bytes, dtype, stream);
+    CascadePlan c;
+    pa_status st = cascade_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                max_seq_len, prefix_len, dtype, &c);
+    if (st != PA_OK) return st;
+    if (prefix_len > max_blocks_per_seq * block_size) return PA_ERR_INVALID;
+    if (num_seqs > 0 && (!out || !aligned16(out))) return PA_ERR_INVALID;
+    DecodeParams prm;
+    st = fill_common(&prm, q, k_pool, v_pool, num_blocks, block_tables, max_blocks_per_seq,
+                     seq_lens, max_seq_len, num_seqs, num_q_heads, num_kv_heads, block_size,
+                     scale);
+    if (st != PA_OK) return st;
+    prm.out = out;
+    if (k_new) {
+        if (num_seqs > 0 && (!v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)))
+            return PA_ERR_INVALID;
+        prm.k_new = static_cast<const uint16_t *>(k_new);
+        prm.v_new = static_cast<const uint16_t *>(v_new);
+        prm.slot_mapping = slot_mapping;
+    }
+    const WorkspaceLayout w =
+        workspace_layout(num_seqs, num_q_heads, head_dim, c.ws_parts, num_kv_heads);
+    if (num_seqs > 0 &&
+        (!workspace || workspace_bytes < w.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255)))
+        return PA_ERR_INVALID;
+    if (num_seqs == 0) return PA_OK;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    prm.part_m = reinterpret_cast<float *>(ws + w.m_off);
+    prm.part_l = reinterpret_cast<float *>(ws + w.l_off);
+    prm.part_o = reinterpret_cast<float *>(ws + w.o_off);
+    cudaStream_t s = as_stream(stream);
+
+    CascadeParams cp;
+    cp.q = prm.q;
+    cp.block_tables = block_tables;
+    cp.seq_lens = seq_lens;
+    cp.part_m = prm.part_m;
+    cp.part_l = prm.part_l;
+    cp.part_o = prm.part_o;
+    cp.err = prm.err;
+    cp.num_seqs = num_seqs;
+    cp.num_q_heads = num_q_heads;
+    cp.num_kv_heads = num_kv_heads;
+    cp.group = prm.group;
+    cp.num_blocks = num_blocks;
+    cp.max_blocks_per_seq = max_blocks_per_seq;
+    cp.block_size = block_size;
+    cp.log2_block = prm.log2_block;
+    cp.prefix_len = prefix_len;
+    cp.chunk_tokens = c.chunk_tokens;
+    cp.num_chunks = c.num_chunks;
+    cp.ws_parts = c.ws_parts;
+    cp.scale_log2 = prm.scale_log2;
+    st = launch_cascade_prefix(cp, k_pool, v_pool, dtype == PA_BF16, head_dim, s);
+    if (st != PA_OK) return st;
+
+    prm.mode = 1;
+    prm.len_offset = prefix_len;
+    prm.table_offset = prefix_len / block_size;
+    prm.ws_parts = c.ws_parts;
+    prm.part_base = c.num_chunks;
+    prm.prefix_parts = c.num_chunks;
+    prm.partition_tokens = c.tail.P > 0 ? c.tail.P : kSinglePassTokens;
+    prm.num_partitions = c.tail.NP;
+    if (c.tail.NP > 1) {
+        prm.counters = reinterpret_cast<unsigned long long *>(ws + w.c_off);
+        prm.epoch = next_epoch();
+    }
+    return launch_decode(c.tail, prm, num_seqs, num_kv_heads, s);
 }
 
 pa_status pa_decode_partitions(const void *q, const void *k_pool, const void *v_pool,

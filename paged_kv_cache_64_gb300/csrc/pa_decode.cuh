@@ -46,6 +46,19 @@ struct DecodeParams {
     // Fused split-KV combine: one arrival counter per (sequence, KV head), or nullptr.
     unsigned long long *counters;
     unsigned int epoch;          // tag of this call in the counters
+    // Sub-range of each sequence (the tail of a cascade step): positions
+    // [len_offset, seq_lens[i]) read through block-table entries from
+    // table_offset on; partials go to slot part_base + part of a workspace laid
+    // out with ws_parts slots per (sequence, query head).
+    int len_offset;
+    int table_offset;
+    int ws_parts;
+    int part_base;
+    // Cascade tail: slots [0, prefix_parts) of each row already hold the
+    // shared prefix's partials (written by an earlier launch); the item's own
+    // partials follow at part_base == prefix_parts, and the CTA that finishes
+    // the item combines all of them into the output.
+    int prefix_parts;
 };
 
 // Length of sequence i, clamped to what the launch covers; a value out of
@@ -70,6 +83,32 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Length of the attended range of sequence `seq` (seq_lens minus
+// len_offset), clamped to what the launch and the block table cover; a value
+// out of range is a bad index.
+__device__ __forceinline__ int item_len(const DecodeParams &p, int seq, bool report) {
+    int L = p.seq_lens[seq] - p.len_offset;
+    const int table_cap = (p.max_blocks_per_seq - p.table_offset) * p.block_size;
+    int cap = p.max_seq_len - p.len_offset;
+    if (table_cap < cap) cap = table_cap;
+    if (cap < 0) cap = 0;
+    if (L < 0 || L > cap) {
+        if (report) record_error(p.err, PA_ERR_BAD_INDEX);
+        L = L < 0 ? 0 : cap;
+    }
+    return L;
+}
+
+// Block-table entries of the attended range of `seq`.
+__device__ __forceinline__ const int32_t *seq_table(const DecodeParams &p, int seq) {
+    return p.block_tables + (int64_t)seq * p.max_blocks_per_seq + p.table_offset;
+}
+
+// Workspace row of partial `part` of (seq, query head h).
+__device__ __forceinline__ int64_t part_row(const DecodeParams &p, int seq, int h, int part) {
+    return ((int64_t)seq * p.num_q_heads + h) * p.ws_parts + p.part_base + part;
+}
+
 // Fused cache write (pa_decode_step): the CTA that owns the newest position
 // L-1 of (seq, kvh) first writes that token's K and V into its slot, so the
 // copies it issues afterwards read it.  The slot must be the one the block
@@ -82,7 +121,7 @@ __device__ __forceinline__ void fused_cache_write(const DecodeParams &p, int seq
     const int t = threadIdx.x;
     if (t >= 2 * pieces) return;
     const int pos = L - 1;
-    const int phys = p.block_tables[(int64_t)seq * p.max_blocks_per_seq + (pos >> p.log2_block)];
+    const int phys = seq_table(p, seq)[pos >> p.log2_block];
     const int off = pos & (p.block_size - 1);
     const int64_t slot = p.slot_mapping[seq];
     if ((unsigned)phys >= (unsigned)p.num_blocks || slot != (int64_t)phys * p.block_size + off) {
@@ -129,37 +168,40 @@ __device__ __forceinline__ bool arrive_last(unsigned long long *ctr, unsigned in
     return false;
 }
 
-// Split-KV step 3 inside the last CTA of (seq, kvh): for its G heads,
-// M = max_k m_k, w_k = l_k 2^(m_k - M) / sum, out = sum_k w_k O_k.  All
-// `nthreads` threads of the CTA call it; wsm holds 8 * kFuseMaxParts floats
-// of shared memory.
+// Split-KV step 3 inside the CTA that finishes (seq, kvh): for each of its
+// G heads, over the slots [0, np) of the row, M = max_k m_k,
+// w_k = l_k 2^(m_k - M) / sum_j l_j 2^(m_j - M), out = sum_k w_k O_k.  All
+// `nthreads` threads of the CTA call it; wsm holds 2 * G floats of shared
+// memory.  Partials are read through L2 (they were written by other CTAs).
 template <bool BF16, int D>
 __device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, float *wsm,
                               int nthreads) {
     const int G = p.group;
     const int tid = threadIdx.x;
+    const int64_t row0 = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * p.ws_parts;
     if (tid < G) {
-        const int64_t row = ((int64_t)seq * p.num_q_heads + kvh * G + tid) * p.num_partitions;
+        const int64_t row = row0 + (int64_t)tid * p.ws_parts;
         float M = -INFINITY;
         for (int k = 0; k < np; ++k) M = fmaxf(M, __ldcg(p.part_m + row + k));
         float tot = 0.f;
         for (int k = 0; k < np; ++k) {
             const float mk = __ldcg(p.part_m + row + k);
-            const float w = (mk == -INFINITY) ? 0.f : __ldcg(p.part_l + row + k) * fast_exp2(mk - M);
-            wsm[tid * kFuseMaxParts + k] = w;
-            tot += w;
+            if (mk != -INFINITY) tot += __ldcg(p.part_l + row + k) * fast_exp2(mk - M);
         }
-        const float inv = tot > 0.f ? 1.0f / tot : 0.f;
-        for (int k = 0; k < np; ++k) wsm[tid * kFuseMaxParts + k] *= inv;
+        wsm[2 * tid] = M;
+        wsm[2 * tid + 1] = tot > 0.f ? 1.0f / tot : 0.f;
     }
     __syncthreads();
     for (int item = tid; item < G * (D / 8); item += nthreads) {
         const int g = item / (D / 8);
         const int x0 = (item % (D / 8)) * 8;
-        const int64_t row = ((int64_t)seq * p.num_q_heads + kvh * G + g) * p.num_partitions;
+        const int64_t row = row0 + (int64_t)g * p.ws_parts;
+        const float M = wsm[2 * g], inv = wsm[2 * g + 1];
         float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int k = 0; k < np; ++k) {
-            const float w = wsm[g * kFuseMaxParts + k];
+            const float mk = __ldcg(p.part_m + row + k);
+            if (mk == -INFINITY) continue;  // empty partial
+            const float w = __ldcg(p.part_l + row + k) * fast_exp2(mk - M) * inv;
             const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (row + k) * D + x0);
             const float4 a = __ldcg(src), b = __ldcg(src + 1);
             o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
@@ -169,6 +211,29 @@ __device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, f
                         ((int64_t)seq * p.num_q_heads + kvh * G + g) * D + x0;
         *reinterpret_cast<uint4 *>(out) = make_uint4(narrow2<BF16>(o[0], o[1]), narrow2<BF16>(o[2], o[3]),
                                                      narrow2<BF16>(o[4], o[5]), narrow2<BF16>(o[6], o[7]));
+    }
+}
+
+// End of a CTA that wrote partials of (seq, kvh): with arrival counters,
+// the last of the item's nparts_seq CTAs combines; a cascade tail of a single
+// partition (no counters), or an empty one, combines at once.  The combined slots are the
+// prefix's and the item's: [0, prefix_parts + nparts_seq).  Called by every
+// thread of the CTA.
+template <bool BF16, int D>
+__device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_seq) {
+    __shared__ int last_flag;
+    __shared__ float wsm[2 * 8];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        last_flag = (p.counters == nullptr || nparts_seq == 0)
+                        ? 1
+                        : arrive_last(p.counters + (int64_t)seq * p.num_kv_heads + kvh, p.epoch,
+                                      nparts_seq, p.err);
+    __syncthreads();
+    if (last_flag) {
+        __threadfence();
+        fused_combine<BF16, D>(p, seq, kvh, p.prefix_parts + nparts_seq, wsm, blockDim.x);
     }
 }
 
@@ -194,5 +259,39 @@ bool tc_supported(int head_dim, int group);
 int tc_ctas_per_sm(bool bf16, int head_dim);
 pa_status launch_decode_tc(const DecodeParams &prm, bool bf16, int head_dim, int num_partitions,
                            int num_kv_heads, int num_seqs, cudaStream_t stream);
+
+// Prefix pass of the shared-prefix (cascade) decode (pa_cascade.cu): the
+// positions [0, prefix_len) that every sequence reaches through the same
+// block-table entries (sequence 0's row gives them), attended once per KV
+// head by the query rows of all sequences.  Leaves the (m, l, O) partial of
+// chunk c of each (sequence, query head) in workspace slot c.
+struct CascadeParams {
+    const uint16_t *q;           // [S][Hq][D]
+    const int32_t *block_tables; // [S][max_blocks_per_seq]
+    const int32_t *seq_lens;     // [S] (checked: >= prefix_len)
+    float *part_m;               // [S][Hq][ws_parts]
+    float *part_l;
+    float *part_o;               // [S][Hq][ws_parts][D]
+    int *err;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int num_blocks;
+    int max_blocks_per_seq;
+    int block_size;
+    int log2_block;
+    int prefix_len;              // a multiple of block_size, > 0
+    int chunk_tokens;            // a multiple of 128
+    int num_chunks;
+    int ws_parts;
+    float scale_log2;
+};
+
+// Chunk length (a multiple of 128 positions) that spreads the prefix pass
+// over about one CTA per SM of the current device.
+int cascade_chunk_tokens(int prefix_len, int num_rows, int num_kv_heads);
+pa_status launch_cascade_prefix(const CascadeParams &cp, const void *k_pool, const void *v_pool,
+                                bool bf16, int head_dim, cudaStream_t stream);
 
 }  // namespace pa

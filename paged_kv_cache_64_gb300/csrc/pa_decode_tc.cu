@@ -39,6 +39,7 @@
 #include "pa_common.cuh"
 #include "pa_decode.cuh"
 #include "pa_internal.h"
+#include "pa_tcgen05.cuh"
 
 namespace pa {
 
@@ -76,114 +77,6 @@ struct TcShape {
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
 };
 
-// ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(slot)),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// D[tmem] (+)= A[smem desc] . B[smem desc], kind::f16 (f16 or bf16 in, f32 accumulate)
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive (once) on `bar` when every MMA this thread issued so far has completed.
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_addr(bar))
-        : "memory");
-}
-// 32 lanes x 16 columns of 32-bit TMEM cells: thread i gets lane (base + i).
-__device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-// 2-D TMA tensor copy (tile mode) global -> shared, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
-        "[%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-        : "memory");
-}
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void softmax_bar() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 layout):
-// start >> 4 at [0,14), leading byte offset >> 4 at [16,30), stride byte
-// offset >> 4 at [32,46), version 1 at [46,48), layout SWIZZLE_128B (2) at [61,64).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Instruction descriptor of kind::f16: f32 accumulator, A/B format
-// (0 = f16, 1 = bf16), A/B major (0 = K, 1 = MN), N >> 3, M >> 4.
-__host__ __device__ constexpr uint32_t f16_idesc(bool bf16, bool a_mn, bool b_mn, int M, int N) {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-           ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-
-// Byte offset of element (row, col) of a K-major operand stored as
-// 128-byte-swizzled atoms of 8 rows x 64 columns (16-bit elements): atoms
-// along the columns are `atom_stride` bytes apart, 8-row groups 1024 bytes.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int col, int atom_stride) {
-    const int chunk = (col & 63) >> 3;
-    return (uint32_t)((col >> 6) * atom_stride + (row >> 3) * 1024 + (row & 7) * 128 +
-                      ((chunk ^ (row & 7)) << 4) + (col & 7) * 2);
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint16_t narrow1(float x) {
-    if constexpr (BF16) {
-        __nv_bfloat16 h = __float2bfloat16_rn(x);
-        uint16_t u;
-        memcpy(&u, &h, 2);
-        return u;
-    } else {
-        __half h = __float2half_rn(x);
-        uint16_t u;
-        memcpy(&u, &h, 2);
-        return u;
-    }
-}
-
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kTcThreads)
     paged_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
@@ -202,8 +95,7 @@ __global__ void __launch_bounds__(kTcThreads)
     const int G = p.group;
     const int P = p.partition_tokens;
     pdl_wait();  // inputs may come from the previous kernel on the stream
-    const int L = checked_len(p.seq_lens, seq, p.max_seq_len, p.max_blocks_per_seq * p.block_size,
-                              p.err, threadIdx.x == 0 && part == 0 && kvh == 0);
+    const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
     const int start = part * P;
     if (start >= L) {  // empty partition: as in the CUDA-core kernel
@@ -216,13 +108,16 @@ __global__ void __launch_bounds__(kTcThreads)
         } else {
             for (int g = 0; g < G; ++g) {
                 const int64_t row =
-                    ((int64_t)seq * p.num_q_heads + kvh * G + g) * p.num_partitions + part;
+                    part_row(p, seq, kvh * G + g, part);
                 if (threadIdx.x == 0) {
                     p.part_m[row] = -INFINITY;
                     p.part_l[row] = 0.f;
                 }
                 for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
             }
+            // empty cascade tail: the output is the prefix's partials combined
+            if (p.prefix_parts > 0 && nparts_seq == 0 && part == 0)
+                finish_item<BF16, D>(p, seq, kvh, 0);
         }
         return;
     }
@@ -255,7 +150,7 @@ __global__ void __launch_bounds__(kTcThreads)
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        const int32_t *table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
+        const int32_t *table = seq_table(p, seq);
         const int rows_per_block = p.block_size;
         bool ok = true;
         for (int u0 = 0; u0 < nunits && ok; u0 += 32) {  // 32 units = 4 tiles
@@ -509,7 +404,7 @@ __global__ void __launch_bounds__(kTcThreads)
                     uint16_t *out = static_cast<uint16_t *>(p.out);
                     out[((int64_t)seq * p.num_q_heads + h) * D + r] = narrow1<BF16>(o);
                 } else {
-                    const int64_t row = ((int64_t)seq * p.num_q_heads + h) * p.num_partitions + part;
+                    const int64_t row = part_row(p, seq, h, part);
                     p.part_o[row * D + r] = o;
                     if (r == 0) {
                         p.part_m[row] = m_true[g];
@@ -535,20 +430,8 @@ __global__ void __launch_bounds__(kTcThreads)
         tc_fence_after();
         tmem_dealloc(tmem, kTcCols);
     }
-    if (!direct && p.counters != nullptr && !*abort_flag) {
-        __shared__ int last_flag;
-        __shared__ float wsm[8 * kFuseMaxParts];
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0)
-            last_flag = arrive_last(p.counters + (int64_t)seq * p.num_kv_heads + kvh, p.epoch,
-                                    nparts_seq, p.err);
-        __syncthreads();
-        if (last_flag) {
-            __threadfence();
-            fused_combine<BF16, D>(p, seq, kvh, nparts_seq, wsm, blockDim.x);
-        }
-    }
+    if (!direct && !*abort_flag && (p.counters != nullptr || p.prefix_parts > 0))
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq);
 }
 
 // ------------------------------------------------------------------ host side
@@ -573,7 +456,7 @@ static EncodeTiledFn tensor_map_encoder() {
 
 // The pool [NB][Hkv][B][d] viewed as a 2-D tensor of NB*Hkv*B rows of d
 // elements; boxes of 16 rows x 64 columns, 128-byte swizzle.
-static bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, bool bf16) {
+bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, bool bf16) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};

@@ -79,6 +79,18 @@ def test_validation_before_launch(lib):
     assert lib.pa_copy_blocks(arr, arr, 0, vp(16), 2, 8, 4096, None) == 1
 
 
+def test_cascade_validation_before_launch(lib):
+    vp = ctypes.c_void_p
+    args = lambda P, maxlen=64: (vp(16), vp(16), None, None, None, vp(16), vp(16), 10, vp(16), 4,
+                                 vp(16), maxlen, 2, 8, 4, 128, 16, 1.0, P, vp(256), 1 << 20, 1,
+                                 None)
+    assert lib.pa_decode_cascade(*args(24)) == 1       # not a whole number of blocks
+    assert lib.pa_decode_cascade(*args(80)) == 1       # longer than max_seq_len
+    assert lib.pa_decode_cascade(*args(-16)) == 1
+    assert lib.pa_decode_cascade_workspace_size(2, 8, 4, 128, 16, 64, 24, 1) == 0
+    assert lib.pa_decode_cascade_workspace_size(2, 8, 4, 128, 16, 64, 80, 1) == 0
+
+
 def test_workspace_size_layout(lib):
     # explicit partition: m, l (256-aligned) then O
     S, hq, hkv, d, maxlen, P = 3, 8, 2, 128, 1000, 256
