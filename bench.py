@@ -138,7 +138,8 @@ def source_digest():
     """Hash of the decode kernel source, to tell whether a stored ncu traffic
     figure still describes the kernel being timed."""
     h = hashlib.sha256()
-    for f in ("pa_decode.cu", "pa_decode_tc.cu", "pa_decode.cuh", "pa_common.cuh"):
+    for f in ("pa_decode.cu", "pa_decode_tc.cu", "pa_decode.cuh", "pa_common.cuh",
+              "pa_tcgen05.cuh", "pa_cascade.cu"):
         with open(os.path.join(ROOT, "paged_kv_cache_64_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -257,7 +258,7 @@ def run_reference(args, rank, world):
 class GpuStep:
     """Device state of one workload and the calls of one decode step."""
 
-    def __init__(self, plan, device, partition_tokens=None):
+    def __init__(self, plan, device, partition_tokens=None, cascade=False):
         import torch
         from paged_kv_cache_64_gb300 import api, workloads
 
@@ -278,9 +279,20 @@ class GpuStep:
         size = api.workspace_size(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads,
                                   spec.head_dim, spec.block_size, self.max_seq_len, self.P,
                                   self.vals.q.dtype)
+        # shared-prefix (cascade) path: the prefix every sequence reaches
+        # through the same block-table entries, attended once per KV head
+        self.prefix_len = (api.shared_prefix_len(self.lay.block_tables, self.lay.seq_lens,
+                                                 spec.block_size) if cascade else 0)
+        if self.prefix_len:
+            size = api.cascade_workspace_size(spec.num_seqs, spec.num_q_heads,
+                                              spec.num_kv_heads, spec.head_dim, spec.block_size,
+                                              self.max_seq_len, self.prefix_len,
+                                              self.vals.q.dtype)
         self.ws = api.alloc_workspace(size, device) if size else None
         self.out = [torch.empty_like(self.vals.q) for _ in range(spec.num_layers)]
-        self.decode_bytes = workloads.algorithmic_bytes(spec, self.lay.seq_lens)
+        self.logical_bytes = workloads.algorithmic_bytes(spec, self.lay.seq_lens)
+        self.decode_bytes = (workloads.cascade_bytes(spec, self.lay.seq_lens, self.prefix_len)
+                             if self.prefix_len else self.logical_bytes)
         self.write_bytes = workloads.cache_write_bytes(spec, spec.num_seqs)
         self.copy_bytes = 2 * 2 * len(self.lay.pre_copies) * spec.num_kv_heads * \
             spec.block_size * spec.head_dim * workloads.DTYPE_BYTES[spec.dtype]
@@ -288,6 +300,8 @@ class GpuStep:
         # fused write + decode (+ combine) launch, a separate combine above 8
         # partitions, and the copy-on-write copies when there are any
         per_layer = 1 + (1 if NP > 8 else 0) + (1 if len(self.lay.pre_copies) else 0)
+        if self.prefix_len:  # prefix pass + tail pass (write, decode and merge)
+            per_layer = 2 + (1 if len(self.lay.pre_copies) else 0)
         self.launches_per_step = per_layer * spec.num_layers
 
     def step_bytes(self):
@@ -306,11 +320,21 @@ class GpuStep:
                 a = self.torch.cuda.Event(enable_timing=True)
                 b = self.torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-            # the new token's cache write and the decode, one launch
-            api.decode_step(self.out[layer], q, v.k_new[layer] if k_new is None else k_new[layer],
-                            v.v_new[layer] if v_new is None else v_new[layer], self.slots, kp, vp,
-                            self.tables, self.lens, self.max_seq_len, self.plan.scale,
-                            partition_tokens=self.P, workspace=self.ws, stream=stream)
+            if self.prefix_len:
+                # prefix pass, then the tails with the new token's write and the merge
+                api.decode_cascade(self.out[layer], q, kp, vp, self.tables, self.lens,
+                                   self.max_seq_len, self.plan.scale, self.prefix_len,
+                                   k_new=v.k_new[layer] if k_new is None else k_new[layer],
+                                   v_new=v.v_new[layer] if v_new is None else v_new[layer],
+                                   slot_mapping=self.slots, workspace=self.ws, stream=stream)
+            else:
+                # the new token's cache write and the decode, one launch
+                api.decode_step(self.out[layer], q,
+                                v.k_new[layer] if k_new is None else k_new[layer],
+                                v.v_new[layer] if v_new is None else v_new[layer], self.slots,
+                                kp, vp, self.tables, self.lens, self.max_seq_len,
+                                self.plan.scale, partition_tokens=self.P, workspace=self.ws,
+                                stream=stream)
             if ev is not None:
                 b.record(stream)
                 ev.append((a, b))
@@ -326,7 +350,7 @@ def run_gpu(args, rank, world, local_rank):
     base = workloads.SPECS[args.workload]
     plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs,
                                seed=base.seed + 1000 * rank if rank else None)
-    st = GpuStep(plan, device, args.partition_tokens)
+    st = GpuStep(plan, device, args.partition_tokens, cascade=args.cascade)
     stream = torch.cuda.current_stream()
     spec = st.spec
     flush = None
@@ -395,6 +419,9 @@ def run_gpu(args, rank, world, local_rank):
         dec_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
         kernel_note = ("pa_decode_step launch (new-token cache write + split-KV decode + combine), "
                        "CUDA events")
+        if st.prefix_len:
+            kernel_note = ("pa_decode_cascade call (tensor-core prefix pass + tail pass with the "
+                           "new-token write and the merge), CUDA events")
     else:
         # graph replay: a step's time spread over its layers (cache write included)
         dec_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in step_ev) / spec.num_layers
@@ -403,7 +430,7 @@ def run_gpu(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     launch_bytes = st.decode_bytes + st.write_bytes  # what one decode_step launch must move
     achieved = launch_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = stored_traffic(args.workload)
+    traffic = stored_traffic(args.workload + ("_cascade" if st.prefix_len else ""))
 
     # ------------------------------------------------ end to end (host buffers)
     # Every step copies its inputs from pinned host memory into the step's
@@ -457,7 +484,11 @@ def run_gpu(args, rank, world, local_rank):
             "decode_ctas_per_sm": api.ctas_per_sm(spec.head_dim,
                                                   spec.num_q_heads // spec.num_kv_heads,
                                                   st.vals.q.dtype),
-            "step": "copy_blocks (if any) + pa_decode_step (cache write + decode), every layer",
+            "step": ("copy_blocks (if any) + pa_decode_cascade (prefix pass; tails with the "
+                     "cache write and the merge), every layer" if st.prefix_len else
+                     "copy_blocks (if any) + pa_decode_step (cache write + decode), every layer"),
+            "decode_path": (f"cascade, shared prefix {st.prefix_len} positions"
+                            if st.prefix_len else "paged"),
             "launch": "CUDA graph replay" if graph is not None else "eager",
             "decode_kernel": ("CUDA cores" if args.decode_impl == "cuda_cores"
                               else "tensor cores (tcgen05)"),
@@ -465,6 +496,9 @@ def run_gpu(args, rank, world, local_rank):
             if flush is None else "L2 flushed (256 MiB write) before every step",
         },
         "pct_of_peak": 100.0 * value / peak,
+        # bytes plain paged decode would read for the same attention, per second
+        "logical_gbs": value * (st.logical_bytes + st.write_bytes + st.copy_bytes) /
+        (st.decode_bytes + st.write_bytes + st.copy_bytes),
         "tokens_per_s": spec.num_seqs * world / (secs / args.steps),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -504,6 +538,9 @@ def main(argv=None):
     ap.add_argument("--decode-impl", default="auto",
                     choices=["auto", "cuda_cores", "tensor_cores"],
                     help="decode kernel (default: the library's automatic choice)")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared-prefix decode: attend the prefix every sequence shares "
+                         "through its block table once per KV head (prefix workload)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -195,6 +195,20 @@ def decode_step(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables
     return workspace
 
 
+def shared_prefix_len(block_tables, seq_lens, block_size):
+    """Longest whole-block prefix that every sequence reaches through the
+    same block-table entries (host arrays), capped by the shortest sequence:
+    the prefix_len decode_cascade can be given for this batch."""
+    t = np.asarray(block_tables)
+    lens = np.asarray(seq_lens)
+    if t.shape[0] == 0:
+        return 0
+    nb = int(lens.min()) // block_size
+    same = np.all(t[:, :nb] == t[:1, :nb], axis=0)
+    n = nb if same.all() else int(np.argmin(same))
+    return n * block_size
+
+
 def cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                            max_seq_len, prefix_len, dtype):
     return _lib.load().pa_decode_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads,

@@ -167,19 +167,33 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             *abort_flag = 1;
         }
         // The prefix is only shared if every sequence of this tile reaches it
-        // through the same entries and is at least as long: check the
-        // entries of this chunk (once, in the CTAs of KV head 0).
-        if (kvh == 0) {
+        // through the same entries and is at least as long.  The (sequence,
+        // block) pairs of this tile and chunk are dealt to the KV heads' CTAs
+        // and their lanes, four loads in flight per lane.
+        {
             const int s_lo = mt * kCsRows / G;
             int s_hi = ((mt + 1) * kCsRows + G - 1) / G;
             if (s_hi > p.num_seqs) s_hi = p.num_seqs;
             const int b_lo = cstart >> p.log2_block, nb = (cend - cstart) >> p.log2_block;
+            const int npairs = (s_hi - s_lo) * nb;
+            const int stride = 32 * p.num_kv_heads;
             bool bad = false;
-            for (int i = lane; i < (s_hi - s_lo) * nb; i += 32) {
-                const int s = s_lo + i / nb, b = b_lo + i % nb;
-                bad |= p.block_tables[(int64_t)s * p.max_blocks_per_seq + b] != prefix_table[b];
+            for (int i0 = kvh * 32 + lane; i0 < npairs; i0 += 4 * stride) {
+                int got[4], want[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int i = i0 + j * stride;
+                    got[j] = want[j] = 0;
+                    if (i < npairs) {
+                        const int s = s_lo + i / nb, b = b_lo + i % nb;
+                        got[j] = p.block_tables[(int64_t)s * p.max_blocks_per_seq + b];
+                        want[j] = prefix_table[b];
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) bad |= got[j] != want[j];
             }
-            if (chunk == 0)
+            if (chunk == 0 && kvh == 0)
                 for (int s = s_lo + lane; s < s_hi; s += 32) bad |= p.seq_lens[s] < p.prefix_len;
             if (bad) record_error(p.err, PA_ERR_BAD_INDEX);
         }
@@ -240,14 +254,24 @@ __global__ void __launch_bounds__(kCsThreads, 1)
 
         // Q tile (128 rows x d, K-major, 128-byte swizzle), rows past the last
         // sequence zero.  Unscaled: the scale is applied to S in fp32.
-        for (int ci = st_id; ci < kCsRows * (D / 8); ci += 128) {
+        // all of the thread's loads in flight before the first store
+        constexpr int kQPer = kCsRows * (D / 8) / 128;
+        uint4 qv[kQPer];
+#pragma unroll
+        for (int i = 0; i < kQPer; ++i) {
+            const int ci = st_id + 128 * i;
             const int rr = ci / (D / 8), c = ci % (D / 8);
             const int gr = mt * kCsRows + rr;
-            uint4 v = make_uint4(0, 0, 0, 0);
+            qv[i] = make_uint4(0, 0, 0, 0);
             if (gr < rows_total)
-                v = *reinterpret_cast<const uint4 *>(
+                qv[i] = *reinterpret_cast<const uint4 *>(
                     p.q + ((int64_t)(gr / G) * p.num_q_heads + (int64_t)kvh * G + gr % G) * D + c * 8);
-            *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(rr, c * 8, S::SLAB)) = v;
+        }
+#pragma unroll
+        for (int i = 0; i < kQPer; ++i) {
+            const int ci = st_id + 128 * i;
+            const int rr = ci / (D / 8), c = ci % (D / 8);
+            *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(rr, c * 8, S::SLAB)) = qv[i];
         }
         fence_async_smem();
         __syncwarp();

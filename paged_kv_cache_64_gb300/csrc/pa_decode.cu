@@ -106,6 +106,7 @@ struct DecodeShape {
     static_assert(K <= GP, "a lane's sums belong to one row");
     static_assert(kConsumerWarps * GP * D * 4 + 3 * kConsumerWarps * GP * 4 <= RING_BYTES,
                   "merge scratch must fit in the ring");
+    static_assert(2 * 8 * kCombineMaxParts * 4 <= RING_BYTES, "combine scratch must fit in the ring");
 };
 
 
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
             }
             // empty cascade tail: the output is the prefix's partials combined
             if (p.prefix_parts > 0 && nparts_seq == 0 && part == 0)
-                finish_item<BF16, D>(p, seq, kvh, 0);
+                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem));
         }
         return;
     }
@@ -556,7 +557,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
         }
     }
     if (!direct && (p.counters != nullptr || p.prefix_parts > 0))
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq);
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem));
 }
 
 // ------------------------------------------------------------------ reduce
@@ -937,7 +938,7 @@ static pa_status cascade_plan(int num_seqs, int num_q_heads, int num_kv_heads, i
     c->chunk_tokens = cascade_chunk_tokens(prefix_len, num_seqs * G, num_kv_heads);
     c->num_chunks = (prefix_len + c->chunk_tokens - 1) / c->chunk_tokens;
     c->ws_parts = c->num_chunks + c->tail.NP;
-    return PA_OK;
+    return c->ws_parts <= kCombineMaxParts ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
 }  // namespace pa

@@ -168,44 +168,71 @@ __device__ __forceinline__ bool arrive_last(unsigned long long *ctr, unsigned in
     return false;
 }
 
+// Most partials one combine merges (the cascade's prefix chunks plus the
+// tail's partitions); the host keeps every launch within it.
+constexpr int kCombineMaxParts = 256;
+
 // Split-KV step 3 inside the CTA that finishes (seq, kvh): for each of its
 // G heads, over the slots [0, np) of the row, M = max_k m_k,
 // w_k = l_k 2^(m_k - M) / sum_j l_j 2^(m_j - M), out = sum_k w_k O_k.  All
-// `nthreads` threads of the CTA call it; wsm holds 2 * G floats of shared
-// memory.  Partials are read through L2 (they were written by other CTAs).
+// `nthreads` threads of the CTA call it.  `scratch` is shared memory the CTA
+// no longer needs, 2 * G * np floats.  Partials are read through L2 (other
+// CTAs wrote them), every (m, l) pair at once and four O rows in flight per
+// thread, so the merge costs a few L2 round trips rather than one per partial.
 template <bool BF16, int D>
-__device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, float *wsm,
+__device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, float *scratch,
                               int nthreads) {
     const int G = p.group;
     const int tid = threadIdx.x;
     const int64_t row0 = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * p.ws_parts;
+    float *ms = scratch, *ws = scratch + G * np;
+    for (int i = tid; i < G * np; i += nthreads) {
+        const int g = i / np, k = i - g * np;
+        ms[i] = __ldcg(p.part_m + row0 + (int64_t)g * p.ws_parts + k);
+        ws[i] = __ldcg(p.part_l + row0 + (int64_t)g * p.ws_parts + k);
+    }
+    __syncthreads();
     if (tid < G) {
-        const int64_t row = row0 + (int64_t)tid * p.ws_parts;
         float M = -INFINITY;
-        for (int k = 0; k < np; ++k) M = fmaxf(M, __ldcg(p.part_m + row + k));
+        for (int k = 0; k < np; ++k) M = fmaxf(M, ms[tid * np + k]);
         float tot = 0.f;
         for (int k = 0; k < np; ++k) {
-            const float mk = __ldcg(p.part_m + row + k);
-            if (mk != -INFINITY) tot += __ldcg(p.part_l + row + k) * fast_exp2(mk - M);
+            const float mk = ms[tid * np + k];
+            const float w = (mk == -INFINITY) ? 0.f : ws[tid * np + k] * fast_exp2(mk - M);
+            ws[tid * np + k] = w;
+            tot += w;
         }
-        wsm[2 * tid] = M;
-        wsm[2 * tid + 1] = tot > 0.f ? 1.0f / tot : 0.f;
+        const float inv = tot > 0.f ? 1.0f / tot : 0.f;
+        for (int k = 0; k < np; ++k) ws[tid * np + k] *= inv;
     }
     __syncthreads();
     for (int item = tid; item < G * (D / 8); item += nthreads) {
         const int g = item / (D / 8);
         const int x0 = (item % (D / 8)) * 8;
-        const int64_t row = row0 + (int64_t)g * p.ws_parts;
-        const float M = wsm[2 * g], inv = wsm[2 * g + 1];
+        const float *src = p.part_o + (row0 + (int64_t)g * p.ws_parts) * D + x0;
+        const float *w = ws + g * np;
         float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int k = 0; k < np; ++k) {
-            const float mk = __ldcg(p.part_m + row + k);
-            if (mk == -INFINITY) continue;  // empty partial
-            const float w = __ldcg(p.part_l + row + k) * fast_exp2(mk - M) * inv;
-            const float4 *src = reinterpret_cast<const float4 *>(p.part_o + (row + k) * D + x0);
-            const float4 a = __ldcg(src), b = __ldcg(src + 1);
-            o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
-            o[4] += w * b.x; o[5] += w * b.y; o[6] += w * b.z; o[7] += w * b.w;
+        int k = 0;
+        for (; k + 4 <= np; k += 4) {
+            float4 a[4], b[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                a[j] = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)(k + j) * D));
+                b[j] = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)(k + j) * D) + 1);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float wk = w[k + j];
+                o[0] += wk * a[j].x; o[1] += wk * a[j].y; o[2] += wk * a[j].z; o[3] += wk * a[j].w;
+                o[4] += wk * b[j].x; o[5] += wk * b[j].y; o[6] += wk * b[j].z; o[7] += wk * b[j].w;
+            }
+        }
+        for (; k < np; ++k) {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)k * D));
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)k * D) + 1);
+            const float wk = w[k];
+            o[0] += wk * a.x; o[1] += wk * a.y; o[2] += wk * a.z; o[3] += wk * a.w;
+            o[4] += wk * b.x; o[5] += wk * b.y; o[6] += wk * b.z; o[7] += wk * b.w;
         }
         uint16_t *out = static_cast<uint16_t *>(p.out) +
                         ((int64_t)seq * p.num_q_heads + kvh * G + g) * D + x0;
@@ -216,13 +243,13 @@ __device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, f
 
 // End of a CTA that wrote partials of (seq, kvh): with arrival counters,
 // the last of the item's nparts_seq CTAs combines; a cascade tail of a single
-// partition (no counters), or an empty one, combines at once.  The combined slots are the
-// prefix's and the item's: [0, prefix_parts + nparts_seq).  Called by every
-// thread of the CTA.
+// partition (no counters), or an empty one, combines at once.  The combined
+// slots are the prefix's and the item's: [0, prefix_parts + nparts_seq).
+// Called by every thread of the CTA; scratch as in fused_combine.
 template <bool BF16, int D>
-__device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_seq) {
+__device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_seq,
+                            float *scratch) {
     __shared__ int last_flag;
-    __shared__ float wsm[2 * 8];
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0)
@@ -233,7 +260,7 @@ __device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_
     __syncthreads();
     if (last_flag) {
         __threadfence();
-        fused_combine<BF16, D>(p, seq, kvh, p.prefix_parts + nparts_seq, wsm, blockDim.x);
+        fused_combine<BF16, D>(p, seq, kvh, p.prefix_parts + nparts_seq, scratch, blockDim.x);
     }
 }
 

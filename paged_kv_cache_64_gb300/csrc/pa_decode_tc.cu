@@ -75,6 +75,7 @@ struct TcShape {
     static constexpr int OFF_MISC = OFF_BAR + kNumTcBars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
+    static_assert(K_BYTES >= 2 * kTcG * kCombineMaxParts * 4, "combine scratch in the K tile");
 };
 
 template <bool BF16, int D>
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kTcThreads)
             }
             // empty cascade tail: the output is the prefix's partials combined
             if (p.prefix_parts > 0 && nparts_seq == 0 && part == 0)
-                finish_item<BF16, D>(p, seq, kvh, 0);
+                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem + S::OFF_K));
         }
         return;
     }
@@ -431,7 +432,8 @@ __global__ void __launch_bounds__(kTcThreads)
         tmem_dealloc(tmem, kTcCols);
     }
     if (!direct && !*abort_flag && (p.counters != nullptr || p.prefix_parts > 0))
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq);
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq,
+                              reinterpret_cast<float *>(smem + S::OFF_K));
 }
 
 // ------------------------------------------------------------------ host side

@@ -242,3 +242,17 @@ def cache_write_bytes(spec, num_tokens):
     """Bytes of one layer's cache write: read and write K and V of each token."""
     b = DTYPE_BYTES[spec.dtype]
     return int(2 * 2 * num_tokens * spec.num_kv_heads * spec.head_dim * b + 8 * num_tokens)
+
+
+def cascade_bytes(spec, seq_lens, prefix_len):
+    """Bytes a shared-prefix (cascade) decode must move for one layer: the
+    prefix's K and V once per KV head, each sequence's tail, the block-table
+    entries read (the prefix's once), q in and out, the length words."""
+    b = DTYPE_BYTES[spec.dtype]
+    L = np.asarray(seq_lens, dtype=np.int64)
+    per_token = 2 * spec.num_kv_heads * spec.head_dim * b
+    kv = per_token * (prefix_len + (L - prefix_len).sum())
+    B = spec.block_size
+    table = 4 * (prefix_len // B + sum(_blocks(x, B) - prefix_len // B for x in L))
+    qo = 2 * len(L) * spec.num_q_heads * spec.head_dim * b
+    return int(kv + table + qo + 4 * len(L))

@@ -238,3 +238,19 @@ def test_workload_layouts_agree(lib, name, cow):
         assert len(a.pre_copies) == 63  # the 64th writer owns the shared block alone
     if name == "prefix" and not cow:
         assert len(a.pre_copies) == 0   # full shared blocks are never written
+
+
+def test_shared_prefix_len():
+    """Whole blocks that every sequence reaches through the same entries,
+    capped by the shortest sequence."""
+    t = np.array([[4, 7, 9, 1], [4, 7, 9, 2], [4, 7, 3, 5]], dtype=np.int32)
+    assert api.shared_prefix_len(t, [64, 64, 64], 16) == 32
+    assert api.shared_prefix_len(t[:2], [64, 64], 16) == 48
+    assert api.shared_prefix_len(t[:2], [64, 40], 16) == 32      # shortest: 2 whole blocks
+    assert api.shared_prefix_len(t[:1], [50], 16) == 48          # one sequence: its whole blocks
+    assert api.shared_prefix_len(t[[0, 2]][:, ::-1], [64, 64], 16) == 0
+    assert api.shared_prefix_len(np.zeros((0, 4), np.int32), [], 16) == 0
+    for cow in (False, True):
+        plan = workloads.make_plan("prefix", cow=cow)
+        lay = workloads.layout(plan, BlockAllocatorModel)
+        assert api.shared_prefix_len(lay.block_tables, lay.seq_lens, 32) == 4096
