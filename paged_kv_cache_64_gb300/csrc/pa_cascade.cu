@@ -30,11 +30,16 @@
 //   warps 2..5  softmax / epilogue, one query row (TMEM lane) per thread:
 //               the whole 128-position score row is in the thread's
 //               registers, so row max and sum need no shuffles.
-// Each CTA leaves, for each of its rows, the (m, l, O) partial of its chunk
-// in workspace slot `chunk` (m the true base-2 maximum, l relative to it, O
+// The CTAs of consecutive chunks form a thread-block cluster (up to 8); at
+// the end they merge their chunks' partials through distributed shared
+// memory, and the cluster leaves one (m, l, O) partial per row in workspace
+// slot blockIdx.y / cluster (m the true base-2 maximum, l relative to it, O
 // normalised), as the split-KV partition kernels do.
 #include <cmath>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "pa_common.cuh"
 #include "pa_decode.cuh"
@@ -49,6 +54,7 @@ constexpr int kCsWarps = 6;
 constexpr int kCsThreads = kCsWarps * 32;
 constexpr int kCsCols = 512;   // TMEM columns: S x2 (128 each) and O (d)
 constexpr int kCsS0 = 0, kCsO = 256;
+constexpr int kCsMaxCluster = 8;  // chunks merged through distributed shared memory
 
 enum CsBar { kCsFull0 = 0, kCsFull1, kCsEmpty0, kCsEmpty1, kCsQReady, kCsSFull0, kCsSFull1,
              kCsPReady0, kCsPReady1, kCsODone, kNumCsBars };
@@ -69,7 +75,45 @@ struct CsShape {
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_P % 1024 == 0 && OFF_STAGE % 1024 == 0 && STAGE % 1024 == 0, "atoms");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(kCsRows * (D + 4) * 4 + 2 * kCsRows * 4 <= 2 * STAGE, "merge staging in the ring");
+    static_assert(3 * kCsRows * 4 <= P_BYTES, "merge weights in the P tile");
 };
+
+// Cluster merge, last step, in the CTA of rank `rank`: rows
+// [rank * R, rank * R + R) of the tile (R = 128 / CL) summed over the CL
+// chunks' weighted O rows that the cluster's CTAs pushed into this CTA's
+// shared memory (slot [c][row][D + 4]), with the weights already in
+// wts[R][CL]; written as one partial per row.  128 threads.
+template <int D, int CL>
+__device__ __forceinline__ void owner_sum(const CascadeParams &p, const float *ost,
+                                          const float *wts, const float *rowM, const float *rowL,
+                                          uint32_t rank, int t, int mt, int kvh, int slot) {
+    constexpr int R = kCsRows / CL;
+    constexpr int ITEMS = R * (D / 4) / 128;  // float4 outputs per thread
+    const int G = p.group;
+    const int rows_total = p.num_seqs * G;
+#pragma unroll 4
+    for (int i = 0; i < ITEMS; ++i) {
+        const int idx = t + 128 * i;
+        const int jl = idx / (D / 4), q4 = idx % (D / 4);
+        const int gr = mt * kCsRows + (int)rank * R + jl;
+        if (gr >= rows_total) continue;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+            if (wts[jl * CL + c] == 0.f) continue;  // empty or failed chunk pushed nothing
+            const float4 v = *reinterpret_cast<const float4 *>(ost + (c * R + jl) * (D + 4) + q4 * 4);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        const int64_t row =
+            ((int64_t)(gr / G) * p.num_q_heads + (int64_t)kvh * G + gr % G) * p.ws_parts + slot;
+        *reinterpret_cast<float4 *>(p.part_o + row * D + q4 * 4) = acc;
+        if (q4 == 0) {
+            p.part_m[row] = rowM[jl];
+            p.part_l[row] = rowL[jl];
+        }
+    }
+}
 
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kCsThreads, 1)
@@ -88,10 +132,15 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     const int G = p.group;
     const int rows_total = p.num_seqs * G;
     const int cstart = chunk * p.chunk_tokens;
-    const int cend = (cstart + p.chunk_tokens < p.prefix_len) ? cstart + p.chunk_tokens : p.prefix_len;
+    // trailing chunks of the last cluster may lie past the prefix: empty
+    const int cend = max(cstart, min(cstart + p.chunk_tokens, p.prefix_len));
     const int nunits = (cend - cstart) / kUnit;  // whole blocks, so whole 16-position units
     const int ntiles = (cend - cstart + kCsTile - 1) / kCsTile;
 
+    if (threadIdx.x == 0) {  // descriptors are kernel parameters: fetch them early
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
     pdl_wait();  // inputs may come from the previous kernel on the stream
     if (threadIdx.x == 0) {
         const int counts[kNumCsBars] = {1, 1, 1, 1, 4, 1, 1, 4, 4, 1};
@@ -107,13 +156,37 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // staging of the chunk's partial for the cluster merge, in the K/V ring
+    float *ost = reinterpret_cast<float *>(smem + S::OFF_STAGE);  // [128][D + 4]
+    float *cm = ost + kCsRows * (D + 4);
+    float *cl = cm + kCsRows;
+    float keep_inv = 0.f;    // 1 / l of the thread's row (softmax threads)
+    bool keep_have = false;  // the chunk's O is in TMEM
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         const int32_t *prefix_table = p.block_tables;  // sequence 0's row
         bool ok = true;
+        // block-table lookups 32 units (4 tiles) at a time, one round ahead:
+        // lane i holds the first row of unit 32 r + i in the 2-D view
+        // [NB*Hkv*B, d] of the pool
+        auto unit_row = [&](int u) -> int {
+            if (u >= nunits) return 0;
+            const int pos = cstart + u * kUnit;
+            int phys = prefix_table[pos >> p.log2_block];
+            if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                record_error(p.err, PA_ERR_BAD_INDEX);
+                phys = 0;
+            }
+            return (phys * p.num_kv_heads + kvh) * p.block_size + (pos & (p.block_size - 1));
+        };
+        int rows_cur = unit_row(lane), rows_next = unit_row(32 + lane);
         for (int t = 0; t < ntiles; ++t) {
             const int st = t & 1;
+            if (t > 0 && (t & 3) == 0) {
+                rows_cur = rows_next;
+                rows_next = unit_row(32 * ((t >> 2) + 1) + lane);
+            }
             if (t >= 2) {
                 const bool done = mbar_wait(&bar[kCsEmpty0 + st], ((t >> 1) - 1) & 1);
                 if (!__all_sync(kFullMask, done)) {
@@ -136,28 +209,18 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                 }
                 fence_async_smem();
             }
-            int row0 = 0;  // first row of the unit in the 2-D view [NB*Hkv*B, d]
-            if (lane < nu) {
-                const int pos = cstart + (u0 + lane) * kUnit;
-                int phys = prefix_table[pos >> p.log2_block];
-                if ((unsigned)phys >= (unsigned)p.num_blocks) {
-                    record_error(p.err, PA_ERR_BAD_INDEX);
-                    phys = 0;
-                }
-                row0 = (phys * p.num_kv_heads + kvh) * p.block_size + (pos & (p.block_size - 1));
-            }
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&bar[kCsFull0 + st], nu * S::KH * 2048 * 2);
-            for (int j = 0; j < nu; ++j) {
-                const int r0 = __shfl_sync(kFullMask, row0, j);
-                if (lane == 0) {
+            // lane j < nu copies unit j of the tile: one instruction issues
+            // the tile's copies
+            const int r0 = __shfl_sync(kFullMask, rows_cur, ((t & 3) * 8 + lane) & 31);
+            if (lane < nu) {
 #pragma unroll
-                    for (int h = 0; h < S::KH; ++h) {
-                        tma_load_2d(kbuf + h * S::SLAB + j * 2048, &tmap_k, 64 * h, r0,
-                                    &bar[kCsFull0 + st]);
-                        tma_load_2d(vbuf + h * S::SLAB + j * 2048, &tmap_v, 64 * h, r0,
-                                    &bar[kCsFull0 + st]);
-                    }
+                for (int h = 0; h < S::KH; ++h) {
+                    tma_load_2d(kbuf + h * S::SLAB + lane * 2048, &tmap_k, 64 * h, r0,
+                                &bar[kCsFull0 + st]);
+                    tma_load_2d(vbuf + h * S::SLAB + lane * 2048, &tmap_v, 64 * h, r0,
+                                &bar[kCsFull0 + st]);
                 }
             }
             __syncwarp();
@@ -217,18 +280,8 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                 tc_commit(&bar[kCsSFull0 + st]);
                 return true;
             };
-            bool ok = mbar_wait(&bar[kCsQReady], 0) && issue_qk(0);
-            for (int t = 0; t < ntiles && ok; ++t) {
-                // q.K^T of the next tile runs while the softmax works on this one
-                if (t + 1 < ntiles && !issue_qk(t + 1)) {
-                    ok = false;
-                    break;
-                }
+            auto issue_pv = [&](int t) {
                 const int st = t & 1;
-                if (!mbar_wait(&bar[kCsPReady0 + st], (t >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
                 tc_fence_after();
                 const uint32_t vb = sbase + S::OFF_STAGE + st * S::STAGE + S::KV_BYTES;
 #pragma unroll
@@ -239,6 +292,33 @@ __global__ void __launch_bounds__(kCsThreads, 1)
                 }
                 tc_commit(&bar[kCsEmpty0 + st]);
                 tc_commit(&bar[kCsODone]);
+            };
+            bool ok = ntiles == 0 || mbar_wait(&bar[kCsQReady], 0);
+            // Whichever is ready first: q.K^T of tile nq once its K has landed
+            // (its S buffer was released with tile nq-2's P, seen before P.V of
+            // nq-2 was issued), or P.V of tile nv once its P is written.  A
+            // P.V never waits behind a later tile's copies.
+            int nq = 0, nv = 0;
+            unsigned long long since = global_timer_ns();
+            unsigned spins = 0;
+            while (ok && nv < ntiles) {
+                bool moved = false;
+                if (nq < ntiles && nq <= nv + 1 &&
+                    mbar_try_wait(&bar[kCsFull0 + (nq & 1)], (nq >> 1) & 1)) {
+                    ok = issue_qk(nq);  // landed: returns at once
+                    ++nq;
+                    moved = true;
+                }
+                if (ok && nv < nq && mbar_try_wait(&bar[kCsPReady0 + (nv & 1)], (nv >> 1) & 1)) {
+                    issue_pv(nv);
+                    ++nv;
+                    moved = true;
+                }
+                if (moved) {
+                    since = global_timer_ns();
+                } else if ((++spins & 31) == 0 && global_timer_ns() - since > kWaitLimitNs) {
+                    ok = false;
+                }
             }
             if (!ok) {
                 record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
@@ -348,71 +428,128 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kCsPReady0 + b]);
         }
-        if (!failed) {
+        if (!failed && ntiles > 0) {
             const bool done = mbar_wait(&bar[kCsODone], (ntiles - 1) & 1);
             failed = !__all_sync(kFullMask, done);
         }
-        if (failed) {
-            if (lane == 0) {
-                record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
-                *abort_flag = 1;
-            }
-        } else {
-            tc_fence_after();
-            const int gr = mt * kCsRows + r;
-            const bool row_valid = gr < rows_total;
-            const int64_t row =
-                ((int64_t)(gr / G) * p.num_q_heads + (int64_t)kvh * G + gr % G) * p.ws_parts + chunk;
-            const float inv = 1.0f / l_run;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                tmem_ld32(tmem + lane_addr + kCsO + 32 * c, o);
-                    if (row_valid) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + row * D + 32 * c);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                             o[4 * i + 3] * inv);
-                }
-            }
-            if (row_valid) {
-                p.part_m[row] = m_true;
-                p.part_l[row] = l_run * fast_exp2(m_run - m_true);
-            }
+        if (failed && lane == 0) {
+            record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
         }
+        // This chunk's partial of row r, staged in shared memory for the
+        // cluster merge: m the true maximum, l relative to it, O normalised.
+        // The K/V ring is free: every copy has landed and every MMA is done.
+        // A failed or empty chunk contributes l = 0.
+        keep_have = !failed && ntiles > 0;  // warp-uniform
+        keep_inv = keep_have ? 1.0f / l_run : 0.f;
+        cm[r] = keep_have ? m_true : -INFINITY;
+        cl[r] = keep_have ? l_run * fast_exp2(m_run - m_true) : 0.f;
     }
 
     pdl_trigger();
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) {
+    if (*abort_flag && threadIdx.x == 0 && ntiles > 0) {
         // let copies and MMAs still in flight finish before shared memory and
         // TMEM are released (each wait is bounded)
         const int last = ntiles - 1;
         (void)mbar_wait(&bar[kCsFull0 + (last & 1)], (last >> 1) & 1);
         (void)mbar_wait(&bar[kCsEmpty0 + (last & 1)], (last >> 1) & 1);
     }
+
+    // ---------------------------------------------------------- cluster merge
+    // The cluster's CTAs hold consecutive chunks of the same rows (split-KV
+    // step 3 through distributed shared memory).  Every CTA reads the CL
+    // (m, l) pairs of each row, scales its own O row by its weight and pushes
+    // it into the shared memory of the CTA that owns the row (rank r / R);
+    // each owner sums what it received and writes one partial per row to
+    // slot blockIdx.y / cluster.  The K/V ring is free by now: every copy
+    // has landed and every MMA is done.
+    const int CL = p.cluster;
+    const int R = kCsRows / CL;
+    const uint32_t rank = cluster_ctarank();
+    float *wts = reinterpret_cast<float *>(smem + S::OFF_P);  // [R][CL] (R * CL = 128)
+    float *rowM = wts + kCsRows;
+    float *rowL = rowM + kCsRows;
+    __syncwarp();
+    cluster_sync();  // every chunk's (m, l) is visible
+    if (warp >= 2) {
+        const int r = (warp & 3) * 32 + lane;  // row of the tile = TMEM lane
+        float mc[kCsMaxCluster], lc[kCsMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kCsMaxCluster; ++c) {
+            mc[c] = -INFINITY;
+            lc[c] = 0.f;
+            if (c < CL) {
+                mc[c] = ld_cluster_f32(map_cluster(smem_addr(cm + r), c));
+                lc[c] = ld_cluster_f32(map_cluster(smem_addr(cl + r), c));
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kCsMaxCluster; ++c) M = fmaxf(M, (lc[c] > 0.f) ? mc[c] : -INFINITY);
+        float w[kCsMaxCluster], L = 0.f;
+#pragma unroll
+        for (int c = 0; c < kCsMaxCluster; ++c) {
+            w[c] = (lc[c] > 0.f) ? lc[c] * fast_exp2(mc[c] - M) : 0.f;
+            L += w[c];
+        }
+        const float invL = L > 0.f ? 1.0f / L : 0.f;
+        float w_self = 0.f;
+#pragma unroll
+        for (int c = 0; c < kCsMaxCluster; ++c) {
+            w[c] *= invL;
+            if (c == (int)rank) w_self = w[c];
+        }
+        if (r / R == (int)rank) {  // this CTA owns row r
+            const int jl = r % R;
+#pragma unroll
+            for (int c = 0; c < kCsMaxCluster; ++c)
+                if (c < CL) wts[jl * CL + c] = w[c];
+            rowM[jl] = M;
+            rowL[jl] = L;
+        }
+        if (keep_have) {
+            tc_fence_after();
+            const float sc = w_self * keep_inv;  // normalise, then weigh
+            const uint32_t dst = map_cluster(
+                smem_addr(ost + ((int)rank * R + r % R) * (D + 4)), (uint32_t)(r / R));
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + kCsO + 32 * c, o);
+                if (w_self != 0.f) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        st_cluster_f4(dst + (32 * c + 4 * i) * 4,
+                                      make_float4(o[4 * i] * sc, o[4 * i + 1] * sc,
+                                                  o[4 * i + 2] * sc, o[4 * i + 3] * sc));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kCsCols);
     }
+    __syncwarp();
+    cluster_sync();  // every pushed row has landed
+    if (warp >= 2) {
+        const int t = threadIdx.x - 64;
+        const int slot = blockIdx.y / CL;
+        switch (CL) {
+            case 1: owner_sum<D, 1>(p, ost, wts, rowM, rowL, rank, t, mt, kvh, slot); break;
+            case 2: owner_sum<D, 2>(p, ost, wts, rowM, rowL, rank, t, mt, kvh, slot); break;
+            case 4: owner_sum<D, 4>(p, ost, wts, rowM, rowL, rank, t, mt, kvh, slot); break;
+            default: owner_sum<D, 8>(p, ost, wts, rowM, rowL, rank, t, mt, kvh, slot); break;
+        }
+    }
 }
 
 // ------------------------------------------------------------------ host side
-int cascade_chunk_tokens(int prefix_len, int num_rows, int num_kv_heads) {
-    const int ntiles = (prefix_len + kCsTile - 1) / kCsTile;
-    const int per_chunk = ((num_rows + kCsRows - 1) / kCsRows) * num_kv_heads;
-    const int sms = sm_count();
-    int n = per_chunk > 0 ? (sms > 0 ? sms : 1) / per_chunk : 1;
-    if (n < 1) n = 1;
-    if (n > ntiles) n = ntiles;
-    if (n < 1) n = 1;
-    const int tiles_per_chunk = (ntiles + n - 1) / n;
-    return tiles_per_chunk * kCsTile;
-}
-
 using CsKernel = void (*)(const CascadeParams, const CUtensorMap, const CUtensorMap);
 
 static CsKernel pick_cascade(bool bf16, int D, int *smem) {
@@ -422,6 +559,75 @@ static CsKernel pick_cascade(bool bf16, int D, int *smem) {
     }
     *smem = CsShape<64>::SMEM_BYTES;
     return bf16 ? cascade_prefix_kernel<true, 64> : cascade_prefix_kernel<false, 64>;
+}
+
+// Clusters of `cl` CTAs of this kernel that can be resident at once on the
+// current device (0 if the query fails), cached per (kernel, size).
+static int active_clusters(CsKernel k, int smem, int cl) {
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const auto key = std::make_pair(reinterpret_cast<const void *>(k), dev * 16 + cl);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, (unsigned)cl, 1);
+    cfg.blockDim = dim3(kCsThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)cl;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(k), &cfg) != cudaSuccess)
+        n = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = n;
+    return n;
+}
+
+CascadeChunks cascade_chunks(int prefix_len, int num_rows, int num_kv_heads, int head_dim,
+                             bool bf16) {
+    const int ntiles = (prefix_len + kCsTile - 1) / kCsTile;
+    const int per_chunk = ((num_rows + kCsRows - 1) / kCsRows) * num_kv_heads;
+    const int sms = sm_count();
+    int n = per_chunk > 0 ? (sms > 0 ? sms : 1) / per_chunk : 1;
+    if (n > ntiles) n = ntiles;
+    if (n < 1) n = 1;
+    const int tiles_per_chunk = (ntiles + n - 1) / n;
+    n = (ntiles + tiles_per_chunk - 1) / tiles_per_chunk;
+    CascadeChunks c;
+    c.chunk_tokens = tiles_per_chunk * kCsTile;
+    // Clusters of 1, 2, 4 or 8 consecutive chunks (portable sizes that divide
+    // the grid; chunks added to fill the last cluster are empty): the largest
+    // that still lets the whole grid be resident at once, as one CTA per
+    // cluster-free SM would be.
+    int smem = 0;
+    CsKernel k = pick_cascade(bf16, head_dim, &smem);
+    c.cluster = 1;
+    c.num_chunks = n;
+    for (int cl = kCsMaxCluster; cl >= 2; cl /= 2) {
+        if (cl >= 2 * n) continue;  // more empty chunks than real ones
+        const int nc = (n + cl - 1) / cl * cl;
+        const int ctas = nc * per_chunk;
+        const int fit = active_clusters(k, smem, cl) * cl;
+        const int plain = sms > 0 ? sms : 1;
+        const bool one_wave = n * per_chunk <= plain;
+        if (fit >= (ctas < plain ? ctas : plain) && (!one_wave || ctas <= fit)) {
+            c.cluster = cl;
+            c.num_chunks = nc;
+            break;
+        }
+    }
+    return c;
 }
 
 pa_status launch_cascade_prefix(const CascadeParams &cp, const void *k_pool, const void *v_pool,
@@ -437,9 +643,23 @@ pa_status launch_cascade_prefix(const CascadeParams &cp, const void *k_pool, con
     if (!pool_tensor_map(&mk, k_pool, rows, head_dim, bf16) ||
         !pool_tensor_map(&mv, v_pool, rows, head_dim, bf16))
         return PA_ERR_CUDA;
-    dim3 grid((unsigned)mtiles, (unsigned)cp.num_chunks, (unsigned)cp.num_kv_heads);
-    if (launch_pdl(k, grid, dim3(kCsThreads), (size_t)smem, stream, cp, mk, mv) != cudaSuccess)
-        return PA_ERR_CUDA;
+    if (cp.cluster < 1 || cp.cluster > kCsMaxCluster || cp.num_chunks % cp.cluster)
+        return PA_ERR_INVALID;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)mtiles, (unsigned)cp.num_chunks, (unsigned)cp.num_kv_heads);
+    cfg.blockDim = dim3(kCsThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = (unsigned)cp.cluster;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, k, cp, mk, mv) != cudaSuccess) return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -180,8 +180,12 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
     if (start >= L) {
         // Empty partition.  Mode 0: the zero-length sequence's output row is
         // zeros (written by partition 0); nothing else is ever read.  Mode 1:
-        // write the empty partial (m = -inf, l = 0, O = 0).
-        if (p.mode == 0) {
+        // write the empty partial (m = -inf, l = 0, O = 0).  Empty cascade
+        // tail: the output is the prefix's partials combined.
+        if (p.prefix_parts > 0) {
+            if (nparts_seq == 0 && part == 0)
+                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem));
+        } else if (p.mode == 0) {
             if (part == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
                 const int64_t base = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * D / 2;
@@ -196,15 +200,13 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
                 }
                 for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
             }
-            // empty cascade tail: the output is the prefix's partials combined
-            if (p.prefix_parts > 0 && nparts_seq == 0 && part == 0)
-                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem));
         }
         return;
     }
     const int end = (start + P < L) ? start + P : L;
     const int nunits = (end - start + kUnit - 1) / kUnit;
-    const bool direct = (p.mode == 0) && (nparts_seq <= 1);
+    // a cascade tail writes its partial and merges it with the prefix's
+    const bool direct = (p.mode == 0) && (nparts_seq <= 1) && (p.prefix_parts == 0);
 
     if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write<D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
@@ -921,9 +923,9 @@ static pa_status decode_impl(void *out, const void *q, const void *k_new, const 
 // launch (positions [prefix_len, L) of each sequence).
 struct CascadePlan {
     ResolvedDecode tail;   // the tail launch (positions [prefix_len, L))
-    int chunk_tokens;
-    int num_chunks;
-    int ws_parts;          // num_chunks prefix slots + the tail's partitions
+    CascadeChunks chunks;  // the prefix pass
+    int prefix_slots;      // merged prefix partials per row
+    int ws_parts;          // prefix slots + the tail's partitions
 };
 static pa_status cascade_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                               int block_size, int max_seq_len, int prefix_len, pa_dtype dtype,
@@ -935,9 +937,9 @@ static pa_status cascade_plan(int num_seqs, int num_q_heads, int num_kv_heads, i
                            max_seq_len - prefix_len, 0, dtype, &c->tail);
     if (st != PA_OK) return st;
     const int G = num_q_heads / num_kv_heads;
-    c->chunk_tokens = cascade_chunk_tokens(prefix_len, num_seqs * G, num_kv_heads);
-    c->num_chunks = (prefix_len + c->chunk_tokens - 1) / c->chunk_tokens;
-    c->ws_parts = c->num_chunks + c->tail.NP;
+    c->chunks = cascade_chunks(prefix_len, num_seqs * G, num_kv_heads, head_dim, dtype == PA_BF16);
+    c->prefix_slots = c->chunks.num_chunks / c->chunks.cluster;
+    c->ws_parts = c->prefix_slots + c->tail.NP;
     return c->ws_parts <= kCombineMaxParts ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
@@ -1082,19 +1084,22 @@ pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, const v
     cp.block_size = block_size;
     cp.log2_block = prm.log2_block;
     cp.prefix_len = prefix_len;
-    cp.chunk_tokens = c.chunk_tokens;
-    cp.num_chunks = c.num_chunks;
+    cp.chunk_tokens = c.chunks.chunk_tokens;
+    cp.num_chunks = c.chunks.num_chunks;
+    cp.cluster = c.chunks.cluster;
     cp.ws_parts = c.ws_parts;
     cp.scale_log2 = prm.scale_log2;
     st = launch_cascade_prefix(cp, k_pool, v_pool, dtype == PA_BF16, head_dim, s);
     if (st != PA_OK) return st;
 
-    prm.mode = 1;
+    // one tail partition: the tail kernel merges the prefix's partials and
+    // writes the output; several: partials, and the last CTA merges
+    prm.mode = c.tail.NP > 1 ? 1 : 0;
     prm.len_offset = prefix_len;
     prm.table_offset = prefix_len / block_size;
     prm.ws_parts = c.ws_parts;
-    prm.part_base = c.num_chunks;
-    prm.prefix_parts = c.num_chunks;
+    prm.part_base = c.prefix_slots;
+    prm.prefix_parts = c.prefix_slots;
     prm.partition_tokens = c.tail.P > 0 ? c.tail.P : kSinglePassTokens;
     prm.num_partitions = c.tail.NP;
     if (c.tail.NP > 1) {

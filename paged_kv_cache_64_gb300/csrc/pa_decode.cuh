@@ -310,14 +310,23 @@ struct CascadeParams {
     int log2_block;
     int prefix_len;              // a multiple of block_size, > 0
     int chunk_tokens;            // a multiple of 128
-    int num_chunks;
-    int ws_parts;
+    int num_chunks;              // a multiple of cluster (trailing chunks may be empty)
+    int cluster;                 // CTAs of consecutive chunks merged in one cluster (1, 2, 4, 8)
+    int ws_parts;                // the merged partial of cluster c goes to slot c
     float scale_log2;
 };
 
-// Chunk length (a multiple of 128 positions) that spreads the prefix pass
-// over about one CTA per SM of the current device.
-int cascade_chunk_tokens(int prefix_len, int num_rows, int num_kv_heads);
+// Chunking of the prefix pass: chunk length (a multiple of 128 positions),
+// number of chunks and cluster size, spreading the pass over about one CTA
+// per SM of the current device.  The pass leaves num_chunks / cluster
+// partials per (sequence, query head).
+struct CascadeChunks {
+    int chunk_tokens;
+    int num_chunks;
+    int cluster;
+};
+CascadeChunks cascade_chunks(int prefix_len, int num_rows, int num_kv_heads, int head_dim,
+                             bool bf16);
 pa_status launch_cascade_prefix(const CascadeParams &cp, const void *k_pool, const void *v_pool,
                                 bool bf16, int head_dim, cudaStream_t stream);
 

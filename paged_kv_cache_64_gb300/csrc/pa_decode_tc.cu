@@ -54,7 +54,7 @@ constexpr int kSCol0 = 0, kOCol0 = 32;
 enum TcBar {
     kKFull = 0, kVFull, kKEmpty, kVEmpty, kQReady,
     kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kOFull0, kOFull1, kOEmpty0, kOEmpty1,
-    kNumTcBars
+    kPreReady, kNumTcBars
 };
 
 template <int D>
@@ -71,7 +71,10 @@ struct TcShape {
     static constexpr int OFF_P = OFF_Q + Q_BYTES;     // two buffers
     static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;
     static constexpr int RED_BYTES = 3 * 4 * kTcN * 4;  // two tile-max buffers + the final sums
-    static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+    // cascade tail: the shared prefix's partials merged per head (O, then m, l)
+    static constexpr int OFF_PRE = OFF_RED + RED_BYTES;
+    static constexpr int PRE_BYTES = kTcG * D * 4 + 2 * kTcG * 4;
+    static constexpr int OFF_BAR = OFF_PRE + PRE_BYTES;
     static constexpr int OFF_MISC = OFF_BAR + kNumTcBars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
@@ -95,12 +98,20 @@ __global__ void __launch_bounds__(kTcThreads)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
     const int P = p.partition_tokens;
+    if (threadIdx.x == 0) {  // descriptors are kernel parameters: fetch them early
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
     pdl_wait();  // inputs may come from the previous kernel on the stream
     const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
     const int start = part * P;
     if (start >= L) {  // empty partition: as in the CUDA-core kernel
-        if (p.mode == 0) {
+        if (p.prefix_parts > 0) {
+            // empty cascade tail: the output is the prefix's partials combined
+            if (nparts_seq == 0 && part == 0)
+                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem + S::OFF_K));
+        } else if (p.mode == 0) {
             if (part == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
                 const int64_t base = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * D / 2;
@@ -116,9 +127,6 @@ __global__ void __launch_bounds__(kTcThreads)
                 }
                 for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
             }
-            // empty cascade tail: the output is the prefix's partials combined
-            if (p.prefix_parts > 0 && nparts_seq == 0 && part == 0)
-                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem + S::OFF_K));
         }
         return;
     }
@@ -126,10 +134,14 @@ __global__ void __launch_bounds__(kTcThreads)
     const int nunits = (end - start + kUnit - 1) / kUnit;
     const int ntiles = (end - start + kTcTile - 1) / kTcTile;
     const bool direct = (p.mode == 0) && (nparts_seq <= 1);
+    // single-partition cascade tail: merge the prefix's partials here and
+    // write the output directly
+    const bool merge_prefix = direct && p.prefix_parts > 0;
+    float *pre = reinterpret_cast<float *>(smem + S::OFF_PRE);
 
     if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write<D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
-        const int counts[kNumTcBars] = {1, 1, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4};
+        const int counts[kNumTcBars] = {1, 1, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4, 1};
         for (int b = 0; b < kNumTcBars; ++b) mbar_init(&bar[b], counts[b]);
         *abort_flag = 0;
         mbar_init_fence();
@@ -180,14 +192,14 @@ __global__ void __launch_bounds__(kTcThreads)
                     const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
                     uint64_t *full = &bar[kv ? kVFull : kKFull];
                     if (lane == 0) mbar_arrive_expect_tx(full, nu * S::KH * 2048);
-                    for (int j = 0; j < nu; ++j) {
-                        const int r0 = __shfl_sync(kFullMask, row0, 8 * t + j - u0);
-                        if (lane == 0) {
+                    // lane j < nu copies unit j of the tile: one instruction issues
+                    // the tile's copies
+                    const int r0 = __shfl_sync(kFullMask, row0, (8 * t - u0 + lane) & 31);
+                    if (lane < nu) {
 #pragma unroll
-                            for (int h = 0; h < S::KH; ++h)
-                                tma_load_2d(smem + base_off + h * S::SLAB + j * 2048, map, 64 * h,
-                                            r0, full);
-                        }
+                        for (int h = 0; h < S::KH; ++h)
+                            tma_load_2d(smem + base_off + h * S::SLAB + lane * 2048, map, 64 * h,
+                                        r0, full);
                     }
                     __syncwarp();
                 }
@@ -196,6 +208,72 @@ __global__ void __launch_bounds__(kTcThreads)
         if (!ok && lane == 0) {
             record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
             *abort_flag = 1;
+        }
+        if (merge_prefix) {
+            // The shared prefix's partials of the group's heads, merged with
+            // the online-softmax rescale while the tail is computed (they were
+            // complete before this launch); four heads per round of loads,
+            // lane owns D/32 dims.
+            constexpr int V = D / 32;
+            const int np = p.prefix_parts;
+            const int64_t row0 = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * p.ws_parts;
+            for (int g0 = 0; g0 < G; g0 += 4) {
+                float M[4], Ls[4], acc[4][V];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    M[j] = -INFINITY;
+                    Ls[j] = 0.f;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) acc[j][v] = 0.f;
+                }
+                for (int k = 0; k < np; ++k) {
+                    float mk[4], lk[4], ov[4][V];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        mk[j] = -INFINITY;
+                        lk[j] = 0.f;
+#pragma unroll
+                        for (int v = 0; v < V; ++v) ov[j][v] = 0.f;
+                        if (g0 + j < G) {
+                            const int64_t row = row0 + (int64_t)(g0 + j) * p.ws_parts + k;
+                            mk[j] = __ldcg(p.part_m + row);
+                            lk[j] = __ldcg(p.part_l + row);
+                            const float *src = p.part_o + row * D + lane * V;
+                            if constexpr (V == 4) {
+                                const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+                                ov[j][0] = t.x; ov[j][1] = t.y; ov[j][2] = t.z; ov[j][3] = t.w;
+                            } else {
+                                const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+                                ov[j][0] = t.x; ov[j][1] = t.y;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (mk[j] == -INFINITY) continue;  // empty partial
+                        const float nm = fmaxf(M[j], mk[j]);
+                        const float a = fast_exp2(M[j] - nm), b = lk[j] * fast_exp2(mk[j] - nm);
+                        Ls[j] = Ls[j] * a + b;
+#pragma unroll
+                        for (int v = 0; v < V; ++v) acc[j][v] = acc[j][v] * a + b * ov[j][v];
+                        M[j] = nm;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int g = g0 + j;
+                    if (g >= G) break;
+                    const float inv = Ls[j] > 0.f ? 1.0f / Ls[j] : 0.f;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) pre[g * D + lane * V + v] = acc[j][v] * inv;
+                    if (lane == 0) {
+                        pre[kTcG * D + g] = M[j];
+                        pre[kTcG * D + kTcG + g] = Ls[j];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kPreReady]);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
@@ -388,6 +466,10 @@ __global__ void __launch_bounds__(kTcThreads)
             if (lane == 0) lsum[sw * kTcN + g] = v;
         }
         softmax_bar();
+        if (merge_prefix && !failed) {
+            const bool ready = mbar_wait(&bar[kPreReady], 0);
+            if (!__all_sync(kFullMask, ready)) failed = true;
+        }
         if (failed) {
             if (st == 0) {
                 record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
@@ -399,8 +481,16 @@ __global__ void __launch_bounds__(kTcThreads)
                 if (g >= G) break;
                 const float lt =
                     lsum[g] + lsum[kTcN + g] + lsum[2 * kTcN + g] + lsum[3 * kTcN + g];
-                const float o = acc[g] / lt;
+                float o = acc[g] / lt;
                 const int h = kvh * G + g;
+                if (merge_prefix) {
+                    // softmax over prefix and tail: the two partials' log-sum-exp merge
+                    const float Mp = pre[kTcG * D + g], Lp = pre[kTcG * D + kTcG + g];
+                    const float M = fmaxf(m_run[g], Mp);
+                    const float wo = fast_exp2(m_run[g] - M);
+                    const float wp = (Mp == -INFINITY) ? 0.f : Lp * fast_exp2(Mp - M);
+                    o = (acc[g] * wo + wp * pre[g * D + r]) / (lt * wo + wp);
+                }
                 if (direct) {
                     uint16_t *out = static_cast<uint16_t *>(p.out);
                     out[((int64_t)seq * p.num_q_heads + h) * D + r] = narrow1<BF16>(o);
