@@ -423,6 +423,88 @@ pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n_ou
 /* Reference count of a block (-1 if out of range). */
 int pa_block_refcount(const pa_alloc *a, int block);
 
+/* ------------------------------------------------------------------------
+ * Prefix-caching block pool (host): the allocator with automatic prefix
+ * caching.  [P4] section 9 (KVCacheManager over BlockPool: get_computed_blocks,
+ * allocate_slots, free in reverse order; the doubly linked free queue;
+ * get_new_blocks / free_blocks / touch with reference counts); [P1] "A
+ * separate mechanism: automatic prefix caching" (block hash chain over the
+ * previous block's hash and the block's token ids, block-aligned matches,
+ * nothing copied on a hit, cached blocks evicted oldest-first) and "Where the
+ * analogy stops" (cache_salt mixed into the first block's hash).
+ *
+ * Every block is in use (refcount > 0) or in the free queue.  New blocks come
+ * off the queue's head; taking a cached block evicts its hash.  A request's
+ * block fills -> it is hashed: FNV-1a 64 (offset basis 0xcbf29ce484222325,
+ * prime 0x100000001b3) over the previous block's hash (the request's salt for
+ * its first block) as 8 little-endian bytes, then each token id as 4
+ * little-endian bytes; it is cached under that hash unless a block already
+ * holds the same content.  A lookup matches the longest run of a prompt's
+ * leading full blocks whose chain is cached (stored token ids and previous
+ * hash compared, so a hash collision only costs a hit), at most
+ * (n - 1) / block_size blocks: the last prompt token is always computed.
+ * Freeing visits the request's blocks tail first; each loses a reference;
+ * blocks reaching zero go to the queue's head when unhashed (the first one
+ * freed becomes the head) and to its tail when hashed (LRU eviction).  Only
+ * full blocks are shared, so no block is ever copied.  Single-threaded;
+ * every failing call leaves the pool unchanged.  All pointers are host.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_pcache pa_pcache;
+
+/* num_blocks >= 1, block_size >= 1; free_order: NULL (0 .. num_blocks-1) or
+ * a permutation of the block ids, the initial queue from the head. */
+pa_status pa_pcache_create(int num_blocks, int block_size, const int32_t *free_order,
+                           pa_pcache **out);
+void pa_pcache_destroy(pa_pcache *pc);
+
+/* The block hash above, for n token ids after `prev`. */
+uint64_t pa_pcache_hash_block(uint64_t prev, const int32_t *tokens, int n);
+
+/* Number of leading full blocks of the n-token prompt that are cached
+ * (get_computed_blocks); nothing changes. */
+pa_status pa_pcache_lookup(const pa_pcache *pc, const int32_t *tokens, int n, uint64_t salt,
+                           int *num_blocks_out);
+
+/* New request seq_id with its n-token prompt: the cached run is shared
+ * (touch: references, no copy), the rest of the prompt gets new blocks, and
+ * the prompt's newly full blocks are hashed.  *num_cached_out = tokens found
+ * (a multiple of block_size); slots_out[p] (n entries) = slot of prompt
+ * position p (block * block_size + offset); the caller writes K/V for
+ * positions >= *num_cached_out.  PA_ERR_OUT_OF_BLOCKS if the queue (after
+ * the hits are taken out of it) is too short; PA_ERR_INVALID for a
+ * duplicate id. */
+pa_status pa_pcache_add(pa_pcache *pc, int64_t seq_id, const int32_t *tokens, int n,
+                        uint64_t salt, int *num_cached_out, int64_t *slots_out);
+
+/* One generated token: its slot; a block that fills is hashed.
+ * PA_ERR_NOT_FOUND for an unknown id, PA_ERR_OUT_OF_BLOCKS when a block is
+ * needed and the queue is empty. */
+pa_status pa_pcache_append(pa_pcache *pc, int64_t seq_id, int32_t token, int64_t *slot_out);
+
+/* End of a request: its blocks freed tail first (see above). */
+pa_status pa_pcache_free(pa_pcache *pc, int64_t seq_id);
+
+/* Block table of a request into out (cap entries); *n_out gets its length;
+ * PA_ERR_INVALID if cap is too small (nothing written). */
+pa_status pa_pcache_block_table(const pa_pcache *pc, int64_t seq_id, int32_t *out, int cap,
+                                int *n_out);
+
+/* Tokens of a request (prompt and generated). */
+pa_status pa_pcache_len(const pa_pcache *pc, int64_t seq_id, int64_t *len_out);
+
+int pa_pcache_num_free(const pa_pcache *pc);
+
+/* Free queue, head first (cap entries); *n_out gets its length;
+ * PA_ERR_INVALID if cap is too small. */
+pa_status pa_pcache_free_queue(const pa_pcache *pc, int32_t *out, int cap, int *n_out);
+
+/* Reference count of a block (-1 if out of range). */
+int pa_pcache_refcount(const pa_pcache *pc, int block);
+
+/* Whether a block is cached and under which hash (0 when not). */
+pa_status pa_pcache_block_hash(const pa_pcache *pc, int block, uint64_t *hash_out,
+                               int *cached_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -48,6 +48,19 @@ SIGNATURES = {
                                    _c_int, _vp, _c_sz, _c_int, _vp]),
     "pa_decode_cascade_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                  _c_int, _c_int]),
+    "pa_pcache_create": (_c_int, [_c_int, _c_int, _i32p, ctypes.POINTER(_vp)]),
+    "pa_pcache_destroy": (None, [_vp]),
+    "pa_pcache_hash_block": (ctypes.c_uint64, [ctypes.c_uint64, _i32p, _c_int]),
+    "pa_pcache_lookup": (_c_int, [_vp, _i32p, _c_int, ctypes.c_uint64, _intp]),
+    "pa_pcache_add": (_c_int, [_vp, ctypes.c_int64, _i32p, _c_int, ctypes.c_uint64, _intp, _i64p]),
+    "pa_pcache_append": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int32, _i64p]),
+    "pa_pcache_free": (_c_int, [_vp, ctypes.c_int64]),
+    "pa_pcache_block_table": (_c_int, [_vp, ctypes.c_int64, _i32p, _c_int, _intp]),
+    "pa_pcache_len": (_c_int, [_vp, ctypes.c_int64, _i64p]),
+    "pa_pcache_num_free": (_c_int, [_vp]),
+    "pa_pcache_free_queue": (_c_int, [_vp, _i32p, _c_int, _intp]),
+    "pa_pcache_refcount": (_c_int, [_vp, _c_int]),
+    "pa_pcache_block_hash": (_c_int, [_vp, _c_int, ctypes.POINTER(ctypes.c_uint64), _intp]),
     "pa_decode_auto_partition": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           _c_int]),
     "pa_decode_ctas_per_sm": (_c_int, [_c_int, _c_int, _c_int]),

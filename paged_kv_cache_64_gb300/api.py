@@ -397,3 +397,102 @@ class BlockAllocator:
 
     def refcount(self, block):
         return self._lib.pa_block_refcount(self._h, int(block))
+
+
+class PrefixCachePool:
+    """Host block pool with automatic prefix caching (pa_pcache_*): requests
+    whose prompts begin with cached full blocks share them; freed hashed
+    blocks stay cached until the pool needs them (LRU)."""
+
+    def __init__(self, num_blocks, block_size, free_order=None):
+        self._lib = _lib.load()
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        handle = ctypes.c_void_p()
+        order = None
+        if free_order is not None:
+            arr = np.ascontiguousarray(free_order, dtype=np.int32)
+            if arr.shape != (self.num_blocks,):
+                raise ValueError("free_order must list every block once")
+            self._order = arr
+            order = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        _lib.check("pa_pcache_create", self._lib.pa_pcache_create(
+            self.num_blocks, self.block_size, order, ctypes.byref(handle)))
+        self._h = handle
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.pa_pcache_destroy(h)
+            self._h = None
+
+    @staticmethod
+    def _tokens(tokens):
+        arr = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+        return arr, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+    def lookup(self, tokens, salt=0):
+        """Number of leading full blocks of the prompt that are cached."""
+        arr, ptr = self._tokens(tokens)
+        n = ctypes.c_int()
+        _lib.check("pa_pcache_lookup", self._lib.pa_pcache_lookup(
+            self._h, ptr, arr.size, int(salt) & (2**64 - 1), ctypes.byref(n)))
+        return n.value
+
+    def add_request(self, seq, tokens, salt=0):
+        """Returns (cached tokens, slot of every prompt position)."""
+        arr, ptr = self._tokens(tokens)
+        slots = np.empty(max(arr.size, 1), dtype=np.int64)
+        cached = ctypes.c_int()
+        _lib.check("pa_pcache_add", self._lib.pa_pcache_add(
+            self._h, int(seq), ptr, arr.size, int(salt) & (2**64 - 1), ctypes.byref(cached),
+            slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))))
+        return cached.value, slots[:arr.size].tolist()
+
+    def append(self, seq, token):
+        slot = ctypes.c_int64()
+        _lib.check("pa_pcache_append", self._lib.pa_pcache_append(
+            self._h, int(seq), int(token), ctypes.byref(slot)))
+        return slot.value
+
+    def release(self, seq):
+        _lib.check("pa_pcache_free", self._lib.pa_pcache_free(self._h, int(seq)))
+
+    def table(self, seq):
+        n = ctypes.c_int()
+        out = np.empty(max(self.num_blocks, 1), dtype=np.int32)
+        _lib.check("pa_pcache_block_table", self._lib.pa_pcache_block_table(
+            self._h, int(seq), out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            self.num_blocks, ctypes.byref(n)))
+        return out[:n.value].tolist()
+
+    def length(self, seq):
+        v = ctypes.c_int64()
+        _lib.check("pa_pcache_len", self._lib.pa_pcache_len(self._h, int(seq), ctypes.byref(v)))
+        return v.value
+
+    def free_list(self):
+        n = ctypes.c_int()
+        out = np.empty(max(self.num_blocks, 1), dtype=np.int32)
+        _lib.check("pa_pcache_free_queue", self._lib.pa_pcache_free_queue(
+            self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), self.num_blocks,
+            ctypes.byref(n)))
+        return out[:n.value].tolist()
+
+    def num_free(self):
+        return self._lib.pa_pcache_num_free(self._h)
+
+    def refcount(self, blk):
+        return self._lib.pa_pcache_refcount(self._h, int(blk))
+
+    def block_hash(self, blk):
+        """The block's hash, or None when it is not cached."""
+        h = ctypes.c_uint64()
+        c = ctypes.c_int()
+        _lib.check("pa_pcache_block_hash", self._lib.pa_pcache_block_hash(
+            self._h, int(blk), ctypes.byref(h), ctypes.byref(c)))
+        return h.value if c.value else None
+
+    def hash_block(self, prev, tokens):
+        arr, ptr = self._tokens(tokens)
+        return int(self._lib.pa_pcache_hash_block(int(prev) & (2**64 - 1), ptr, arr.size))
