@@ -169,10 +169,11 @@ def oracle_sample(plan, budget_s, rng_seed=0):
 
     import oracle
     from oracle.allocator import BlockAllocatorModel
+    from oracle.prefix_cache import PrefixCachePoolModel
     from paged_kv_cache_64_gb300 import workloads
 
     spec = plan.spec
-    lay = workloads.layout(plan, BlockAllocatorModel)
+    lay = workloads.layout(plan, PrefixCachePoolModel if plan.apc else BlockAllocatorModel)
     B = spec.block_size
     shape = (plan.num_blocks, spec.num_kv_heads, B, spec.head_dim)
     k = np.zeros(shape, dtype=np.uint16)  # pages are only touched where filled
@@ -254,6 +255,36 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def host_pool_timing(plan, reps=5):
+    """Host time of the prefix-caching pool on the plan's requests, through
+    the Python binding: every request's add (prefix lookup, touch, new
+    blocks, hashing), one decode-step append per request, then the frees.
+    Median of `reps` fresh pools, microseconds per call."""
+    from paged_kv_cache_64_gb300 import api
+    S = plan.spec.num_seqs
+    add, app, free = [], [], []
+    for _ in range(reps):
+        pool = api.PrefixCachePool(plan.num_blocks, plan.spec.block_size, plan.free_order)
+        t0 = time.perf_counter()
+        for op in plan.ops:
+            pool.add_request(op[1], op[2])
+        t1 = time.perf_counter()
+        for s in range(S):
+            pool.append(s, int(plan.step_tokens[s]))
+        t2 = time.perf_counter()
+        for s in range(S):
+            pool.release(s)
+        t3 = time.perf_counter()
+        add.append((t1 - t0) / len(plan.ops))
+        app.append((t2 - t1) / S)
+        free.append((t3 - t2) / S)
+    return {"add_request_us": 1e6 * statistics.median(add),
+            "append_us": 1e6 * statistics.median(app),
+            "free_us": 1e6 * statistics.median(free),
+            "prompt_tokens": int(len(plan.ops[0][2])), "requests": len(plan.ops),
+            "via": "Python binding (ctypes) on the host cores"}
+
+
 # -------------------------------------------------------------------- GPU arm
 class GpuStep:
     """Device state of one workload and the calls of one decode step."""
@@ -265,7 +296,7 @@ class GpuStep:
         self.api, self.torch = api, torch
         self.plan, self.spec = plan, plan.spec
         self.device = device
-        self.lay = workloads.layout(plan, api.BlockAllocator)
+        self.lay = workloads.layout(plan, workloads.native_allocator(plan))
         self.vals = workloads.make_values(plan, self.lay, device)
         t = lambda a: torch.as_tensor(a, device=device)
         self.tables, self.lens = t(self.lay.block_tables), t(self.lay.seq_lens)
@@ -349,7 +380,7 @@ def run_gpu(args, rank, world, local_rank):
     api.set_decode_impl(args.decode_impl)
     base = workloads.SPECS[args.workload]
     plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs,
-                               seed=base.seed + 1000 * rank if rank else None)
+                               seed=base.seed + 1000 * rank if rank else None, apc=args.apc)
     st = GpuStep(plan, device, args.partition_tokens, cascade=args.cascade)
     stream = torch.cuda.current_stream()
     spec = st.spec
@@ -512,6 +543,10 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": st.launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    if plan.apc:
+        line["config"]["layout"] = ("separate requests with one prompt, shared by the "
+                                    "prefix-caching pool (pa_pcache)")
+        line["host_allocator"] = host_pool_timing(plan)
     if world == 1 and not args.no_cpu_baseline:
         secs_c, nbytes_c, toks_c, nseq_c, threads = oracle_sample(plan, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -541,12 +576,17 @@ def main(argv=None):
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix decode: attend the prefix every sequence shares "
                          "through its block table once per KV head (prefix workload)")
+    ap.add_argument("--apc", action="store_true",
+                    help="prefix workload as separate requests laid out by the prefix-caching "
+                         "pool (automatic prefix caching) instead of forks")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.apc and args.workload != "prefix":
+        ap.error("--apc applies to the prefix workload")
     rank, world, local_rank = dist_env()
     if world > 1:
         import torch.distributed as dist

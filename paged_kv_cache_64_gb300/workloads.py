@@ -72,6 +72,11 @@ class Plan:
     ops: list                        # allocator operations before the step
     pre_write_seqs: list = field(default_factory=list)  # (seq, n) whose tokens get written
     cow_case: bool = False
+    # automatic prefix caching: separate requests with their prompts' token
+    # ids, laid out by a prefix-caching pool; step_tokens are the ids the
+    # decode step appends
+    apc: bool = False
+    step_tokens: np.ndarray = None
 
     @property
     def scale(self):
@@ -82,7 +87,7 @@ def _blocks(n, B):
     return -(-int(n) // B)
 
 
-def make_plan(name, num_seqs=None, len_range=None, cow=False, seed=None):
+def make_plan(name, num_seqs=None, len_range=None, cow=False, seed=None, apc=False):
     """Draw the plan of a workload.  num_seqs / len_range shrink a workload for
     tests (same structure, fewer or shorter sequences)."""
     base = SPECS[name]
@@ -105,6 +110,22 @@ def make_plan(name, num_seqs=None, len_range=None, cow=False, seed=None):
         lo, hi = len_range or ((512, 8192) if name == "llama" else (16384, 32768))
         lens = rng.integers(lo, hi, S, endpoint=True).astype(np.int64)
         nb = int(math.ceil(1.2 * sum(_blocks(L + 1, B) for L in lens)))
+    elif name == "prefix" and apc:
+        # the same 4,096-token prompt in 64 separate requests, each with its
+        # own tail: the pool's prefix cache, not a fork, shares the prompt
+        lo, hi = len_range or (1, 256)
+        prefix = 4096
+        tails = rng.integers(lo, hi, S, endpoint=True).astype(np.int64)
+        lens = prefix + tails
+        prompt = rng.integers(0, 32000, prefix).astype(np.int32)
+        uniq = _blocks(prefix, B) + sum(_blocks(prefix + t + 1, B) - prefix // B for t in tails)
+        nb = int(math.ceil(1.2 * uniq))
+        for s in range(S):
+            tail = rng.integers(0, 32000, int(tails[s])).astype(np.int32)
+            ops.append(("request", s, np.concatenate([prompt, tail])))
+        step_tokens = rng.integers(0, 32000, S).astype(np.int32)
+        free_order = rng.permutation(nb).astype(np.int32)
+        return Plan(spec, lens, nb, free_order, ops, pre, False, True, step_tokens)
     elif name == "prefix":
         lo, hi = len_range or (1, 256)
         prefix = 4096 + (16 if cow else 0)
@@ -143,7 +164,9 @@ class Layout:
 
 def layout(plan, allocator_factory):
     """Run the plan's operations and the decode step's appends on an allocator
-    made by allocator_factory(num_blocks, block_size, free_order)."""
+    made by allocator_factory(num_blocks, block_size, free_order): a block
+    allocator (add / append / fork), or for a plan with apc a prefix-caching
+    pool (add_request / append)."""
     spec = plan.spec
     alloc = allocator_factory(plan.num_blocks, spec.block_size, plan.free_order)
     pre_copies, pre_slots = [], []
@@ -157,8 +180,15 @@ def layout(plan, allocator_factory):
             pre_copies.extend(copies)
             if len(op) > 3 and op[3] == "write":
                 pre_slots.extend(slots)
+        elif op[0] == "request":
+            # prompt positions the cache already holds are not written again
+            cached, slots = alloc.add_request(op[1], op[2])
+            pre_slots.extend(slots[cached:])
     step_slots, step_copies = [], []
     for s in range(spec.num_seqs):
+        if plan.apc:
+            step_slots.append(alloc.append(s, int(plan.step_tokens[s])))
+            continue
         slots, copies = alloc.append(s, 1)
         step_slots.extend(slots)
         step_copies.extend(copies)
@@ -175,6 +205,12 @@ def layout(plan, allocator_factory):
                   np.asarray(pre_slots, dtype=np.int64),
                   np.asarray(step_copies, dtype=np.int64).reshape(-1, 2),
                   int(max(lens)) if lens else 0)
+
+
+def native_allocator(plan):
+    """The library's allocator class that lays the plan out."""
+    from . import api
+    return api.PrefixCachePool if plan.apc else api.BlockAllocator
 
 
 def torch_dtype(name):

@@ -11,6 +11,7 @@ import torch
 
 import oracle
 from oracle.allocator import BlockAllocatorModel
+from oracle.prefix_cache import PrefixCachePoolModel
 from paged_kv_cache_64_gb300 import api, workloads
 
 # Tolerance for fp16/bf16 outputs: |gpu - ref| <= TOL_ABS + TOL_REL * |ref|.
@@ -45,8 +46,9 @@ class Case:
     def __init__(self, plan, device="cuda", layers=1):
         self.plan = plan
         self.spec = spec = plan.spec
-        self.lay = workloads.layout(plan, api.BlockAllocator)
-        self.ref_lay = workloads.layout(plan, BlockAllocatorModel)
+        self.lay = workloads.layout(plan, workloads.native_allocator(plan))
+        self.ref_lay = workloads.layout(plan, PrefixCachePoolModel if plan.apc
+                                        else BlockAllocatorModel)
         for f in ("block_tables", "seq_lens", "slot_mapping", "pre_copies", "pre_slots",
                   "step_copies"):
             assert np.array_equal(getattr(self.lay, f), getattr(self.ref_lay, f)), f

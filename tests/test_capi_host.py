@@ -254,3 +254,21 @@ def test_shared_prefix_len():
         plan = workloads.make_plan("prefix", cow=cow)
         lay = workloads.layout(plan, BlockAllocatorModel)
         assert api.shared_prefix_len(lay.block_tables, lay.seq_lens, 32) == 4096
+
+
+def test_prefix_caching_layout_agrees(lib):
+    """The prefix workload as 64 separate requests laid out by the
+    prefix-caching pool: native pool and model agree, and the prompt's 128
+    blocks are shared by every request."""
+    from oracle.prefix_cache import PrefixCachePoolModel
+    plan = workloads.make_plan("prefix", apc=True)
+    a = workloads.layout(plan, api.PrefixCachePool)
+    b = workloads.layout(plan, PrefixCachePoolModel)
+    for f in ("block_tables", "seq_lens", "slot_mapping", "pre_copies", "pre_slots",
+              "step_copies"):
+        assert np.array_equal(getattr(a, f), getattr(b, f)), f
+    assert api.shared_prefix_len(a.block_tables, a.seq_lens, 32) == 4096
+    assert len(a.pre_copies) == 0
+    tails = plan.cached_lens - 4096
+    # written before the step: the first prompt in full, then only each tail
+    assert len(a.pre_slots) == 4096 + int(tails.sum())

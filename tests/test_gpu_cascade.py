@@ -251,3 +251,31 @@ def test_graph_replay():
         g.replay()
         torch.cuda.synchronize()
         assert_close(out, ref, "cascade graph replay")
+
+
+# ------------------------------------------------------------ prefix caching layout
+@pytest.mark.parametrize("cascade", [False, True])
+def test_prefix_caching_layout_small(cascade):
+    """Separate requests with one prompt, laid out by the prefix-caching pool:
+    plain decode and the cascade both match the oracle."""
+    case = Case(workloads.make_plan("prefix", num_seqs=6, apc=True))
+    hk, hv = case.snapshot(0)
+    if cascade:
+        out = cascade_step(case, 4096)
+    else:
+        out = case.gpu_step_fused(0)
+    ref = case.oracle_step(0, hk, hv)
+    api.check_error()
+    assert_close(out, ref, f"prefix caching layout, cascade={cascade}")
+    assert np.array_equal(bits(case.vals.k_pools[0]), hk)
+
+
+def test_prefix_caching_layout_full_size_sampled():
+    case = Case(workloads.make_plan("prefix", apc=True))
+    lens = case.lay.seq_lens
+    seqs = sorted({0, 1, 31, 32, 63, int(np.argmax(lens)), int(np.argmin(lens))})
+    hk, hv = case.snapshot(0)
+    out = cascade_step(case, 4096)
+    ref = case.oracle_step(0, hk, hv, seqs)
+    api.check_error()
+    assert_close(out, ref, "prefix caching layout full size", mask_rows=np.asarray(seqs))
