@@ -66,6 +66,17 @@ def _load():
     lib.pa_oracle_reduce.argtypes = [dp, dp, dp, dp, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
     lib.pa_oracle_widen.restype = None
     lib.pa_oracle_widen.argtypes = [dp, u16p, ctypes.c_int64, ctypes.c_int]
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    fp = ctypes.POINTER(ctypes.c_float)
+    lib.pa_oracle_decode_fp8.restype = ctypes.c_int
+    lib.pa_oracle_decode_fp8.argtypes = [dp, u16p, u8p, u8p, ctypes.c_int, ctypes.c_double,
+                                         ctypes.c_double, i32p, ctypes.c_int, i32p, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_double, i32p, ctypes.c_int]
+    lib.pa_oracle_e4m3_decode.restype = None
+    lib.pa_oracle_e4m3_decode.argtypes = [dp, u8p, ctypes.c_int64]
+    lib.pa_oracle_e4m3_encode.restype = None
+    lib.pa_oracle_e4m3_encode.argtypes = [u8p, fp, ctypes.c_int64]
     lib.pa_oracle_num_threads.restype = ctypes.c_int
     lib.pa_oracle_set_num_threads.argtypes = [ctypes.c_int]
     _lib = lib
@@ -200,3 +211,60 @@ def copy_blocks(pools, block_mapping):
     for src, dst in np.asarray(block_mapping).reshape(-1, 2).tolist():
         for pool in pools:
             pool[dst] = pool[src]
+
+
+# ----------------------------------------------------------------- FP8 variant
+def e4m3_decode(codes):
+    """Values (float64) of OCP E4M3 codes (uint8)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().pa_oracle_e4m3_decode(_ptr(out, ctypes.c_double), _ptr(c, ctypes.c_uint8), c.size)
+    return out
+
+
+def e4m3_encode(values):
+    """Nearest E4M3 codes (ties to even, saturating at +-448) of fp32 values."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().pa_oracle_e4m3_encode(_ptr(out, ctypes.c_uint8), _ptr(v, ctypes.c_float), v.size)
+    return out
+
+
+def quantize_fp8(bits, dtype, scale):
+    """E4M3 codes of 16-bit values (bit patterns) under a pool scale: the fp32
+    value times fl32(1 / scale), rounded to the nearest code."""
+    x = widen(bits, dtype).astype(np.float32)  # exact: every 16-bit value is an fp32 value
+    inv = np.float32(1.0) / np.float32(scale)
+    return e4m3_encode(x * inv)
+
+
+def cache_write_fp8(k_pool, v_pool, k_new, v_new, slot_mapping, dtype, k_scale, v_scale):
+    """cache_write into E4M3 pools (uint8 [NB, Hkv, B, d]): token t's K/V
+    (16-bit bit patterns [T, Hkv, d]) quantized with the pools' scales."""
+    cache_write(k_pool, v_pool, quantize_fp8(k_new, dtype, k_scale),
+                quantize_fp8(v_new, dtype, v_scale), slot_mapping)
+
+
+def decode_fp8(q, k_pool, v_pool, block_tables, seq_lens, scale, dtype, k_scale, v_scale,
+               seqs=None):
+    """Paged decode attention in fp64 over E4M3 pools (uint8 codes): K element
+    = k_scale * code value, V element = v_scale * code value.  q (16-bit bit
+    patterns of `dtype`) as in decode()."""
+    q = _u16(q)
+    k_pool = np.ascontiguousarray(k_pool, dtype=np.uint8)
+    v_pool = np.ascontiguousarray(v_pool, dtype=np.uint8)
+    bt, sl = _i32(block_tables), _i32(seq_lens)
+    S, Hq, d = q.shape
+    _, Hkv, B, d2 = k_pool.shape
+    assert d2 == d and v_pool.shape == k_pool.shape and bt.shape[0] == S and sl.shape == (S,)
+    out = np.full((S, Hq, d), np.nan)
+    sub = None if seqs is None else _i32(seqs)
+    rc = _load().pa_oracle_decode_fp8(
+        _ptr(out, ctypes.c_double), _ptr(q, ctypes.c_uint16), _ptr(k_pool, ctypes.c_uint8),
+        _ptr(v_pool, ctypes.c_uint8), _DT[dtype], float(k_scale), float(v_scale),
+        _ptr(bt, ctypes.c_int32), bt.shape[1], _ptr(sl, ctypes.c_int32), S, Hq, Hkv, d, B,
+        float(scale), None if sub is None else _ptr(sub, ctypes.c_int32),
+        0 if sub is None else sub.size)
+    if rc:
+        raise ValueError("oracle decode: bad dimensions")
+    return out
