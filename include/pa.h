@@ -234,6 +234,45 @@ size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int num_k
                                         int head_dim, int block_size, int max_seq_len,
                                         int prefix_len, pa_dtype dtype);
 
+/* ------------------------------------------------------------------------
+ * FP8 KV cache (a variant).  [P3] section 1 gives b = 1 byte per element for
+ * FP8 in the KV-size formula and nothing more; the format and the scale are
+ * this library's conventions: pools hold OCP E4M3 codes (1 sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits, subnormals, no infinities, S.1111.111
+ * NaN, largest finite 448), one byte per element, in the same
+ * [num_blocks][num_kv_heads][block_size][head_dim] layout, and each pool has
+ * one scale: element = scale * code value.
+ *
+ * pa_cache_write_fp8: pa_cache_write into E4M3 pools.  Each element x of
+ * k_new / v_new (16-bit, dtype) becomes the code nearest (ties to even) to
+ * the fp32 product x * fl32(1 / scale), saturating at +-448.  Other
+ * arguments as pa_cache_write; scales finite and > 0.
+ * ---------------------------------------------------------------------- */
+pa_status pa_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                             int num_tokens, void *k_pool, void *v_pool, int num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, float k_scale,
+                             float v_scale, pa_dtype dtype, void *stream);
+
+/* pa_decode over E4M3 pools: out[i][h] = sum_p softmax(s)_p * v_scale * V_i[p]
+ * with s_p = scale * dot(q[i][h], k_scale * K_i[p]) (code values).  q and out
+ * are 16-bit (dtype).  With k_new != NULL, each sequence's newest token is
+ * first quantised and written as pa_cache_write_fp8 would (the fused step of
+ * pa_decode_step).  The tensor-core kernel widens the codes to f16 (exactly)
+ * in shared memory and runs its products in f16 with fp32 accumulation.
+ * head_dim in {64, 128}, G <= 8, block_size in {16, 32}; partition_tokens
+ * and workspace as pa_decode (size from pa_decode_fp8_workspace_size). */
+pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, const void *v_new,
+                        const int64_t *slot_mapping, void *k_pool, void *v_pool, int num_blocks,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *seq_lens, int max_seq_len, int num_seqs, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, float scale,
+                        float k_scale, float v_scale, int partition_tokens, void *workspace,
+                        size_t workspace_bytes, pa_dtype dtype, void *stream);
+
+size_t pa_decode_fp8_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int max_seq_len,
+                                    int partition_tokens, pa_dtype dtype);
+
 /* Partition size pa_decode uses for these shapes when partition_tokens = 0
  * (-1 means it will run single pass).  Needs the current CUDA device. */
 int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,

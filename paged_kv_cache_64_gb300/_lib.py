@@ -61,6 +61,13 @@ SIGNATURES = {
     "pa_pcache_free_queue": (_c_int, [_vp, _i32p, _c_int, _intp]),
     "pa_pcache_refcount": (_c_int, [_vp, _c_int]),
     "pa_pcache_block_hash": (_c_int, [_vp, _c_int, ctypes.POINTER(ctypes.c_uint64), _intp]),
+    "pa_cache_write_fp8": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int,
+                                    _c_int, _c_f, _c_f, _c_int, _vp]),
+    "pa_decode_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _vp,
+                               _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_f, _c_f,
+                               _c_int, _vp, _c_sz, _c_int, _vp]),
+    "pa_decode_fp8_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                             _c_int, _c_int]),
     "pa_decode_auto_partition": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           _c_int]),
     "pa_decode_ctas_per_sm": (_c_int, [_c_int, _c_int, _c_int]),

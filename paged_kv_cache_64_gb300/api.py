@@ -209,6 +209,67 @@ def shared_prefix_len(block_tables, seq_lens, block_size):
     return n * block_size
 
 
+def cache_write_fp8(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale, v_scale, stream=None):
+    """reshape_and_cache into E4M3 pools (uint8 [NB, Hkv, B, d]): k_new /
+    v_new (16-bit [T, Hkv, d]) quantised with the pools' scales."""
+    nb, hkv, bs, d = k_pool.shape
+    T = k_new.shape[0]
+    if k_pool.dtype != torch.uint8 or v_pool.dtype != torch.uint8:
+        raise ValueError("E4M3 pools are uint8 tensors of codes")
+    if k_new.shape != (T, hkv, d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [T, Hkv, d]")
+    rc = _lib.load().pa_cache_write_fp8(
+        _cuda(k_new, "k_new"), _cuda(v_new, "v_new"),
+        _cuda(slot_mapping, "slot_mapping", torch.int64), T, _cuda(k_pool, "k_pool"),
+        _cuda(v_pool, "v_pool"), nb, hkv, d, bs, float(k_scale), float(v_scale), _dt(k_new),
+        _stream_handle(stream))
+    _lib.check("pa_cache_write_fp8", rc)
+
+
+def fp8_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                       partition_tokens, dtype):
+    return _lib.load().pa_decode_fp8_workspace_size(num_seqs, num_q_heads, num_kv_heads,
+                                                    head_dim, block_size, max_seq_len,
+                                                    partition_tokens, _DTYPES[dtype])
+
+
+def decode_fp8(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale, k_scale,
+               v_scale, partition_tokens=0, k_new=None, v_new=None, slot_mapping=None,
+               workspace=None, stream=None):
+    """Paged decode over E4M3 pools (uint8 codes, element = scale * code);
+    q / out 16-bit.  With k_new / v_new / slot_mapping, each sequence's newest
+    token is quantised and written first (the fused step)."""
+    S, hq, d = q.shape
+    nb, hkv, bs, d2 = k_pool.shape
+    if d2 != d or block_tables.dim() != 2 or block_tables.shape[0] != S or seq_lens.shape != (S,):
+        raise ValueError("shapes of q, pools, block_tables, seq_lens disagree")
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    if k_pool.dtype != torch.uint8 or v_pool.dtype != torch.uint8:
+        raise ValueError("E4M3 pools are uint8 tensors of codes")
+    step = k_new is not None
+    if step and (k_new.shape != (S, hkv, d) or v_new is None or v_new.shape != k_new.shape
+                 or slot_mapping is None or slot_mapping.shape != (S,)):
+        raise ValueError("k_new/v_new must be [S, Hkv, d] and slot_mapping [S]")
+    need = fp8_workspace_size(S, hq, hkv, d, bs, max_seq_len, partition_tokens, q.dtype)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = alloc_workspace(need, q.device)
+    ws = _cuda(workspace, "workspace") if workspace is not None else ctypes.c_void_p(0)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    null = ctypes.c_void_p(0)
+    rc = _lib.load().pa_decode_fp8(
+        _cuda(out, "out"), _cuda(q, "q"), _cuda(k_new, "k_new") if step else null,
+        _cuda(v_new, "v_new") if step else null,
+        _cuda(slot_mapping, "slot_mapping", torch.int64) if step else null,
+        _cuda(k_pool, "k_pool"), _cuda(v_pool, "v_pool"), nb,
+        _cuda(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _cuda(seq_lens, "seq_lens", torch.int32), int(max_seq_len), S, hq, hkv, d, bs,
+        float(scale), float(k_scale), float(v_scale), int(partition_tokens), ws, wbytes, _dt(q),
+        _stream_handle(stream))
+    _lib.check("pa_decode_fp8", rc)
+    return workspace
+
+
 def cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                            max_seq_len, prefix_len, dtype):
     return _lib.load().pa_decode_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads,

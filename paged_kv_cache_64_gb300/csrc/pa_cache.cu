@@ -5,6 +5,7 @@
 // piece per iteration, consecutive threads move consecutive pieces, so every
 // warp reads and writes whole 512-byte runs.  They are bound by HBM (copy
 // bytes), and tiny next to decode.
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 #include <set>
@@ -111,6 +112,44 @@ struct PoolPtrs {
 
 // grid.y: pair, grid.z: layer * 2 + (0 = K, 1 = V); x covers the block's
 // 16-byte pieces.
+// FP8 cache write: token t's K/V (16-bit, [T][Hkv][d]) quantised to E4M3
+// codes with the pools' scales (code = nearest(x * inv_scale), fp32) and
+// stored at its slot.  One work item is 16 elements: 32 bytes read, 16
+// written.
+template <bool BF16>
+__global__ void cache_write_fp8_kernel(const uint4 *__restrict__ k_new,
+                                       const uint4 *__restrict__ v_new,
+                                       const int64_t *__restrict__ slot_mapping, int num_tokens,
+                                       uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool,
+                                       int64_t num_slots, int num_kv_heads, int chunks,
+                                       int block_size, float k_inv, float v_inv, int *err) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
+    const int64_t per_token = 2ll * num_kv_heads * chunks;
+    const int64_t total = per_token * num_tokens;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / per_token;
+        const int64_t r = i - t * per_token;
+        const int is_v = (int)(r / ((int64_t)num_kv_heads * chunks));
+        const int64_t r2 = r - (int64_t)is_v * num_kv_heads * chunks;
+        const int h = (int)(r2 / chunks);
+        const int c = (int)(r2 - (int64_t)h * chunks);
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            record_error(err, PA_ERR_BAD_INDEX);
+            continue;
+        }
+        const int64_t blk = slot / block_size;
+        const int64_t off = slot - blk * block_size;
+        const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * chunks + c;
+        const int64_t src = (((int64_t)t * num_kv_heads + h) * chunks + c) * 2;
+        const uint4 *in = is_v ? v_new : k_new;
+        const uint4 q = quantize16_e4m3<BF16>(in[src], in[src + 1], is_v ? v_inv : k_inv);
+        (is_v ? v_pool : k_pool)[dst] = q;
+    }
+}
+
 __global__ void copy_blocks_kernel(const PoolPtrs pools, const int64_t *__restrict__ mapping,
                                    int num_blocks, int64_t pieces, int *err) {
     const int pair = blockIdx.y;
@@ -161,6 +200,37 @@ const char *pa_status_string(pa_status s) {
         case PA_ERR_TOO_LARGE: return "split-KV partials exceed the fixed static scratch";
     }
     return "unknown status";
+}
+
+pa_status pa_cache_write_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                             int num_tokens, void *k_pool, void *v_pool, int num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, float k_scale,
+                             float v_scale, pa_dtype dtype, void *stream) {
+    if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || block_size <= 0)
+        return PA_ERR_INVALID;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return PA_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return PA_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PA_ERR_INVALID;
+    int *err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    const int chunks = head_dim / 16;
+    const int64_t total = 2ll * num_tokens * num_kv_heads * chunks;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    const int64_t cap = 16ll * (sm_count() > 0 ? sm_count() : 148);
+    if (blocks > cap) blocks = cap;
+    const float k_inv = 1.0f / k_scale, v_inv = 1.0f / v_scale;
+    auto kern = dtype == PA_BF16 ? cache_write_fp8_kernel<true> : cache_write_fp8_kernel<false>;
+    kern<<<(unsigned)blocks, threads, 0, as_stream(stream)>>>(
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
+        num_tokens, static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool),
+        (int64_t)num_blocks * block_size, num_kv_heads, chunks, block_size, k_inv, v_inv, err);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_cache_write(const void *k_new, const void *v_new, const int64_t *slot_mapping,

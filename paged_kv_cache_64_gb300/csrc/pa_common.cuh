@@ -125,4 +125,36 @@ __device__ __forceinline__ uint32_t narrow2(float a, float b) {
     return w;
 }
 
+// FP8 KV cache (OCP E4M3 codes, one scale per pool).  Two fp32 values to
+// two codes, nearest with ties to even, saturating at +-448 (PTX
+// cvt.rn.satfinite.e4m3x2.f32; the first value in the low byte).
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two codes (low byte first) to two f16 values, exactly (PTX
+// cvt.rn.f16x2.e4m3x2: every E4M3 value is an f16 value).
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint16_t c) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+    return r;
+}
+
+// 16 16-bit values (two uint4, low element first) times `inv` in fp32, as
+// 16 E4M3 codes.
+template <bool BF16>
+__device__ __forceinline__ uint4 quantize16_e4m3(uint4 a, uint4 b, float inv) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 x = widen2<BF16>(w[2 * i]), y = widen2<BF16>(w[2 * i + 1]);
+        c[i] = e4m3x2_from_f32(x.x * inv, x.y * inv) |
+               (e4m3x2_from_f32(y.x * inv, y.y * inv) << 16);
+    }
+    return make_uint4(c[0], c[1], c[2], c[3]);
+}
+
 }  // namespace pa

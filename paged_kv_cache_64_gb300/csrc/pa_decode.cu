@@ -738,6 +738,13 @@ struct ResolvedDecode {
     int head_dim;
     int P;    // -1 single pass, else partition size
     int NP;   // partitions in the grid
+    bool fp8 = false;  // E4M3 pools: the FP8 tensor-core kernel (pa_decode_fp8.cu)
+};
+
+// Scales of E4M3 pools (element = scale * code value).
+struct KvFp8 {
+    float k_scale;
+    float v_scale;
 };
 
 // Process-wide choice of decode kernel: 0 automatic, 1 CUDA cores, 2 tensor cores.
@@ -754,7 +761,7 @@ static bool use_tensor_cores(int head_dim, int group) {
 
 static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                          int block_size, int max_seq_len, int partition_tokens, pa_dtype dtype,
-                         ResolvedDecode *r) {
+                         ResolvedDecode *r, bool fp8 = false) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0)
         return PA_ERR_INVALID;
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID;
@@ -764,12 +771,15 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
         return PA_ERR_UNSUPPORTED;
     if (!pick_decode(dtype, head_dim, group_pad(G), &r->entry)) return PA_ERR_UNSUPPORTED;
     r->tc = use_tensor_cores(head_dim, G);
+    r->fp8 = fp8;
+    if (fp8 && !fp8_supported(head_dim, G)) return PA_ERR_UNSUPPORTED;
     r->bf16 = dtype == PA_BF16;
     r->head_dim = head_dim;
     int P = partition_tokens;
     if (P == 0) {
-        const int per_sm =
-            r->tc ? tc_ctas_per_sm(dtype == PA_BF16, head_dim) : decode_ctas_per_sm(r->entry);
+        const int per_sm = r->fp8  ? fp8_ctas_per_sm(dtype == PA_BF16, head_dim)
+                           : r->tc ? tc_ctas_per_sm(dtype == PA_BF16, head_dim)
+                                   : decode_ctas_per_sm(r->entry);
         P = auto_partition(num_seqs, num_kv_heads, max_seq_len, per_sm, block_size);
     }
     if (P < -1) return PA_ERR_INVALID;
@@ -786,6 +796,10 @@ static pa_status launch_decode(const ResolvedDecode &r, DecodeParams prm, int nu
     if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_INVALID;
     if (prm.ws_parts == 0) prm.ws_parts = prm.num_partitions;  // plain launch: own workspace
     if (!prm.out && (prm.mode == 0 || prm.counters || prm.prefix_parts)) return PA_ERR_INVALID;
+    if (r.fp8) {
+        if (prm.prefix_parts) return PA_ERR_UNSUPPORTED;  // no cascade over E4M3 pools
+        return launch_decode_fp8(prm, r.bf16, r.head_dim, r.NP, num_kv_heads, num_seqs, stream);
+    }
     if (r.tc)
         return launch_decode_tc(prm, r.bf16, r.head_dim, r.NP, num_kv_heads, num_seqs, stream);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(r.entry.fn), r.entry.smem))
@@ -853,10 +867,14 @@ static pa_status decode_impl(void *out, const void *q, const void *k_new, const 
                              const int32_t *seq_lens, int max_seq_len, int num_seqs,
                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                              float scale, int partition_tokens, void *workspace,
-                             size_t workspace_bytes, pa_dtype dtype, void *stream) {
+                             size_t workspace_bytes, pa_dtype dtype, void *stream,
+                             const KvFp8 *fp8 = nullptr) {
     ResolvedDecode r;
+    if (fp8 && (!(fp8->k_scale > 0.f) || !(fp8->v_scale > 0.f) || !std::isfinite(fp8->k_scale) ||
+                !std::isfinite(fp8->v_scale)))
+        return PA_ERR_INVALID;
     pa_status st = resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                           max_seq_len, partition_tokens, dtype, &r);
+                           max_seq_len, partition_tokens, dtype, &r, fp8 != nullptr);
     if (st != PA_OK) return st;
     if (num_seqs > 0 && (!out || !aligned16(out))) return PA_ERR_INVALID;
     DecodeParams prm;
@@ -866,6 +884,12 @@ static pa_status decode_impl(void *out, const void *q, const void *k_new, const 
     if (st != PA_OK) return st;
     prm.out = out;
     prm.mode = 0;
+    if (fp8) {
+        prm.scale_log2 *= fp8->k_scale;  // K elements are k_scale * codes
+        prm.k_inv = 1.0f / fp8->k_scale;
+        prm.v_inv = 1.0f / fp8->v_scale;
+        prm.v_scale = fp8->v_scale;
+    }
     if (k_new) {
         if (num_seqs > 0 && (!v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)))
             return PA_ERR_INVALID;
@@ -994,6 +1018,31 @@ pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_
                        block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
                        num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_tokens,
                        workspace, workspace_bytes, dtype, stream);
+}
+
+size_t pa_decode_fp8_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int max_seq_len,
+                                    int partition_tokens, pa_dtype dtype) {
+    ResolvedDecode r;
+    if (resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                partition_tokens, dtype, &r, true) != PA_OK)
+        return 0;
+    if (r.P <= 0) return 0;
+    return workspace_layout(num_seqs, num_q_heads, head_dim, r.NP, num_kv_heads).bytes;
+}
+
+pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, const void *v_new,
+                        const int64_t *slot_mapping, void *k_pool, void *v_pool, int num_blocks,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *seq_lens, int max_seq_len, int num_seqs, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, float scale,
+                        float k_scale, float v_scale, int partition_tokens, void *workspace,
+                        size_t workspace_bytes, pa_dtype dtype, void *stream) {
+    const KvFp8 fp8 = {k_scale, v_scale};
+    return decode_impl(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, num_blocks,
+                       block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, scale, partition_tokens,
+                       workspace, workspace_bytes, dtype, stream, &fp8);
 }
 
 pa_status pa_decode_step(void *out, const void *q, const void *k_new, const void *v_new,

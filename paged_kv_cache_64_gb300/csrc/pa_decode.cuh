@@ -59,6 +59,12 @@ struct DecodeParams {
     // partials follow at part_base == prefix_parts, and the CTA that finishes
     // the item combines all of them into the output.
     int prefix_parts;
+    // FP8 pools (E4M3 codes): fl32(1 / scale) of each pool for the fused
+    // write, and the V scale applied to the output (the K scale is folded
+    // into scale_log2).
+    float k_inv;
+    float v_inv;
+    float v_scale;
 };
 
 // Length of sequence i, clamped to what the launch covers; a value out of
@@ -286,6 +292,12 @@ bool tc_supported(int head_dim, int group);
 int tc_ctas_per_sm(bool bf16, int head_dim);
 pa_status launch_decode_tc(const DecodeParams &prm, bool bf16, int head_dim, int num_partitions,
                            int num_kv_heads, int num_seqs, cudaStream_t stream);
+
+// Tensor-core decode over E4M3 pools (pa_decode_fp8.cu).
+bool fp8_supported(int head_dim, int group);
+int fp8_ctas_per_sm(bool bf16, int head_dim);
+pa_status launch_decode_fp8(const DecodeParams &prm, bool bf16, int head_dim, int num_partitions,
+                            int num_kv_heads, int num_seqs, cudaStream_t stream);
 
 // Prefix pass of the shared-prefix (cascade) decode (pa_cascade.cu): the
 // positions [0, prefix_len) that every sequence reaches through the same

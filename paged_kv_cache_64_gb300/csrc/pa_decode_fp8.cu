@@ -1,0 +1,586 @@
+// Paged decode over an FP8 KV cache for GB300 (sm_103a).
+//
+// The pools hold OCP E4M3 codes (one byte per element), one scale per K or V
+// pool: element = scale * code value ("b = 1 for FP8" in the KV-size formula
+// of "PagedAttention and Virtual Memory Management: Mathematical Foundations
+// ..." (llms.blog), section 1; format and scale are this build's readings).
+// Same computation as the tensor-core kernel in pa_decode_tc.cu (whose header
+// describes the products, the roles and the online softmax), with half the
+// K/V bytes moved:
+//   - the producer's TMA copies land the E4M3 tiles in a staging buffer
+//     (row-major, 16 rows of d bytes per box);
+//   - four converter warps widen them exactly to f16 (PTX
+//     cvt.rn.f16x2.e4m3x2: every E4M3 value is an f16 value) into the
+//     128-byte-swizzled K and V operand tiles, zeroing V rows past the end;
+//   - the MMAs run in kind::f16 with f16 operands (q converted to f16, P
+//     written as f16); the K scale is folded into the softmax scale and the V
+//     scale into the output.
+// The staging buffer and the operand tiles form a two-deep pipeline: the
+// copies of tile i+1 land while tile i is converted or multiplied.
+// Roles (10 warps): 0 producer, 1 TMEM owner and MMA issuer, 2..5 softmax and
+// epilogue, 6..9 converters.
+#include <cuda.h>  // CUtensorMap and its enums only; the encoder comes from the driver at run time
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pa_common.cuh"
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kF8Tile = 128;       // positions per tile (MMA M of q.K^T)
+constexpr int kF8N = 16;           // MMA N: the query heads of a group, zero-padded
+constexpr int kF8G = 8;            // largest group the kernel serves
+constexpr int kF8Warps = 10;
+constexpr int kF8Threads = kF8Warps * 32;
+constexpr int kF8Cols = 64;        // TMEM columns: S x2 and O x2, 16 fp32 columns each
+constexpr int kF8S0 = 0, kF8O0 = 32;
+constexpr int kF8Conv0 = 6;        // first converter warp
+
+enum F8Bar {
+    kStgFull = 0, kStgEmpty, kKFull, kVFull, kKEmpty, kVEmpty, kQReady,
+    kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kOFull0, kOFull1, kOEmpty0, kOEmpty1,
+    kNumF8Bars
+};
+
+template <int D>
+struct F8Shape {
+    static constexpr int KH = D / 64;                 // 64-dim (128-byte) f16 slabs along d
+    static constexpr int SLAB = kF8Tile * 128;        // one slab of a tile: 16 KiB
+    static constexpr int K_BYTES = KH * SLAB;
+    static constexpr int V_BYTES = 2 * SLAB;          // V^T is M = 128 dims; d = 64 pads with zeros
+    static constexpr int Q_BYTES = KH * kF8N * 128;   // q as a 16-row K-major operand
+    static constexpr int P_BYTES = 2 * kF8N * 128;    // P^T: 16 rows x 128 positions (two atoms)
+    static constexpr int STG_BYTES = kF8Tile * D;     // E4M3 tile of K (or V), row-major
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + K_BYTES;
+    static constexpr int OFF_Q = OFF_V + V_BYTES;
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;     // two buffers
+    static constexpr int OFF_SK = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_SV = OFF_SK + STG_BYTES;
+    static constexpr int OFF_RED = OFF_SV + STG_BYTES;
+    static constexpr int RED_BYTES = 3 * 4 * kF8N * 4;  // two tile-max buffers + the final sums
+    static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+    static constexpr int OFF_MISC = OFF_BAR + kNumF8Bars * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
+    static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
+    static_assert(OFF_SK % 128 == 0 && OFF_SV % 128 == 0, "TMA destinations");
+    static_assert(K_BYTES >= 2 * kF8G * kCombineMaxParts * 4, "combine scratch in the K tile");
+};
+
+// Fused cache write of the newest token into the E4M3 pools: quantise its K
+// and V (x * inv_scale in fp32, nearest code) and store them at its slot,
+// which must be the slot the block table gives for position L-1.  Threads
+// [0, 2 * d/16) take 16 elements each.
+template <bool BF16, int D>
+__device__ __forceinline__ void fused_cache_write_fp8(const DecodeParams &p, int seq, int kvh,
+                                                      int L) {
+    constexpr int chunks = D / 16;
+    const int t = threadIdx.x;
+    if (t >= 2 * chunks) return;
+    const int pos = L - 1;
+    const int phys = seq_table(p, seq)[pos >> p.log2_block];
+    const int off = pos & (p.block_size - 1);
+    const int64_t slot = p.slot_mapping[seq];
+    if ((unsigned)phys >= (unsigned)p.num_blocks || slot != (int64_t)phys * p.block_size + off) {
+        if (t == 0) record_error(p.err, PA_ERR_BAD_INDEX);
+        return;
+    }
+    const bool is_v = t >= chunks;
+    const int c = t % chunks;
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+                           (is_v ? p.v_new : p.k_new) + ((int64_t)seq * p.num_kv_heads + kvh) * D) +
+                       2 * c;
+    const uint4 q = quantize16_e4m3<BF16>(src[0], src[1], is_v ? p.v_inv : p.k_inv);
+    const uint8_t *pool = reinterpret_cast<const uint8_t *>(is_v ? p.v_pool : p.k_pool);
+    uint4 *dst = reinterpret_cast<uint4 *>(const_cast<uint8_t *>(pool) +
+                                           (((int64_t)phys * p.num_kv_heads + kvh) * p.block_size +
+                                            off) * D) +
+                 c;
+    *dst = q;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t narrow_f16(float x) {
+    __half h = __float2half_rn(x);
+    uint16_t u;
+    memcpy(&u, &h, 2);
+    return u;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t narrow_out(float x) {
+    if constexpr (BF16) {
+        __nv_bfloat16 h = __float2bfloat16_rn(x);
+        uint16_t u;
+        memcpy(&u, &h, 2);
+        return u;
+    } else {
+        return narrow_f16<false>(x);
+    }
+}
+
+template <bool BF16, int D>
+__global__ void __launch_bounds__(kF8Threads)
+    paged_decode_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v) {
+    using S = F8Shape<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::OFF_MISC + 8);
+    float *red = reinterpret_cast<float *>(smem + S::OFF_RED);
+
+    const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.group;
+    const int P = p.partition_tokens;
+    if (threadIdx.x == 0) {  // descriptors are kernel parameters: fetch them early
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
+    pdl_wait();  // inputs may come from the previous kernel on the stream
+    const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
+    const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
+    const int start = part * P;
+    if (start >= L) {  // empty partition: as in the other decode kernels
+        if (p.mode == 0) {
+            if (part == 0) {
+                uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
+                const int64_t base = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * D / 2;
+                for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) o[base + i] = 0u;
+            }
+        } else {
+            for (int g = 0; g < G; ++g) {
+                const int64_t row = part_row(p, seq, kvh * G + g, part);
+                if (threadIdx.x == 0) {
+                    p.part_m[row] = -INFINITY;
+                    p.part_l[row] = 0.f;
+                }
+                for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
+            }
+        }
+        return;
+    }
+    const int end = (start + P < L) ? start + P : L;
+    const int nunits = (end - start + kUnit - 1) / kUnit;
+    const int ntiles = (end - start + kF8Tile - 1) / kF8Tile;
+    const bool direct = (p.mode == 0) && (nparts_seq <= 1);
+
+    if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write_fp8<BF16, D>(p, seq, kvh, L);
+    if (threadIdx.x == 0) {
+        const int counts[kNumF8Bars] = {1, 4, 4, 4, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4};
+        for (int b = 0; b < kNumF8Bars; ++b) mbar_init(&bar[b], counts[b]);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kF8Cols);
+        tmem_relinquish();
+    }
+    if constexpr (D == 64) {
+        // rows 64..127 of the V^T operand: zero once, never written again
+        uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_V + S::SLAB);
+        for (int i = threadIdx.x; i < S::SLAB / 16; i += kF8Threads) z[i] = make_uint4(0, 0, 0, 0);
+        fence_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        const int32_t *table = seq_table(p, seq);
+        bool ok = true;
+        for (int u0 = 0; u0 < nunits && ok; u0 += 32) {  // 32 units = 4 tiles
+            const int u = u0 + lane;
+            int row0 = 0;  // first row of the unit in the 2-D view [NB*Hkv*B, d]
+            if (u < nunits) {
+                const int pos = start + u * kUnit;
+                int phys = table[pos >> p.log2_block];
+                if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                    record_error(p.err, PA_ERR_BAD_INDEX);
+                    phys = 0;
+                }
+                row0 = (phys * p.num_kv_heads + kvh) * p.block_size + (pos & (p.block_size - 1));
+            }
+            for (int t = u0 / 8; t < ntiles && t < (u0 + 32) / 8; ++t) {
+                const int nu = (nunits - 8 * t < 8) ? nunits - 8 * t : 8;
+                if (t >= 1) {  // the converters have read the previous tile's staging
+                    const bool done = mbar_wait(&bar[kStgEmpty], (t - 1) & 1);
+                    if (!__all_sync(kFullMask, done)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&bar[kStgFull], nu * 2 * kUnit * D);
+                // lane j < nu copies unit j of the tile (K and V): one
+                // instruction issues the tile's copies
+                const int r0 = __shfl_sync(kFullMask, row0, (8 * t - u0 + lane) & 31);
+                if (lane < nu) {
+                    tma_load_2d(smem + S::OFF_SK + lane * kUnit * D, &tmap_k, 0, r0, &bar[kStgFull]);
+                    tma_load_2d(smem + S::OFF_SV + lane * kUnit * D, &tmap_v, 0, r0, &bar[kStgFull]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) {
+            record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else if (warp >= kF8Conv0) {
+        // ---------------------------------------------------------- converters
+        // E4M3 staging -> f16 operand tiles: item = (row, 16 codes); rows past
+        // the end of the range get zeros in V (0 * NaN would poison P.V) and
+        // are masked in S.
+        const int ct = threadIdx.x - kF8Conv0 * 32;  // 0..127
+        bool ok = true;
+        auto convert = [&](int stg_off, int op_off, int nvalid, bool zero_stale) {
+            for (int it = ct; it < kF8Tile * (D / 16); it += 128) {
+                const int row = it / (D / 16), c = it % (D / 16);
+                uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+                if (!zero_stale || row < nvalid) {
+                    const uint4 raw =
+                        *reinterpret_cast<const uint4 *>(smem + stg_off + row * D + c * 16);
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        h[2 * i] = f16x2_from_e4m3x2((uint16_t)(w[i] & 0xffffu));
+                        h[2 * i + 1] = f16x2_from_e4m3x2((uint16_t)(w[i] >> 16));
+                    }
+                    lo = make_uint4(h[0], h[1], h[2], h[3]);
+                    hi = make_uint4(h[4], h[5], h[6], h[7]);
+                }
+                *reinterpret_cast<uint4 *>(smem + op_off + sw128_offset(row, c * 16, S::SLAB)) = lo;
+                *reinterpret_cast<uint4 *>(smem + op_off + sw128_offset(row, c * 16 + 8, S::SLAB)) = hi;
+            }
+            fence_async_smem();  // generic-proxy writes, read by the tensor cores
+            __syncwarp();
+        };
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int nvalid = (end - start - t * kF8Tile < kF8Tile) ? end - start - t * kF8Tile
+                                                                      : kF8Tile;
+            ok = __all_sync(kFullMask, mbar_wait(&bar[kStgFull], t & 1)) &&
+                 (t == 0 || __all_sync(kFullMask, mbar_wait(&bar[kKEmpty], (t - 1) & 1)));
+            if (!ok) break;
+            convert(S::OFF_SK, S::OFF_K, nvalid, false);
+            if (lane == 0) mbar_arrive(&bar[kKFull]);
+            ok = t == 0 || __all_sync(kFullMask, mbar_wait(&bar[kVEmpty], (t - 1) & 1));
+            if (!ok) break;
+            convert(S::OFF_SV, S::OFF_V, nvalid, true);
+            if (lane == 0) {
+                mbar_arrive(&bar[kVFull]);
+                mbar_arrive(&bar[kStgEmpty]);
+            }
+        }
+        if (!ok && lane == 0) {
+            record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = f16_idesc(false, false, false, kF8Tile, kF8N);
+            constexpr uint32_t idesc_pv = f16_idesc(false, true, false, 128, kF8N);
+            const uint32_t sbase = smem_addr(smem);
+            bool ok = mbar_wait(&bar[kQReady], 0);
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int b = i & 1;
+                ok = mbar_wait(&bar[kKFull], i & 1) &&
+                     (i < 2 || mbar_wait(&bar[kSEmpty0 + b], ((i >> 1) - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
+                    const uint32_t qoff = (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
+                    tc_mma(tmem + kF8S0 + 16 * b, sw128_desc(sbase + S::OFF_K + koff, 16, 1024),
+                           sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
+                }
+                tc_commit(&bar[kSFull0 + b]);
+                tc_commit(&bar[kKEmpty]);
+                ok = mbar_wait(&bar[kVFull], i & 1) && mbar_wait(&bar[kPFull0 + b], (i >> 1) & 1) &&
+                     (i < 2 || mbar_wait(&bar[kOEmpty0 + b], ((i >> 1) - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kF8Tile / 16; ++ks) {
+                    const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
+                    const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
+                    tc_mma(tmem + kF8O0 + 16 * b,
+                           sw128_desc(sbase + S::OFF_V + voff, S::SLAB, 1024),
+                           sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
+                }
+                tc_commit(&bar[kOFull0 + b]);
+                tc_commit(&bar[kVEmpty]);
+            }
+            if (!ok) {
+                record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- softmax / epilogue
+        const int sw = warp - 2;                 // softmax warp 0..3
+        const int quad = warp & 3;               // TMEM lane quadrant this warp may access
+        const int r = quad * 32 + lane;          // TMEM lane: position (S) or dimension (O)
+        const int st = threadIdx.x - 64;         // 0..127
+        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+
+        // q of the group as the K-major B operand in f16 (16 rows, 128-byte
+        // swizzle), rows >= G zero.  Unscaled: the scales are applied in fp32.
+        for (int ci = st; ci < kF8N * (D / 8); ci += 128) {
+            const int g = ci / (D / 8), c = ci % (D / 8);
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (g < G) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(
+                    p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * 8);
+                if constexpr (BF16) {
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                    uint32_t h[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = widen2<true>(w[i]);
+                        h[i] = narrow2<false>(f.x, f.y);
+                    }
+                    v = make_uint4(h[0], h[1], h[2], h[3]);
+                } else {
+                    v = raw;
+                }
+            }
+            *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(g, c * 8, kF8N * 128)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kQReady]);
+
+        float m_run[kF8G], m_true[kF8G], l_part[kF8G], acc[kF8G], alpha_prev[kF8G];
+#pragma unroll
+        for (int g = 0; g < kF8G; ++g) {
+            m_run[g] = -INFINITY;
+            m_true[g] = -INFINITY;
+            l_part[g] = 0.f;
+            acc[g] = 0.f;
+            alpha_prev[g] = 1.f;
+        }
+        bool failed = false;
+        auto accumulate = [&](int k) -> bool {
+            const int b = k & 1;
+            const bool landed = mbar_wait(&bar[kOFull0 + b], (k >> 1) & 1);
+            if (!__all_sync(kFullMask, landed)) return false;
+            tc_fence_after();
+            float o[16];
+            tmem_load16(tmem + lane_addr + kF8O0 + 16 * b, o);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kOEmpty0 + b]);
+#pragma unroll
+            for (int g = 0; g < kF8G; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
+            return true;
+        };
+
+        for (int i = 0; i < ntiles; ++i) {
+            const int b = i & 1;
+            const bool landed = !failed && mbar_wait(&bar[kSFull0 + b], (i >> 1) & 1);
+            const bool ok = __all_sync(kFullMask, landed);
+            float s[16];
+            if (ok) {
+                tc_fence_after();
+                tmem_load16(tmem + lane_addr + kF8S0 + 16 * b, s);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kSEmpty0 + b]);
+            } else {
+#pragma unroll
+                for (int g = 0; g < 16; ++g) s[g] = 0.f;
+            }
+            const int tile0 = start + i * kF8Tile;
+            const int nvalid = (end - tile0 < kF8Tile) ? end - tile0 : kF8Tile;
+            const bool valid = r < nvalid;
+            // tile max of each head over the 128 positions
+            float *tmax = red + b * (4 * kF8N);
+#pragma unroll
+            for (int g = 0; g < kF8G; ++g) {
+                s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;  // select: NaN-safe
+                float v = s[g];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
+                if (lane == 0) tmax[sw * kF8N + g] = v;
+            }
+            if (lane == 0) tmax[sw * kF8N + kF8N - 1] = ok ? 1.f : 0.f;  // column 15: health flag
+            softmax_bar();
+            bool all_ok = true;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) all_ok &= tmax[w * kF8N + kF8N - 1] != 0.f;
+            if (!all_ok) {
+                failed = true;
+                break;
+            }
+            bool need = false;
+            float mx[kF8G];
+#pragma unroll
+            for (int g = 0; g < kF8G; ++g) {
+                mx[g] = fmaxf(fmaxf(tmax[g], tmax[kF8N + g]),
+                              fmaxf(tmax[2 * kF8N + g], tmax[3 * kF8N + g]));
+                need |= (g < G) && (mx[g] > m_run[g] + kLazyRescale);
+            }
+            float alpha[kF8G];
+#pragma unroll
+            for (int g = 0; g < kF8G; ++g) {
+                alpha[g] = 1.f;
+                if (need) {  // block-uniform
+                    const float mn = fmaxf(m_run[g], mx[g]);
+                    alpha[g] = fast_exp2(m_run[g] - mn);
+                    m_run[g] = mn;
+                    l_part[g] *= alpha[g];
+                }
+                m_true[g] = fmaxf(m_true[g], mx[g]);
+            }
+            // P^T (16 rows = heads, 128 positions) in the operand layout, f16
+            uint8_t *pbuf = smem + S::OFF_P + b * S::P_BYTES;
+#pragma unroll
+            for (int g = 0; g < kF8N; ++g) {
+                float pv = 0.f;
+                if (g < kF8G && g < G) {
+                    pv = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
+                    l_part[g] += pv;
+                }
+                *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kF8N * 128)) =
+                    narrow_f16<false>(pv);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kPFull0 + b]);
+            if (i >= 1 && !accumulate(i - 1)) failed = true;
+#pragma unroll
+            for (int g = 0; g < kF8G; ++g) alpha_prev[g] = alpha[g];
+        }
+        if (!failed && !accumulate(ntiles - 1)) failed = true;
+
+        // l over the 128 position-threads, per head
+        float *lsum = red + 2 * (4 * kF8N);
+#pragma unroll
+        for (int g = 0; g < kF8G; ++g) {
+            float v = l_part[g];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
+            if (lane == 0) lsum[sw * kF8N + g] = v;
+        }
+        softmax_bar();
+        if (failed) {
+            if (st == 0) {
+                record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+        } else if (r < D) {
+#pragma unroll
+            for (int g = 0; g < kF8G; ++g) {
+                if (g >= G) break;
+                const float lt =
+                    lsum[g] + lsum[kF8N + g] + lsum[2 * kF8N + g] + lsum[3 * kF8N + g];
+                const float o = acc[g] / lt * p.v_scale;  // V elements are v_scale * codes
+                const int h = kvh * G + g;
+                if (direct) {
+                    uint16_t *out = static_cast<uint16_t *>(p.out);
+                    out[((int64_t)seq * p.num_q_heads + h) * D + r] = narrow_out<BF16>(o);
+                } else {
+                    const int64_t row = part_row(p, seq, h, part);
+                    p.part_o[row * D + r] = o;
+                    if (r == 0) {
+                        p.part_m[row] = m_true[g];
+                        p.part_l[row] = lt * fast_exp2(m_run[g] - m_true[g]);
+                    }
+                }
+            }
+        }
+    }
+
+    pdl_trigger();
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // let copies and MMAs still in flight finish before shared memory and
+        // TMEM are released (each wait is bounded)
+        (void)mbar_wait(&bar[kStgFull], (ntiles - 1) & 1);
+        (void)mbar_wait(&bar[kVEmpty], (ntiles - 1) & 1);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kF8Cols);
+    }
+    if (!direct && !*abort_flag && p.counters != nullptr)
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_K));
+}
+
+using F8Kernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
+
+F8Kernel pick_fp8(bool bf16, int D, int *smem) {
+    if (D == 128) {
+        *smem = F8Shape<128>::SMEM_BYTES;
+        return bf16 ? paged_decode_fp8_kernel<true, 128> : paged_decode_fp8_kernel<false, 128>;
+    }
+    *smem = F8Shape<64>::SMEM_BYTES;
+    return bf16 ? paged_decode_fp8_kernel<true, 64> : paged_decode_fp8_kernel<false, 64>;
+}
+
+}  // namespace
+
+bool fp8_supported(int head_dim, int group) {
+    return (head_dim == 64 || head_dim == 128) && group >= 1 && group <= kF8G;
+}
+
+// Resident CTAs per SM from the kernel's footprint (shared memory, registers
+// per sub-partition, TMEM), as for the 16-bit tensor-core kernel.
+int fp8_ctas_per_sm(bool bf16, int head_dim) {
+    int smem = 0;
+    F8Kernel k = pick_fp8(bf16, head_dim, &smem);
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return 1;
+    int dev = 0, smem_sm = 0, reserved = 0;
+    cudaFuncAttributes a;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess ||
+        cudaFuncGetAttributes(&a, k) != cudaSuccess)
+        return 1;
+    const int by_smem = smem_sm / (smem + (int)a.sharedSizeBytes + reserved);
+    const int regs = (a.numRegs + 7) / 8 * 8;
+    const int warps_per_subpartition = 16384 / (regs * 32);
+    const int by_regs = 4 * warps_per_subpartition / kF8Warps;
+    const int by_tmem = 512 / kF8Cols;
+    int n = by_smem < by_regs ? by_smem : by_regs;
+    n = n < by_tmem ? n : by_tmem;
+    return n > 0 ? n : 1;
+}
+
+pa_status launch_decode_fp8(const DecodeParams &prm, bool bf16, int head_dim, int num_partitions,
+                            int num_kv_heads, int num_seqs, cudaStream_t stream) {
+    if (num_seqs == 0) return PA_OK;
+    int smem = 0;
+    F8Kernel k = pick_fp8(bf16, head_dim, &smem);
+    if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return PA_ERR_CUDA;
+    const int64_t rows = (int64_t)prm.num_blocks * num_kv_heads * prm.block_size;
+    CUtensorMap mk, mv;
+    if (!pool_tensor_map_fp8(&mk, prm.k_pool, rows, head_dim) ||
+        !pool_tensor_map_fp8(&mv, prm.v_pool, rows, head_dim))
+        return PA_ERR_CUDA;
+    dim3 grid((unsigned)num_partitions, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    if (launch_pdl(k, grid, dim3(kF8Threads), (size_t)smem, stream, prm, mk, mv) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa

@@ -561,6 +561,21 @@ bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, bo
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An E4M3 pool [NB][Hkv][B][d] (one byte per element) viewed the same way;
+// boxes of 16 rows x d bytes, no swizzle (the copy lands in a row-major
+// staging tile).
+bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D};
+    const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)kUnit};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 using TcKernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
 
 static TcKernel pick_tc(bool bf16, int D, int *smem) {

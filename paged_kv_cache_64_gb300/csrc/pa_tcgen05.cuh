@@ -212,5 +212,7 @@ __device__ __forceinline__ void cluster_sync() {
 // The pool [NB][Hkv][B][d] viewed as a 2-D tensor of `rows` rows of d
 // elements, boxes of 16 rows x 64 columns, 128-byte swizzle (host side).
 bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, bool bf16);
+// The same for an E4M3 pool: boxes of 16 rows x d bytes, no swizzle.
+bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D);
 
 }  // namespace pa
