@@ -139,7 +139,7 @@ def source_digest():
     figure still describes the kernel being timed."""
     h = hashlib.sha256()
     for f in ("pa_decode.cu", "pa_decode_tc.cu", "pa_decode.cuh", "pa_common.cuh",
-              "pa_tcgen05.cuh", "pa_cascade.cu"):
+              "pa_tcgen05.cuh", "pa_cascade.cu", "pa_decode_fp8.cu"):
         with open(os.path.join(ROOT, "paged_kv_cache_64_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -289,7 +289,9 @@ def host_pool_timing(plan, reps=5):
 class GpuStep:
     """Device state of one workload and the calls of one decode step."""
 
-    def __init__(self, plan, device, partition_tokens=None, cascade=False):
+    FP8_SCALE = 1.0 / 64  # E4M3 pools of N(0, 1) values: +-448 codes cover +-7 sigma
+
+    def __init__(self, plan, device, partition_tokens=None, cascade=False, kv="16bit"):
         import torch
         from paged_kv_cache_64_gb300 import api, workloads
 
@@ -298,6 +300,12 @@ class GpuStep:
         self.device = device
         self.lay = workloads.layout(plan, workloads.native_allocator(plan))
         self.vals = workloads.make_values(plan, self.lay, device)
+        self.fp8 = kv == "fp8"
+        if self.fp8:
+            # the same N(0, 1) values, quantised into E4M3 pools (setup, untimed)
+            self.vals.k_pools = [self._quantize(p) for p in self.vals.k_pools]
+            self.vals.v_pools = [self._quantize(p) for p in self.vals.v_pools]
+            torch.cuda.empty_cache()
         t = lambda a: torch.as_tensor(a, device=device)
         self.tables, self.lens = t(self.lay.block_tables), t(self.lay.seq_lens)
         self.slots, self.copies = t(self.lay.slot_mapping), t(self.lay.pre_copies)
@@ -307,9 +315,9 @@ class GpuStep:
         self.resolved_P = self.P if self.P else api.auto_partition(
             spec.num_seqs, spec.num_kv_heads, self.max_seq_len, spec.head_dim, spec.block_size,
             spec.num_q_heads // spec.num_kv_heads, self.vals.q.dtype)
-        size = api.workspace_size(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads,
-                                  spec.head_dim, spec.block_size, self.max_seq_len, self.P,
-                                  self.vals.q.dtype)
+        wsize = api.fp8_workspace_size if self.fp8 else api.workspace_size
+        size = wsize(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                     spec.block_size, self.max_seq_len, self.P, self.vals.q.dtype)
         # shared-prefix (cascade) path: the prefix every sequence reaches
         # through the same block-table entries, attended once per KV head
         self.prefix_len = (api.shared_prefix_len(self.lay.block_tables, self.lay.seq_lens,
@@ -321,12 +329,13 @@ class GpuStep:
                                               self.vals.q.dtype)
         self.ws = api.alloc_workspace(size, device) if size else None
         self.out = [torch.empty_like(self.vals.q) for _ in range(spec.num_layers)]
-        self.logical_bytes = workloads.algorithmic_bytes(spec, self.lay.seq_lens)
+        kvb = 1 if self.fp8 else None
+        self.logical_bytes = workloads.algorithmic_bytes(spec, self.lay.seq_lens, kvb)
         self.decode_bytes = (workloads.cascade_bytes(spec, self.lay.seq_lens, self.prefix_len)
                              if self.prefix_len else self.logical_bytes)
-        self.write_bytes = workloads.cache_write_bytes(spec, spec.num_seqs)
+        self.write_bytes = workloads.cache_write_bytes(spec, spec.num_seqs, kvb)
         self.copy_bytes = 2 * 2 * len(self.lay.pre_copies) * spec.num_kv_heads * \
-            spec.block_size * spec.head_dim * workloads.DTYPE_BYTES[spec.dtype]
+            spec.block_size * spec.head_dim * (kvb or workloads.DTYPE_BYTES[spec.dtype])
         NP = -(-self.max_seq_len // self.resolved_P) if self.resolved_P and self.resolved_P > 0 else 1
         # fused write + decode (+ combine) launch, a separate combine above 8
         # partitions, and the copy-on-write copies when there are any
@@ -334,6 +343,20 @@ class GpuStep:
         if self.prefix_len:  # prefix pass + tail pass (write, decode and merge)
             per_layer = 2 + (1 if len(self.lay.pre_copies) else 0)
         self.launches_per_step = per_layer * spec.num_layers
+
+    def _quantize(self, pool16):
+        """E4M3 copy of a 16-bit pool, by the library's quantising cache
+        write over every slot, in chunks."""
+        torch, api = self.torch, self.api
+        nb, hkv, B, d = pool16.shape
+        out = torch.empty((nb, hkv, B, d), dtype=torch.uint8, device=pool16.device)
+        step = 4096
+        for b0 in range(0, nb, step):
+            b1 = min(nb, b0 + step)
+            tok = pool16[b0:b1].permute(0, 2, 1, 3).reshape(-1, hkv, d).contiguous()
+            slots = torch.arange(b0 * B, b1 * B, dtype=torch.int64, device=pool16.device)
+            api.cache_write_fp8(tok, tok, slots, out, out, self.FP8_SCALE, self.FP8_SCALE)
+        return out
 
     def step_bytes(self):
         return self.spec.num_layers * (self.decode_bytes + self.write_bytes + self.copy_bytes)
@@ -351,7 +374,15 @@ class GpuStep:
                 a = self.torch.cuda.Event(enable_timing=True)
                 b = self.torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-            if self.prefix_len:
+            if self.fp8:
+                # E4M3 pools: quantised write of the new token and the decode, one launch
+                api.decode_fp8(self.out[layer], q, kp, vp, self.tables, self.lens,
+                               self.max_seq_len, self.plan.scale, self.FP8_SCALE, self.FP8_SCALE,
+                               partition_tokens=self.P,
+                               k_new=v.k_new[layer] if k_new is None else k_new[layer],
+                               v_new=v.v_new[layer] if v_new is None else v_new[layer],
+                               slot_mapping=self.slots, workspace=self.ws, stream=stream)
+            elif self.prefix_len:
                 # prefix pass, then the tails with the new token's write and the merge
                 api.decode_cascade(self.out[layer], q, kp, vp, self.tables, self.lens,
                                    self.max_seq_len, self.plan.scale, self.prefix_len,
@@ -381,7 +412,7 @@ def run_gpu(args, rank, world, local_rank):
     base = workloads.SPECS[args.workload]
     plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs,
                                seed=base.seed + 1000 * rank if rank else None, apc=args.apc)
-    st = GpuStep(plan, device, args.partition_tokens, cascade=args.cascade)
+    st = GpuStep(plan, device, args.partition_tokens, cascade=args.cascade, kv=args.kv)
     stream = torch.cuda.current_stream()
     spec = st.spec
     flush = None
@@ -450,6 +481,9 @@ def run_gpu(args, rank, world, local_rank):
         dec_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
         kernel_note = ("pa_decode_step launch (new-token cache write + split-KV decode + combine), "
                        "CUDA events")
+        if st.fp8:
+            kernel_note = ("pa_decode_fp8 launch (quantised new-token write + decode over E4M3 "
+                           "pools + combine), CUDA events")
         if st.prefix_len:
             kernel_note = ("pa_decode_cascade call (tensor-core prefix pass + tail pass with the "
                            "new-token write and the merge), CUDA events")
@@ -461,7 +495,8 @@ def run_gpu(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     launch_bytes = st.decode_bytes + st.write_bytes  # what one decode_step launch must move
     achieved = launch_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = stored_traffic(args.workload + ("_cascade" if st.prefix_len else ""))
+    traffic = stored_traffic(args.workload + ("_cascade" if st.prefix_len else "") +
+                             ("_fp8" if st.fp8 else ""))
 
     # ------------------------------------------------ end to end (host buffers)
     # Every step copies its inputs from pinned host memory into the step's
@@ -504,7 +539,8 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": spec.dtype, "data": "synthetic",
+        "dtype": (f"e4m3 K/V ({spec.dtype} q/out, f16 products, fp32 accumulate)" if st.fp8
+                  else spec.dtype), "data": "synthetic",
         "config": {
             "workload": f"{spec.name}: {spec.describe}",
             "num_seqs": spec.num_seqs, "q_heads": spec.num_q_heads,
@@ -521,7 +557,10 @@ def run_gpu(args, rank, world, local_rank):
             "decode_path": (f"cascade, shared prefix {st.prefix_len} positions"
                             if st.prefix_len else "paged"),
             "launch": "CUDA graph replay" if graph is not None else "eager",
-            "decode_kernel": ("CUDA cores" if args.decode_impl == "cuda_cores"
+            "kv_format": ("E4M3 codes, scale 1/64 per pool, quantised from the same N(0,1) "
+                          "values" if st.fp8 else spec.dtype),
+            "decode_kernel": "tensor cores, E4M3 widened to f16 in shared memory" if st.fp8 else
+                             ("CUDA cores" if args.decode_impl == "cuda_cores"
                               else "tensor cores (tcgen05)"),
             "l2": ("inputs larger than L2 (%.2f GB per step)" % (st.step_bytes() / 1e9))
             if flush is None else "L2 flushed (256 MiB write) before every step",
@@ -576,6 +615,9 @@ def main(argv=None):
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix decode: attend the prefix every sequence shares "
                          "through its block table once per KV head (prefix workload)")
+    ap.add_argument("--kv", default="16bit", choices=["16bit", "fp8"],
+                    help="K/V pool format: the workload's 16-bit type, or E4M3 codes with one "
+                         "scale per pool (q and out stay 16-bit)")
     ap.add_argument("--apc", action="store_true",
                     help="prefix workload as separate requests laid out by the prefix-caching "
                          "pool (automatic prefix caching) instead of forks")
@@ -587,6 +629,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.apc and args.workload != "prefix":
         ap.error("--apc applies to the prefix workload")
+    if args.kv == "fp8" and args.cascade:
+        ap.error("--cascade reads 16-bit pools")
     rank, world, local_rank = dist_env()
     if world > 1:
         import torch.distributed as dist

@@ -304,12 +304,12 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             while (ok && nv < ntiles) {
                 bool moved = false;
                 if (nq < ntiles && nq <= nv + 1 &&
-                    mbar_try_wait(&bar[kCsFull0 + (nq & 1)], (nq >> 1) & 1)) {
+                    mbar_test_wait(&bar[kCsFull0 + (nq & 1)], (nq >> 1) & 1)) {
                     ok = issue_qk(nq);  // landed: returns at once
                     ++nq;
                     moved = true;
                 }
-                if (ok && nv < nq && mbar_try_wait(&bar[kCsPReady0 + (nv & 1)], (nv >> 1) & 1)) {
+                if (ok && nv < nq && mbar_test_wait(&bar[kCsPReady0 + (nv & 1)], (nv >> 1) & 1)) {
                     issue_pv(nv);
                     ++nv;
                     moved = true;

@@ -9,16 +9,17 @@
 // K/V bytes moved:
 //   - the producer's TMA copies land the E4M3 tiles in a staging buffer
 //     (row-major, 16 rows of d bytes per box);
-//   - four converter warps widen them exactly to f16 (PTX
+//   - converter warps (four for K, four for V) widen them exactly to f16 (PTX
 //     cvt.rn.f16x2.e4m3x2: every E4M3 value is an f16 value) into the
 //     128-byte-swizzled K and V operand tiles, zeroing V rows past the end;
 //   - the MMAs run in kind::f16 with f16 operands (q converted to f16, P
 //     written as f16); the K scale is folded into the softmax scale and the V
 //     scale into the output.
-// The staging buffer and the operand tiles form a two-deep pipeline: the
-// copies of tile i+1 land while tile i is converted or multiplied.
-// Roles (10 warps): 0 producer, 1 TMEM owner and MMA issuer, 2..5 softmax and
-// epilogue, 6..9 converters.
+// The staging buffer is a ring of several tiles (one CTA per SM holds it),
+// so the copies run that many tiles ahead of the conversion and the
+// products: the bytes in flight per SM, not the conversion, set the rate.
+// Roles (14 warps): 0 producer, 1 TMEM owner and MMA issuer, 2..5 softmax and
+// epilogue, 6..9 K converters, 10..13 V converters.
 #include <cuda.h>  // CUtensorMap and its enums only; the encoder comes from the driver at run time
 
 #include <cmath>
@@ -37,16 +38,20 @@ namespace {
 constexpr int kF8Tile = 128;       // positions per tile (MMA M of q.K^T)
 constexpr int kF8N = 16;           // MMA N: the query heads of a group, zero-padded
 constexpr int kF8G = 8;            // largest group the kernel serves
-constexpr int kF8Warps = 10;
+constexpr int kF8Warps = 14;
 constexpr int kF8Threads = kF8Warps * 32;
 constexpr int kF8Cols = 64;        // TMEM columns: S x2 and O x2, 16 fp32 columns each
 constexpr int kF8S0 = 0, kF8O0 = 32;
 constexpr int kF8Conv0 = 6;        // first converter warp
 
+constexpr int kF8MaxStages = 8;
+
 enum F8Bar {
-    kStgFull = 0, kStgEmpty, kKFull, kVFull, kKEmpty, kVEmpty, kQReady,
+    kKFull = 0, kVFull, kKEmpty, kVEmpty, kQReady,
     kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kOFull0, kOFull1, kOEmpty0, kOEmpty1,
-    kNumF8Bars
+    kStgFull0,                                // kF8MaxStages of each
+    kStgEmpty0 = kStgFull0 + kF8MaxStages,
+    kNumF8Bars = kStgEmpty0 + kF8MaxStages
 };
 
 template <int D>
@@ -58,19 +63,21 @@ struct F8Shape {
     static constexpr int Q_BYTES = KH * kF8N * 128;   // q as a 16-row K-major operand
     static constexpr int P_BYTES = 2 * kF8N * 128;    // P^T: 16 rows x 128 positions (two atoms)
     static constexpr int STG_BYTES = kF8Tile * D;     // E4M3 tile of K (or V), row-major
+    static constexpr int NSTG = D == 128 ? 4 : 8;     // staging ring: tiles in flight
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + K_BYTES;
     static constexpr int OFF_Q = OFF_V + V_BYTES;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;     // two buffers
-    static constexpr int OFF_SK = OFF_P + 2 * P_BYTES;
-    static constexpr int OFF_SV = OFF_SK + STG_BYTES;
-    static constexpr int OFF_RED = OFF_SV + STG_BYTES;
+    static constexpr int OFF_STG = OFF_P + 2 * P_BYTES;  // stage s: K at s * 2 * STG, V after it
+    static constexpr int OFF_RED = OFF_STG + NSTG * 2 * STG_BYTES;
     static constexpr int RED_BYTES = 3 * 4 * kF8N * 4;  // two tile-max buffers + the final sums
     static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
     static constexpr int OFF_MISC = OFF_BAR + kNumF8Bars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
-    static_assert(OFF_SK % 128 == 0 && OFF_SV % 128 == 0, "TMA destinations");
+    static_assert(OFF_STG % 128 == 0 && STG_BYTES % 128 == 0, "TMA destinations");
+    static_assert(NSTG <= kF8MaxStages, "stage barriers");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(K_BYTES >= 2 * kF8G * kCombineMaxParts * 4, "combine scratch in the K tile");
 };
 
@@ -128,7 +135,7 @@ __device__ __forceinline__ uint16_t narrow_out(float x) {
 }
 
 template <bool BF16, int D>
-__global__ void __launch_bounds__(kF8Threads)
+__global__ void __launch_bounds__(kF8Threads, 1)
     paged_decode_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v) {
     using S = F8Shape<D>;
@@ -178,8 +185,12 @@ __global__ void __launch_bounds__(kF8Threads)
 
     if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write_fp8<BF16, D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
-        const int counts[kNumF8Bars] = {1, 4, 4, 4, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4};
-        for (int b = 0; b < kNumF8Bars; ++b) mbar_init(&bar[b], counts[b]);
+        const int counts[kStgFull0] = {4, 4, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4};
+        for (int b = 0; b < kStgFull0; ++b) mbar_init(&bar[b], counts[b]);
+        for (int b = 0; b < kF8MaxStages; ++b) {
+            mbar_init(&bar[kStgFull0 + b], 1);   // the producer's expect-tx arrival
+            mbar_init(&bar[kStgEmpty0 + b], 8);  // one per converter warp (K and V groups)
+        }
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -216,20 +227,23 @@ __global__ void __launch_bounds__(kF8Threads)
             }
             for (int t = u0 / 8; t < ntiles && t < (u0 + 32) / 8; ++t) {
                 const int nu = (nunits - 8 * t < 8) ? nunits - 8 * t : 8;
-                if (t >= 1) {  // the converters have read the previous tile's staging
-                    const bool done = mbar_wait(&bar[kStgEmpty], (t - 1) & 1);
+                const int sg = t % S::NSTG;
+                if (t >= S::NSTG) {  // the converters have read this stage's previous tile
+                    const bool done = mbar_wait(&bar[kStgEmpty0 + sg], ((t / S::NSTG) - 1) & 1);
                     if (!__all_sync(kFullMask, done)) {
                         ok = false;
                         break;
                     }
                 }
-                if (lane == 0) mbar_arrive_expect_tx(&bar[kStgFull], nu * 2 * kUnit * D);
+                uint64_t *full = &bar[kStgFull0 + sg];
+                uint8_t *stg = smem + S::OFF_STG + sg * 2 * S::STG_BYTES;
+                if (lane == 0) mbar_arrive_expect_tx(full, nu * 2 * kUnit * D);
                 // lane j < nu copies unit j of the tile (K and V): one
                 // instruction issues the tile's copies
                 const int r0 = __shfl_sync(kFullMask, row0, (8 * t - u0 + lane) & 31);
                 if (lane < nu) {
-                    tma_load_2d(smem + S::OFF_SK + lane * kUnit * D, &tmap_k, 0, r0, &bar[kStgFull]);
-                    tma_load_2d(smem + S::OFF_SV + lane * kUnit * D, &tmap_v, 0, r0, &bar[kStgFull]);
+                    tma_load_2d(stg + lane * kUnit * D, &tmap_k, 0, r0, full);
+                    tma_load_2d(stg + S::STG_BYTES + lane * kUnit * D, &tmap_v, 0, r0, full);
                 }
                 __syncwarp();
             }
@@ -240,48 +254,56 @@ __global__ void __launch_bounds__(kF8Threads)
         }
     } else if (warp >= kF8Conv0) {
         // ---------------------------------------------------------- converters
-        // E4M3 staging -> f16 operand tiles: item = (row, 16 codes); rows past
+        // E4M3 staging -> f16 operand tiles, K by warps 6..9 and V by warps
+        // 10..13, each group at its own pace (K of the next tiles converts
+        // while V waits for the previous P.V).  Item = (row, 16 codes); every
+        // load of a thread is issued before the first conversion.  Rows past
         // the end of the range get zeros in V (0 * NaN would poison P.V) and
         // are masked in S.
-        const int ct = threadIdx.x - kF8Conv0 * 32;  // 0..127
+        const bool is_v = warp >= kF8Conv0 + 4;
+        const int ct = threadIdx.x - (kF8Conv0 + (is_v ? 4 : 0)) * 32;  // 0..127
+        constexpr int NIT = kF8Tile * (D / 16) / 128;
+        const int op_off = is_v ? S::OFF_V : S::OFF_K;
         bool ok = true;
-        auto convert = [&](int stg_off, int op_off, int nvalid, bool zero_stale) {
-            for (int it = ct; it < kF8Tile * (D / 16); it += 128) {
-                const int row = it / (D / 16), c = it % (D / 16);
-                uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-                if (!zero_stale || row < nvalid) {
-                    const uint4 raw =
-                        *reinterpret_cast<const uint4 *>(smem + stg_off + row * D + c * 16);
-                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                    uint32_t h[8];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        h[2 * i] = f16x2_from_e4m3x2((uint16_t)(w[i] & 0xffffu));
-                        h[2 * i + 1] = f16x2_from_e4m3x2((uint16_t)(w[i] >> 16));
-                    }
-                    lo = make_uint4(h[0], h[1], h[2], h[3]);
-                    hi = make_uint4(h[4], h[5], h[6], h[7]);
-                }
-                *reinterpret_cast<uint4 *>(smem + op_off + sw128_offset(row, c * 16, S::SLAB)) = lo;
-                *reinterpret_cast<uint4 *>(smem + op_off + sw128_offset(row, c * 16 + 8, S::SLAB)) = hi;
-            }
-            fence_async_smem();  // generic-proxy writes, read by the tensor cores
-            __syncwarp();
-        };
         for (int t = 0; t < ntiles && ok; ++t) {
             const int nvalid = (end - start - t * kF8Tile < kF8Tile) ? end - start - t * kF8Tile
                                                                       : kF8Tile;
-            ok = __all_sync(kFullMask, mbar_wait(&bar[kStgFull], t & 1)) &&
-                 (t == 0 || __all_sync(kFullMask, mbar_wait(&bar[kKEmpty], (t - 1) & 1)));
+            const int sg = t % S::NSTG;
+            const int stg = S::OFF_STG + sg * 2 * S::STG_BYTES + (is_v ? S::STG_BYTES : 0);
+            ok = __all_sync(kFullMask, mbar_wait(&bar[kStgFull0 + sg], (t / S::NSTG) & 1)) &&
+                 (t == 0 ||
+                  __all_sync(kFullMask, mbar_wait(&bar[is_v ? kVEmpty : kKEmpty], (t - 1) & 1)));
             if (!ok) break;
-            convert(S::OFF_SK, S::OFF_K, nvalid, false);
-            if (lane == 0) mbar_arrive(&bar[kKFull]);
-            ok = t == 0 || __all_sync(kFullMask, mbar_wait(&bar[kVEmpty], (t - 1) & 1));
-            if (!ok) break;
-            convert(S::OFF_SV, S::OFF_V, nvalid, true);
+            uint4 raw[NIT];
+#pragma unroll
+            for (int i = 0; i < NIT; ++i) {
+                const int it = ct + 128 * i;
+                const int row = it / (D / 16), c = it % (D / 16);
+                raw[i] = (is_v && row >= nvalid)
+                             ? make_uint4(0, 0, 0, 0)  // code 0 is +0
+                             : *reinterpret_cast<const uint4 *>(smem + stg + row * D + c * 16);
+            }
+#pragma unroll
+            for (int i = 0; i < NIT; ++i) {
+                const int it = ct + 128 * i;
+                const int row = it / (D / 16), c = it % (D / 16);
+                const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+                uint32_t h[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    h[2 * j] = f16x2_from_e4m3x2((uint16_t)(w[j] & 0xffffu));
+                    h[2 * j + 1] = f16x2_from_e4m3x2((uint16_t)(w[j] >> 16));
+                }
+                *reinterpret_cast<uint4 *>(smem + op_off + sw128_offset(row, c * 16, S::SLAB)) =
+                    make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(smem + op_off + sw128_offset(row, c * 16 + 8, S::SLAB)) =
+                    make_uint4(h[4], h[5], h[6], h[7]);
+            }
+            fence_async_smem();  // generic-proxy writes, read by the tensor cores
+            __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&bar[kVFull]);
-                mbar_arrive(&bar[kStgEmpty]);
+                mbar_arrive(&bar[is_v ? kVFull : kKFull]);
+                mbar_arrive(&bar[kStgEmpty0 + sg]);
             }
         }
         if (!ok && lane == 0) {
@@ -295,35 +317,54 @@ __global__ void __launch_bounds__(kF8Threads)
             constexpr uint32_t idesc_pv = f16_idesc(false, true, false, 128, kF8N);
             const uint32_t sbase = smem_addr(smem);
             bool ok = mbar_wait(&bar[kQReady], 0);
-            for (int i = 0; i < ntiles && ok; ++i) {
-                const int b = i & 1;
-                ok = mbar_wait(&bar[kKFull], i & 1) &&
-                     (i < 2 || mbar_wait(&bar[kSEmpty0 + b], ((i >> 1) - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
+            // Whichever is ready first: q.K^T of tile nq once its K has landed
+            // and its S buffer is free, or P.V of tile nv once its V, P and O
+            // buffer are.  q.K^T of the next tile therefore runs while the
+            // softmax works on this one, instead of waiting behind this P.V.
+            int nq = 0, nv = 0;
+            unsigned long long since = global_timer_ns();
+            unsigned spins = 0;
+            while (ok && nv < ntiles) {
+                bool moved = false;
+                if (nq < ntiles && mbar_test_wait(&bar[kKFull], nq & 1) &&
+                    (nq < 2 || mbar_test_wait(&bar[kSEmpty0 + (nq & 1)], ((nq >> 1) - 1) & 1))) {
+                    const int b = nq & 1;
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
-                    const uint32_t qoff = (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
-                    tc_mma(tmem + kF8S0 + 16 * b, sw128_desc(sbase + S::OFF_K + koff, 16, 1024),
-                           sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
+                        const uint32_t qoff = (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
+                        tc_mma(tmem + kF8S0 + 16 * b, sw128_desc(sbase + S::OFF_K + koff, 16, 1024),
+                               sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
+                    }
+                    tc_commit(&bar[kSFull0 + b]);
+                    tc_commit(&bar[kKEmpty]);
+                    ++nq;
+                    moved = true;
                 }
-                tc_commit(&bar[kSFull0 + b]);
-                tc_commit(&bar[kKEmpty]);
-                ok = mbar_wait(&bar[kVFull], i & 1) && mbar_wait(&bar[kPFull0 + b], (i >> 1) & 1) &&
-                     (i < 2 || mbar_wait(&bar[kOEmpty0 + b], ((i >> 1) - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
+                if (nv < nq && mbar_test_wait(&bar[kVFull], nv & 1) &&
+                    mbar_test_wait(&bar[kPFull0 + (nv & 1)], (nv >> 1) & 1) &&
+                    (nv < 2 || mbar_test_wait(&bar[kOEmpty0 + (nv & 1)], ((nv >> 1) - 1) & 1))) {
+                    const int b = nv & 1;
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < kF8Tile / 16; ++ks) {
-                    const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
-                    const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
-                    tc_mma(tmem + kF8O0 + 16 * b,
-                           sw128_desc(sbase + S::OFF_V + voff, S::SLAB, 1024),
-                           sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
+                    for (int ks = 0; ks < kF8Tile / 16; ++ks) {
+                        const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
+                        const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
+                        tc_mma(tmem + kF8O0 + 16 * b,
+                               sw128_desc(sbase + S::OFF_V + voff, S::SLAB, 1024),
+                               sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
+                    }
+                    tc_commit(&bar[kOFull0 + b]);
+                    tc_commit(&bar[kVEmpty]);
+                    ++nv;
+                    moved = true;
                 }
-                tc_commit(&bar[kOFull0 + b]);
-                tc_commit(&bar[kVEmpty]);
+                if (moved) {
+                    since = global_timer_ns();
+                } else if ((++spins & 31) == 0 && global_timer_ns() - since > kWaitLimitNs) {
+                    ok = false;
+                }
             }
             if (!ok) {
                 record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
@@ -512,8 +553,9 @@ __global__ void __launch_bounds__(kF8Threads)
     if (*abort_flag && threadIdx.x == 0) {
         // let copies and MMAs still in flight finish before shared memory and
         // TMEM are released (each wait is bounded)
-        (void)mbar_wait(&bar[kStgFull], (ntiles - 1) & 1);
-        (void)mbar_wait(&bar[kVEmpty], (ntiles - 1) & 1);
+        const int last = ntiles - 1;
+        (void)mbar_wait(&bar[kStgFull0 + last % S::NSTG], (last / S::NSTG) & 1);
+        (void)mbar_wait(&bar[kVEmpty], last & 1);
     }
     if (warp == 1) {
         __syncwarp();

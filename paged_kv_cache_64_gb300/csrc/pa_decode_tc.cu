@@ -282,35 +282,54 @@ __global__ void __launch_bounds__(kTcThreads)
             constexpr uint32_t idesc_pv = f16_idesc(BF16, true, false, 128, kTcN);
             const uint32_t sbase = smem_addr(smem);
             bool ok = mbar_wait(&bar[kQReady], 0);
-            for (int i = 0; i < ntiles && ok; ++i) {
-                const int b = i & 1;
-                ok = mbar_wait(&bar[kKFull], i & 1) &&
-                     (i < 2 || mbar_wait(&bar[kSEmpty0 + b], ((i >> 1) - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
+            // Whichever is ready first: q.K^T of tile nq once its K has landed
+            // and its S buffer is free, or P.V of tile nv once its V, P and O
+            // buffer are.  q.K^T of the next tile therefore runs while the
+            // softmax works on this one, instead of waiting behind this P.V.
+            int nq = 0, nv = 0;
+            unsigned long long since = global_timer_ns();
+            unsigned spins = 0;
+            while (ok && nv < ntiles) {
+                bool moved = false;
+                if (nq < ntiles && mbar_test_wait(&bar[kKFull], nq & 1) &&
+                    (nq < 2 || mbar_test_wait(&bar[kSEmpty0 + (nq & 1)], ((nq >> 1) - 1) & 1))) {
+                    const int b = nq & 1;
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
-                    const uint32_t qoff = (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
-                    tc_mma(tmem + kSCol0 + 16 * b, sw128_desc(sbase + S::OFF_K + koff, 16, 1024),
-                           sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
+                        const uint32_t qoff = (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
+                        tc_mma(tmem + kSCol0 + 16 * b, sw128_desc(sbase + S::OFF_K + koff, 16, 1024),
+                               sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
+                    }
+                    tc_commit(&bar[kSFull0 + b]);
+                    tc_commit(&bar[kKEmpty]);
+                    ++nq;
+                    moved = true;
                 }
-                tc_commit(&bar[kSFull0 + b]);
-                tc_commit(&bar[kKEmpty]);
-                ok = mbar_wait(&bar[kVFull], i & 1) && mbar_wait(&bar[kPFull0 + b], (i >> 1) & 1) &&
-                     (i < 2 || mbar_wait(&bar[kOEmpty0 + b], ((i >> 1) - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
+                if (nv < nq && mbar_test_wait(&bar[kVFull], nv & 1) &&
+                    mbar_test_wait(&bar[kPFull0 + (nv & 1)], (nv >> 1) & 1) &&
+                    (nv < 2 || mbar_test_wait(&bar[kOEmpty0 + (nv & 1)], ((nv >> 1) - 1) & 1))) {
+                    const int b = nv & 1;
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < kTcTile / 16; ++ks) {
-                    const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
-                    const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
-                    tc_mma(tmem + kOCol0 + 16 * b,
-                           sw128_desc(sbase + S::OFF_V + voff, S::SLAB, 1024),
-                           sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
+                    for (int ks = 0; ks < kTcTile / 16; ++ks) {
+                        const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
+                        const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
+                        tc_mma(tmem + kOCol0 + 16 * b,
+                               sw128_desc(sbase + S::OFF_V + voff, S::SLAB, 1024),
+                               sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
+                    }
+                    tc_commit(&bar[kOFull0 + b]);
+                    tc_commit(&bar[kVEmpty]);
+                    ++nv;
+                    moved = true;
                 }
-                tc_commit(&bar[kOFull0 + b]);
-                tc_commit(&bar[kVEmpty]);
+                if (moved) {
+                    since = global_timer_ns();
+                } else if ((++spins & 31) == 0 && global_timer_ns() - since > kWaitLimitNs) {
+                    ok = false;
+                }
             }
             if (!ok) {
                 record_error(p.err, PA_ERR_DEVICE_TIMEOUT);

@@ -263,21 +263,25 @@ def make_values(plan, lay, device, layers=None):
     return Values(q, kp, vp, kn, vn, kpre, vpre)
 
 
-def algorithmic_bytes(spec, seq_lens):
+def algorithmic_bytes(spec, seq_lens, kv_bytes=None):
     """Bytes the decode must move for one layer (K and V of every cached
-    token, the block-table entries used, q in, out, the length word)."""
+    token, the block-table entries used, q in, out, the length word).
+    kv_bytes: bytes per K/V element when the pools differ from q (1 for
+    E4M3 pools)."""
     b = DTYPE_BYTES[spec.dtype]
     L = np.asarray(seq_lens, dtype=np.int64)
-    kv = 2 * L.sum() * spec.num_kv_heads * spec.head_dim * b
+    kv = 2 * L.sum() * spec.num_kv_heads * spec.head_dim * (kv_bytes or b)
     table = 4 * sum(_blocks(x, spec.block_size) for x in L)
     qo = 2 * len(L) * spec.num_q_heads * spec.head_dim * b
     return int(kv + table + qo + 4 * len(L))
 
 
-def cache_write_bytes(spec, num_tokens):
-    """Bytes of one layer's cache write: read and write K and V of each token."""
+def cache_write_bytes(spec, num_tokens, kv_bytes=None):
+    """Bytes of one layer's cache write: read K and V of each token (16-bit)
+    and write them into the pools (kv_bytes per element, default 16-bit)."""
     b = DTYPE_BYTES[spec.dtype]
-    return int(2 * 2 * num_tokens * spec.num_kv_heads * spec.head_dim * b + 8 * num_tokens)
+    per = b + (kv_bytes or b)
+    return int(2 * per * num_tokens * spec.num_kv_heads * spec.head_dim + 8 * num_tokens)
 
 
 def cascade_bytes(spec, seq_lens, prefix_len):
