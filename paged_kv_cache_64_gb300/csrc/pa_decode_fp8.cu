@@ -9,7 +9,7 @@
 // K/V bytes moved:
 //   - the producer's TMA copies land the E4M3 tiles in a staging buffer
 //     (row-major, 16 rows of d bytes per box);
-//   - converter warps (four for K, four for V) widen them exactly to f16 (PTX
+//   - converter warps (three for K, three for V) widen them exactly to f16 (PTX
 //     cvt.rn.f16x2.e4m3x2: every E4M3 value is an f16 value) into the
 //     128-byte-swizzled K and V operand tiles, zeroing V rows past the end;
 //   - the MMAs run in kind::f16 with f16 operands (q converted to f16, P
@@ -18,8 +18,12 @@
 // The staging buffer is a ring of several tiles (one CTA per SM holds it),
 // so the copies run that many tiles ahead of the conversion and the
 // products: the bytes in flight per SM, not the conversion, set the rate.
-// Roles (14 warps): 0 producer, 1 TMEM owner and MMA issuer, 2..5 softmax and
-// epilogue, 6..9 K converters, 10..13 V converters.
+// Two softmax warpgroups take alternate tiles (even tiles with S, P and O
+// buffers 0, odd tiles with buffers 1), each with its own running maximum,
+// sum and accumulator, merged at the end, so two tiles' softmax run at once.
+// Roles (16 warps): 0 producer, 1 TMEM owner and MMA issuer, 2..5 and 6..9
+// softmax / epilogue groups A and B, 10..12 K converters, 13..15 V
+// converters.
 #include <cuda.h>  // CUtensorMap and its enums only; the encoder comes from the driver at run time
 
 #include <cmath>
@@ -38,16 +42,17 @@ namespace {
 constexpr int kF8Tile = 128;       // positions per tile (MMA M of q.K^T)
 constexpr int kF8N = 16;           // MMA N: the query heads of a group, zero-padded
 constexpr int kF8G = 8;            // largest group the kernel serves
-constexpr int kF8Warps = 14;
+constexpr int kF8Warps = 16;  // 4 per SM sub-partition: up to 128 registers a thread
 constexpr int kF8Threads = kF8Warps * 32;
 constexpr int kF8Cols = 64;        // TMEM columns: S x2 and O x2, 16 fp32 columns each
 constexpr int kF8S0 = 0, kF8O0 = 32;
-constexpr int kF8Conv0 = 6;        // first converter warp
+constexpr int kF8Conv0 = 10;       // first converter warp
+constexpr int kF8ConvWarps = 3;    // converter warps for K, and as many for V
 
 constexpr int kF8MaxStages = 8;
 
 enum F8Bar {
-    kKFull = 0, kVFull, kKEmpty, kVEmpty, kQReady,
+    kKFull0 = 0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1, kQReady,
     kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kOFull0, kOFull1, kOEmpty0, kOEmpty1,
     kStgFull0,                                // kF8MaxStages of each
     kStgEmpty0 = kStgFull0 + kF8MaxStages,
@@ -63,15 +68,22 @@ struct F8Shape {
     static constexpr int Q_BYTES = KH * kF8N * 128;   // q as a 16-row K-major operand
     static constexpr int P_BYTES = 2 * kF8N * 128;    // P^T: 16 rows x 128 positions (two atoms)
     static constexpr int STG_BYTES = kF8Tile * D;     // E4M3 tile of K (or V), row-major
-    static constexpr int NSTG = D == 128 ? 4 : 8;     // staging ring: tiles in flight
+    static constexpr int NSTG = D == 128 ? 2 : 4;     // staging ring: tiles in flight
+    static constexpr int NVB = 2;                     // V operand buffers (K has two)
+    // K and V operand tiles, two of each: tile t converts into buffer t & 1
+    // while the tensor cores still read the other
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = OFF_K + K_BYTES;
-    static constexpr int OFF_Q = OFF_V + V_BYTES;
+    static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
+    static constexpr int OFF_Q = OFF_V + NVB * V_BYTES;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;     // two buffers
     static constexpr int OFF_STG = OFF_P + 2 * P_BYTES;  // stage s: K at s * 2 * STG, V after it
     static constexpr int OFF_RED = OFF_STG + NSTG * 2 * STG_BYTES;
-    static constexpr int RED_BYTES = 3 * 4 * kF8N * 4;  // two tile-max buffers + the final sums
-    static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+    // per softmax group: two tile-max buffers and the final sums
+    static constexpr int RED_BYTES = 2 * 3 * 4 * kF8N * 4;
+    // group B's state for the final merge: acc [G][D], then m_run, m_true, l
+    static constexpr int OFF_XCH = OFF_RED + RED_BYTES;
+    static constexpr int XCH_BYTES = kF8G * D * 4 + 4 * kF8G * 4;
+    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
     static constexpr int OFF_MISC = OFF_BAR + kNumF8Bars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
@@ -112,6 +124,12 @@ __device__ __forceinline__ void fused_cache_write_fp8(const DecodeParams &p, int
                  c;
     *dst = q;
     asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Named barrier `id` over `n` threads (ids 1..3 are the softmax groups' own
+// and their joint one; 0 is __syncthreads).
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 template <bool BF16>
@@ -185,11 +203,14 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
     if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write_fp8<BF16, D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
-        const int counts[kStgFull0] = {4, 4, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4};
+        // kKFull / kVFull: the converter warps of K / V; kQReady, kSEmpty,
+        // kPFull, kOEmpty: the 4 warps of a softmax group
+        const int counts[kStgFull0] = {kF8ConvWarps, kF8ConvWarps, kF8ConvWarps, kF8ConvWarps,
+                                       1, 1, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4};
         for (int b = 0; b < kStgFull0; ++b) mbar_init(&bar[b], counts[b]);
         for (int b = 0; b < kF8MaxStages; ++b) {
             mbar_init(&bar[kStgFull0 + b], 1);   // the producer's expect-tx arrival
-            mbar_init(&bar[kStgEmpty0 + b], 8);  // one per converter warp (K and V groups)
+            mbar_init(&bar[kStgEmpty0 + b], 2 * kF8ConvWarps);  // every converter warp
         }
         *abort_flag = 0;
         mbar_init_fence();
@@ -199,9 +220,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         tmem_relinquish();
     }
     if constexpr (D == 64) {
-        // rows 64..127 of the V^T operand: zero once, never written again
-        uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_V + S::SLAB);
-        for (int i = threadIdx.x; i < S::SLAB / 16; i += kF8Threads) z[i] = make_uint4(0, 0, 0, 0);
+        // rows 64..127 of both V^T operand buffers: zero once, never written again
+        for (int vb = 0; vb < S::NVB; ++vb) {
+            uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_V + vb * S::V_BYTES + S::SLAB);
+            for (int i = threadIdx.x; i < S::SLAB / 16; i += kF8Threads) z[i] = make_uint4(0, 0, 0, 0);
+        }
         fence_async_smem();
     }
     tc_fence_before();
@@ -254,38 +277,43 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
     } else if (warp >= kF8Conv0) {
         // ---------------------------------------------------------- converters
-        // E4M3 staging -> f16 operand tiles, K by warps 6..9 and V by warps
-        // 10..13, each group at its own pace (K of the next tiles converts
+        // E4M3 staging -> f16 operand tiles, K by warps 10..12 and V by warps
+        // 13..15, each group at its own pace (K of the next tiles converts
         // while V waits for the previous P.V).  Item = (row, 16 codes); every
         // load of a thread is issued before the first conversion.  Rows past
         // the end of the range get zeros in V (0 * NaN would poison P.V) and
         // are masked in S.
-        const bool is_v = warp >= kF8Conv0 + 4;
-        const int ct = threadIdx.x - (kF8Conv0 + (is_v ? 4 : 0)) * 32;  // 0..127
-        constexpr int NIT = kF8Tile * (D / 16) / 128;
-        const int op_off = is_v ? S::OFF_V : S::OFF_K;
+        constexpr int NCT = kF8ConvWarps * 32;                 // threads per group
+        constexpr int NITEMS = kF8Tile * (D / 16);
+        constexpr int NIT = (NITEMS + NCT - 1) / NCT;
+        const bool is_v = warp >= kF8Conv0 + kF8ConvWarps;
+        const int ct = threadIdx.x - (kF8Conv0 + (is_v ? kF8ConvWarps : 0)) * 32;
         bool ok = true;
         for (int t = 0; t < ntiles && ok; ++t) {
             const int nvalid = (end - start - t * kF8Tile < kF8Tile) ? end - start - t * kF8Tile
                                                                       : kF8Tile;
             const int sg = t % S::NSTG;
             const int stg = S::OFF_STG + sg * 2 * S::STG_BYTES + (is_v ? S::STG_BYTES : 0);
+            const int nb = is_v ? S::NVB : 2;  // operand buffers
+            const int ob = t % nb;
+            const int op_off = is_v ? S::OFF_V + ob * S::V_BYTES : S::OFF_K + ob * S::K_BYTES;
             ok = __all_sync(kFullMask, mbar_wait(&bar[kStgFull0 + sg], (t / S::NSTG) & 1)) &&
-                 (t == 0 ||
-                  __all_sync(kFullMask, mbar_wait(&bar[is_v ? kVEmpty : kKEmpty], (t - 1) & 1)));
+                 (t < nb || __all_sync(kFullMask, mbar_wait(&bar[(is_v ? kVEmpty0 : kKEmpty0) + ob],
+                                                             ((t / nb) - 1) & 1)));
             if (!ok) break;
             uint4 raw[NIT];
 #pragma unroll
             for (int i = 0; i < NIT; ++i) {
-                const int it = ct + 128 * i;
+                const int it = ct + NCT * i;
                 const int row = it / (D / 16), c = it % (D / 16);
-                raw[i] = (is_v && row >= nvalid)
+                raw[i] = (it >= NITEMS || (is_v && row >= nvalid))
                              ? make_uint4(0, 0, 0, 0)  // code 0 is +0
                              : *reinterpret_cast<const uint4 *>(smem + stg + row * D + c * 16);
             }
 #pragma unroll
             for (int i = 0; i < NIT; ++i) {
-                const int it = ct + 128 * i;
+                const int it = ct + NCT * i;
+                if (it >= NITEMS) break;
                 const int row = it / (D / 16), c = it % (D / 16);
                 const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
                 uint32_t h[8];
@@ -302,7 +330,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             fence_async_smem();  // generic-proxy writes, read by the tensor cores
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&bar[is_v ? kVFull : kKFull]);
+                mbar_arrive(&bar[(is_v ? kVFull0 : kKFull0) + ob]);
                 mbar_arrive(&bar[kStgEmpty0 + sg]);
             }
         }
@@ -326,7 +354,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             unsigned spins = 0;
             while (ok && nv < ntiles) {
                 bool moved = false;
-                if (nq < ntiles && mbar_test_wait(&bar[kKFull], nq & 1) &&
+                if (nq < ntiles && mbar_test_wait(&bar[kKFull0 + (nq & 1)], (nq >> 1) & 1) &&
                     (nq < 2 || mbar_test_wait(&bar[kSEmpty0 + (nq & 1)], ((nq >> 1) - 1) & 1))) {
                     const int b = nq & 1;
                     tc_fence_after();
@@ -334,15 +362,16 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
                         const uint32_t qoff = (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
-                        tc_mma(tmem + kF8S0 + 16 * b, sw128_desc(sbase + S::OFF_K + koff, 16, 1024),
+                        tc_mma(tmem + kF8S0 + 16 * b,
+                               sw128_desc(sbase + S::OFF_K + b * S::K_BYTES + koff, 16, 1024),
                                sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
                     }
                     tc_commit(&bar[kSFull0 + b]);
-                    tc_commit(&bar[kKEmpty]);
+                    tc_commit(&bar[kKEmpty0 + b]);
                     ++nq;
                     moved = true;
                 }
-                if (nv < nq && mbar_test_wait(&bar[kVFull], nv & 1) &&
+                if (nv < nq && mbar_test_wait(&bar[kVFull0 + nv % S::NVB], (nv / S::NVB) & 1) &&
                     mbar_test_wait(&bar[kPFull0 + (nv & 1)], (nv >> 1) & 1) &&
                     (nv < 2 || mbar_test_wait(&bar[kOEmpty0 + (nv & 1)], ((nv >> 1) - 1) & 1))) {
                     const int b = nv & 1;
@@ -352,11 +381,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                         const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
                         const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
                         tc_mma(tmem + kF8O0 + 16 * b,
-                               sw128_desc(sbase + S::OFF_V + voff, S::SLAB, 1024),
+                               sw128_desc(sbase + S::OFF_V + (nv % S::NVB) * S::V_BYTES + voff,
+                                          S::SLAB, 1024),
                                sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
                     }
                     tc_commit(&bar[kOFull0 + b]);
-                    tc_commit(&bar[kVEmpty]);
+                    tc_commit(&bar[kVEmpty0 + nv % S::NVB]);
                     ++nv;
                     moved = true;
                 }
@@ -373,38 +403,44 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
     } else {
         // ---------------------------------------------------------- softmax / epilogue
-        const int sw = warp - 2;                 // softmax warp 0..3
+        const int grp = (warp - 2) >> 2;         // 0: even tiles, 1: odd tiles
+        const int sw = (warp - 2) & 3;           // warp within the group
         const int quad = warp & 3;               // TMEM lane quadrant this warp may access
         const int r = quad * 32 + lane;          // TMEM lane: position (S) or dimension (O)
-        const int st = threadIdx.x - 64;         // 0..127
+        const int st = sw * 32 + lane;           // 0..127 within the group
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        float *gred = red + grp * (3 * 4 * kF8N);  // this group's exchange area
+        float *xch = reinterpret_cast<float *>(smem + S::OFF_XCH);
 
-        // q of the group as the K-major B operand in f16 (16 rows, 128-byte
-        // swizzle), rows >= G zero.  Unscaled: the scales are applied in fp32.
-        for (int ci = st; ci < kF8N * (D / 8); ci += 128) {
-            const int g = ci / (D / 8), c = ci % (D / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (g < G) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(
-                    p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * 8);
-                if constexpr (BF16) {
-                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                    uint32_t h[4];
+        if (grp == 0) {
+            // q of the group of heads as the K-major B operand in f16 (16
+            // rows, 128-byte swizzle), rows >= G zero.  Unscaled: the scales
+            // are applied in fp32.
+            for (int ci = st; ci < kF8N * (D / 8); ci += 128) {
+                const int g = ci / (D / 8), c = ci % (D / 8);
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (g < G) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(
+                        p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * 8);
+                    if constexpr (BF16) {
+                        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                        uint32_t h[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = widen2<true>(w[i]);
-                        h[i] = narrow2<false>(f.x, f.y);
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 f = widen2<true>(w[i]);
+                            h[i] = narrow2<false>(f.x, f.y);
+                        }
+                        v = make_uint4(h[0], h[1], h[2], h[3]);
+                    } else {
+                        v = raw;
                     }
-                    v = make_uint4(h[0], h[1], h[2], h[3]);
-                } else {
-                    v = raw;
                 }
+                *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(g, c * 8, kF8N * 128)) = v;
             }
-            *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(g, c * 8, kF8N * 128)) = v;
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kQReady]);
         }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kQReady]);
 
         float m_run[kF8G], m_true[kF8G], l_part[kF8G], acc[kF8G], alpha_prev[kF8G];
 #pragma unroll
@@ -416,32 +452,32 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             alpha_prev[g] = 1.f;
         }
         bool failed = false;
+        // O of tile k (this group's buffer) into the accumulator
         auto accumulate = [&](int k) -> bool {
-            const int b = k & 1;
-            const bool landed = mbar_wait(&bar[kOFull0 + b], (k >> 1) & 1);
+            const bool landed = mbar_wait(&bar[kOFull0 + grp], (k >> 1) & 1);
             if (!__all_sync(kFullMask, landed)) return false;
             tc_fence_after();
             float o[16];
-            tmem_load16(tmem + lane_addr + kF8O0 + 16 * b, o);
+            tmem_load16(tmem + lane_addr + kF8O0 + 16 * grp, o);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kOEmpty0 + b]);
+            if (lane == 0) mbar_arrive(&bar[kOEmpty0 + grp]);
 #pragma unroll
             for (int g = 0; g < kF8G; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
             return true;
         };
 
-        for (int i = 0; i < ntiles; ++i) {
-            const int b = i & 1;
-            const bool landed = !failed && mbar_wait(&bar[kSFull0 + b], (i >> 1) & 1);
+        int last = -1;
+        for (int i = grp; i < ntiles; i += 2) {
+            const bool landed = !failed && mbar_wait(&bar[kSFull0 + grp], (i >> 1) & 1);
             const bool ok = __all_sync(kFullMask, landed);
             float s[16];
             if (ok) {
                 tc_fence_after();
-                tmem_load16(tmem + lane_addr + kF8S0 + 16 * b, s);
+                tmem_load16(tmem + lane_addr + kF8S0 + 16 * grp, s);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[kSEmpty0 + b]);
+                if (lane == 0) mbar_arrive(&bar[kSEmpty0 + grp]);
             } else {
 #pragma unroll
                 for (int g = 0; g < 16; ++g) s[g] = 0.f;
@@ -450,7 +486,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             const int nvalid = (end - tile0 < kF8Tile) ? end - tile0 : kF8Tile;
             const bool valid = r < nvalid;
             // tile max of each head over the 128 positions
-            float *tmax = red + b * (4 * kF8N);
+            float *tmax = gred + ((i >> 1) & 1) * (4 * kF8N);
 #pragma unroll
             for (int g = 0; g < kF8G; ++g) {
                 s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;  // select: NaN-safe
@@ -460,7 +496,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 if (lane == 0) tmax[sw * kF8N + g] = v;
             }
             if (lane == 0) tmax[sw * kF8N + kF8N - 1] = ok ? 1.f : 0.f;  // column 15: health flag
-            softmax_bar();
+            named_bar(1 + grp, 128);
             bool all_ok = true;
 #pragma unroll
             for (int w = 0; w < 4; ++w) all_ok &= tmax[w * kF8N + kF8N - 1] != 0.f;
@@ -480,7 +516,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 #pragma unroll
             for (int g = 0; g < kF8G; ++g) {
                 alpha[g] = 1.f;
-                if (need) {  // block-uniform
+                if (need) {  // group-uniform
                     const float mn = fmaxf(m_run[g], mx[g]);
                     alpha[g] = fast_exp2(m_run[g] - mn);
                     m_run[g] = mn;
@@ -488,29 +524,35 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 }
                 m_true[g] = fmaxf(m_true[g], mx[g]);
             }
-            // P^T (16 rows = heads, 128 positions) in the operand layout, f16
-            uint8_t *pbuf = smem + S::OFF_P + b * S::P_BYTES;
+            float pv[kF8G];
 #pragma unroll
-            for (int g = 0; g < kF8N; ++g) {
-                float pv = 0.f;
-                if (g < kF8G && g < G) {
-                    pv = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
-                    l_part[g] += pv;
+            for (int g = 0; g < kF8G; ++g) {
+                pv[g] = 0.f;
+                if (g < G) {
+                    pv[g] = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
+                    l_part[g] += pv[g];
                 }
-                *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kF8N * 128)) =
-                    narrow_f16<false>(pv);
             }
+            // this group's previous tile: its P.V, which reads the P buffer
+            // about to be rewritten, must be complete
+            if (last >= 0 && !accumulate(last)) failed = true;
+            // P^T (16 rows = heads, 128 positions) in the operand layout, f16
+            uint8_t *pbuf = smem + S::OFF_P + grp * S::P_BYTES;
+#pragma unroll
+            for (int g = 0; g < kF8N; ++g)
+                *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kF8N * 128)) =
+                    narrow_f16<false>(g < kF8G ? pv[g] : 0.f);
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kPFull0 + b]);
-            if (i >= 1 && !accumulate(i - 1)) failed = true;
+            if (lane == 0) mbar_arrive(&bar[kPFull0 + grp]);
 #pragma unroll
             for (int g = 0; g < kF8G; ++g) alpha_prev[g] = alpha[g];
+            last = i;
         }
-        if (!failed && !accumulate(ntiles - 1)) failed = true;
+        if (!failed && last >= 0 && !accumulate(last)) failed = true;
 
-        // l over the 128 position-threads, per head
-        float *lsum = red + 2 * (4 * kF8N);
+        // l over the group's 128 position-threads, per head
+        float *lsum = gred + 2 * (4 * kF8N);
 #pragma unroll
         for (int g = 0; g < kF8G; ++g) {
             float v = l_part[g];
@@ -518,29 +560,61 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
             if (lane == 0) lsum[sw * kF8N + g] = v;
         }
-        softmax_bar();
-        if (failed) {
-            if (st == 0) {
-                record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
-                *abort_flag = 1;
-            }
-        } else if (r < D) {
+        named_bar(1 + grp, 128);
+        float lt[kF8G];
 #pragma unroll
-            for (int g = 0; g < kF8G; ++g) {
-                if (g >= G) break;
-                const float lt =
-                    lsum[g] + lsum[kF8N + g] + lsum[2 * kF8N + g] + lsum[3 * kF8N + g];
-                const float o = acc[g] / lt * p.v_scale;  // V elements are v_scale * codes
-                const int h = kvh * G + g;
-                if (direct) {
-                    uint16_t *out = static_cast<uint16_t *>(p.out);
-                    out[((int64_t)seq * p.num_q_heads + h) * D + r] = narrow_out<BF16>(o);
-                } else {
-                    const int64_t row = part_row(p, seq, h, part);
-                    p.part_o[row * D + r] = o;
-                    if (r == 0) {
-                        p.part_m[row] = m_true[g];
-                        p.part_l[row] = lt * fast_exp2(m_run[g] - m_true[g]);
+        for (int g = 0; g < kF8G; ++g)
+            lt[g] = lsum[g] + lsum[kF8N + g] + lsum[2 * kF8N + g] + lsum[3 * kF8N + g];
+        // group B hands its state to group A
+        float *xacc = xch;                  // [kF8G][D]
+        float *xm = xch + kF8G * D;         // m_run, m_true, l, failed
+        if (grp == 1) {
+            if (r < D) {
+#pragma unroll
+                for (int g = 0; g < kF8G; ++g) xacc[g * D + r] = acc[g];
+            }
+            if (st == 0) {
+#pragma unroll
+                for (int g = 0; g < kF8G; ++g) {
+                    xm[g] = m_run[g];
+                    xm[kF8G + g] = m_true[g];
+                    xm[2 * kF8G + g] = lt[g];
+                }
+                xm[3 * kF8G] = failed ? 1.f : 0.f;
+            }
+        }
+        named_bar(3, 256);
+        if (grp == 0) {
+            failed |= xm[3 * kF8G] != 0.f;
+            if (failed) {
+                if (st == 0) {
+                    record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                }
+            } else if (r < D) {
+#pragma unroll
+                for (int g = 0; g < kF8G; ++g) {
+                    if (g >= G) break;
+                    // merge of the two groups' partial softmaxes
+                    const float mb = xm[g];
+                    const float M = fmaxf(m_run[g], mb);
+                    const float sa = fast_exp2(m_run[g] - M);
+                    const float sb = mb == -INFINITY ? 0.f : fast_exp2(mb - M);
+                    const float l = lt[g] * sa + xm[2 * kF8G + g] * sb;
+                    const float a = acc[g] * sa + xacc[g * D + r] * sb;
+                    const float mt = fmaxf(m_true[g], xm[kF8G + g]);
+                    const float o = a / l * p.v_scale;  // V elements are v_scale * codes
+                    const int h = kvh * G + g;
+                    if (direct) {
+                        uint16_t *out = static_cast<uint16_t *>(p.out);
+                        out[((int64_t)seq * p.num_q_heads + h) * D + r] = narrow_out<BF16>(o);
+                    } else {
+                        const int64_t row = part_row(p, seq, h, part);
+                        p.part_o[row * D + r] = o;
+                        if (r == 0) {
+                            p.part_m[row] = mt;
+                            p.part_l[row] = l * fast_exp2(M - mt);
+                        }
                     }
                 }
             }
@@ -555,7 +629,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         // TMEM are released (each wait is bounded)
         const int last = ntiles - 1;
         (void)mbar_wait(&bar[kStgFull0 + last % S::NSTG], (last / S::NSTG) & 1);
-        (void)mbar_wait(&bar[kVEmpty], last & 1);
+        (void)mbar_wait(&bar[kVEmpty0 + last % S::NVB], (last / S::NVB) & 1);
     }
     if (warp == 1) {
         __syncwarp();
