@@ -16,6 +16,7 @@ torch.distributed.run; every rank decodes its own batch (weak scaling, no
 collective on the data path); value = bytes of all ranks / max time.
 """
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -412,6 +413,8 @@ def run_gpu(args, rank, world, local_rank):
     base = workloads.SPECS[args.workload]
     plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs,
                                seed=base.seed + 1000 * rank if rank else None, apc=args.apc)
+    if args.layers:
+        plan.spec = dataclasses.replace(plan.spec, num_layers=int(args.layers))
     st = GpuStep(plan, device, args.partition_tokens, cascade=args.cascade, kv=args.kv)
     stream = torch.cuda.current_stream()
     spec = st.spec
@@ -604,6 +607,8 @@ def main(argv=None):
                     choices=["tiny", "qwen", "llama", "prefix", "long"])
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="shrink the batch (profiling of small cases only)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (profiling of small cases only)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
                     help="replay the step as a CUDA graph (auto: when the step has >1 layer)")
