@@ -6,24 +6,31 @@
 // ..." (llms.blog), section 1; format and scale are this build's readings).
 // Same computation as the tensor-core kernel in pa_decode_tc.cu (whose header
 // describes the products, the roles and the online softmax), with half the
-// K/V bytes moved:
-//   - the producer's TMA copies land the E4M3 tiles in a staging buffer
-//     (row-major, 16 rows of d bytes per box);
-//   - converter warps (three for K, three for V) widen them exactly to f16 (PTX
-//     cvt.rn.f16x2.e4m3x2: every E4M3 value is an f16 value) into the
-//     128-byte-swizzled K and V operand tiles, zeroing V rows past the end;
-//   - the MMAs run in kind::f16 with f16 operands (q converted to f16, P
-//     written as f16); the K scale is folded into the softmax scale and the V
-//     scale into the output.
-// The staging buffer is a ring of several tiles (one CTA per SM holds it),
-// so the copies run that many tiles ahead of the conversion and the
-// products: the bytes in flight per SM, not the conversion, set the rate.
-// Two softmax warpgroups take alternate tiles (even tiles with S, P and O
-// buffers 0, odd tiles with buffers 1), each with its own running maximum,
-// sum and accumulator, merged at the end, so two tiles' softmax run at once.
+// K/V bytes moved.  Per tile of 128 positions:
+//
+//   S^T[128 pos x 32] = K_codes[128 x d] . Qs^T[d x 32]   kind::f8f6f4, E4M3 x E4M3
+//   O^T[128 x 16]     = V^T[128 x 128 pos] . P^T[128 x 16] kind::f16
+//
+// q.K^T reads the E4M3 K tile exactly as the TMA copy lands it (K-major,
+// swizzled), so K is never converted.  Its other operand, Qs, holds each query
+// head as three E4M3 terms: with 2^e_g the power of two that brings head g's
+// largest |q| into [128, 256), q_g * 2^e_g = t1 + t2 + t3, t1 the nearest
+// E4M3 value, t2 that of the remainder, t3 that of the next remainder (each
+// remainder is exact in fp32).  A 16-bit q has at most 11 significant bits
+// and each term carries 4, so the sum equals q * 2^e_g except for elements
+// below 2^-17 of the head's largest (E4M3's subnormal floor), and the three
+// S columns of a head add up, times 2^-e_g, to q.K^T within fp32 rounding.
+// V goes through the f16 path: converter warps widen its codes exactly to f16
+// (cvt.rn.f16x2.e4m3x2: every E4M3 value is an f16 value) into the MN-major
+// V^T operand, zeroing rows past the end; P is written as f16.  The K scale is
+// folded into the softmax scale, the V scale into the output.
+// The staging ring (4 tiles of K and V at d = 128, 8 at d = 64) is the only
+// large buffer besides the two f16 V operands, so the copies run that many
+// tiles ahead.  Two softmax warpgroups take alternate tiles (even tiles with
+// S, P and O buffers 0, odd tiles with buffers 1), each with its own running
+// maximum, sum and accumulator, merged at the end.
 // Roles (16 warps): 0 producer, 1 TMEM owner and MMA issuer, 2..5 and 6..9
-// softmax / epilogue groups A and B, 10..12 K converters, 13..15 V
-// converters.
+// softmax / epilogue groups A and B (A also builds Qs), 10..15 V converters.
 #include <cuda.h>  // CUtensorMap and its enums only; the encoder comes from the driver at run time
 
 #include <cmath>
@@ -40,19 +47,20 @@ namespace pa {
 namespace {
 
 constexpr int kF8Tile = 128;       // positions per tile (MMA M of q.K^T)
-constexpr int kF8N = 16;           // MMA N: the query heads of a group, zero-padded
+constexpr int kF8N = 16;           // MMA N of P.V: the query heads of a group, zero-padded
+constexpr int kF8QN = 32;          // MMA N of q.K^T: three E4M3 terms x 8 heads, zero-padded
 constexpr int kF8G = 8;            // largest group the kernel serves
 constexpr int kF8Warps = 16;  // 4 per SM sub-partition: up to 128 registers a thread
 constexpr int kF8Threads = kF8Warps * 32;
-constexpr int kF8Cols = 64;        // TMEM columns: S x2 and O x2, 16 fp32 columns each
-constexpr int kF8S0 = 0, kF8O0 = 32;
+constexpr int kF8Cols = 128;       // TMEM columns: S x2 (32 each) at 0, O x2 (16 each) at 64
+constexpr int kF8S0 = 0, kF8O0 = 64;
 constexpr int kF8Conv0 = 10;       // first converter warp
-constexpr int kF8ConvWarps = 3;    // converter warps for K, and as many for V
+constexpr int kF8ConvWarps = 6;    // converter warps (V)
 
 constexpr int kF8MaxStages = 8;
 
 enum F8Bar {
-    kKFull0 = 0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1, kQReady,
+    kVFull0 = 0, kVFull1, kVEmpty0, kVEmpty1, kQReady,
     kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kOFull0, kOFull1, kOEmpty0, kOEmpty1,
     kStgFull0,                                // kF8MaxStages of each
     kStgEmpty0 = kStgFull0 + kF8MaxStages,
@@ -61,37 +69,63 @@ enum F8Bar {
 
 template <int D>
 struct F8Shape {
-    static constexpr int KH = D / 64;                 // 64-dim (128-byte) f16 slabs along d
-    static constexpr int SLAB = kF8Tile * 128;        // one slab of a tile: 16 KiB
-    static constexpr int K_BYTES = KH * SLAB;
+    static constexpr int SLAB = kF8Tile * 128;        // one 64-dim f16 slab of a tile: 16 KiB
     static constexpr int V_BYTES = 2 * SLAB;          // V^T is M = 128 dims; d = 64 pads with zeros
-    static constexpr int Q_BYTES = KH * kF8N * 128;   // q as a 16-row K-major operand
+    static constexpr int STG_BYTES = kF8Tile * D;     // E4M3 tile of K (or V): 128 rows of d bytes
+    // K tiles and Qs: K-major E4M3 operands of d-byte rows, in atoms of 8 rows
+    // (128-byte swizzle for d = 128, 64-byte for d = 64)
+    static constexpr int Q_BYTES = kF8QN * D;
     static constexpr int P_BYTES = 2 * kF8N * 128;    // P^T: 16 rows x 128 positions (two atoms)
-    static constexpr int STG_BYTES = kF8Tile * D;     // E4M3 tile of K (or V), row-major
-    static constexpr int NSTG = D == 128 ? 2 : 4;     // staging ring: tiles in flight
-    static constexpr int NVB = 2;                     // V operand buffers (K has two)
-    // K and V operand tiles, two of each: tile t converts into buffer t & 1
-    // while the tensor cores still read the other
-    static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
+    static constexpr int NSTG = D == 128 ? 4 : 8;     // staging ring: tiles in flight
+    static constexpr int NVB = 2;                     // V operand buffers
+    static constexpr int OFF_STG = 0;                 // stage s: K at s * 2 * STG, V after it
+    static constexpr int OFF_V = OFF_STG + NSTG * 2 * STG_BYTES;
     static constexpr int OFF_Q = OFF_V + NVB * V_BYTES;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;     // two buffers
-    static constexpr int OFF_STG = OFF_P + 2 * P_BYTES;  // stage s: K at s * 2 * STG, V after it
-    static constexpr int OFF_RED = OFF_STG + NSTG * 2 * STG_BYTES;
+    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;
     // per softmax group: two tile-max buffers and the final sums
     static constexpr int RED_BYTES = 2 * 3 * 4 * kF8N * 4;
+    // per head: softmax scale (log2 units, K scale included) times 2^-e_g
+    static constexpr int OFF_QMUL = OFF_RED + RED_BYTES;
     // group B's state for the final merge: acc [G][D], then m_run, m_true, l
-    static constexpr int OFF_XCH = OFF_RED + RED_BYTES;
+    static constexpr int OFF_XCH = OFF_QMUL + kF8G * 4;
     static constexpr int XCH_BYTES = kF8G * D * 4 + 4 * kF8G * 4;
     static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
     static constexpr int OFF_MISC = OFF_BAR + kNumF8Bars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
-    static_assert(OFF_STG % 128 == 0 && STG_BYTES % 128 == 0, "TMA destinations");
+    static_assert((2 * STG_BYTES) % 1024 == 0 && STG_BYTES % 1024 == 0, "TMA swizzle alignment");
     static_assert(NSTG <= kF8MaxStages, "stage barriers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-    static_assert(K_BYTES >= 2 * kF8G * kCombineMaxParts * 4, "combine scratch in the K tile");
+    static_assert(NSTG * 2 * STG_BYTES >= 2 * kF8G * kCombineMaxParts * 4,
+                  "combine scratch in the staging ring");
 };
+
+// Byte offset of element (row, k) in a K-major E4M3 operand of D-byte rows
+// stored in swizzled atoms of 8 rows (the layout the TMA copy writes): the
+// 16-byte chunk c of row r sits at chunk c ^ (r & 7) for d = 128 (128-byte
+// swizzle) and c ^ ((r >> 1) & 3) for d = 64 (64-byte swizzle).
+template <int D>
+__device__ __forceinline__ uint32_t e4m3_operand_offset(int row, int k) {
+    const int sw = D == 128 ? (row & 7) : ((row >> 1) & 3);
+    return (uint32_t)((row >> 3) * 8 * D + (row & 7) * D + ((((k >> 4) ^ sw)) << 4) + (k & 15));
+}
+
+template <int D>
+__device__ __forceinline__ uint64_t e4m3_operand_desc(uint32_t saddr) {
+    return D == 128 ? sw128_desc(saddr, 16, 8 * D) : sw64_desc(saddr, 16, 8 * D);
+}
+
+// 2^e for e in [-126, 127], exactly.
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// E4M3 code (low byte) back to fp32, exactly.
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t codes) {
+    const uint32_t h = f16x2_from_e4m3x2((uint16_t)codes);
+    __half2 hh;
+    memcpy(&hh, &h, 4);
+    return __half22float2(hh);
+}
 
 // Fused cache write of the newest token into the E4M3 pools: quantise its K
 // and V (x * inv_scale in fp32, nearest code) and store them at its slot,
@@ -164,6 +198,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::OFF_MISC + 8);
     float *red = reinterpret_cast<float *>(smem + S::OFF_RED);
+    float *qmul = reinterpret_cast<float *>(smem + S::OFF_QMUL);
 
     const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,14 +238,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
     if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write_fp8<BF16, D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
-        // kKFull / kVFull: the converter warps of K / V; kQReady, kSEmpty,
-        // kPFull, kOEmpty: the 4 warps of a softmax group
-        const int counts[kStgFull0] = {kF8ConvWarps, kF8ConvWarps, kF8ConvWarps, kF8ConvWarps,
-                                       1, 1, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4};
+        // kVFull: the converter warps; kQReady, kSEmpty, kPFull, kOEmpty: the
+        // 4 warps of a softmax group; kStgEmpty: the converters and the
+        // commit of q.K^T (which reads the stage's K tile)
+        const int counts[kStgFull0] = {kF8ConvWarps, kF8ConvWarps, 1, 1, 4, 1, 1, 4, 4,
+                                       4, 4, 1, 1, 4, 4};
         for (int b = 0; b < kStgFull0; ++b) mbar_init(&bar[b], counts[b]);
         for (int b = 0; b < kF8MaxStages; ++b) {
             mbar_init(&bar[kStgFull0 + b], 1);   // the producer's expect-tx arrival
-            mbar_init(&bar[kStgEmpty0 + b], 2 * kF8ConvWarps);  // every converter warp
+            mbar_init(&bar[kStgEmpty0 + b], kF8ConvWarps + 1);
         }
         *abort_flag = 0;
         mbar_init_fence();
@@ -251,7 +287,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             for (int t = u0 / 8; t < ntiles && t < (u0 + 32) / 8; ++t) {
                 const int nu = (nunits - 8 * t < 8) ? nunits - 8 * t : 8;
                 const int sg = t % S::NSTG;
-                if (t >= S::NSTG) {  // the converters have read this stage's previous tile
+                if (t >= S::NSTG) {  // q.K^T and the converters are done with the stage
                     const bool done = mbar_wait(&bar[kStgEmpty0 + sg], ((t / S::NSTG) - 1) & 1);
                     if (!__all_sync(kFullMask, done)) {
                         ok = false;
@@ -276,37 +312,33 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             *abort_flag = 1;
         }
     } else if (warp >= kF8Conv0) {
-        // ---------------------------------------------------------- converters
-        // E4M3 staging -> f16 operand tiles, K by warps 10..12 and V by warps
-        // 13..15, each group at its own pace (K of the next tiles converts
-        // while V waits for the previous P.V).  Item = (row, 16 codes); every
-        // load of a thread is issued before the first conversion.  Rows past
-        // the end of the range get zeros in V (0 * NaN would poison P.V) and
-        // are masked in S.
-        constexpr int NCT = kF8ConvWarps * 32;                 // threads per group
+        // ---------------------------------------------------------- V converters
+        // E4M3 staging (row-major) -> f16 V^T operand (MN-major, 128-byte
+        // swizzle).  Item = (row, 16 codes); every load of a thread is issued
+        // before the first conversion.  Rows past the end of the range get
+        // zeros (0 * NaN would poison P.V).
+        constexpr int NCT = kF8ConvWarps * 32;
         constexpr int NITEMS = kF8Tile * (D / 16);
         constexpr int NIT = (NITEMS + NCT - 1) / NCT;
-        const bool is_v = warp >= kF8Conv0 + kF8ConvWarps;
-        const int ct = threadIdx.x - (kF8Conv0 + (is_v ? kF8ConvWarps : 0)) * 32;
+        const int ct = threadIdx.x - kF8Conv0 * 32;
         bool ok = true;
         for (int t = 0; t < ntiles && ok; ++t) {
             const int nvalid = (end - start - t * kF8Tile < kF8Tile) ? end - start - t * kF8Tile
                                                                       : kF8Tile;
             const int sg = t % S::NSTG;
-            const int stg = S::OFF_STG + sg * 2 * S::STG_BYTES + (is_v ? S::STG_BYTES : 0);
-            const int nb = is_v ? S::NVB : 2;  // operand buffers
-            const int ob = t % nb;
-            const int op_off = is_v ? S::OFF_V + ob * S::V_BYTES : S::OFF_K + ob * S::K_BYTES;
+            const int stg = S::OFF_STG + sg * 2 * S::STG_BYTES + S::STG_BYTES;
+            const int ob = t % S::NVB;
+            const int op_off = S::OFF_V + ob * S::V_BYTES;
             ok = __all_sync(kFullMask, mbar_wait(&bar[kStgFull0 + sg], (t / S::NSTG) & 1)) &&
-                 (t < nb || __all_sync(kFullMask, mbar_wait(&bar[(is_v ? kVEmpty0 : kKEmpty0) + ob],
-                                                             ((t / nb) - 1) & 1)));
+                 (t < S::NVB ||
+                  __all_sync(kFullMask, mbar_wait(&bar[kVEmpty0 + ob], ((t / S::NVB) - 1) & 1)));
             if (!ok) break;
             uint4 raw[NIT];
 #pragma unroll
             for (int i = 0; i < NIT; ++i) {
                 const int it = ct + NCT * i;
                 const int row = it / (D / 16), c = it % (D / 16);
-                raw[i] = (it >= NITEMS || (is_v && row >= nvalid))
+                raw[i] = (it >= NITEMS || row >= nvalid)
                              ? make_uint4(0, 0, 0, 0)  // code 0 is +0
                              : *reinterpret_cast<const uint4 *>(smem + stg + row * D + c * 16);
             }
@@ -330,7 +362,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             fence_async_smem();  // generic-proxy writes, read by the tensor cores
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&bar[(is_v ? kVFull0 : kKFull0) + ob]);
+                mbar_arrive(&bar[kVFull0 + ob]);
                 mbar_arrive(&bar[kStgEmpty0 + sg]);
             }
         }
@@ -341,33 +373,30 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = f16_idesc(false, false, false, kF8Tile, kF8N);
+            constexpr uint32_t idesc_qk = e4m3_idesc(kF8Tile, kF8QN);
             constexpr uint32_t idesc_pv = f16_idesc(false, true, false, 128, kF8N);
             const uint32_t sbase = smem_addr(smem);
             bool ok = mbar_wait(&bar[kQReady], 0);
-            // Whichever is ready first: q.K^T of tile nq once its K has landed
-            // and its S buffer is free, or P.V of tile nv once its V, P and O
-            // buffer are.  q.K^T of the next tile therefore runs while the
-            // softmax works on this one, instead of waiting behind this P.V.
+            // Whichever is ready first: q.K^T of tile nq once its stage has
+            // landed and its S buffer is free, or P.V of tile nv once its V,
+            // P and O buffer are.
             int nq = 0, nv = 0;
             unsigned long long since = global_timer_ns();
             unsigned spins = 0;
             while (ok && nv < ntiles) {
                 bool moved = false;
-                if (nq < ntiles && mbar_test_wait(&bar[kKFull0 + (nq & 1)], (nq >> 1) & 1) &&
+                if (nq < ntiles &&
+                    mbar_test_wait(&bar[kStgFull0 + nq % S::NSTG], (nq / S::NSTG) & 1) &&
                     (nq < 2 || mbar_test_wait(&bar[kSEmpty0 + (nq & 1)], ((nq >> 1) - 1) & 1))) {
-                    const int b = nq & 1;
+                    const int b = nq & 1, sg = nq % S::NSTG;
+                    const uint32_t kaddr = sbase + S::OFF_STG + sg * 2 * S::STG_BYTES;
                     tc_fence_after();
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
-                        const uint32_t qoff = (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
-                        tc_mma(tmem + kF8S0 + 16 * b,
-                               sw128_desc(sbase + S::OFF_K + b * S::K_BYTES + koff, 16, 1024),
-                               sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
-                    }
+                    for (int ks = 0; ks < D / 32; ++ks)  // 32 codes (bytes) of d per MMA
+                        tc_mma_f8(tmem + kF8S0 + kF8QN * b, e4m3_operand_desc<D>(kaddr + ks * 32),
+                                  e4m3_operand_desc<D>(sbase + S::OFF_Q + ks * 32), idesc_qk, ks > 0);
                     tc_commit(&bar[kSFull0 + b]);
-                    tc_commit(&bar[kKEmpty0 + b]);
+                    tc_commit(&bar[kStgEmpty0 + sg]);
                     ++nq;
                     moved = true;
                 }
@@ -380,7 +409,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     for (int ks = 0; ks < kF8Tile / 16; ++ks) {
                         const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
                         const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
-                        tc_mma(tmem + kF8O0 + 16 * b,
+                        tc_mma(tmem + kF8O0 + kF8N * b,
                                sw128_desc(sbase + S::OFF_V + (nv % S::NVB) * S::V_BYTES + voff,
                                           S::SLAB, 1024),
                                sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
@@ -413,34 +442,83 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         float *xch = reinterpret_cast<float *>(smem + S::OFF_XCH);
 
         if (grp == 0) {
-            // q of the group of heads as the K-major B operand in f16 (16
-            // rows, 128-byte swizzle), rows >= G zero.  Unscaled: the scales
-            // are applied in fp32.
-            for (int ci = st; ci < kF8N * (D / 8); ci += 128) {
-                const int g = ci / (D / 8), c = ci % (D / 8);
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (g < G) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(
-                        p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * 8);
-                    if constexpr (BF16) {
-                        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                        uint32_t h[4];
+            // Qs: head g's q times 2^e_g as three E4M3 terms in rows g, 8 + g
+            // and 16 + g of a 32-row K-major operand (rows 24.. and the rows
+            // of absent heads zero).  Thread (g, j) takes d/16 elements.
+            constexpr int EPT = D / 16;
+            const int g = st >> 4, j = st & 15;
+            float x[EPT];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float2 f = widen2<true>(w[i]);
-                            h[i] = narrow2<false>(f.x, f.y);
-                        }
-                        v = make_uint4(h[0], h[1], h[2], h[3]);
-                    } else {
-                        v = raw;
+            for (int e = 0; e < EPT; ++e) x[e] = 0.f;
+            if (g < G) {
+                const uint16_t *src =
+                    p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + j * EPT;
+                uint32_t w[EPT / 2];
+                if constexpr (EPT == 8) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(src);
+                    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+                } else {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(src);
+                    w[0] = v.x; w[1] = v.y;
+                }
+#pragma unroll
+                for (int e = 0; e < EPT / 2; ++e) {
+                    const float2 f = widen2<BF16>(w[e]);
+                    x[2 * e] = f.x;
+                    x[2 * e + 1] = f.y;
+                }
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
+            // 2^e_g brings amax into [128, 256): e_g = 7 - floor(log2 amax)
+            int eg = 0;
+            if (amax > 0.f) {
+                const int ex = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+                eg = 7 - (ex < -126 ? -126 : ex);
+                eg = eg < -120 ? -120 : (eg > 120 ? 120 : eg);
+            }
+            const float up = exp2i(eg);
+            uint32_t code[3][EPT / 4];  // EPT codes per term, 4 per word
+#pragma unroll
+            for (int w4 = 0; w4 < EPT / 4; ++w4) {
+                uint32_t c[3][2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float a = x[4 * w4 + 2 * h] * up, b = x[4 * w4 + 2 * h + 1] * up;
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        c[t][h] = e4m3x2_from_f32(a, b);
+                        const float2 back = e4m3x2_to_f32(c[t][h]);
+                        a -= back.x;  // exact: the remainder is representable
+                        b -= back.y;
                     }
                 }
-                *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(g, c * 8, kF8N * 128)) = v;
+#pragma unroll
+                for (int t = 0; t < 3; ++t) code[t][w4] = c[t][0] | (c[t][1] << 16);
             }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {  // term rows, then a zero row (24 + g)
+                const int row = 8 * t + g;
+                uint8_t *dst = smem + S::OFF_Q + e4m3_operand_offset<D>(row, j * EPT);
+                if constexpr (EPT == 8) {
+                    *reinterpret_cast<uint2 *>(dst) =
+                        t < 3 ? make_uint2(code[t][0], code[t][1]) : make_uint2(0u, 0u);
+                } else {
+                    *reinterpret_cast<uint32_t *>(dst) = t < 3 ? code[t][0] : 0u;
+                }
+            }
+            if (j == 0) qmul[g] = g < G ? p.scale_log2 * exp2i(-eg) : 0.f;
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kQReady]);
         }
+        named_bar(3, 256);  // qmul is written
+        float qm[kF8G];
+#pragma unroll
+        for (int g = 0; g < kF8G; ++g) qm[g] = qmul[g];
 
         float m_run[kF8G], m_true[kF8G], l_part[kF8G], acc[kF8G], alpha_prev[kF8G];
 #pragma unroll
@@ -458,7 +536,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             if (!__all_sync(kFullMask, landed)) return false;
             tc_fence_after();
             float o[16];
-            tmem_load16(tmem + lane_addr + kF8O0 + 16 * grp, o);
+            tmem_load16(tmem + lane_addr + kF8O0 + kF8N * grp, o);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kOEmpty0 + grp]);
@@ -471,16 +549,20 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         for (int i = grp; i < ntiles; i += 2) {
             const bool landed = !failed && mbar_wait(&bar[kSFull0 + grp], (i >> 1) & 1);
             const bool ok = __all_sync(kFullMask, landed);
-            float s[16];
+            float s[kF8G];
             if (ok) {
                 tc_fence_after();
-                tmem_load16(tmem + lane_addr + kF8S0 + 16 * grp, s);
+                float t12[16], t3[8];
+                tmem_load16(tmem + lane_addr + kF8S0 + kF8QN * grp, t12);
+                tmem_load8(tmem + lane_addr + kF8S0 + kF8QN * grp + 16, t3);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[kSEmpty0 + grp]);
+#pragma unroll
+                for (int g = 0; g < kF8G; ++g) s[g] = (t12[g] + t12[8 + g]) + t3[g];
             } else {
 #pragma unroll
-                for (int g = 0; g < 16; ++g) s[g] = 0.f;
+                for (int g = 0; g < kF8G; ++g) s[g] = 0.f;
             }
             const int tile0 = start + i * kF8Tile;
             const int nvalid = (end - tile0 < kF8Tile) ? end - tile0 : kF8Tile;
@@ -489,7 +571,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             float *tmax = gred + ((i >> 1) & 1) * (4 * kF8N);
 #pragma unroll
             for (int g = 0; g < kF8G; ++g) {
-                s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;  // select: NaN-safe
+                s[g] = valid ? s[g] * qm[g] : -INFINITY;  // select: NaN-safe
                 float v = s[g];
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
@@ -550,7 +632,6 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             last = i;
         }
         if (!failed && last >= 0 && !accumulate(last)) failed = true;
-
         // l over the group's 128 position-threads, per head
         float *lsum = gred + 2 * (4 * kF8N);
 #pragma unroll
@@ -637,7 +718,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         tmem_dealloc(tmem, kF8Cols);
     }
     if (!direct && !*abort_flag && p.counters != nullptr)
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_K));
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_STG));
 }
 
 using F8Kernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
@@ -690,8 +771,9 @@ pa_status launch_decode_fp8(const DecodeParams &prm, bool bf16, int head_dim, in
     if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return PA_ERR_CUDA;
     const int64_t rows = (int64_t)prm.num_blocks * num_kv_heads * prm.block_size;
     CUtensorMap mk, mv;
-    if (!pool_tensor_map_fp8(&mk, prm.k_pool, rows, head_dim) ||
-        !pool_tensor_map_fp8(&mv, prm.v_pool, rows, head_dim))
+    // K lands swizzled (the q.K^T operand), V row-major (the converters' input)
+    if (!pool_tensor_map_fp8(&mk, prm.k_pool, rows, head_dim, true) ||
+        !pool_tensor_map_fp8(&mv, prm.v_pool, rows, head_dim, false))
         return PA_ERR_CUDA;
     dim3 grid((unsigned)num_partitions, (unsigned)num_kv_heads, (unsigned)num_seqs);
     if (launch_pdl(k, grid, dim3(kF8Threads), (size_t)smem, stream, prm, mk, mv) != cudaSuccess)

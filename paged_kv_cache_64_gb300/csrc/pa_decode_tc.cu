@@ -291,7 +291,10 @@ __global__ void __launch_bounds__(kTcThreads)
             unsigned spins = 0;
             while (ok && nv < ntiles) {
                 bool moved = false;
-                if (nq < ntiles && mbar_test_wait(&bar[kKFull], nq & 1) &&
+                // (q.K^T of the last tile only once P.V of every earlier tile
+                // is issued: see the stale-row zeroing in the softmax)
+                if (nq < ntiles && (nq + 1 < ntiles || nv == nq) &&
+                    mbar_test_wait(&bar[kKFull], nq & 1) &&
                     (nq < 2 || mbar_test_wait(&bar[kSEmpty0 + (nq & 1)], ((nq >> 1) - 1) & 1))) {
                     const int b = nq & 1;
                     tc_fence_after();
@@ -455,6 +458,9 @@ __global__ void __launch_bounds__(kTcThreads)
             if (!valid) {
                 // Stale rows of the last tile: V must be finite there (0 * NaN
                 // would poison the product), so zero the row once it has landed.
+                // Tile i-1's V has been consumed (the MMA issuer holds back
+                // q.K^T of the last tile until every earlier P.V is issued), so
+                // the parity wait below can only mean tile i's phase.
                 if (mbar_wait(&bar[kVFull], i & 1)) {
 #pragma unroll
                     for (int h = 0; h < S::KH; ++h) {
@@ -581,9 +587,8 @@ bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, bo
 }
 
 // An E4M3 pool [NB][Hkv][B][d] (one byte per element) viewed the same way;
-// boxes of 16 rows x d bytes, no swizzle (the copy lands in a row-major
-// staging tile).
-bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D) {
+// boxes of 16 rows x d bytes, row-major or swizzled as a K-major operand.
+bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D, bool swizzle) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
@@ -591,7 +596,9 @@ bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D
     const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)kUnit};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               !swizzle ? CU_TENSOR_MAP_SWIZZLE_NONE
+                        : (D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B),
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

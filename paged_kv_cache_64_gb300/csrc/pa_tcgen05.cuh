@@ -44,6 +44,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[smem desc] . B[smem desc], kind::f8f6f4 (here E4M3 x E4M3
+// in, f32 accumulate; K = 32 elements, i.e. 32 bytes, per instruction).
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive (once) on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile(
@@ -65,6 +76,19 @@ __device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 32 lanes x 8 columns of 32-bit TMEM cells (wait inside the statement).
+__device__ __forceinline__ void tmem_load8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 // 2-D TMA tensor copy (tile mode) global -> shared, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -95,12 +119,25 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same with 64-byte swizzle (layout SWIZZLE_64B (4)): atoms of 8 rows x
+// 64 bytes, 16-byte chunk c of row r stored at chunk c ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
+}
+
 // Instruction descriptor of kind::f16: f32 accumulator, A/B format
 // (0 = f16, 1 = bf16), A/B major (0 = K, 1 = MN), N >> 3, M >> 4.
 __host__ __device__ constexpr uint32_t f16_idesc(bool bf16, bool a_mn, bool b_mn, int M, int N) {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
            ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0
+// in both fields), f32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t e4m3_idesc(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Byte offset of element (row, col) of a K-major operand stored as
@@ -212,7 +249,9 @@ __device__ __forceinline__ void cluster_sync() {
 // The pool [NB][Hkv][B][d] viewed as a 2-D tensor of `rows` rows of d
 // elements, boxes of 16 rows x 64 columns, 128-byte swizzle (host side).
 bool pool_tensor_map(CUtensorMap *map, const void *pool, int64_t rows, int D, bool bf16);
-// The same for an E4M3 pool: boxes of 16 rows x d bytes, no swizzle.
-bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D);
+// The same for an E4M3 pool: boxes of 16 rows x d bytes, either unswizzled
+// (row-major) or with the swizzle of a K-major operand of d-byte rows
+// (128-byte swizzle for d = 128, 64-byte for d = 64).
+bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D, bool swizzle);
 
 }  // namespace pa
