@@ -22,7 +22,7 @@ Semantics follow "Why AI servers waste memory, and how paging fixes it"
 * Free: walk the table in order, drop one reference per block, and put a block
   at the back of the free list when its count reaches zero.
 
-Extensions of this build, each a plain reading:
+Extensions of the library, each a plain reading:
 * append(seq, n) with n > 1 is the same as n single appends, but all or
   nothing: the free-list check covers the whole request before any change.
 * The initial free-list order may be given (a seeded permutation of the block

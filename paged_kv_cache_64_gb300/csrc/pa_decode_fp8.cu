@@ -3,13 +3,15 @@
 // The pools hold OCP E4M3 codes (one byte per element), one scale per K or V
 // pool: element = scale * code value ("b = 1 for FP8" in the KV-size formula
 // of "PagedAttention and Virtual Memory Management: Mathematical Foundations
-// ..." (llms.blog), section 1; format and scale are this build's readings).
+// ..." (llms.blog), section 1; the format and the scale are this library's
+// conventions).
 // Same computation as the tensor-core kernel in pa_decode_tc.cu (whose header
 // describes the products, the roles and the online softmax), with half the
 // K/V bytes moved.  Per tile of 128 positions:
 //
-//   S^T[128 pos x 32] = K_codes[128 x d] . Qs^T[d x 32]   kind::f8f6f4, E4M3 x E4M3
-//   O^T[128 x 16]     = V^T[128 x 128 pos] . P^T[128 x 16] kind::f16
+//   S^T[128 pos x 32] = K_codes[128 x d] . Qs^T[d x 32]       kind::f8f6f4, E4M3 x E4M3
+//   d = 128: O^T[128 x 32] = V_codes^T[128 x 128 pos] . Ps^T  kind::f8f6f4, E4M3 x E4M3
+//   d = 64:  O^T[128 x 16] = V16^T[128 x 128 pos] . P16^T     kind::f16 (rows 64.. zero)
 //
 // q.K^T reads the E4M3 K tile exactly as the TMA copy lands it (K-major,
 // swizzled), so K is never converted.  Its other operand, Qs, holds each query
@@ -17,20 +19,28 @@
 // largest |q| into [128, 256), q_g * 2^e_g = t1 + t2 + t3, t1 the nearest
 // E4M3 value, t2 that of the remainder, t3 that of the next remainder (each
 // remainder is exact in fp32).  A 16-bit q has at most 11 significant bits
-// and each term carries 4, so the sum equals q * 2^e_g except for elements
-// below 2^-17 of the head's largest (E4M3's subnormal floor), and the three
-// S columns of a head add up, times 2^-e_g, to q.K^T within fp32 rounding.
-// V goes through the f16 path: converter warps widen its codes exactly to f16
-// (cvt.rn.f16x2.e4m3x2: every E4M3 value is an f16 value) into the MN-major
-// V^T operand, zeroing rows past the end; P is written as f16.  The K scale is
-// folded into the softmax scale, the V scale into the output.
-// The staging ring (4 tiles of K and V at d = 128, 8 at d = 64) is the only
-// large buffer besides the two f16 V operands, so the copies run that many
-// tiles ahead.  Two softmax warpgroups take alternate tiles (even tiles with
-// S, P and O buffers 0, odd tiles with buffers 1), each with its own running
-// maximum, sum and accumulator, merged at the end.
-// Roles (16 warps): 0 producer, 1 TMEM owner and MMA issuer, 2..5 and 6..9
-// softmax / epilogue groups A and B (A also builds Qs), 10..15 V converters.
+// and the three terms carry 12, so the sum equals q * 2^e_g except for
+// elements below 2^-17 of the head's largest (E4M3's subnormal floor), and
+// the three S columns of a head add up, times 2^-e_g, to q.K^T within fp32
+// rounding.
+// At d = 128 P.V reads V the same way: the staged V tile (128-byte swizzle)
+// is V^T as an MN-major operand, and P is split like q (Ps: three E4M3 terms
+// per head of P times 2^k, the power of two that brings the tile's largest P
+// into [128, 256); the tile's O is scaled back by 2^-k), so nothing is
+// converted and the tensor cores run 8 instructions a tile.  Stale V rows of
+// the last tile are zeroed in the staged tile before P.V (0 * NaN would
+// poison the product).  At d = 64 a V row is 64 bytes, half an MN-major
+// atom, so converter warps widen V exactly to f16 (cvt.rn.f16x2.e4m3x2: every
+// E4M3 value is an f16 value) into a zero-padded V^T operand instead.
+// The K scale is folded into the softmax scale, the V scale into the output.
+// The staging ring (6 tiles of K and V at d = 128, 8 at d = 64) is the only
+// large buffer besides the f16 V operands of d = 64, so the copies run that
+// many tiles ahead.  Two softmax warpgroups take alternate tiles (even tiles
+// with S, P and O buffers 0, odd tiles with buffers 1), each with its own
+// running maximum, sum and accumulator, merged at the end.
+// Roles: 0 producer, 1 TMEM owner and MMA issuer, 2..5 and 6..9 softmax /
+// epilogue groups A and B (A also builds Qs); at d = 64 also 10..15 V
+// converters.
 #include <cuda.h>  // CUtensorMap and its enums only; the encoder comes from the driver at run time
 
 #include <cmath>
@@ -47,42 +57,61 @@ namespace pa {
 namespace {
 
 constexpr int kF8Tile = 128;       // positions per tile (MMA M of q.K^T)
-constexpr int kF8N = 16;           // MMA N of P.V: the query heads of a group, zero-padded
-constexpr int kF8QN = 32;          // MMA N of q.K^T: three E4M3 terms x 8 heads, zero-padded
+constexpr int kF8N = 16;           // MMA N of P.V in f16: the query heads of a group, zero-padded
+constexpr int kF8QN = 32;          // MMA N over E4M3 terms: three terms x 8 heads, zero-padded
 constexpr int kF8G = 8;            // largest group the kernel serves
-constexpr int kF8Warps = 16;  // 4 per SM sub-partition: up to 128 registers a thread
-constexpr int kF8Threads = kF8Warps * 32;
-constexpr int kF8Cols = 128;       // TMEM columns: S x2 (32 each) at 0, O x2 (16 each) at 64
+// TMEM columns: S of each softmax group at 0 and 32, O of tile t at
+// 64 + 32 * (2 * (t & 1) + ((t >> 1) & 1)) (two per group), 32 columns each
+constexpr int kF8Cols = 256;
 constexpr int kF8S0 = 0, kF8O0 = 64;
-constexpr int kF8Conv0 = 10;       // first converter warp
+constexpr int kF8Conv0 = 10;       // first converter warp (f16 P.V only)
+constexpr int kF8VProd = 10;       // the V producer warp (E4M3 P.V only)
 constexpr int kF8ConvWarps = 6;    // converter warps (V)
 
-constexpr int kF8MaxStages = 8;
+constexpr int kF8MaxRing = 12;     // slots of a staging ring
 
 enum F8Bar {
-    kVFull0 = 0, kVFull1, kVEmpty0, kVEmpty1, kQReady,
-    kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kOFull0, kOFull1, kOEmpty0, kOEmpty1,
-    kStgFull0,                                // kF8MaxStages of each
-    kStgEmpty0 = kStgFull0 + kF8MaxStages,
-    kNumF8Bars = kStgEmpty0 + kF8MaxStages
+    // the f16 V operand buffers of d = 64
+    kVOpFull0 = 0, kVOpFull1, kVOpEmpty0, kVOpEmpty1, kQReady,
+    kSFull0, kSFull1, kSEmpty0, kSEmpty1,
+    kPFull0, kOFull0 = kPFull0 + 4, kOEmpty0 = kOFull0 + 4,  // 4 of each: tile t uses 2*(t&1) + ((t>>1)&1)
+    // the K and V staging rings, kF8MaxRing of each
+    kKFull0 = kOEmpty0 + 4,
+    kKEmpty0 = kKFull0 + kF8MaxRing,
+    kVFull0 = kKEmpty0 + kF8MaxRing,
+    kVEmpty0 = kVFull0 + kF8MaxRing,
+    kNumF8Bars = kVEmpty0 + kF8MaxRing
 };
 
 template <int D>
 struct F8Shape {
+    // d = 128: P.V on E4M3 codes too (V^T straight from the staged tile, P as
+    // three E4M3 terms); d = 64: V widened to f16 by converter warps
+    static constexpr bool DIRECT = D == 128;
+    // d = 128: producer K, MMA, 8 softmax, producer V; d = 64: producer,
+    // MMA, 8 softmax, 6 converters (4 per sub-partition, 128 registers)
+    static constexpr int WARPS = DIRECT ? 11 : 16;
+    static constexpr int THREADS = WARPS * 32;
     static constexpr int SLAB = kF8Tile * 128;        // one 64-dim f16 slab of a tile: 16 KiB
     static constexpr int V_BYTES = 2 * SLAB;          // V^T is M = 128 dims; d = 64 pads with zeros
     static constexpr int STG_BYTES = kF8Tile * D;     // E4M3 tile of K (or V): 128 rows of d bytes
     // K tiles and Qs: K-major E4M3 operands of d-byte rows, in atoms of 8 rows
     // (128-byte swizzle for d = 128, 64-byte for d = 64)
     static constexpr int Q_BYTES = kF8QN * D;
-    static constexpr int P_BYTES = 2 * kF8N * 128;    // P^T: 16 rows x 128 positions (two atoms)
-    static constexpr int NSTG = D == 128 ? 4 : 8;     // staging ring: tiles in flight
-    static constexpr int NVB = 2;                     // V operand buffers
-    static constexpr int OFF_STG = 0;                 // stage s: K at s * 2 * STG, V after it
-    static constexpr int OFF_V = OFF_STG + NSTG * 2 * STG_BYTES;
+    // P^T: 16 rows of 128 f16 positions, or 32 rows of 128 E4M3 positions
+    static constexpr int P_BYTES = 4096;
+    // Staging rings of E4M3 tiles: a K slot is free once q.K^T has read it,
+    // a V slot only once P.V (d = 128) or the converters (d = 64) have, so
+    // the V ring is the deeper one.
+    static constexpr int NK = DIRECT ? 5 : 6;
+    static constexpr int NV = DIRECT ? 7 : 10;
+    static constexpr int NVB = DIRECT ? 0 : 2;        // f16 V operand buffers
+    static constexpr int OFF_STG = 0;                 // K slots, then V slots
+    static constexpr int OFF_VSTG = OFF_STG + NK * STG_BYTES;
+    static constexpr int OFF_V = OFF_VSTG + NV * STG_BYTES;
     static constexpr int OFF_Q = OFF_V + NVB * V_BYTES;
-    static constexpr int OFF_P = OFF_Q + Q_BYTES;     // two buffers
-    static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;     // four buffers: two per softmax group
+    static constexpr int OFF_RED = OFF_P + 4 * P_BYTES;
     // per softmax group: two tile-max buffers and the final sums
     static constexpr int RED_BYTES = 2 * 3 * 4 * kF8N * 4;
     // per head: softmax scale (log2 units, K scale included) times 2^-e_g
@@ -94,11 +123,11 @@ struct F8Shape {
     static constexpr int OFF_MISC = OFF_BAR + kNumF8Bars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
-    static_assert((2 * STG_BYTES) % 1024 == 0 && STG_BYTES % 1024 == 0, "TMA swizzle alignment");
-    static_assert(NSTG <= kF8MaxStages, "stage barriers");
+    static_assert(STG_BYTES % 1024 == 0, "TMA swizzle alignment");
+    static_assert(NK <= kF8MaxRing && NV <= kF8MaxRing, "ring barriers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-    static_assert(NSTG * 2 * STG_BYTES >= 2 * kF8G * kCombineMaxParts * 4,
-                  "combine scratch in the staging ring");
+    static_assert((NK + NV) * STG_BYTES >= 2 * kF8G * kCombineMaxParts * 4,
+                  "combine scratch in the staging rings");
 };
 
 // Byte offset of element (row, k) in a K-major E4M3 operand of D-byte rows
@@ -187,7 +216,7 @@ __device__ __forceinline__ uint16_t narrow_out(float x) {
 }
 
 template <bool BF16, int D>
-__global__ void __launch_bounds__(kF8Threads, 1)
+__global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
     paged_decode_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v) {
     using S = F8Shape<D>;
@@ -238,15 +267,18 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
     if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write_fp8<BF16, D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
-        // kVFull: the converter warps; kQReady, kSEmpty, kPFull, kOEmpty: the
-        // 4 warps of a softmax group; kStgEmpty: the converters and the
-        // commit of q.K^T (which reads the stage's K tile)
-        const int counts[kStgFull0] = {kF8ConvWarps, kF8ConvWarps, 1, 1, 4, 1, 1, 4, 4,
-                                       4, 4, 1, 1, 4, 4};
-        for (int b = 0; b < kStgFull0; ++b) mbar_init(&bar[b], counts[b]);
-        for (int b = 0; b < kF8MaxStages; ++b) {
-            mbar_init(&bar[kStgFull0 + b], 1);   // the producer's expect-tx arrival
-            mbar_init(&bar[kStgEmpty0 + b], kF8ConvWarps + 1);
+        // kVOpFull: the converter warps; kQReady, kSEmpty, kPFull, kOEmpty:
+        // the 4 warps of a softmax group; kKFull, kVFull: the producer's
+        // expect-tx arrival; kKEmpty: the commit of q.K^T; kVEmpty: the commit
+        // of P.V (d = 128) or the converter warps (d = 64)
+        const int counts[kKFull0] = {kF8ConvWarps, kF8ConvWarps, 1, 1, 4, 1, 1, 4, 4,
+                                     4, 4, 4, 4, 1, 1, 1, 1, 4, 4, 4, 4};
+        for (int b = 0; b < kKFull0; ++b) mbar_init(&bar[b], counts[b]);
+        for (int b = 0; b < kF8MaxRing; ++b) {
+            mbar_init(&bar[kKFull0 + b], 1);
+            mbar_init(&bar[kKEmpty0 + b], 1);
+            mbar_init(&bar[kVFull0 + b], 1);
+            mbar_init(&bar[kVEmpty0 + b], S::DIRECT ? 1 : kF8ConvWarps);
         }
         *abort_flag = 0;
         mbar_init_fence();
@@ -255,11 +287,19 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         tmem_alloc(tmem_slot, kF8Cols);
         tmem_relinquish();
     }
-    if constexpr (D == 64) {
+    if constexpr (S::DIRECT) {
+        // rows 24..31 (the last 8-row atom) of the four E4M3 P^T buffers: zero
+        // once, never written again
+        for (int i = threadIdx.x; i < 4 * 64; i += S::THREADS) {
+            uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_P + (i >> 6) * S::P_BYTES + 3 * 1024);
+            z[i & 63] = make_uint4(0, 0, 0, 0);
+        }
+        fence_async_smem();
+    } else {
         // rows 64..127 of both V^T operand buffers: zero once, never written again
         for (int vb = 0; vb < S::NVB; ++vb) {
             uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_V + vb * S::V_BYTES + S::SLAB);
-            for (int i = threadIdx.x; i < S::SLAB / 16; i += kF8Threads) z[i] = make_uint4(0, 0, 0, 0);
+            for (int i = threadIdx.x; i < S::SLAB / 16; i += S::THREADS) z[i] = make_uint4(0, 0, 0, 0);
         }
         fence_async_smem();
     }
@@ -268,42 +308,56 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- producer
+    if (warp == 0 || (S::DIRECT && warp == kF8VProd)) {
+        // ---------------------------------------------------------- producers
+        // d = 128: warp 0 copies the K tiles and warp kF8VProd the V tiles,
+        // each in tile order as its ring's slots free up (K runs ahead: its
+        // slots free up first); d = 64: warp 0 copies K then V of each tile.
+        // Lane j of the window holds the pool row of unit w + j, 32 units (4
+        // tiles) a window; the block-table entries of the next window are
+        // loaded when a window opens, so no copy waits for a table load.
+        const int kv0 = (S::DIRECT && warp != 0) ? 1 : 0;
+        const int kv1 = S::DIRECT ? kv0 : 1;
         const int32_t *table = seq_table(p, seq);
-        bool ok = true;
-        for (int u0 = 0; u0 < nunits && ok; u0 += 32) {  // 32 units = 4 tiles
-            const int u = u0 + lane;
-            int row0 = 0;  // first row of the unit in the 2-D view [NB*Hkv*B, d]
-            if (u < nunits) {
-                const int pos = start + u * kUnit;
-                int phys = table[pos >> p.log2_block];
-                if ((unsigned)phys >= (unsigned)p.num_blocks) {
-                    record_error(p.err, PA_ERR_BAD_INDEX);
-                    phys = 0;
-                }
-                row0 = (phys * p.num_kv_heads + kvh) * p.block_size + (pos & (p.block_size - 1));
+        auto table_entry = [&](int u) -> int {
+            return u < nunits ? __ldg(table + ((start + u * kUnit) >> p.log2_block)) : 0;
+        };
+        auto unit_row = [&](int u, int phys) -> int {  // first row of unit u in [NB*Hkv*B, d]
+            if (u >= nunits) return 0;
+            if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                if (kv0 == 0) record_error(p.err, PA_ERR_BAD_INDEX);
+                phys = 0;
             }
-            for (int t = u0 / 8; t < ntiles && t < (u0 + 32) / 8; ++t) {
-                const int nu = (nunits - 8 * t < 8) ? nunits - 8 * t : 8;
-                const int sg = t % S::NSTG;
-                if (t >= S::NSTG) {  // q.K^T and the converters are done with the stage
-                    const bool done = mbar_wait(&bar[kStgEmpty0 + sg], ((t / S::NSTG) - 1) & 1);
+            const int pos = start + u * kUnit;
+            return (phys * p.num_kv_heads + kvh) * p.block_size + (pos & (p.block_size - 1));
+        };
+        int w = -32, rows = 0, next = table_entry(lane);
+        bool ok = true;
+        for (int t = 0; t < ntiles && ok; ++t) {
+            if (8 * t >= w + 32) {  // windows open in order: w + 32 == 8 * t
+                w = 8 * t;
+                rows = unit_row(w + lane, next);
+                next = table_entry(w + 32 + lane);
+            }
+            const int nu = (nunits - 8 * t < 8) ? nunits - 8 * t : 8;
+            const int r0 = __shfl_sync(kFullMask, rows, (8 * t - w + lane) & 31);
+            for (int kv = kv0; kv <= kv1; ++kv) {
+                const int n = kv ? S::NV : S::NK;
+                const int slot = t % n;
+                if (t >= n) {  // the slot's readers are done with its previous tile
+                    const bool done =
+                        mbar_wait(&bar[(kv ? kVEmpty0 : kKEmpty0) + slot], ((t / n) - 1) & 1);
                     if (!__all_sync(kFullMask, done)) {
                         ok = false;
                         break;
                     }
                 }
-                uint64_t *full = &bar[kStgFull0 + sg];
-                uint8_t *stg = smem + S::OFF_STG + sg * 2 * S::STG_BYTES;
-                if (lane == 0) mbar_arrive_expect_tx(full, nu * 2 * kUnit * D);
-                // lane j < nu copies unit j of the tile (K and V): one
-                // instruction issues the tile's copies
-                const int r0 = __shfl_sync(kFullMask, row0, (8 * t - u0 + lane) & 31);
-                if (lane < nu) {
-                    tma_load_2d(stg + lane * kUnit * D, &tmap_k, 0, r0, full);
-                    tma_load_2d(stg + S::STG_BYTES + lane * kUnit * D, &tmap_v, 0, r0, full);
-                }
+                uint64_t *full = &bar[(kv ? kVFull0 : kKFull0) + slot];
+                uint8_t *dst = smem + (kv ? S::OFF_VSTG : S::OFF_STG) + slot * S::STG_BYTES;
+                if (lane == 0) mbar_arrive_expect_tx(full, nu * kUnit * D);
+                // lane j < nu copies unit j of the tile: one instruction
+                // issues the tile's copies
+                if (lane < nu) tma_load_2d(dst + lane * kUnit * D, kv ? &tmap_v : &tmap_k, 0, r0, full);
                 __syncwarp();
             }
         }
@@ -311,7 +365,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
             *abort_flag = 1;
         }
-    } else if (warp >= kF8Conv0) {
+    } else if (!S::DIRECT && warp >= kF8Conv0) {
+      if constexpr (!S::DIRECT) {
         // ---------------------------------------------------------- V converters
         // E4M3 staging (row-major) -> f16 V^T operand (MN-major, 128-byte
         // swizzle).  Item = (row, 16 codes); every load of a thread is issued
@@ -325,13 +380,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         for (int t = 0; t < ntiles && ok; ++t) {
             const int nvalid = (end - start - t * kF8Tile < kF8Tile) ? end - start - t * kF8Tile
                                                                       : kF8Tile;
-            const int sg = t % S::NSTG;
-            const int stg = S::OFF_STG + sg * 2 * S::STG_BYTES + S::STG_BYTES;
+            const int slot = t % S::NV;
+            const int stg = S::OFF_VSTG + slot * S::STG_BYTES;
             const int ob = t % S::NVB;
             const int op_off = S::OFF_V + ob * S::V_BYTES;
-            ok = __all_sync(kFullMask, mbar_wait(&bar[kStgFull0 + sg], (t / S::NSTG) & 1)) &&
+            ok = __all_sync(kFullMask, mbar_wait(&bar[kVFull0 + slot], (t / S::NV) & 1)) &&
                  (t < S::NVB ||
-                  __all_sync(kFullMask, mbar_wait(&bar[kVEmpty0 + ob], ((t / S::NVB) - 1) & 1)));
+                  __all_sync(kFullMask, mbar_wait(&bar[kVOpEmpty0 + ob], ((t / S::NVB) - 1) & 1)));
             if (!ok) break;
             uint4 raw[NIT];
 #pragma unroll
@@ -362,69 +417,80 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             fence_async_smem();  // generic-proxy writes, read by the tensor cores
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&bar[kVFull0 + ob]);
-                mbar_arrive(&bar[kStgEmpty0 + sg]);
+                mbar_arrive(&bar[kVOpFull0 + ob]);
+                mbar_arrive(&bar[kVEmpty0 + slot]);
             }
         }
         if (!ok && lane == 0) {
             record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
             *abort_flag = 1;
         }
+      }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = e4m3_idesc(kF8Tile, kF8QN);
+            constexpr uint32_t idesc_qk = e4m3_idesc(kF8Tile, kF8QN, false);
             constexpr uint32_t idesc_pv = f16_idesc(false, true, false, 128, kF8N);
+            constexpr uint32_t idesc_pv8 = e4m3_idesc(128, kF8QN, true);  // V^T MN-major
             const uint32_t sbase = smem_addr(smem);
-            bool ok = mbar_wait(&bar[kQReady], 0);
-            // Whichever is ready first: q.K^T of tile nq once its stage has
-            // landed and its S buffer is free, or P.V of tile nv once its V,
-            // P and O buffer are.
-            int nq = 0, nv = 0;
-            unsigned long long since = global_timer_ns();
-            unsigned spins = 0;
-            while (ok && nv < ntiles) {
-                bool moved = false;
-                if (nq < ntiles &&
-                    mbar_test_wait(&bar[kStgFull0 + nq % S::NSTG], (nq / S::NSTG) & 1) &&
-                    (nq < 2 || mbar_test_wait(&bar[kSEmpty0 + (nq & 1)], ((nq >> 1) - 1) & 1))) {
-                    const int b = nq & 1, sg = nq % S::NSTG;
-                    const uint32_t kaddr = sbase + S::OFF_STG + sg * 2 * S::STG_BYTES;
-                    tc_fence_after();
+            // q.K^T of tile t (its K landed, its S buffer read by the softmax)
+            auto issue_qk = [&](int t) -> bool {
+                const int b = t & 1, slot = t % S::NK;
+                if (!mbar_wait(&bar[kKFull0 + slot], (t / S::NK) & 1)) return false;
+                if (t >= 2 && !mbar_wait(&bar[kSEmpty0 + b], ((t >> 1) - 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t kaddr = sbase + S::OFF_STG + slot * S::STG_BYTES;
 #pragma unroll
-                    for (int ks = 0; ks < D / 32; ++ks)  // 32 codes (bytes) of d per MMA
-                        tc_mma_f8(tmem + kF8S0 + kF8QN * b, e4m3_operand_desc<D>(kaddr + ks * 32),
-                                  e4m3_operand_desc<D>(sbase + S::OFF_Q + ks * 32), idesc_qk, ks > 0);
-                    tc_commit(&bar[kSFull0 + b]);
-                    tc_commit(&bar[kStgEmpty0 + sg]);
-                    ++nq;
-                    moved = true;
-                }
-                if (nv < nq && mbar_test_wait(&bar[kVFull0 + nv % S::NVB], (nv / S::NVB) & 1) &&
-                    mbar_test_wait(&bar[kPFull0 + (nv & 1)], (nv >> 1) & 1) &&
-                    (nv < 2 || mbar_test_wait(&bar[kOEmpty0 + (nv & 1)], ((nv >> 1) - 1) & 1))) {
-                    const int b = nv & 1;
-                    tc_fence_after();
+                for (int ks = 0; ks < D / 32; ++ks)  // 32 codes (bytes) of d per MMA
+                    tc_mma_f8(tmem + kF8S0 + kF8QN * b, e4m3_operand_desc<D>(kaddr + ks * 32),
+                              e4m3_operand_desc<D>(sbase + S::OFF_Q + ks * 32), idesc_qk, ks > 0);
+                tc_commit(&bar[kSFull0 + b]);
+                tc_commit(&bar[kKEmpty0 + slot]);
+                return true;
+            };
+            // P.V of tile t (its V landed or converted, its P written, its O
+            // buffer accumulated from tile t-4)
+            auto issue_pv = [&](int t) -> bool {
+                const int b = 2 * (t & 1) + ((t >> 1) & 1);  // P and O buffer
+                if (!mbar_wait(&bar[S::DIRECT ? kVFull0 + t % S::NV : kVOpFull0 + (t & 1)],
+                               S::DIRECT ? (t / S::NV) & 1 : (t >> 1) & 1))
+                    return false;
+                if (!mbar_wait(&bar[kPFull0 + b], (t >> 2) & 1)) return false;
+                if (t >= 4 && !mbar_wait(&bar[kOEmpty0 + b], ((t >> 2) - 1) & 1)) return false;
+                tc_fence_after();
+                if constexpr (S::DIRECT) {
+                    // V^T straight from the staged tile: MN-major, 8-position
+                    // atoms 1024 bytes apart, 32 positions per MMA
+                    const int slot = t % S::NV;
+                    const uint32_t vaddr = sbase + S::OFF_VSTG + slot * S::STG_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < kF8Tile / 32; ++ks)
+                        tc_mma_f8(tmem + kF8O0 + kF8QN * b, sw128_desc(vaddr + ks * 4096, 16, 1024),
+                                  sw128_desc(sbase + S::OFF_P + b * S::P_BYTES + ks * 32, 16, 1024),
+                                  idesc_pv8, ks > 0);
+                    tc_commit(&bar[kOFull0 + b]);
+                    tc_commit(&bar[kVEmpty0 + slot]);
+                } else {
 #pragma unroll
                     for (int ks = 0; ks < kF8Tile / 16; ++ks) {
                         const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
                         const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
-                        tc_mma(tmem + kF8O0 + kF8N * b,
-                               sw128_desc(sbase + S::OFF_V + (nv % S::NVB) * S::V_BYTES + voff,
-                                          S::SLAB, 1024),
+                        tc_mma(tmem + kF8O0 + kF8QN * b,
+                               sw128_desc(sbase + S::OFF_V + (t & 1) * S::V_BYTES + voff, S::SLAB, 1024),
                                sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
                     }
                     tc_commit(&bar[kOFull0 + b]);
-                    tc_commit(&bar[kVEmpty0 + nv % S::NVB]);
-                    ++nv;
-                    moved = true;
+                    tc_commit(&bar[kVOpEmpty0 + (t & 1)]);
                 }
-                if (moved) {
-                    since = global_timer_ns();
-                } else if ((++spins & 31) == 0 && global_timer_ns() - since > kWaitLimitNs) {
-                    ok = false;
-                }
-            }
+                return true;
+            };
+            // Fixed order q.K^T 0, 1, then q.K^T t+2 and P.V t: q.K^T of tile
+            // t+2 only needs the softmax to have read S of tile t (the first
+            // thing it does with tile t), so a softmax group finds its next S
+            // ready when it has written P of this tile.
+            bool ok = mbar_wait(&bar[kQReady], 0) && issue_qk(0) && (ntiles < 2 || issue_qk(1));
+            for (int t = 0; ok && t < ntiles; ++t)
+                ok = (t + 2 >= ntiles || issue_qk(t + 2)) && issue_pv(t);
             if (!ok) {
                 record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
@@ -521,6 +587,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         for (int g = 0; g < kF8G; ++g) qm[g] = qmul[g];
 
         float m_run[kF8G], m_true[kF8G], l_part[kF8G], acc[kF8G], alpha_prev[kF8G];
+        // 2^-k of the previous tile's P scale (E4M3 P only)
+        float kinv_prev[kF8G];
 #pragma unroll
         for (int g = 0; g < kF8G; ++g) {
             m_run[g] = -INFINITY;
@@ -528,18 +596,28 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             l_part[g] = 0.f;
             acc[g] = 0.f;
             alpha_prev[g] = 1.f;
+            kinv_prev[g] = 1.f;
         }
         bool failed = false;
-        // O of tile k (this group's buffer) into the accumulator
+        // O of tile k (one of this group's two buffers) into the accumulator
         auto accumulate = [&](int k) -> bool {
-            const bool landed = mbar_wait(&bar[kOFull0 + grp], (k >> 1) & 1);
+            const int ob = 2 * grp + ((k >> 1) & 1);
+            const bool landed = mbar_wait(&bar[kOFull0 + ob], (k >> 2) & 1);
             if (!__all_sync(kFullMask, landed)) return false;
             tc_fence_after();
             float o[16];
-            tmem_load16(tmem + lane_addr + kF8O0 + kF8N * grp, o);
+            tmem_load16(tmem + lane_addr + kF8O0 + kF8QN * ob, o);
+            if constexpr (S::DIRECT) {
+                // a head's three P terms are three columns: add them, undo the
+                // tile's power-of-two P scale
+                float o3[8];
+                tmem_load8(tmem + lane_addr + kF8O0 + kF8QN * ob + 16, o3);
+#pragma unroll
+                for (int g = 0; g < kF8G; ++g) o[g] = ((o[g] + o[8 + g]) + o3[g]) * kinv_prev[g];
+            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kOEmpty0 + grp]);
+            if (lane == 0) mbar_arrive(&bar[kOEmpty0 + ob]);
 #pragma unroll
             for (int g = 0; g < kF8G; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
             return true;
@@ -606,29 +684,82 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 }
                 m_true[g] = fmaxf(m_true[g], mx[g]);
             }
-            float pv[kF8G];
+            // E4M3 P: each head's P is taken times 2^k, the power of two that
+            // brings the tile's largest P into [128, 256), so that its three
+            // E4M3 terms keep 12 bits of every value down to 2^-17 of that
+            // largest (the sum l keeps the unscaled values)
+            float pv[kF8G], kinv[kF8G];
 #pragma unroll
             for (int g = 0; g < kF8G; ++g) {
                 pv[g] = 0.f;
+                kinv[g] = 1.f;
                 if (g < G) {
-                    pv[g] = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
-                    l_part[g] += pv[g];
+                    float kf = 0.f;
+                    if constexpr (S::DIRECT) {
+                        const float dm = mx[g] - m_run[g];  // <= lazy-rescale threshold
+                        int k = 0;
+                        if (dm > -INFINITY) {
+                            k = 7 - (int)floorf(dm);
+                            k = k > 126 ? 126 : k;
+                        }
+                        kf = (float)k;
+                        kinv[g] = exp2i(-k);
+                    }
+                    pv[g] = fast_exp2(s[g] - m_run[g] + kf);  // masked: 2^-inf = 0
+                    l_part[g] += pv[g] * kinv[g];
                 }
             }
-            // this group's previous tile: its P.V, which reads the P buffer
-            // about to be rewritten, must be complete
-            if (last >= 0 && !accumulate(last)) failed = true;
-            // P^T (16 rows = heads, 128 positions) in the operand layout, f16
-            uint8_t *pbuf = smem + S::OFF_P + grp * S::P_BYTES;
+            // P buffer of this tile: last read by P.V of tile i-4, whose O this
+            // group accumulated (after waiting for it) two tiles ago
+            uint8_t *pbuf = smem + S::OFF_P + (2 * grp + ((i >> 1) & 1)) * S::P_BYTES;
+            if constexpr (S::DIRECT) {
+                // P^T as three E4M3 terms: rows t*8 + g (t = term, g = head),
+                // 128 positions of one byte, K-major with 128-byte swizzle
 #pragma unroll
-            for (int g = 0; g < kF8N; ++g)
-                *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kF8N * 128)) =
-                    narrow_f16<false>(g < kF8G ? pv[g] : 0.f);
+                for (int g = 0; g < kF8G; g += 2) {
+                    float a = pv[g], b = pv[g + 1];
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        const uint32_t c = e4m3x2_from_f32(a, b);
+                        const float2 back = e4m3x2_to_f32(c);
+                        a -= back.x;  // exact: the remainder is representable
+                        b -= back.y;
+                        pbuf[e4m3_operand_offset<128>(8 * t + g, r)] = (uint8_t)(c & 0xffu);
+                        pbuf[e4m3_operand_offset<128>(8 * t + g + 1, r)] = (uint8_t)(c >> 8);
+                    }
+                }
+                if (!valid) {
+                    // Stale rows of the last tile: P is 0 there but V must be
+                    // finite (0 * NaN would poison the product), so zero them
+                    // once the V tile has landed (its slot cannot move on
+                    // before P.V of this tile, which waits for this P).
+                    const int slot = i % S::NV;
+                    if (mbar_wait(&bar[kVFull0 + slot], (i / S::NV) & 1)) {
+                        uint4 *vrow = reinterpret_cast<uint4 *>(smem + S::OFF_VSTG +
+                                                                slot * S::STG_BYTES + r * D);
+#pragma unroll
+                        for (int c = 0; c < D / 16; ++c) vrow[c] = make_uint4(0, 0, 0, 0);
+                    } else {
+                        failed = true;
+                    }
+                }
+            } else {
+                // P^T (16 rows = heads, 128 positions) in the operand layout, f16
+#pragma unroll
+                for (int g = 0; g < kF8N; ++g)
+                    *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kF8N * 128)) =
+                        narrow_f16<false>(g < kF8G ? pv[g] : 0.f);
+            }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kPFull0 + grp]);
+            if (lane == 0) mbar_arrive(&bar[kPFull0 + 2 * grp + ((i >> 1) & 1)]);
+            // this group's previous tile, while P.V of this one runs
+            if (last >= 0 && !accumulate(last)) failed = true;
 #pragma unroll
-            for (int g = 0; g < kF8G; ++g) alpha_prev[g] = alpha[g];
+            for (int g = 0; g < kF8G; ++g) {
+                alpha_prev[g] = alpha[g];
+                kinv_prev[g] = kinv[g];
+            }
             last = i;
         }
         if (!failed && last >= 0 && !accumulate(last)) failed = true;
@@ -709,8 +840,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         // let copies and MMAs still in flight finish before shared memory and
         // TMEM are released (each wait is bounded)
         const int last = ntiles - 1;
-        (void)mbar_wait(&bar[kStgFull0 + last % S::NSTG], (last / S::NSTG) & 1);
-        (void)mbar_wait(&bar[kVEmpty0 + last % S::NVB], (last / S::NVB) & 1);
+        (void)mbar_wait(&bar[kKFull0 + last % S::NK], (last / S::NK) & 1);
+        (void)mbar_wait(&bar[kVFull0 + last % S::NV], (last / S::NV) & 1);
     }
     if (warp == 1) {
         __syncwarp();
@@ -723,12 +854,14 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
 using F8Kernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
 
-F8Kernel pick_fp8(bool bf16, int D, int *smem) {
+F8Kernel pick_fp8(bool bf16, int D, int *smem, int *threads) {
     if (D == 128) {
         *smem = F8Shape<128>::SMEM_BYTES;
+        *threads = F8Shape<128>::THREADS;
         return bf16 ? paged_decode_fp8_kernel<true, 128> : paged_decode_fp8_kernel<false, 128>;
     }
     *smem = F8Shape<64>::SMEM_BYTES;
+    *threads = F8Shape<64>::THREADS;
     return bf16 ? paged_decode_fp8_kernel<true, 64> : paged_decode_fp8_kernel<false, 64>;
 }
 
@@ -741,8 +874,8 @@ bool fp8_supported(int head_dim, int group) {
 // Resident CTAs per SM from the kernel's footprint (shared memory, registers
 // per sub-partition, TMEM), as for the 16-bit tensor-core kernel.
 int fp8_ctas_per_sm(bool bf16, int head_dim) {
-    int smem = 0;
-    F8Kernel k = pick_fp8(bf16, head_dim, &smem);
+    int smem = 0, threads = 0;
+    F8Kernel k = pick_fp8(bf16, head_dim, &smem, &threads);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return 1;
     int dev = 0, smem_sm = 0, reserved = 0;
     cudaFuncAttributes a;
@@ -756,7 +889,7 @@ int fp8_ctas_per_sm(bool bf16, int head_dim) {
     const int by_smem = smem_sm / (smem + (int)a.sharedSizeBytes + reserved);
     const int regs = (a.numRegs + 7) / 8 * 8;
     const int warps_per_subpartition = 16384 / (regs * 32);
-    const int by_regs = 4 * warps_per_subpartition / kF8Warps;
+    const int by_regs = 4 * warps_per_subpartition / (threads / 32);
     const int by_tmem = 512 / kF8Cols;
     int n = by_smem < by_regs ? by_smem : by_regs;
     n = n < by_tmem ? n : by_tmem;
@@ -766,17 +899,18 @@ int fp8_ctas_per_sm(bool bf16, int head_dim) {
 pa_status launch_decode_fp8(const DecodeParams &prm, bool bf16, int head_dim, int num_partitions,
                             int num_kv_heads, int num_seqs, cudaStream_t stream) {
     if (num_seqs == 0) return PA_OK;
-    int smem = 0;
-    F8Kernel k = pick_fp8(bf16, head_dim, &smem);
+    int smem = 0, threads = 0;
+    F8Kernel k = pick_fp8(bf16, head_dim, &smem, &threads);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return PA_ERR_CUDA;
     const int64_t rows = (int64_t)prm.num_blocks * num_kv_heads * prm.block_size;
     CUtensorMap mk, mv;
-    // K lands swizzled (the q.K^T operand), V row-major (the converters' input)
+    // K lands swizzled (the q.K^T operand); V too at d = 128 (the MN-major
+    // P.V operand), row-major at d = 64 (the converters' input)
     if (!pool_tensor_map_fp8(&mk, prm.k_pool, rows, head_dim, true) ||
-        !pool_tensor_map_fp8(&mv, prm.v_pool, rows, head_dim, false))
+        !pool_tensor_map_fp8(&mv, prm.v_pool, rows, head_dim, head_dim == 128))
         return PA_ERR_CUDA;
     dim3 grid((unsigned)num_partitions, (unsigned)num_kv_heads, (unsigned)num_seqs);
-    if (launch_pdl(k, grid, dim3(kF8Threads), (size_t)smem, stream, prm, mk, mv) != cudaSuccess)
+    if (launch_pdl(k, grid, dim3((unsigned)threads), (size_t)smem, stream, prm, mk, mv) != cudaSuccess)
         return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -135,9 +135,10 @@ __host__ __device__ constexpr uint32_t f16_idesc(bool bf16, bool a_mn, bool b_mn
 }
 
 // Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0
-// in both fields), f32 accumulator, both K-major.
-__host__ __device__ constexpr uint32_t e4m3_idesc(int M, int N) {
-    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// in both fields), f32 accumulator, B K-major, A K-major or MN-major.
+__host__ __device__ constexpr uint32_t e4m3_idesc(int M, int N, bool a_mn) {
+    return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
 
 // Byte offset of element (row, col) of a K-major operand stored as
