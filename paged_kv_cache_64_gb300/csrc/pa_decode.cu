@@ -777,7 +777,7 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
     r->head_dim = head_dim;
     int P = partition_tokens;
     if (P == 0) {
-        const int per_sm = r->fp8  ? fp8_ctas_per_sm(dtype == PA_BF16, head_dim)
+        const int per_sm = r->fp8  ? fp8_ctas_per_sm(dtype == PA_BF16, head_dim, G)
                            : r->tc ? tc_ctas_per_sm(dtype == PA_BF16, head_dim)
                                    : decode_ctas_per_sm(r->entry);
         P = auto_partition(num_seqs, num_kv_heads, max_seq_len, per_sm, block_size);

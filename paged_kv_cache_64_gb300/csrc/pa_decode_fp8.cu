@@ -58,14 +58,10 @@ namespace {
 
 constexpr int kF8Tile = 128;       // positions per tile (MMA M of q.K^T)
 constexpr int kF8N = 16;           // MMA N of P.V in f16: the query heads of a group, zero-padded
-constexpr int kF8QN = 32;          // MMA N over E4M3 terms: three terms x 8 heads, zero-padded
 constexpr int kF8G = 8;            // largest group the kernel serves
-// TMEM columns: S of each softmax group at 0 and 32, O of tile t at
-// 64 + 32 * (2 * (t & 1) + ((t >> 1) & 1)) (two per group), 32 columns each
-constexpr int kF8Cols = 256;
-constexpr int kF8S0 = 0, kF8O0 = 64;
 constexpr int kF8Conv0 = 10;       // first converter warp (f16 P.V only)
 constexpr int kF8VProd = 10;       // the V producer warp (E4M3 P.V only)
+constexpr int kF8PvWarp = 11;      // the P.V issuer (E4M3 P.V only)
 constexpr int kF8ConvWarps = 6;    // converter warps (V)
 
 constexpr int kF8MaxRing = 12;     // slots of a staging ring
@@ -83,21 +79,29 @@ enum F8Bar {
     kNumF8Bars = kVEmpty0 + kF8MaxRing
 };
 
-template <int D>
+template <int D, int GM>
 struct F8Shape {
     // d = 128: P.V on E4M3 codes too (V^T straight from the staged tile, P as
     // three E4M3 terms); d = 64: V widened to f16 by converter warps
     static constexpr bool DIRECT = D == 128;
-    // d = 128: producer K, MMA, 8 softmax, producer V; d = 64: producer,
-    // MMA, 8 softmax, 6 converters (4 per sub-partition, 128 registers)
-    static constexpr int WARPS = DIRECT ? 11 : 16;
+    // GM (4 or 8): the heads a KV head's group may have.  E4M3 operands hold
+    // three terms per head in rows t * GM + g, zero-padded to QN rows (the
+    // MMA N).  TMEM: S of each softmax group at 0 and QN, O of tile t at
+    // 2 * QN + QN * (2 * (t & 1) + ((t >> 1) & 1)) (two per group).
+    static constexpr int QN = (3 * GM + 15) / 16 * 16;
+    static constexpr int S0 = 0, O0 = 2 * QN;
+    static constexpr int COLS = 6 * QN <= 128 ? 128 : 256;
+    // d = 128: producer K, q.K^T issuer, 8 softmax, producer V, P.V issuer;
+    // d = 64: producer, MMA issuer, 8 softmax, 6 converters (4 per
+    // sub-partition, 128 registers)
+    static constexpr int WARPS = DIRECT ? 12 : 16;
     static constexpr int THREADS = WARPS * 32;
     static constexpr int SLAB = kF8Tile * 128;        // one 64-dim f16 slab of a tile: 16 KiB
     static constexpr int V_BYTES = 2 * SLAB;          // V^T is M = 128 dims; d = 64 pads with zeros
     static constexpr int STG_BYTES = kF8Tile * D;     // E4M3 tile of K (or V): 128 rows of d bytes
     // K tiles and Qs: K-major E4M3 operands of d-byte rows, in atoms of 8 rows
     // (128-byte swizzle for d = 128, 64-byte for d = 64)
-    static constexpr int Q_BYTES = kF8QN * D;
+    static constexpr int Q_BYTES = QN * D;
     // P^T: 16 rows of 128 f16 positions, or 32 rows of 128 E4M3 positions
     static constexpr int P_BYTES = 4096;
     // Staging rings of E4M3 tiles: a K slot is free once q.K^T has read it,
@@ -143,6 +147,21 @@ __device__ __forceinline__ uint32_t e4m3_operand_offset(int row, int k) {
 template <int D>
 __device__ __forceinline__ uint64_t e4m3_operand_desc(uint32_t saddr) {
     return D == 128 ? sw128_desc(saddr, 16, 8 * D) : sw64_desc(saddr, 16, 8 * D);
+}
+
+// Two f16 values (low half first) to two E4M3 codes (low byte first),
+// nearest with ties to even, saturating (PTX cvt.rn.satfinite.e4m3x2.f16x2).
+__device__ __forceinline__ uint32_t e4m3x2_from_f16x2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    return r;
+}
+
+// a - b on packed f16 pairs.
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 // 2^e for e in [-126, 127], exactly.
@@ -215,11 +234,11 @@ __device__ __forceinline__ uint16_t narrow_out(float x) {
     }
 }
 
-template <bool BF16, int D>
-__global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
+template <bool BF16, int D, int GM>
+__global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
     paged_decode_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v) {
-    using S = F8Shape<D>;
+    using S = F8Shape<D, GM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -284,15 +303,16 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
         mbar_init_fence();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kF8Cols);
+        tmem_alloc(tmem_slot, S::COLS);
         tmem_relinquish();
     }
     if constexpr (S::DIRECT) {
-        // rows 24..31 (the last 8-row atom) of the four E4M3 P^T buffers: zero
-        // once, never written again
-        for (int i = threadIdx.x; i < 4 * 64; i += S::THREADS) {
-            uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_P + (i >> 6) * S::P_BYTES + 3 * 1024);
-            z[i & 63] = make_uint4(0, 0, 0, 0);
+        // rows 3 * GM .. QN-1 of the four E4M3 P^T buffers (whole 128-byte
+        // rows, contiguous): zero once, never written again
+        constexpr int Z0 = (3 * GM / 8) * 1024 + (3 * GM % 8) * 128, ZN = (S::QN * 128 - Z0) / 16;
+        for (int i = threadIdx.x; i < 4 * ZN; i += S::THREADS) {
+            uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_P + (i / ZN) * S::P_BYTES + Z0);
+            z[i % ZN] = make_uint4(0, 0, 0, 0);
         }
         fence_async_smem();
     } else {
@@ -426,12 +446,14 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
             *abort_flag = 1;
         }
       }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (S::DIRECT && warp == kF8PvWarp)) {
         // ---------------------------------------------------------- MMA issue
+        // (d = 128: q.K^T from warp 1 and P.V from warp kF8PvWarp, two
+        // independent streams; d = 64: both from warp 1)
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = e4m3_idesc(kF8Tile, kF8QN, false);
+            constexpr uint32_t idesc_qk = e4m3_idesc(kF8Tile, S::QN, false);
             constexpr uint32_t idesc_pv = f16_idesc(false, true, false, 128, kF8N);
-            constexpr uint32_t idesc_pv8 = e4m3_idesc(128, kF8QN, true);  // V^T MN-major
+            constexpr uint32_t idesc_pv8 = e4m3_idesc(128, S::QN, true);  // V^T MN-major
             const uint32_t sbase = smem_addr(smem);
             // q.K^T of tile t (its K landed, its S buffer read by the softmax)
             auto issue_qk = [&](int t) -> bool {
@@ -442,7 +464,7 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
                 const uint32_t kaddr = sbase + S::OFF_STG + slot * S::STG_BYTES;
 #pragma unroll
                 for (int ks = 0; ks < D / 32; ++ks)  // 32 codes (bytes) of d per MMA
-                    tc_mma_f8(tmem + kF8S0 + kF8QN * b, e4m3_operand_desc<D>(kaddr + ks * 32),
+                    tc_mma_f8(tmem + S::S0 + S::QN * b, e4m3_operand_desc<D>(kaddr + ks * 32),
                               e4m3_operand_desc<D>(sbase + S::OFF_Q + ks * 32), idesc_qk, ks > 0);
                 tc_commit(&bar[kSFull0 + b]);
                 tc_commit(&bar[kKEmpty0 + slot]);
@@ -465,7 +487,7 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
                     const uint32_t vaddr = sbase + S::OFF_VSTG + slot * S::STG_BYTES;
 #pragma unroll
                     for (int ks = 0; ks < kF8Tile / 32; ++ks)
-                        tc_mma_f8(tmem + kF8O0 + kF8QN * b, sw128_desc(vaddr + ks * 4096, 16, 1024),
+                        tc_mma_f8(tmem + S::O0 + S::QN * b, sw128_desc(vaddr + ks * 4096, 16, 1024),
                                   sw128_desc(sbase + S::OFF_P + b * S::P_BYTES + ks * 32, 16, 1024),
                                   idesc_pv8, ks > 0);
                     tc_commit(&bar[kOFull0 + b]);
@@ -475,7 +497,7 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
                     for (int ks = 0; ks < kF8Tile / 16; ++ks) {
                         const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
                         const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kF8N * 128) + (ks & 3) * 32;
-                        tc_mma(tmem + kF8O0 + kF8QN * b,
+                        tc_mma(tmem + S::O0 + S::QN * b,
                                sw128_desc(sbase + S::OFF_V + (t & 1) * S::V_BYTES + voff, S::SLAB, 1024),
                                sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
                     }
@@ -488,9 +510,17 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
             // t+2 only needs the softmax to have read S of tile t (the first
             // thing it does with tile t), so a softmax group finds its next S
             // ready when it has written P of this tile.
-            bool ok = mbar_wait(&bar[kQReady], 0) && issue_qk(0) && (ntiles < 2 || issue_qk(1));
-            for (int t = 0; ok && t < ntiles; ++t)
-                ok = (t + 2 >= ntiles || issue_qk(t + 2)) && issue_pv(t);
+            bool ok = true;
+            if (S::DIRECT && warp == kF8PvWarp) {
+                for (int t = 0; ok && t < ntiles; ++t) ok = issue_pv(t);
+            } else if (S::DIRECT) {
+                ok = mbar_wait(&bar[kQReady], 0);
+                for (int t = 0; ok && t < ntiles; ++t) ok = issue_qk(t);
+            } else {
+                ok = mbar_wait(&bar[kQReady], 0) && issue_qk(0) && (ntiles < 2 || issue_qk(1));
+                for (int t = 0; ok && t < ntiles; ++t)
+                    ok = (t + 2 >= ntiles || issue_qk(t + 2)) && issue_pv(t);
+            }
             if (!ok) {
                 record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
                 *abort_flag = 1;
@@ -508,11 +538,11 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
         float *xch = reinterpret_cast<float *>(smem + S::OFF_XCH);
 
         if (grp == 0) {
-            // Qs: head g's q times 2^e_g as three E4M3 terms in rows g, 8 + g
-            // and 16 + g of a 32-row K-major operand (rows 24.. and the rows
-            // of absent heads zero).  Thread (g, j) takes d/16 elements.
-            constexpr int EPT = D / 16;
-            const int g = st >> 4, j = st & 15;
+            // Qs: head g's q times 2^e_g as three E4M3 terms in rows g, GM + g
+            // and 2 GM + g of a QN-row K-major operand (the rows of absent
+            // heads and rows 3 GM.. zero).  Thread (g, j) takes EPT elements.
+            constexpr int TPH = 128 / GM, EPT = D / TPH;  // threads per head, elements each
+            const int g = st / TPH, j = st % TPH;
             float x[EPT];
 #pragma unroll
             for (int e = 0; e < EPT; ++e) x[e] = 0.f;
@@ -523,9 +553,11 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
                 if constexpr (EPT == 8) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(src);
                     w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-                } else {
+                } else if constexpr (EPT == 4) {
                     const uint2 v = *reinterpret_cast<const uint2 *>(src);
                     w[0] = v.x; w[1] = v.y;
+                } else {
+                    w[0] = *reinterpret_cast<const uint32_t *>(src);
                 }
 #pragma unroll
                 for (int e = 0; e < EPT / 2; ++e) {
@@ -538,7 +570,8 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
 #pragma unroll
             for (int e = 0; e < EPT; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
+            for (int off = TPH / 2; off >= 1; off >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
             // 2^e_g brings amax into [128, 256): e_g = 7 - floor(log2 amax)
             int eg = 0;
             if (amax > 0.f) {
@@ -547,33 +580,34 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
                 eg = eg < -120 ? -120 : (eg > 120 ? 120 : eg);
             }
             const float up = exp2i(eg);
-            uint32_t code[3][EPT / 4];  // EPT codes per term, 4 per word
+            uint32_t code[3][(EPT + 3) / 4];  // EPT codes per term, 4 per word
 #pragma unroll
-            for (int w4 = 0; w4 < EPT / 4; ++w4) {
-                uint32_t c[3][2];
+            for (int t = 0; t < 3; ++t)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float a = x[4 * w4 + 2 * h] * up, b = x[4 * w4 + 2 * h + 1] * up;
+                for (int w4 = 0; w4 < (EPT + 3) / 4; ++w4) code[t][w4] = 0u;
 #pragma unroll
-                    for (int t = 0; t < 3; ++t) {
-                        c[t][h] = e4m3x2_from_f32(a, b);
-                        const float2 back = e4m3x2_to_f32(c[t][h]);
-                        a -= back.x;  // exact: the remainder is representable
-                        b -= back.y;
-                    }
+            for (int e2 = 0; e2 < EPT / 2; ++e2) {  // element pairs
+                float a = x[2 * e2] * up, b = x[2 * e2 + 1] * up;
+#pragma unroll
+                for (int t = 0; t < 3; ++t) {
+                    const uint32_t c = e4m3x2_from_f32(a, b);
+                    const float2 back = e4m3x2_to_f32(c);
+                    a -= back.x;  // exact: the remainder is representable
+                    b -= back.y;
+                    code[t][e2 >> 1] |= c << (16 * (e2 & 1));
                 }
-#pragma unroll
-                for (int t = 0; t < 3; ++t) code[t][w4] = c[t][0] | (c[t][1] << 16);
             }
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {  // term rows, then a zero row (24 + g)
-                const int row = 8 * t + g;
+            for (int t = 0; t < 4; ++t) {  // term rows, then a zero row (3 GM + g)
+                const int row = GM * t + g;
                 uint8_t *dst = smem + S::OFF_Q + e4m3_operand_offset<D>(row, j * EPT);
                 if constexpr (EPT == 8) {
                     *reinterpret_cast<uint2 *>(dst) =
                         t < 3 ? make_uint2(code[t][0], code[t][1]) : make_uint2(0u, 0u);
-                } else {
+                } else if constexpr (EPT == 4) {
                     *reinterpret_cast<uint32_t *>(dst) = t < 3 ? code[t][0] : 0u;
+                } else {
+                    *reinterpret_cast<uint16_t *>(dst) = (uint16_t)(t < 3 ? code[t][0] : 0u);
                 }
             }
             if (j == 0) qmul[g] = g < G ? p.scale_log2 * exp2i(-eg) : 0.f;
@@ -582,15 +616,15 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
             if (lane == 0) mbar_arrive(&bar[kQReady]);
         }
         named_bar(3, 256);  // qmul is written
-        float qm[kF8G];
+        float qm[GM];
 #pragma unroll
-        for (int g = 0; g < kF8G; ++g) qm[g] = qmul[g];
+        for (int g = 0; g < GM; ++g) qm[g] = qmul[g];
 
-        float m_run[kF8G], m_true[kF8G], l_part[kF8G], acc[kF8G], alpha_prev[kF8G];
+        float m_run[GM], m_true[GM], l_part[GM], acc[GM], alpha_prev[GM];
         // 2^-k of the previous tile's P scale (E4M3 P only)
-        float kinv_prev[kF8G];
+        float kinv_prev[GM];
 #pragma unroll
-        for (int g = 0; g < kF8G; ++g) {
+        for (int g = 0; g < GM; ++g) {
             m_run[g] = -INFINITY;
             m_true[g] = -INFINITY;
             l_part[g] = 0.f;
@@ -606,20 +640,21 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
             if (!__all_sync(kFullMask, landed)) return false;
             tc_fence_after();
             float o[16];
-            tmem_load16(tmem + lane_addr + kF8O0 + kF8QN * ob, o);
+            tmem_load16(tmem + lane_addr + S::O0 + S::QN * ob, o);
             if constexpr (S::DIRECT) {
                 // a head's three P terms are three columns: add them, undo the
                 // tile's power-of-two P scale
                 float o3[8];
-                tmem_load8(tmem + lane_addr + kF8O0 + kF8QN * ob + 16, o3);
+                if constexpr (GM == 8) tmem_load8(tmem + lane_addr + S::O0 + S::QN * ob + 16, o3);
 #pragma unroll
-                for (int g = 0; g < kF8G; ++g) o[g] = ((o[g] + o[8 + g]) + o3[g]) * kinv_prev[g];
+                for (int g = 0; g < GM; ++g)
+                    o[g] = ((o[g] + o[GM + g]) + (GM == 8 ? o3[g] : o[2 * GM + g])) * kinv_prev[g];
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kOEmpty0 + ob]);
 #pragma unroll
-            for (int g = 0; g < kF8G; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
+            for (int g = 0; g < GM; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
             return true;
         };
 
@@ -627,33 +662,55 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
         for (int i = grp; i < ntiles; i += 2) {
             const bool landed = !failed && mbar_wait(&bar[kSFull0 + grp], (i >> 1) & 1);
             const bool ok = __all_sync(kFullMask, landed);
-            float s[kF8G];
+            float s[GM];
             if (ok) {
                 tc_fence_after();
                 float t12[16], t3[8];
-                tmem_load16(tmem + lane_addr + kF8S0 + kF8QN * grp, t12);
-                tmem_load8(tmem + lane_addr + kF8S0 + kF8QN * grp + 16, t3);
+                tmem_load16(tmem + lane_addr + S::S0 + S::QN * grp, t12);
+                if constexpr (GM == 8) tmem_load8(tmem + lane_addr + S::S0 + S::QN * grp + 16, t3);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[kSEmpty0 + grp]);
 #pragma unroll
-                for (int g = 0; g < kF8G; ++g) s[g] = (t12[g] + t12[8 + g]) + t3[g];
+                for (int g = 0; g < GM; ++g)
+                    s[g] = (t12[g] + t12[GM + g]) + (GM == 8 ? t3[g] : t12[2 * GM + g]);
             } else {
 #pragma unroll
-                for (int g = 0; g < kF8G; ++g) s[g] = 0.f;
+                for (int g = 0; g < GM; ++g) s[g] = 0.f;
             }
             const int tile0 = start + i * kF8Tile;
             const int nvalid = (end - tile0 < kF8Tile) ? end - tile0 : kF8Tile;
             const bool valid = r < nvalid;
-            // tile max of each head over the 128 positions
+            // tile max of each head over the 128 positions: a halving
+            // butterfly over the warp (each exchange hands the partner the
+            // heads it keeps), after which lane L holds head (L >> 2) & 7
             float *tmax = gred + ((i >> 1) & 1) * (4 * kF8N);
 #pragma unroll
-            for (int g = 0; g < kF8G; ++g) {
-                s[g] = valid ? s[g] * qm[g] : -INFINITY;  // select: NaN-safe
-                float v = s[g];
+            for (int g = 0; g < GM; ++g) s[g] = valid ? s[g] * qm[g] : -INFINITY;  // select: NaN-safe
+            {
+                // GM = 8: lane L ends with head (L >> 2) & 7; GM = 4: (L >> 3) & 3
+                float v4[4], v2[2];
+                if constexpr (GM == 8) {
+                    const bool b4 = lane & 16;
 #pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
-                if (lane == 0) tmax[sw * kF8N + g] = v;
+                    for (int j = 0; j < 4; ++j)
+                        v4[j] = fmaxf(b4 ? s[4 + j] : s[j],
+                                      __shfl_xor_sync(kFullMask, b4 ? s[j] : s[4 + j], 16));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v4[j] = s[j];
+                }
+                constexpr int o2 = GM == 8 ? 8 : 16, o1 = o2 / 2;
+                const bool c2 = lane & o2, c1 = lane & o1;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    v2[j] = fmaxf(c2 ? v4[2 + j] : v4[j],
+                                  __shfl_xor_sync(kFullMask, c2 ? v4[j] : v4[2 + j], o2));
+                float v = fmaxf(c1 ? v2[1] : v2[0], __shfl_xor_sync(kFullMask, c1 ? v2[0] : v2[1], o1));
+#pragma unroll
+                for (int off = o1 / 2; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
+                constexpr int sh = GM == 8 ? 2 : 3;
+                if ((lane & ((1 << sh) - 1)) == 0) tmax[sw * kF8N + ((lane >> sh) & (GM - 1))] = v;
             }
             if (lane == 0) tmax[sw * kF8N + kF8N - 1] = ok ? 1.f : 0.f;  // column 15: health flag
             named_bar(1 + grp, 128);
@@ -665,16 +722,16 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
                 break;
             }
             bool need = false;
-            float mx[kF8G];
+            float mx[GM];
 #pragma unroll
-            for (int g = 0; g < kF8G; ++g) {
+            for (int g = 0; g < GM; ++g) {
                 mx[g] = fmaxf(fmaxf(tmax[g], tmax[kF8N + g]),
                               fmaxf(tmax[2 * kF8N + g], tmax[3 * kF8N + g]));
                 need |= (g < G) && (mx[g] > m_run[g] + kLazyRescale);
             }
-            float alpha[kF8G];
+            float alpha[GM];
 #pragma unroll
-            for (int g = 0; g < kF8G; ++g) {
+            for (int g = 0; g < GM; ++g) {
                 alpha[g] = 1.f;
                 if (need) {  // group-uniform
                     const float mn = fmaxf(m_run[g], mx[g]);
@@ -688,44 +745,45 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
             // brings the tile's largest P into [128, 256), so that its three
             // E4M3 terms keep 12 bits of every value down to 2^-17 of that
             // largest (the sum l keeps the unscaled values)
-            float pv[kF8G], kinv[kF8G];
+            float pv[GM], kinv[GM];
 #pragma unroll
-            for (int g = 0; g < kF8G; ++g) {
+            for (int g = 0; g < GM; ++g) {
                 pv[g] = 0.f;
                 kinv[g] = 1.f;
                 if (g < G) {
-                    float kf = 0.f;
+                    float pg = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
+                    l_part[g] += pg;
                     if constexpr (S::DIRECT) {
                         const float dm = mx[g] - m_run[g];  // <= lazy-rescale threshold
                         int k = 0;
                         if (dm > -INFINITY) {
-                            k = 7 - (int)floorf(dm);
+                            k = 7 - __float2int_rd(dm);
                             k = k > 126 ? 126 : k;
                         }
-                        kf = (float)k;
                         kinv[g] = exp2i(-k);
+                        pg *= exp2i(k);  // exact: a power of two, k >= -1
                     }
-                    pv[g] = fast_exp2(s[g] - m_run[g] + kf);  // masked: 2^-inf = 0
-                    l_part[g] += pv[g] * kinv[g];
+                    pv[g] = pg;
                 }
             }
             // P buffer of this tile: last read by P.V of tile i-4, whose O this
             // group accumulated (after waiting for it) two tiles ago
             uint8_t *pbuf = smem + S::OFF_P + (2 * grp + ((i >> 1) & 1)) * S::P_BYTES;
             if constexpr (S::DIRECT) {
-                // P^T as three E4M3 terms: rows t*8 + g (t = term, g = head),
-                // 128 positions of one byte, K-major with 128-byte swizzle
+                // P^T as three E4M3 terms of P rounded to f16 (11 significant
+                // bits: the terms hold it exactly down to E4M3's subnormal
+                // floor), split in packed f16 pairs: rows t*8 + g (t = term,
+                // g = head), 128 positions of one byte, K-major with 128-byte
+                // swizzle
 #pragma unroll
-                for (int g = 0; g < kF8G; g += 2) {
-                    float a = pv[g], b = pv[g + 1];
+                for (int g = 0; g < GM; g += 2) {
+                    uint32_t h = narrow2<false>(pv[g], pv[g + 1]);
 #pragma unroll
                     for (int t = 0; t < 3; ++t) {
-                        const uint32_t c = e4m3x2_from_f32(a, b);
-                        const float2 back = e4m3x2_to_f32(c);
-                        a -= back.x;  // exact: the remainder is representable
-                        b -= back.y;
-                        pbuf[e4m3_operand_offset<128>(8 * t + g, r)] = (uint8_t)(c & 0xffu);
-                        pbuf[e4m3_operand_offset<128>(8 * t + g + 1, r)] = (uint8_t)(c >> 8);
+                        const uint32_t c = e4m3x2_from_f16x2(h);
+                        h = hsub2_bits(h, f16x2_from_e4m3x2((uint16_t)c));  // exact
+                        pbuf[e4m3_operand_offset<128>(GM * t + g, r)] = (uint8_t)(c & 0xffu);
+                        pbuf[e4m3_operand_offset<128>(GM * t + g + 1, r)] = (uint8_t)(c >> 8);
                     }
                 }
                 if (!valid) {
@@ -748,7 +806,7 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
 #pragma unroll
                 for (int g = 0; g < kF8N; ++g)
                     *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kF8N * 128)) =
-                        narrow_f16<false>(g < kF8G ? pv[g] : 0.f);
+                        narrow_f16<false>(g < GM ? pv[g] : 0.f);
             }
             fence_async_smem();
             __syncwarp();
@@ -756,7 +814,7 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
             // this group's previous tile, while P.V of this one runs
             if (last >= 0 && !accumulate(last)) failed = true;
 #pragma unroll
-            for (int g = 0; g < kF8G; ++g) {
+            for (int g = 0; g < GM; ++g) {
                 alpha_prev[g] = alpha[g];
                 kinv_prev[g] = kinv[g];
             }
@@ -766,16 +824,16 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
         // l over the group's 128 position-threads, per head
         float *lsum = gred + 2 * (4 * kF8N);
 #pragma unroll
-        for (int g = 0; g < kF8G; ++g) {
+        for (int g = 0; g < GM; ++g) {
             float v = l_part[g];
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
             if (lane == 0) lsum[sw * kF8N + g] = v;
         }
         named_bar(1 + grp, 128);
-        float lt[kF8G];
+        float lt[GM];
 #pragma unroll
-        for (int g = 0; g < kF8G; ++g)
+        for (int g = 0; g < GM; ++g)
             lt[g] = lsum[g] + lsum[kF8N + g] + lsum[2 * kF8N + g] + lsum[3 * kF8N + g];
         // group B hands its state to group A
         float *xacc = xch;                  // [kF8G][D]
@@ -783,11 +841,11 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
         if (grp == 1) {
             if (r < D) {
 #pragma unroll
-                for (int g = 0; g < kF8G; ++g) xacc[g * D + r] = acc[g];
+                for (int g = 0; g < GM; ++g) xacc[g * D + r] = acc[g];
             }
             if (st == 0) {
 #pragma unroll
-                for (int g = 0; g < kF8G; ++g) {
+                for (int g = 0; g < GM; ++g) {
                     xm[g] = m_run[g];
                     xm[kF8G + g] = m_true[g];
                     xm[2 * kF8G + g] = lt[g];
@@ -805,7 +863,7 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
                 }
             } else if (r < D) {
 #pragma unroll
-                for (int g = 0; g < kF8G; ++g) {
+                for (int g = 0; g < GM; ++g) {
                     if (g >= G) break;
                     // merge of the two groups' partial softmaxes
                     const float mb = xm[g];
@@ -846,7 +904,7 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kF8Cols);
+        tmem_dealloc(tmem, S::COLS);
     }
     if (!direct && !*abort_flag && p.counters != nullptr)
         finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_STG));
@@ -854,15 +912,23 @@ __global__ void __launch_bounds__(F8Shape<D>::THREADS, 1)
 
 using F8Kernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
 
-F8Kernel pick_fp8(bool bf16, int D, int *smem, int *threads) {
-    if (D == 128) {
-        *smem = F8Shape<128>::SMEM_BYTES;
-        *threads = F8Shape<128>::THREADS;
-        return bf16 ? paged_decode_fp8_kernel<true, 128> : paged_decode_fp8_kernel<false, 128>;
-    }
-    *smem = F8Shape<64>::SMEM_BYTES;
-    *threads = F8Shape<64>::THREADS;
-    return bf16 ? paged_decode_fp8_kernel<true, 64> : paged_decode_fp8_kernel<false, 64>;
+struct F8Pick {
+    F8Kernel fn;
+    int smem, threads, cols;
+};
+
+template <int D, int GM>
+F8Pick pick_fp8_shape(bool bf16) {
+    using S = F8Shape<D, GM>;
+    return {bf16 ? paged_decode_fp8_kernel<true, D, GM> : paged_decode_fp8_kernel<false, D, GM>,
+            S::SMEM_BYTES, S::THREADS, S::COLS};
+}
+
+// The instantiation for head size D and a group of `group` query heads
+// (up to 4, or up to 8).
+F8Pick pick_fp8(bool bf16, int D, int group) {
+    if (D == 128) return group <= 4 ? pick_fp8_shape<128, 4>(bf16) : pick_fp8_shape<128, 8>(bf16);
+    return group <= 4 ? pick_fp8_shape<64, 4>(bf16) : pick_fp8_shape<64, 8>(bf16);
 }
 
 }  // namespace
@@ -873,9 +939,10 @@ bool fp8_supported(int head_dim, int group) {
 
 // Resident CTAs per SM from the kernel's footprint (shared memory, registers
 // per sub-partition, TMEM), as for the 16-bit tensor-core kernel.
-int fp8_ctas_per_sm(bool bf16, int head_dim) {
-    int smem = 0, threads = 0;
-    F8Kernel k = pick_fp8(bf16, head_dim, &smem, &threads);
+int fp8_ctas_per_sm(bool bf16, int head_dim, int group) {
+    const F8Pick f = pick_fp8(bf16, head_dim, group);
+    const F8Kernel k = f.fn;
+    const int smem = f.smem, threads = f.threads;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return 1;
     int dev = 0, smem_sm = 0, reserved = 0;
     cudaFuncAttributes a;
@@ -890,7 +957,7 @@ int fp8_ctas_per_sm(bool bf16, int head_dim) {
     const int regs = (a.numRegs + 7) / 8 * 8;
     const int warps_per_subpartition = 16384 / (regs * 32);
     const int by_regs = 4 * warps_per_subpartition / (threads / 32);
-    const int by_tmem = 512 / kF8Cols;
+    const int by_tmem = 512 / f.cols;
     int n = by_smem < by_regs ? by_smem : by_regs;
     n = n < by_tmem ? n : by_tmem;
     return n > 0 ? n : 1;
@@ -899,8 +966,9 @@ int fp8_ctas_per_sm(bool bf16, int head_dim) {
 pa_status launch_decode_fp8(const DecodeParams &prm, bool bf16, int head_dim, int num_partitions,
                             int num_kv_heads, int num_seqs, cudaStream_t stream) {
     if (num_seqs == 0) return PA_OK;
-    int smem = 0, threads = 0;
-    F8Kernel k = pick_fp8(bf16, head_dim, &smem, &threads);
+    const F8Pick f = pick_fp8(bf16, head_dim, prm.group);
+    const F8Kernel k = f.fn;
+    const int smem = f.smem, threads = f.threads;
     if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return PA_ERR_CUDA;
     const int64_t rows = (int64_t)prm.num_blocks * num_kv_heads * prm.block_size;
     CUtensorMap mk, mv;
