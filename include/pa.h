@@ -289,6 +289,16 @@ int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, in
 int pa_set_decode_impl(int impl);
 int pa_get_decode_impl(void);
 
+/* Split-KV partitions one tensor-core CTA computes, process-wide, for every
+ * later call: 0 automatic (default: several consecutive partitions a CTA
+ * when partitions are short and the grid keeps at least two waves of CTAs),
+ * n >= 1 that many wherever partitions are a multiple of 128 positions (1
+ * elsewhere).  Each partition still gets its own (m, l, O) partial, so the
+ * result is the same for any setting (within the output tolerance).  Returns
+ * the previous setting, or -1 (nothing changed) for a negative value.  Not
+ * synchronised with decode calls running on other host threads. */
+int pa_set_decode_span(int span);
+
 /* Resident CTAs per SM of the decode kernel that these shapes select
  * (occupancy query on the current device; 0 if unsupported). */
 int pa_decode_ctas_per_sm(int head_dim, int group_size, pa_dtype dtype);

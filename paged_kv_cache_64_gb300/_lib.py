@@ -73,6 +73,7 @@ SIGNATURES = {
     "pa_decode_ctas_per_sm": (_c_int, [_c_int, _c_int, _c_int]),
     "pa_set_decode_impl": (_c_int, [_c_int]),
     "pa_get_decode_impl": (_c_int, []),
+    "pa_set_decode_span": (_c_int, [_c_int]),
     "pa_decode_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                          _c_int]),
     "pa_decode_partitions": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _c_int, _vp, _c_int, _c_int,

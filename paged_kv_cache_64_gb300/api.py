@@ -132,6 +132,15 @@ def get_decode_impl():
     return {v: k for k, v in DECODE_IMPLS.items()}[_lib.load().pa_get_decode_impl()]
 
 
+def set_decode_span(span):
+    """Split-KV partitions per tensor-core CTA for later calls (0 = automatic);
+    returns the previous setting."""
+    prev = _lib.load().pa_set_decode_span(int(span))
+    if prev < 0:
+        raise ValueError(span)
+    return prev
+
+
 def ctas_per_sm(head_dim, group, dtype):
     return _lib.load().pa_decode_ctas_per_sm(head_dim, group, _DTYPES[dtype])
 

@@ -737,8 +737,9 @@ struct ResolvedDecode {
     bool bf16;
     int head_dim;
     int P;    // -1 single pass, else partition size
-    int NP;   // partitions in the grid
+    int NP;   // partitions (partial slots per row)
     bool fp8 = false;  // E4M3 pools: the FP8 tensor-core kernel (pa_decode_fp8.cu)
+    int span = 1;      // partitions per CTA (tensor-core kernel); grid.x = ceil(NP / span)
 };
 
 // Scales of E4M3 pools (element = scale * code value).
@@ -749,6 +750,8 @@ struct KvFp8 {
 
 // Process-wide choice of decode kernel: 0 automatic, 1 CUDA cores, 2 tensor cores.
 static std::atomic<int> g_decode_impl{0};
+// Process-wide partitions per tensor-core CTA: 0 automatic, else forced.
+static std::atomic<int> g_decode_span{0};
 
 // Automatic choice: the tensor-core kernel wherever it applies (measured
 // faster on every workload shape here; the CUDA-core kernel is bound by
@@ -787,6 +790,23 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
     r->P = P;
     r->NP = (P > 0) ? (max_seq_len + P - 1) / P : 1;
     if (r->NP < 1) r->NP = 1;
+    r->span = 1;
+    if (r->tc && !r->fp8 && P > 0 && P % 128 == 0) {
+        // One CTA computes several consecutive partitions (each still its own
+        // partial) when partitions are short: a CTA's prologue and pipeline
+        // fill are then paid once per ~2048 positions, as long as the grid
+        // keeps at least two waves of CTAs.
+        const int forced = g_decode_span.load(std::memory_order_relaxed);
+        int R = forced > 0 ? forced : 2048 / P;
+        if (R > r->NP) R = r->NP;
+        if (forced <= 0) {
+            const int slots = sm_count() * tc_ctas_per_sm(dtype == PA_BF16, head_dim);
+            while (R > 1 &&
+                   (int64_t)num_seqs * num_kv_heads * ((r->NP + R - 1) / R) < 2ll * slots)
+                --R;
+        }
+        r->span = R > 1 ? R : 1;
+    }
     return PA_OK;
 }
 
@@ -800,8 +820,12 @@ static pa_status launch_decode(const ResolvedDecode &r, DecodeParams prm, int nu
         if (prm.prefix_parts) return PA_ERR_UNSUPPORTED;  // no cascade over E4M3 pools
         return launch_decode_fp8(prm, r.bf16, r.head_dim, r.NP, num_kv_heads, num_seqs, stream);
     }
-    if (r.tc)
-        return launch_decode_tc(prm, r.bf16, r.head_dim, r.NP, num_kv_heads, num_seqs, stream);
+    if (r.tc) {
+        const int span = prm.prefix_parts ? 1 : r.span;  // cascade tails: one partition a CTA
+        prm.span = span;
+        return launch_decode_tc(prm, r.bf16, r.head_dim, (r.NP + span - 1) / span, num_kv_heads,
+                                num_seqs, stream);
+    }
     if (!ensure_smem_attr(reinterpret_cast<const void *>(r.entry.fn), r.entry.smem))
         return PA_ERR_CUDA;
     dim3 grid((unsigned)r.NP, (unsigned)num_kv_heads, (unsigned)num_seqs);
@@ -988,6 +1012,11 @@ int pa_set_decode_impl(int impl) {
 }
 
 int pa_get_decode_impl(void) { return g_decode_impl.load(); }
+
+int pa_set_decode_span(int span) {
+    if (span < 0) return -1;
+    return g_decode_span.exchange(span);
+}
 
 int pa_decode_ctas_per_sm(int head_dim, int group_size, pa_dtype dtype) {
     DecodeEntry e;

@@ -36,7 +36,10 @@ struct DecodeParams {
     int block_size;
     int log2_block;
     int partition_tokens;        // P, multiple of kUnit
-    int num_partitions;          // NP (grid.x)
+    int num_partitions;          // NP (partial slots per (sequence, query head))
+    // Consecutive partitions one CTA computes (tensor-core kernel; 0 or 1:
+    // one).  Each still gets its own partial; grid.x = ceil(NP / span).
+    int span;
     float scale_log2;            // scale * log2(e)
     int mode;                    // 0: decode (direct output when 1 partition), 1: partials only
     // Fused cache write of each sequence's newest token (pa_decode_step), or nullptr.
@@ -248,13 +251,14 @@ __device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, f
 }
 
 // End of a CTA that wrote partials of (seq, kvh): with arrival counters,
-// the last of the item's nparts_seq CTAs combines; a cascade tail of a single
+// the last of the item's CTAs (`arrivals` of them, nparts_seq by default)
+// combines; a cascade tail of a single
 // partition (no counters), or an empty one, combines at once.  The combined
 // slots are the prefix's and the item's: [0, prefix_parts + nparts_seq).
 // Called by every thread of the CTA; scratch as in fused_combine.
 template <bool BF16, int D>
 __device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_seq,
-                            float *scratch) {
+                            float *scratch, int arrivals = -1) {
     __shared__ int last_flag;
     __threadfence();
     __syncthreads();
@@ -262,7 +266,7 @@ __device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_
         last_flag = (p.counters == nullptr || nparts_seq == 0)
                         ? 1
                         : arrive_last(p.counters + (int64_t)seq * p.num_kv_heads + kvh, p.epoch,
-                                      nparts_seq, p.err);
+                                      arrivals < 0 ? nparts_seq : arrivals, p.err);
     __syncthreads();
     if (last_flag) {
         __threadfence();

@@ -81,8 +81,10 @@ struct TcShape {
     static_assert(K_BYTES >= 2 * kTcG * kCombineMaxParts * 4, "combine scratch in the K tile");
 };
 
-template <bool BF16, int D>
-__global__ void __launch_bounds__(kTcThreads)
+// SPAN: a CTA may compute several consecutive partitions (p.span > 1); the
+// variant without it keeps to 96 registers (three CTAs an SM).
+template <bool BF16, int D, bool SPAN>
+__global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
     paged_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v) {
     using S = TcShape<D>;
@@ -105,8 +107,11 @@ __global__ void __launch_bounds__(kTcThreads)
     pdl_wait();  // inputs may come from the previous kernel on the stream
     const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
-    const int start = part * P;
-    if (start >= L) {  // empty partition: as in the CUDA-core kernel
+    // partitions [part0, part0 + R) of the sequence: this CTA's span
+    const int R = (SPAN && p.span > 1) ? p.span : 1;
+    const int part0 = part * R;
+    const int start = part0 * P;
+    if (start >= L) {  // empty partitions: as in the CUDA-core kernel
         if (p.prefix_parts > 0) {
             // empty cascade tail: the output is the prefix's partials combined
             if (nparts_seq == 0 && part == 0)
@@ -118,19 +123,23 @@ __global__ void __launch_bounds__(kTcThreads)
                 for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) o[base + i] = 0u;
             }
         } else {
-            for (int g = 0; g < G; ++g) {
-                const int64_t row =
-                    part_row(p, seq, kvh * G + g, part);
-                if (threadIdx.x == 0) {
-                    p.part_m[row] = -INFINITY;
-                    p.part_l[row] = 0.f;
+            for (int j = 0; j < R && part0 + j < p.num_partitions; ++j)
+                for (int g = 0; g < G; ++g) {
+                    const int64_t row = part_row(p, seq, kvh * G + g, part0 + j);
+                    if (threadIdx.x == 0) {
+                        p.part_m[row] = -INFINITY;
+                        p.part_l[row] = 0.f;
+                    }
+                    for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
                 }
-                for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
-            }
         }
         return;
     }
-    const int end = (start + P < L) ? start + P : L;
+    const int part_end = (part0 + R < nparts_seq) ? part0 + R : nparts_seq;  // past the last
+    const int end = (part_end * P < L) ? part_end * P : L;
+    // tiles per partition when the span has several (P is then a multiple of
+    // the tile), else never reached
+    const int tpp = (SPAN && R > 1) ? P / kTcTile : 1 << 30;
     const int nunits = (end - start + kUnit - 1) / kUnit;
     const int ntiles = (end - start + kTcTile - 1) / kTcTile;
     const bool direct = (p.mode == 0) && (nparts_seq <= 1);
@@ -139,7 +148,7 @@ __global__ void __launch_bounds__(kTcThreads)
     const bool merge_prefix = direct && p.prefix_parts > 0;
     float *pre = reinterpret_cast<float *>(smem + S::OFF_PRE);
 
-    if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write<D>(p, seq, kvh, L);
+    if (p.k_new != nullptr && part_end == nparts_seq) fused_cache_write<D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
         const int counts[kNumTcBars] = {1, 1, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4, 1};
         for (int b = 0; b < kNumTcBars; ++b) mbar_init(&bar[b], counts[b]);
@@ -386,8 +395,51 @@ __global__ void __launch_bounds__(kTcThreads)
             return true;
         };
 
+        // Partial of partition `slot` from the running state (all 128 threads).
+        float *lsum = red + 2 * (4 * kTcN);
+        auto emit_partial = [&](int slot) {
+#pragma unroll
+            for (int g = 0; g < kTcG; ++g) {
+                float v = l_part[g];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
+                if (lane == 0) lsum[sw * kTcN + g] = v;
+            }
+            softmax_bar();
+            if (!failed && r < D) {
+#pragma unroll
+                for (int g = 0; g < kTcG; ++g) {
+                    if (g >= G) break;
+                    const float lt =
+                        lsum[g] + lsum[kTcN + g] + lsum[2 * kTcN + g] + lsum[3 * kTcN + g];
+                    const int64_t row = part_row(p, seq, kvh * G + g, slot);
+                    p.part_o[row * D + r] = acc[g] / lt;
+                    if (r == 0) {
+                        p.part_m[row] = m_true[g];
+                        p.part_l[row] = lt * fast_exp2(m_run[g] - m_true[g]);
+                    }
+                }
+            }
+        };
+
         for (int i = 0; i < ntiles; ++i) {
             const int b = i & 1;
+            bool drained = false;
+            if (SPAN && i > 0 && i % tpp == 0) {
+                // tile i opens the next partition of the span: the previous
+                // one's last O, its partial, then a fresh running state
+                if (!failed && !accumulate(i - 1)) failed = true;
+                drained = true;
+                emit_partial(part0 + i / tpp - 1);
+#pragma unroll
+                for (int g = 0; g < kTcG; ++g) {
+                    m_run[g] = -INFINITY;
+                    m_true[g] = -INFINITY;
+                    l_part[g] = 0.f;
+                    acc[g] = 0.f;
+                    alpha_prev[g] = 1.f;
+                }
+            }
             const bool landed = !failed && mbar_wait(&bar[kSFull0 + b], (i >> 1) & 1);
             const bool ok = __all_sync(kFullMask, landed);
             float s[16];
@@ -475,14 +527,13 @@ __global__ void __launch_bounds__(kTcThreads)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kPFull0 + b]);
-            if (i >= 1 && !accumulate(i - 1)) failed = true;
+            if (i >= 1 && !drained && !accumulate(i - 1)) failed = true;
 #pragma unroll
             for (int g = 0; g < kTcG; ++g) alpha_prev[g] = alpha[g];
         }
         if (!failed && !accumulate(ntiles - 1)) failed = true;
 
         // l over the 128 position-threads, per head
-        float *lsum = red + 2 * (4 * kTcN);
 #pragma unroll
         for (int g = 0; g < kTcG; ++g) {
             float v = l_part[g];
@@ -520,7 +571,7 @@ __global__ void __launch_bounds__(kTcThreads)
                     uint16_t *out = static_cast<uint16_t *>(p.out);
                     out[((int64_t)seq * p.num_q_heads + h) * D + r] = narrow1<BF16>(o);
                 } else {
-                    const int64_t row = part_row(p, seq, h, part);
+                    const int64_t row = part_row(p, seq, h, part_end - 1);
                     p.part_o[row * D + r] = o;
                     if (r == 0) {
                         p.part_m[row] = m_true[g];
@@ -547,8 +598,8 @@ __global__ void __launch_bounds__(kTcThreads)
         tmem_dealloc(tmem, kTcCols);
     }
     if (!direct && !*abort_flag && (p.counters != nullptr || p.prefix_parts > 0))
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq,
-                              reinterpret_cast<float *>(smem + S::OFF_K));
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_K),
+                              (nparts_seq + R - 1) / R);
 }
 
 // ------------------------------------------------------------------ host side
@@ -604,13 +655,17 @@ bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D
 
 using TcKernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
 
-static TcKernel pick_tc(bool bf16, int D, int *smem) {
+static TcKernel pick_tc(bool bf16, int D, int *smem, bool span = false) {
     if (D == 128) {
         *smem = TcShape<128>::SMEM_BYTES;
-        return bf16 ? paged_decode_tc_kernel<true, 128> : paged_decode_tc_kernel<false, 128>;
+        if (span)
+            return bf16 ? paged_decode_tc_kernel<true, 128, true> : paged_decode_tc_kernel<false, 128, true>;
+        return bf16 ? paged_decode_tc_kernel<true, 128, false> : paged_decode_tc_kernel<false, 128, false>;
     }
     *smem = TcShape<64>::SMEM_BYTES;
-    return bf16 ? paged_decode_tc_kernel<true, 64> : paged_decode_tc_kernel<false, 64>;
+    if (span)
+        return bf16 ? paged_decode_tc_kernel<true, 64, true> : paged_decode_tc_kernel<false, 64, true>;
+    return bf16 ? paged_decode_tc_kernel<true, 64, false> : paged_decode_tc_kernel<false, 64, false>;
 }
 
 bool tc_supported(int head_dim, int group) {
@@ -649,7 +704,7 @@ pa_status launch_decode_tc(const DecodeParams &prm, bool bf16, int head_dim, int
                            int num_kv_heads, int num_seqs, cudaStream_t stream) {
     if (num_seqs == 0) return PA_OK;
     int smem = 0;
-    TcKernel k = pick_tc(bf16, head_dim, &smem);
+    TcKernel k = pick_tc(bf16, head_dim, &smem, prm.span > 1);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return PA_ERR_CUDA;
     const int64_t rows = (int64_t)prm.num_blocks * num_kv_heads * prm.block_size;
     CUtensorMap mk, mv;

@@ -467,3 +467,67 @@ def test_bounded_wait_times_out_and_context_survives():
     assert e.value.code == 5
     # the context is still usable
     full_step_parity(Case(workloads.make_plan("tiny")))
+
+
+# ------------------------------------- several partitions per CTA (span)
+@pytest.fixture
+def span():
+    """Force the number of consecutive split-KV partitions a tensor-core CTA
+    computes; restored afterwards."""
+    prev = []
+
+    def set_span(n):
+        prev.append(api.set_decode_span(n))
+
+    yield set_span
+    if prev:
+        api.set_decode_span(prev[0])
+
+
+@pytest.mark.parametrize("name,kw,partition,R", [
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, 512, 2),
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, 512, 3),   # ragged last span
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, 512, 4),
+    ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, 256, 4),  # 2 tiles a partition
+    ("llama", {"num_seqs": 6, "len_range": (100, 700)}, 128, 8),   # 1 tile a partition
+    ("qwen", {"num_seqs": 24}, 128, 3),
+])
+def test_decode_partitions_per_cta_every_output(span, name, kw, partition, R):
+    """A CTA computing R consecutive partitions writes each partition's own
+    partial: every output matches the oracle, with the fused combine (<= 8
+    partitions) or the separate reduce (more)."""
+    span(R)
+    full_step_parity(Case(workloads.make_plan(name, **kw)), partition=partition)
+
+
+@pytest.mark.parametrize("R", [2, 4])
+def test_decode_step_fused_partitions_per_cta(span, R):
+    """The fused cache write runs in the CTA whose span holds the last
+    partition."""
+    span(R)
+    case = Case(workloads.make_plan("long", num_seqs=2, len_range=(1000, 1900)))
+    hk, hv = case.snapshot(0)
+    out = case.gpu_step_fused(0, 256)
+    ref = case.oracle_step(0, hk, hv)
+    api.check_error()
+    assert_close(out, ref, "fused step, span")
+    assert np.array_equal(bits(case.vals.k_pools[0]), hk)
+    assert np.array_equal(bits(case.vals.v_pools[0]), hv)
+
+
+def test_decode_partitions_per_cta_zero_and_one_token(span):
+    span(4)
+    case = Case(workloads.make_plan("llama", num_seqs=6, len_range=(100, 700)))
+    case.gpu_writes(0)
+    lens = case.lay.seq_lens.copy()
+    lens[0], lens[1] = 0, 1
+    lens_t = torch.as_tensor(lens, device="cuda")
+    hk, hv = case.snapshot(0)
+    out = torch.full_like(case.vals.q, float("nan"))
+    api.decode(out, case.vals.q, case.vals.k_pools[0], case.vals.v_pools[0], case.tables,
+               lens_t, case.max_seq_len, case.plan.scale, partition_tokens=128)
+    api.check_error()
+    ref = oracle.decode(bits(case.vals.q), hk, hv, case.lay.block_tables, lens, case.plan.scale,
+                        case.spec.dtype)
+    assert torch.all(out[0] == 0)
+    assert_close(out, ref, "span, zero and one token")
