@@ -292,8 +292,8 @@ int pa_get_decode_impl(void);
 /* Split-KV partitions one tensor-core CTA computes, process-wide, for every
  * later call: 0 automatic (default: several consecutive partitions a CTA
  * when partitions are short and the grid keeps at least two waves of CTAs),
- * n >= 1 that many wherever partitions are a multiple of 128 positions (1
- * elsewhere).  Each partition still gets its own (m, l, O) partial, so the
+ * n >= 1 that many wherever partitions are a multiple of 128 positions (256
+ * over E4M3 pools; 1 elsewhere).  Each partition still gets its own (m, l, O) partial, so the
  * result is the same for any setting (within the output tolerance).  Returns
  * the previous setting, or -1 (nothing changed) for a negative value.  Not
  * synchronised with decode calls running on other host threads. */

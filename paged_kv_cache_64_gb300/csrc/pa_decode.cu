@@ -791,19 +791,24 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
     r->NP = (P > 0) ? (max_seq_len + P - 1) / P : 1;
     if (r->NP < 1) r->NP = 1;
     r->span = 1;
-    if (r->tc && !r->fp8 && P > 0 && P % 128 == 0) {
+    // (E4M3 pools: partitions of an even number of tiles, so that the two
+    // softmax groups meet at each partition's end)
+    if ((r->tc || r->fp8) && P > 0 && P % (r->fp8 ? 256 : 128) == 0) {
         // One CTA computes several consecutive partitions (each still its own
         // partial) when partitions are short: a CTA's prologue and pipeline
-        // fill are then paid once per ~2048 positions, as long as the grid
-        // keeps at least two waves of CTAs.
+        // fill are then paid once per ~2048 positions, as long as a CTA's
+        // span stays within a quarter of one CTA slot's share of the job (the
+        // share taken at the maximum length, an upper bound), so that short,
+        // latency-bound batches keep one partition a CTA.
         const int forced = g_decode_span.load(std::memory_order_relaxed);
         int R = forced > 0 ? forced : 2048 / P;
         if (R > r->NP) R = r->NP;
         if (forced <= 0) {
-            const int slots = sm_count() * tc_ctas_per_sm(dtype == PA_BF16, head_dim);
-            while (R > 1 &&
-                   (int64_t)num_seqs * num_kv_heads * ((r->NP + R - 1) / R) < 2ll * slots)
-                --R;
+            const int slots = sm_count() * (r->fp8 ? fp8_ctas_per_sm(dtype == PA_BF16, head_dim, G)
+                                                   : tc_ctas_per_sm(dtype == PA_BF16, head_dim));
+            const double share =
+                (double)num_seqs * num_kv_heads * max_seq_len / (slots > 0 ? slots : 1);
+            while (R > 1 && 4.0 * R * P > share) --R;
         }
         r->span = R > 1 ? R : 1;
     }
@@ -818,7 +823,9 @@ static pa_status launch_decode(const ResolvedDecode &r, DecodeParams prm, int nu
     if (!prm.out && (prm.mode == 0 || prm.counters || prm.prefix_parts)) return PA_ERR_INVALID;
     if (r.fp8) {
         if (prm.prefix_parts) return PA_ERR_UNSUPPORTED;  // no cascade over E4M3 pools
-        return launch_decode_fp8(prm, r.bf16, r.head_dim, r.NP, num_kv_heads, num_seqs, stream);
+        prm.span = r.span;
+        return launch_decode_fp8(prm, r.bf16, r.head_dim, (r.NP + r.span - 1) / r.span,
+                                 num_kv_heads, num_seqs, stream);
     }
     if (r.tc) {
         const int span = prm.prefix_parts ? 1 : r.span;  // cascade tails: one partition a CTA

@@ -120,10 +120,11 @@ struct F8Shape {
     static constexpr int RED_BYTES = 2 * 3 * 4 * kF8N * 4;
     // per head: softmax scale (log2 units, K scale included) times 2^-e_g
     static constexpr int OFF_QMUL = OFF_RED + RED_BYTES;
-    // group B's state for the final merge: acc [G][D], then m_run, m_true, l
+    // group B's state for a partition's merge: acc [G][D], then m_run,
+    // m_true, l, failed; two buffers (partition parity)
     static constexpr int OFF_XCH = OFF_QMUL + kF8G * 4;
     static constexpr int XCH_BYTES = kF8G * D * 4 + 4 * kF8G * 4;
-    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
+    static constexpr int OFF_BAR = OFF_XCH + 2 * XCH_BYTES;
     static constexpr int OFF_MISC = OFF_BAR + kNumF8Bars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
@@ -259,8 +260,11 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
     pdl_wait();  // inputs may come from the previous kernel on the stream
     const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
-    const int start = part * P;
-    if (start >= L) {  // empty partition: as in the other decode kernels
+    // partitions [part0, part0 + R) of the sequence: this CTA's span
+    const int R = p.span > 1 ? p.span : 1;
+    const int part0 = part * R;
+    const int start = part0 * P;
+    if (start >= L) {  // empty partitions: as in the other decode kernels
         if (p.mode == 0) {
             if (part == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
@@ -268,23 +272,28 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
                 for (int i = threadIdx.x; i < G * D / 2; i += blockDim.x) o[base + i] = 0u;
             }
         } else {
-            for (int g = 0; g < G; ++g) {
-                const int64_t row = part_row(p, seq, kvh * G + g, part);
-                if (threadIdx.x == 0) {
-                    p.part_m[row] = -INFINITY;
-                    p.part_l[row] = 0.f;
+            for (int j = 0; j < R && part0 + j < p.num_partitions; ++j)
+                for (int g = 0; g < G; ++g) {
+                    const int64_t row = part_row(p, seq, kvh * G + g, part0 + j);
+                    if (threadIdx.x == 0) {
+                        p.part_m[row] = -INFINITY;
+                        p.part_l[row] = 0.f;
+                    }
+                    for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
                 }
-                for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
-            }
         }
         return;
     }
-    const int end = (start + P < L) ? start + P : L;
+    const int part_end = (part0 + R < nparts_seq) ? part0 + R : nparts_seq;  // past the last
+    const int end = (part_end * P < L) ? part_end * P : L;
     const int nunits = (end - start + kUnit - 1) / kUnit;
     const int ntiles = (end - start + kF8Tile - 1) / kF8Tile;
     const bool direct = (p.mode == 0) && (nparts_seq <= 1);
+    // tiles per partition (an even number when the span has several; the
+    // host guarantees it), else all of them
+    const int tpp = R > 1 ? P / kF8Tile : ntiles;
 
-    if (p.k_new != nullptr && part == nparts_seq - 1) fused_cache_write_fp8<BF16, D>(p, seq, kvh, L);
+    if (p.k_new != nullptr && part_end == nparts_seq) fused_cache_write_fp8<BF16, D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
         // kVOpFull: the converter warps; kQReady, kSEmpty, kPFull, kOEmpty:
         // the 4 warps of a softmax group; kKFull, kVFull: the producer's
@@ -659,233 +668,254 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
         };
 
         int last = -1;
-        for (int i = grp; i < ntiles; i += 2) {
-            const bool landed = !failed && mbar_wait(&bar[kSFull0 + grp], (i >> 1) & 1);
-            const bool ok = __all_sync(kFullMask, landed);
-            float s[GM];
-            if (ok) {
-                tc_fence_after();
-                float t12[16], t3[8];
-                tmem_load16(tmem + lane_addr + S::S0 + S::QN * grp, t12);
-                if constexpr (GM == 8) tmem_load8(tmem + lane_addr + S::S0 + S::QN * grp + 16, t3);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[kSEmpty0 + grp]);
-#pragma unroll
-                for (int g = 0; g < GM; ++g)
-                    s[g] = (t12[g] + t12[GM + g]) + (GM == 8 ? t3[g] : t12[2 * GM + g]);
-            } else {
-#pragma unroll
-                for (int g = 0; g < GM; ++g) s[g] = 0.f;
+        // Partition by partition of the CTA's span (one partition unless
+        // p.span > 1): tiles [j * tpp, (j + 1) * tpp) of partition j, every
+        // other one this group's.  Both groups meet at each partition's end,
+        // whether or not they had a tile in it.
+        const int nspan = part_end - part0;
+        for (int j = 0; j < nspan; ++j) {
+            const int t1 = ((j + 1) * tpp < ntiles) ? (j + 1) * tpp : ntiles;
+            for (int i = j * tpp + grp; i < t1; i += 2) {
+              const bool landed = !failed && mbar_wait(&bar[kSFull0 + grp], (i >> 1) & 1);
+              const bool ok = __all_sync(kFullMask, landed);
+              float s[GM];
+              if (ok) {
+                  tc_fence_after();
+                  float t12[16], t3[8];
+                  tmem_load16(tmem + lane_addr + S::S0 + S::QN * grp, t12);
+                  if constexpr (GM == 8) tmem_load8(tmem + lane_addr + S::S0 + S::QN * grp + 16, t3);
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(&bar[kSEmpty0 + grp]);
+  #pragma unroll
+                  for (int g = 0; g < GM; ++g)
+                      s[g] = (t12[g] + t12[GM + g]) + (GM == 8 ? t3[g] : t12[2 * GM + g]);
+              } else {
+  #pragma unroll
+                  for (int g = 0; g < GM; ++g) s[g] = 0.f;
+              }
+              const int tile0 = start + i * kF8Tile;
+              const int nvalid = (end - tile0 < kF8Tile) ? end - tile0 : kF8Tile;
+              const bool valid = r < nvalid;
+              // tile max of each head over the 128 positions: a halving
+              // butterfly over the warp (each exchange hands the partner the
+              // heads it keeps), after which lane L holds head (L >> 2) & 7
+              float *tmax = gred + ((i >> 1) & 1) * (4 * kF8N);
+  #pragma unroll
+              for (int g = 0; g < GM; ++g) s[g] = valid ? s[g] * qm[g] : -INFINITY;  // select: NaN-safe
+              {
+                  // GM = 8: lane L ends with head (L >> 2) & 7; GM = 4: (L >> 3) & 3
+                  float v4[4], v2[2];
+                  if constexpr (GM == 8) {
+                      const bool b4 = lane & 16;
+  #pragma unroll
+                      for (int j = 0; j < 4; ++j)
+                          v4[j] = fmaxf(b4 ? s[4 + j] : s[j],
+                                        __shfl_xor_sync(kFullMask, b4 ? s[j] : s[4 + j], 16));
+                  } else {
+  #pragma unroll
+                      for (int j = 0; j < 4; ++j) v4[j] = s[j];
+                  }
+                  constexpr int o2 = GM == 8 ? 8 : 16, o1 = o2 / 2;
+                  const bool c2 = lane & o2, c1 = lane & o1;
+  #pragma unroll
+                  for (int j = 0; j < 2; ++j)
+                      v2[j] = fmaxf(c2 ? v4[2 + j] : v4[j],
+                                    __shfl_xor_sync(kFullMask, c2 ? v4[j] : v4[2 + j], o2));
+                  float v = fmaxf(c1 ? v2[1] : v2[0], __shfl_xor_sync(kFullMask, c1 ? v2[0] : v2[1], o1));
+  #pragma unroll
+                  for (int off = o1 / 2; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
+                  constexpr int sh = GM == 8 ? 2 : 3;
+                  if ((lane & ((1 << sh) - 1)) == 0) tmax[sw * kF8N + ((lane >> sh) & (GM - 1))] = v;
+              }
+              if (lane == 0) tmax[sw * kF8N + kF8N - 1] = ok ? 1.f : 0.f;  // column 15: health flag
+              named_bar(1 + grp, 128);
+              bool all_ok = true;
+  #pragma unroll
+              for (int w = 0; w < 4; ++w) all_ok &= tmax[w * kF8N + kF8N - 1] != 0.f;
+              if (!all_ok) {
+                  failed = true;
+                  break;
+              }
+              bool need = false;
+              float mx[GM];
+  #pragma unroll
+              for (int g = 0; g < GM; ++g) {
+                  mx[g] = fmaxf(fmaxf(tmax[g], tmax[kF8N + g]),
+                                fmaxf(tmax[2 * kF8N + g], tmax[3 * kF8N + g]));
+                  need |= (g < G) && (mx[g] > m_run[g] + kLazyRescale);
+              }
+              float alpha[GM];
+  #pragma unroll
+              for (int g = 0; g < GM; ++g) {
+                  alpha[g] = 1.f;
+                  if (need) {  // group-uniform
+                      const float mn = fmaxf(m_run[g], mx[g]);
+                      alpha[g] = fast_exp2(m_run[g] - mn);
+                      m_run[g] = mn;
+                      l_part[g] *= alpha[g];
+                  }
+                  m_true[g] = fmaxf(m_true[g], mx[g]);
+              }
+              // E4M3 P: each head's P is taken times 2^k, the power of two that
+              // brings the tile's largest P into [128, 256), so that its three
+              // E4M3 terms keep 12 bits of every value down to 2^-17 of that
+              // largest (the sum l keeps the unscaled values)
+              float pv[GM], kinv[GM];
+  #pragma unroll
+              for (int g = 0; g < GM; ++g) {
+                  pv[g] = 0.f;
+                  kinv[g] = 1.f;
+                  if (g < G) {
+                      float pg = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
+                      l_part[g] += pg;
+                      if constexpr (S::DIRECT) {
+                          const float dm = mx[g] - m_run[g];  // <= lazy-rescale threshold
+                          int k = 0;
+                          if (dm > -INFINITY) {
+                              k = 7 - __float2int_rd(dm);
+                              k = k > 126 ? 126 : k;
+                          }
+                          kinv[g] = exp2i(-k);
+                          pg *= exp2i(k);  // exact: a power of two, k >= -1
+                      }
+                      pv[g] = pg;
+                  }
+              }
+              // P buffer of this tile: last read by P.V of tile i-4, whose O this
+              // group accumulated (after waiting for it) two tiles ago
+              uint8_t *pbuf = smem + S::OFF_P + (2 * grp + ((i >> 1) & 1)) * S::P_BYTES;
+              if constexpr (S::DIRECT) {
+                  // P^T as three E4M3 terms of P rounded to f16 (11 significant
+                  // bits: the terms hold it exactly down to E4M3's subnormal
+                  // floor), split in packed f16 pairs: rows t*8 + g (t = term,
+                  // g = head), 128 positions of one byte, K-major with 128-byte
+                  // swizzle
+  #pragma unroll
+                  for (int g = 0; g < GM; g += 2) {
+                      uint32_t h = narrow2<false>(pv[g], pv[g + 1]);
+  #pragma unroll
+                      for (int t = 0; t < 3; ++t) {
+                          const uint32_t c = e4m3x2_from_f16x2(h);
+                          h = hsub2_bits(h, f16x2_from_e4m3x2((uint16_t)c));  // exact
+                          pbuf[e4m3_operand_offset<128>(GM * t + g, r)] = (uint8_t)(c & 0xffu);
+                          pbuf[e4m3_operand_offset<128>(GM * t + g + 1, r)] = (uint8_t)(c >> 8);
+                      }
+                  }
+                  if (!valid) {
+                      // Stale rows of the last tile: P is 0 there but V must be
+                      // finite (0 * NaN would poison the product), so zero them
+                      // once the V tile has landed (its slot cannot move on
+                      // before P.V of this tile, which waits for this P).
+                      const int slot = i % S::NV;
+                      if (mbar_wait(&bar[kVFull0 + slot], (i / S::NV) & 1)) {
+                          uint4 *vrow = reinterpret_cast<uint4 *>(smem + S::OFF_VSTG +
+                                                                  slot * S::STG_BYTES + r * D);
+  #pragma unroll
+                          for (int c = 0; c < D / 16; ++c) vrow[c] = make_uint4(0, 0, 0, 0);
+                      } else {
+                          failed = true;
+                      }
+                  }
+              } else {
+                  // P^T (16 rows = heads, 128 positions) in the operand layout, f16
+  #pragma unroll
+                  for (int g = 0; g < kF8N; ++g)
+                      *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kF8N * 128)) =
+                          narrow_f16<false>(g < GM ? pv[g] : 0.f);
+              }
+              fence_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bar[kPFull0 + 2 * grp + ((i >> 1) & 1)]);
+              // this group's previous tile, while P.V of this one runs
+              if (last >= 0 && !accumulate(last)) failed = true;
+  #pragma unroll
+              for (int g = 0; g < GM; ++g) {
+                  alpha_prev[g] = alpha[g];
+                  kinv_prev[g] = kinv[g];
+              }
+              last = i;
             }
-            const int tile0 = start + i * kF8Tile;
-            const int nvalid = (end - tile0 < kF8Tile) ? end - tile0 : kF8Tile;
-            const bool valid = r < nvalid;
-            // tile max of each head over the 128 positions: a halving
-            // butterfly over the warp (each exchange hands the partner the
-            // heads it keeps), after which lane L holds head (L >> 2) & 7
-            float *tmax = gred + ((i >> 1) & 1) * (4 * kF8N);
+            if (!failed && last >= 0 && !accumulate(last)) failed = true;
+            last = -1;
+            // l over the group's 128 position-threads, per head
+            float *lsum = gred + 2 * (4 * kF8N);
 #pragma unroll
-            for (int g = 0; g < GM; ++g) s[g] = valid ? s[g] * qm[g] : -INFINITY;  // select: NaN-safe
-            {
-                // GM = 8: lane L ends with head (L >> 2) & 7; GM = 4: (L >> 3) & 3
-                float v4[4], v2[2];
-                if constexpr (GM == 8) {
-                    const bool b4 = lane & 16;
+            for (int g = 0; g < GM; ++g) {
+                float v = l_part[g];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        v4[j] = fmaxf(b4 ? s[4 + j] : s[j],
-                                      __shfl_xor_sync(kFullMask, b4 ? s[j] : s[4 + j], 16));
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v4[j] = s[j];
-                }
-                constexpr int o2 = GM == 8 ? 8 : 16, o1 = o2 / 2;
-                const bool c2 = lane & o2, c1 = lane & o1;
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    v2[j] = fmaxf(c2 ? v4[2 + j] : v4[j],
-                                  __shfl_xor_sync(kFullMask, c2 ? v4[j] : v4[2 + j], o2));
-                float v = fmaxf(c1 ? v2[1] : v2[0], __shfl_xor_sync(kFullMask, c1 ? v2[0] : v2[1], o1));
-#pragma unroll
-                for (int off = o1 / 2; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
-                constexpr int sh = GM == 8 ? 2 : 3;
-                if ((lane & ((1 << sh) - 1)) == 0) tmax[sw * kF8N + ((lane >> sh) & (GM - 1))] = v;
+                for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
+                if (lane == 0) lsum[sw * kF8N + g] = v;
             }
-            if (lane == 0) tmax[sw * kF8N + kF8N - 1] = ok ? 1.f : 0.f;  // column 15: health flag
             named_bar(1 + grp, 128);
-            bool all_ok = true;
+            float lt[GM];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) all_ok &= tmax[w * kF8N + kF8N - 1] != 0.f;
-            if (!all_ok) {
-                failed = true;
-                break;
-            }
-            bool need = false;
-            float mx[GM];
+            for (int g = 0; g < GM; ++g)
+                lt[g] = lsum[g] + lsum[kF8N + g] + lsum[2 * kF8N + g] + lsum[3 * kF8N + g];
+            // group B hands its state to group A (two exchange buffers, by
+            // partition parity: B may write the next one while A still reads)
+            float *xacc = xch + (j & 1) * (S::XCH_BYTES / 4);  // [kF8G][D]
+            float *xm = xacc + kF8G * D;                       // m_run, m_true, l, failed
+            if (grp == 1) {
+                if (r < D) {
 #pragma unroll
-            for (int g = 0; g < GM; ++g) {
-                mx[g] = fmaxf(fmaxf(tmax[g], tmax[kF8N + g]),
-                              fmaxf(tmax[2 * kF8N + g], tmax[3 * kF8N + g]));
-                need |= (g < G) && (mx[g] > m_run[g] + kLazyRescale);
-            }
-            float alpha[GM];
-#pragma unroll
-            for (int g = 0; g < GM; ++g) {
-                alpha[g] = 1.f;
-                if (need) {  // group-uniform
-                    const float mn = fmaxf(m_run[g], mx[g]);
-                    alpha[g] = fast_exp2(m_run[g] - mn);
-                    m_run[g] = mn;
-                    l_part[g] *= alpha[g];
+                    for (int g = 0; g < GM; ++g) xacc[g * D + r] = acc[g];
                 }
-                m_true[g] = fmaxf(m_true[g], mx[g]);
-            }
-            // E4M3 P: each head's P is taken times 2^k, the power of two that
-            // brings the tile's largest P into [128, 256), so that its three
-            // E4M3 terms keep 12 bits of every value down to 2^-17 of that
-            // largest (the sum l keeps the unscaled values)
-            float pv[GM], kinv[GM];
-#pragma unroll
-            for (int g = 0; g < GM; ++g) {
-                pv[g] = 0.f;
-                kinv[g] = 1.f;
-                if (g < G) {
-                    float pg = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
-                    l_part[g] += pg;
-                    if constexpr (S::DIRECT) {
-                        const float dm = mx[g] - m_run[g];  // <= lazy-rescale threshold
-                        int k = 0;
-                        if (dm > -INFINITY) {
-                            k = 7 - __float2int_rd(dm);
-                            k = k > 126 ? 126 : k;
-                        }
-                        kinv[g] = exp2i(-k);
-                        pg *= exp2i(k);  // exact: a power of two, k >= -1
-                    }
-                    pv[g] = pg;
-                }
-            }
-            // P buffer of this tile: last read by P.V of tile i-4, whose O this
-            // group accumulated (after waiting for it) two tiles ago
-            uint8_t *pbuf = smem + S::OFF_P + (2 * grp + ((i >> 1) & 1)) * S::P_BYTES;
-            if constexpr (S::DIRECT) {
-                // P^T as three E4M3 terms of P rounded to f16 (11 significant
-                // bits: the terms hold it exactly down to E4M3's subnormal
-                // floor), split in packed f16 pairs: rows t*8 + g (t = term,
-                // g = head), 128 positions of one byte, K-major with 128-byte
-                // swizzle
-#pragma unroll
-                for (int g = 0; g < GM; g += 2) {
-                    uint32_t h = narrow2<false>(pv[g], pv[g + 1]);
-#pragma unroll
-                    for (int t = 0; t < 3; ++t) {
-                        const uint32_t c = e4m3x2_from_f16x2(h);
-                        h = hsub2_bits(h, f16x2_from_e4m3x2((uint16_t)c));  // exact
-                        pbuf[e4m3_operand_offset<128>(GM * t + g, r)] = (uint8_t)(c & 0xffu);
-                        pbuf[e4m3_operand_offset<128>(GM * t + g + 1, r)] = (uint8_t)(c >> 8);
-                    }
-                }
-                if (!valid) {
-                    // Stale rows of the last tile: P is 0 there but V must be
-                    // finite (0 * NaN would poison the product), so zero them
-                    // once the V tile has landed (its slot cannot move on
-                    // before P.V of this tile, which waits for this P).
-                    const int slot = i % S::NV;
-                    if (mbar_wait(&bar[kVFull0 + slot], (i / S::NV) & 1)) {
-                        uint4 *vrow = reinterpret_cast<uint4 *>(smem + S::OFF_VSTG +
-                                                                slot * S::STG_BYTES + r * D);
-#pragma unroll
-                        for (int c = 0; c < D / 16; ++c) vrow[c] = make_uint4(0, 0, 0, 0);
-                    } else {
-                        failed = true;
-                    }
-                }
-            } else {
-                // P^T (16 rows = heads, 128 positions) in the operand layout, f16
-#pragma unroll
-                for (int g = 0; g < kF8N; ++g)
-                    *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kF8N * 128)) =
-                        narrow_f16<false>(g < GM ? pv[g] : 0.f);
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kPFull0 + 2 * grp + ((i >> 1) & 1)]);
-            // this group's previous tile, while P.V of this one runs
-            if (last >= 0 && !accumulate(last)) failed = true;
-#pragma unroll
-            for (int g = 0; g < GM; ++g) {
-                alpha_prev[g] = alpha[g];
-                kinv_prev[g] = kinv[g];
-            }
-            last = i;
-        }
-        if (!failed && last >= 0 && !accumulate(last)) failed = true;
-        // l over the group's 128 position-threads, per head
-        float *lsum = gred + 2 * (4 * kF8N);
-#pragma unroll
-        for (int g = 0; g < GM; ++g) {
-            float v = l_part[g];
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
-            if (lane == 0) lsum[sw * kF8N + g] = v;
-        }
-        named_bar(1 + grp, 128);
-        float lt[GM];
-#pragma unroll
-        for (int g = 0; g < GM; ++g)
-            lt[g] = lsum[g] + lsum[kF8N + g] + lsum[2 * kF8N + g] + lsum[3 * kF8N + g];
-        // group B hands its state to group A
-        float *xacc = xch;                  // [kF8G][D]
-        float *xm = xch + kF8G * D;         // m_run, m_true, l, failed
-        if (grp == 1) {
-            if (r < D) {
-#pragma unroll
-                for (int g = 0; g < GM; ++g) xacc[g * D + r] = acc[g];
-            }
-            if (st == 0) {
-#pragma unroll
-                for (int g = 0; g < GM; ++g) {
-                    xm[g] = m_run[g];
-                    xm[kF8G + g] = m_true[g];
-                    xm[2 * kF8G + g] = lt[g];
-                }
-                xm[3 * kF8G] = failed ? 1.f : 0.f;
-            }
-        }
-        named_bar(3, 256);
-        if (grp == 0) {
-            failed |= xm[3 * kF8G] != 0.f;
-            if (failed) {
                 if (st == 0) {
-                    record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
-                    *abort_flag = 1;
-                }
-            } else if (r < D) {
 #pragma unroll
-                for (int g = 0; g < GM; ++g) {
-                    if (g >= G) break;
-                    // merge of the two groups' partial softmaxes
-                    const float mb = xm[g];
-                    const float M = fmaxf(m_run[g], mb);
-                    const float sa = fast_exp2(m_run[g] - M);
-                    const float sb = mb == -INFINITY ? 0.f : fast_exp2(mb - M);
-                    const float l = lt[g] * sa + xm[2 * kF8G + g] * sb;
-                    const float a = acc[g] * sa + xacc[g * D + r] * sb;
-                    const float mt = fmaxf(m_true[g], xm[kF8G + g]);
-                    const float o = a / l * p.v_scale;  // V elements are v_scale * codes
-                    const int h = kvh * G + g;
-                    if (direct) {
-                        uint16_t *out = static_cast<uint16_t *>(p.out);
-                        out[((int64_t)seq * p.num_q_heads + h) * D + r] = narrow_out<BF16>(o);
-                    } else {
-                        const int64_t row = part_row(p, seq, h, part);
-                        p.part_o[row * D + r] = o;
-                        if (r == 0) {
-                            p.part_m[row] = mt;
-                            p.part_l[row] = l * fast_exp2(M - mt);
+                    for (int g = 0; g < GM; ++g) {
+                        xm[g] = m_run[g];
+                        xm[kF8G + g] = m_true[g];
+                        xm[2 * kF8G + g] = lt[g];
+                    }
+                    xm[3 * kF8G] = failed ? 1.f : 0.f;
+                }
+            }
+            named_bar(3, 256);
+            if (grp == 0) {
+                failed |= xm[3 * kF8G] != 0.f;
+                if (failed) {
+                    if (st == 0) {
+                        record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                } else if (r < D) {
+#pragma unroll
+                    for (int g = 0; g < GM; ++g) {
+                        if (g >= G) break;
+                        // merge of the two groups' partial softmaxes
+                        const float mb = xm[g];
+                        const float M = fmaxf(m_run[g], mb);
+                        const float sa = fast_exp2(m_run[g] - M);
+                        const float sb = mb == -INFINITY ? 0.f : fast_exp2(mb - M);
+                        const float l = lt[g] * sa + xm[2 * kF8G + g] * sb;
+                        const float a = acc[g] * sa + xacc[g * D + r] * sb;
+                        const float mt = fmaxf(m_true[g], xm[kF8G + g]);
+                        const float o = a / l * p.v_scale;  // V elements are v_scale * codes
+                        const int h = kvh * G + g;
+                        if (direct) {
+                            uint16_t *out = static_cast<uint16_t *>(p.out);
+                            out[((int64_t)seq * p.num_q_heads + h) * D + r] = narrow_out<BF16>(o);
+                        } else {
+                            const int64_t row = part_row(p, seq, h, part0 + j);
+                            p.part_o[row * D + r] = o;
+                            if (r == 0) {
+                                p.part_m[row] = mt;
+                                p.part_l[row] = l * fast_exp2(M - mt);
+                            }
                         }
                     }
+                }
+            }
+            if (j + 1 < nspan) {  // a fresh running state for the next partition
+#pragma unroll
+                for (int g = 0; g < GM; ++g) {
+                    m_run[g] = -INFINITY;
+                    m_true[g] = -INFINITY;
+                    l_part[g] = 0.f;
+                    acc[g] = 0.f;
+                    alpha_prev[g] = 1.f;
+                    kinv_prev[g] = 1.f;
                 }
             }
         }
@@ -907,7 +937,8 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
         tmem_dealloc(tmem, S::COLS);
     }
     if (!direct && !*abort_flag && p.counters != nullptr)
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_STG));
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_STG),
+                             (nparts_seq + R - 1) / R);
 }
 
 using F8Kernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);

@@ -185,3 +185,60 @@ def test_fp8_rejects_bad_scale():
         api.decode_fp8(torch.empty_like(c.q), c.q, c.kp, c.vp, c.tables, c.lens, c.max_seq_len,
                        c.plan.scale, 0.0, 1.0)
     assert e.value.code == 1
+
+
+# ------------------------------------------- several partitions per CTA
+@pytest.fixture
+def span():
+    prev = []
+
+    def set_span(n):
+        prev.append(api.set_decode_span(n))
+
+    yield set_span
+    if prev:
+        api.set_decode_span(prev[0])
+
+
+@pytest.mark.parametrize("name,kw,partition,R", [
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, 512, 2),
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, 512, 3),   # ragged last span
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, 256, 4),   # 2 tiles a partition
+    ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, 512, 4),
+    ("llama", {"num_seqs": 6, "len_range": (100, 900)}, 256, 8),
+])
+def test_decode_fp8_partitions_per_cta_every_output(span, name, kw, partition, R):
+    span(R)
+    c = Fp8Case(name, **kw)
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    out = c.gpu(partition)
+    api.check_error()
+    assert_close(out, c.oracle(kc, vc), f"fp8 span {name} P={partition} R={R}")
+
+
+@pytest.mark.parametrize("R", [2, 4])
+def test_decode_fp8_fused_step_partitions_per_cta(span, R):
+    span(R)
+    c = Fp8Case("long", seed=11, num_seqs=2, len_range=(1000, 1900))
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    out = c.gpu(256, step=True)
+    api.check_error()
+    ref = c.oracle(kc, vc, step=True)
+    assert_close(out, ref, "fp8 fused step, span")
+    assert np.array_equal(np_codes(c.kp), kc) and np.array_equal(np_codes(c.vp), vc)
+
+
+def test_decode_fp8_partitions_per_cta_stale_slots_poisoned(span):
+    span(4)
+    c = Fp8Case("long", seed=13, num_seqs=2, len_range=(1000, 1500))
+    B = c.spec.block_size
+    for s, L in enumerate(c.lay.seq_lens):
+        nb = -(-int(L) // B)
+        last = c.lay.block_tables[s, nb - 1]
+        for p in range(int(L), nb * B):
+            c.kp[last, :, p % B, :] = 0x7F
+            c.vp[last, :, p % B, :] = 0xFF
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    out = c.gpu(256)
+    assert torch.isfinite(out).all()
+    assert_close(out, c.oracle(kc, vc), "fp8 span poison")
