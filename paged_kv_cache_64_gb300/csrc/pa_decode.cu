@@ -164,15 +164,20 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
     uint64_t *empty_bar = full_bar + NS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty_bar + NS);
 
-    const int part = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int seq = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = p.group;
     const int P = p.partition_tokens;
 
     pdl_wait();  // inputs may come from the previous kernel on the stream
+    int part, kvh, seq;  // partition, KV head, sequence
+    if (p.compact) {
+        if (!compact_item(p, blockIdx.x, &seq, &part, &kvh)) return;  // past the last item
+    } else {
+        part = blockIdx.x;
+        kvh = blockIdx.y;
+        seq = blockIdx.z;
+    }
     const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
     const int start = part * P;
@@ -820,22 +825,24 @@ static pa_status launch_decode(const ResolvedDecode &r, DecodeParams prm, int nu
     if (num_seqs == 0) return PA_OK;
     if (num_kv_heads > 65535 || num_seqs > 65535) return PA_ERR_INVALID;
     if (prm.ws_parts == 0) prm.ws_parts = prm.num_partitions;  // plain launch: own workspace
+    // CTAs along x: split-KV chunks of each sequence (spans of partitions)
+    const int span = (r.tc || r.fp8) && !prm.prefix_parts ? r.span : 1;
+    const int chunks = (r.NP + span - 1) / span;
+    prm.compact = prm.mode == 0 && prm.prefix_parts == 0 && num_seqs <= kCompactMaxSeqs &&
+                  (int64_t)chunks * num_kv_heads * num_seqs < (1ll << 31);
     if (!prm.out && (prm.mode == 0 || prm.counters || prm.prefix_parts)) return PA_ERR_INVALID;
     if (r.fp8) {
         if (prm.prefix_parts) return PA_ERR_UNSUPPORTED;  // no cascade over E4M3 pools
-        prm.span = r.span;
-        return launch_decode_fp8(prm, r.bf16, r.head_dim, (r.NP + r.span - 1) / r.span,
-                                 num_kv_heads, num_seqs, stream);
+        prm.span = span;
+        return launch_decode_fp8(prm, r.bf16, r.head_dim, chunks, num_kv_heads, num_seqs, stream);
     }
     if (r.tc) {
-        const int span = prm.prefix_parts ? 1 : r.span;  // cascade tails: one partition a CTA
-        prm.span = span;
-        return launch_decode_tc(prm, r.bf16, r.head_dim, (r.NP + span - 1) / span, num_kv_heads,
-                                num_seqs, stream);
+        prm.span = span;  // cascade tails: one partition a CTA
+        return launch_decode_tc(prm, r.bf16, r.head_dim, chunks, num_kv_heads, num_seqs, stream);
     }
     if (!ensure_smem_attr(reinterpret_cast<const void *>(r.entry.fn), r.entry.smem))
         return PA_ERR_CUDA;
-    dim3 grid((unsigned)r.NP, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    const dim3 grid = decode_grid(prm, chunks, num_kv_heads, num_seqs);
     if (launch_pdl(r.entry.fn, grid, dim3(kDecodeThreads), (size_t)r.entry.smem, stream, prm) !=
         cudaSuccess)
         return PA_ERR_CUDA;

@@ -40,6 +40,11 @@ struct DecodeParams {
     // Consecutive partitions one CTA computes (tensor-core kernel; 0 or 1:
     // one).  Each still gets its own partial; grid.x = ceil(NP / span).
     int span;
+    // Compact grid (decode mode, no cascade, batches of up to
+    // kCompactMaxSeqs): a 1-D grid whose CTAs map, in order, onto the work
+    // items that exist (see compact_item), so CTAs with nothing to do come
+    // last and are dispatched after every CTA with work.
+    int compact;
     float scale_log2;            // scale * log2(e)
     int mode;                    // 0: decode (direct output when 1 partition), 1: partials only
     // Fused cache write of each sequence's newest token (pa_decode_step), or nullptr.
@@ -106,6 +111,54 @@ __device__ __forceinline__ int item_len(const DecodeParams &p, int seq, bool rep
         L = L < 0 ? 0 : cap;
     }
     return L;
+}
+
+constexpr int kCompactMaxSeqs = 128;
+
+// Work item of CTA `c` of a compact grid.  Items are, sequence by sequence,
+// the chunks of span * P positions of each sequence (at least one, so a
+// zero-length sequence still has its CTA), each split over the KV heads:
+// c = item * Hkv + kvh.  Every thread of a warp calls it (converged); it
+// scans the sequence lengths 32 at a time (an inclusive warp prefix sum)
+// and returns false for c past the last item.
+__device__ __forceinline__ bool compact_item(const DecodeParams &p, int c, int *seq, int *chunk,
+                                             int *kvh) {
+    const int lane = threadIdx.x & 31;
+    const int item = c / p.num_kv_heads;
+    const int chunk_tok = p.partition_tokens * (p.span > 1 ? p.span : 1);
+    int base = 0;  // items of the sequences before this group of 32
+    for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
+        const int s = s0 + lane;
+        int n = 0;
+        if (s < p.num_seqs) {
+            const int L = item_len(p, s, false);
+            n = L == 0 ? 1 : (L - 1) / chunk_tok + 1;
+        }
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += t;
+        }
+        const int total = base + __shfl_sync(0xffffffffu, incl, 31);
+        if (item < total) {
+            const unsigned m = __ballot_sync(0xffffffffu, base + incl > item);
+            const int l = __ffs(m) - 1;
+            *seq = s0 + l;
+            *chunk = item - (base + __shfl_sync(0xffffffffu, incl - n, l));
+            *kvh = c - item * p.num_kv_heads;
+            return true;
+        }
+        base = total;
+    }
+    return false;
+}
+
+// Grid of a decode launch: chunks x KV heads x sequences, or the same count
+// as a 1-D compact grid.
+inline dim3 decode_grid(const DecodeParams &p, int chunks, int num_kv_heads, int num_seqs) {
+    if (p.compact) return dim3((unsigned)((int64_t)chunks * num_kv_heads * num_seqs));
+    return dim3((unsigned)chunks, (unsigned)num_kv_heads, (unsigned)num_seqs);
 }
 
 // Block-table entries of the attended range of `seq`.

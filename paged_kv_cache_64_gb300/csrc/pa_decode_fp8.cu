@@ -249,7 +249,6 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
     float *red = reinterpret_cast<float *>(smem + S::OFF_RED);
     float *qmul = reinterpret_cast<float *>(smem + S::OFF_QMUL);
 
-    const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
     const int P = p.partition_tokens;
@@ -258,6 +257,14 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
         prefetch_tensormap(&tmap_v);
     }
     pdl_wait();  // inputs may come from the previous kernel on the stream
+    int part, kvh, seq;  // split-KV chunk (span of partitions), KV head, sequence
+    if (p.compact) {
+        if (!compact_item(p, blockIdx.x, &seq, &part, &kvh)) return;  // past the last item
+    } else {
+        part = blockIdx.x;
+        kvh = blockIdx.y;
+        seq = blockIdx.z;
+    }
     const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
     // partitions [part0, part0 + R) of the sequence: this CTA's span
@@ -1008,7 +1015,7 @@ pa_status launch_decode_fp8(const DecodeParams &prm, bool bf16, int head_dim, in
     if (!pool_tensor_map_fp8(&mk, prm.k_pool, rows, head_dim, true) ||
         !pool_tensor_map_fp8(&mv, prm.v_pool, rows, head_dim, head_dim == 128))
         return PA_ERR_CUDA;
-    dim3 grid((unsigned)num_partitions, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    const dim3 grid = decode_grid(prm, num_partitions, num_kv_heads, num_seqs);
     if (launch_pdl(k, grid, dim3((unsigned)threads), (size_t)smem, stream, prm, mk, mv) != cudaSuccess)
         return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -82,8 +82,9 @@ struct TcShape {
 };
 
 // SPAN: a CTA may compute several consecutive partitions (p.span > 1); the
-// variant without it keeps to 96 registers (three CTAs an SM).
-template <bool BF16, int D, bool SPAN>
+// variant without it keeps to 96 registers (three CTAs an SM).  COMPACT: the
+// launch uses a compact grid (p.compact).
+template <bool BF16, int D, bool SPAN, bool COMPACT>
 __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
     paged_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v) {
@@ -96,7 +97,6 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::OFF_MISC + 8);
     float *red = reinterpret_cast<float *>(smem + S::OFF_RED);
 
-    const int part = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
     const int P = p.partition_tokens;
@@ -105,6 +105,14 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
         prefetch_tensormap(&tmap_v);
     }
     pdl_wait();  // inputs may come from the previous kernel on the stream
+    int part, kvh, seq;  // split-KV chunk (span of partitions), KV head, sequence
+    if constexpr (COMPACT) {
+        if (!compact_item(p, blockIdx.x, &seq, &part, &kvh)) return;  // past the last item
+    } else {
+        part = blockIdx.x;
+        kvh = blockIdx.y;
+        seq = blockIdx.z;
+    }
     const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
     // partitions [part0, part0 + R) of the sequence: this CTA's span
@@ -655,17 +663,19 @@ bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D
 
 using TcKernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
 
-static TcKernel pick_tc(bool bf16, int D, int *smem, bool span = false) {
-    if (D == 128) {
-        *smem = TcShape<128>::SMEM_BYTES;
-        if (span)
-            return bf16 ? paged_decode_tc_kernel<true, 128, true> : paged_decode_tc_kernel<false, 128, true>;
-        return bf16 ? paged_decode_tc_kernel<true, 128, false> : paged_decode_tc_kernel<false, 128, false>;
-    }
-    *smem = TcShape<64>::SMEM_BYTES;
-    if (span)
-        return bf16 ? paged_decode_tc_kernel<true, 64, true> : paged_decode_tc_kernel<false, 64, true>;
-    return bf16 ? paged_decode_tc_kernel<true, 64, false> : paged_decode_tc_kernel<false, 64, false>;
+template <int D, bool SPAN, bool COMPACT>
+static TcKernel tc_variant(bool bf16) {
+    return bf16 ? paged_decode_tc_kernel<true, D, SPAN, COMPACT>
+                : paged_decode_tc_kernel<false, D, SPAN, COMPACT>;
+}
+
+static TcKernel pick_tc(bool bf16, int D, int *smem, bool span = false, bool compact = false) {
+    *smem = D == 128 ? TcShape<128>::SMEM_BYTES : TcShape<64>::SMEM_BYTES;
+    if (D == 128)
+        return span ? (compact ? tc_variant<128, true, true>(bf16) : tc_variant<128, true, false>(bf16))
+                    : (compact ? tc_variant<128, false, true>(bf16) : tc_variant<128, false, false>(bf16));
+    return span ? (compact ? tc_variant<64, true, true>(bf16) : tc_variant<64, true, false>(bf16))
+                : (compact ? tc_variant<64, false, true>(bf16) : tc_variant<64, false, false>(bf16));
 }
 
 bool tc_supported(int head_dim, int group) {
@@ -704,14 +714,14 @@ pa_status launch_decode_tc(const DecodeParams &prm, bool bf16, int head_dim, int
                            int num_kv_heads, int num_seqs, cudaStream_t stream) {
     if (num_seqs == 0) return PA_OK;
     int smem = 0;
-    TcKernel k = pick_tc(bf16, head_dim, &smem, prm.span > 1);
+    TcKernel k = pick_tc(bf16, head_dim, &smem, prm.span > 1, prm.compact != 0);
     if (!ensure_smem_attr(reinterpret_cast<const void *>(k), smem)) return PA_ERR_CUDA;
     const int64_t rows = (int64_t)prm.num_blocks * num_kv_heads * prm.block_size;
     CUtensorMap mk, mv;
     if (!pool_tensor_map(&mk, prm.k_pool, rows, head_dim, bf16) ||
         !pool_tensor_map(&mv, prm.v_pool, rows, head_dim, bf16))
         return PA_ERR_CUDA;
-    dim3 grid((unsigned)num_partitions, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    const dim3 grid = decode_grid(prm, num_partitions, num_kv_heads, num_seqs);
     if (launch_pdl(k, grid, dim3(kTcThreads), (size_t)smem, stream, prm, mk, mv) != cudaSuccess)
         return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
