@@ -9,10 +9,12 @@
 // describes the products, the roles and the online softmax), with half the
 // K/V bytes moved.  Per tile of 128 positions:
 //
-//   S^T[128 pos x 32] = K_codes[128 x d] . Qs^T[d x 32]       kind::f8f6f4, E4M3 x E4M3
-//   d = 128: O^T[128 x 32] = V_codes^T[128 x 128 pos] . Ps^T  kind::f8f6f4, E4M3 x E4M3
-//   d = 64:  O^T[128 x 16] = V16^T[128 x 128 pos] . P16^T     kind::f16 (rows 64.. zero)
+//   S^T[128 pos x N] = K_codes[128 x d] . Qs^T[d x N]       kind::f8f6f4, E4M3 x E4M3
+//   d = 128: O^T[128 x N] = V_codes^T[128 x 128 pos] . Ps^T  kind::f8f6f4, E4M3 x E4M3
+//   d = 64:  O^T[128 x 16] = V16^T[128 x 128 pos] . P16^T    kind::f16 (rows 64.. zero)
 //
+// with N = 16 for groups of up to 4 query heads, 32 for up to 8 (three
+// E4M3 terms a head, zero-padded).
 // q.K^T reads the E4M3 K tile exactly as the TMA copy lands it (K-major,
 // swizzled), so K is never converted.  Its other operand, Qs, holds each query
 // head as three E4M3 terms: with 2^e_g the power of two that brings head g's
@@ -26,21 +28,25 @@
 // At d = 128 P.V reads V the same way: the staged V tile (128-byte swizzle)
 // is V^T as an MN-major operand, and P is split like q (Ps: three E4M3 terms
 // per head of P times 2^k, the power of two that brings the tile's largest P
-// into [128, 256); the tile's O is scaled back by 2^-k), so nothing is
-// converted and the tensor cores run 8 instructions a tile.  Stale V rows of
-// the last tile are zeroed in the staged tile before P.V (0 * NaN would
-// poison the product).  At d = 64 a V row is 64 bytes, half an MN-major
-// atom, so converter warps widen V exactly to f16 (cvt.rn.f16x2.e4m3x2: every
-// E4M3 value is an f16 value) into a zero-padded V^T operand instead.
-// The K scale is folded into the softmax scale, the V scale into the output.
-// The staging ring (6 tiles of K and V at d = 128, 8 at d = 64) is the only
-// large buffer besides the f16 V operands of d = 64, so the copies run that
-// many tiles ahead.  Two softmax warpgroups take alternate tiles (even tiles
-// with S, P and O buffers 0, odd tiles with buffers 1), each with its own
-// running maximum, sum and accumulator, merged at the end.
-// Roles: 0 producer, 1 TMEM owner and MMA issuer, 2..5 and 6..9 softmax /
-// epilogue groups A and B (A also builds Qs); at d = 64 also 10..15 V
-// converters.
+// into [128, 256), rounded to f16 first; the tile's O is scaled back by
+// 2^-k), so nothing is converted and the tensor cores run 8 instructions a
+// tile.  Stale V rows of the last tile are zeroed in the staged tile before
+// P.V (0 * NaN would poison the product).  At d = 64 a V row is 64 bytes,
+// half an MN-major atom, so converter warps widen V exactly to f16
+// (cvt.rn.f16x2.e4m3x2: every E4M3 value is an f16 value) into a zero-padded
+// V^T operand instead.  The K scale is folded into the softmax scale, the V
+// scale into the output.
+// Separate K and V staging rings (5 and 7 tiles at d = 128: a K slot frees
+// when its q.K^T has run, a V slot only after P.V; 6 and 10 at d = 64) are
+// the large buffers, each filled in tile order by its own producer at
+// d = 128.  Two softmax warpgroups take alternate tiles (even tiles with S
+// buffer 0, odd ones with S buffer 1; P and O double-buffered per group),
+// each with its own running maximum, sum and accumulator; the groups merge
+// their states at the end of each split-KV partition the CTA computes.
+// Roles: 0 producer (K at d = 128), 1 TMEM owner and q.K^T issuer (all MMAs
+// at d = 64), 2..5 and 6..9 softmax / epilogue groups A and B (A also builds
+// Qs); at d = 128 also 10 the V producer and 11 the P.V issuer, at d = 64
+// 10..15 V converters.
 #include <cuda.h>  // CUtensorMap and its enums only; the encoder comes from the driver at run time
 
 #include <cmath>

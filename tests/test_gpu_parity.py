@@ -531,3 +531,30 @@ def test_decode_partitions_per_cta_zero_and_one_token(span):
                         case.spec.dtype)
     assert torch.all(out[0] == 0)
     assert_close(out, ref, "span, zero and one token")
+
+
+# ------------------------------------------------ compact grid (<= 128 seqs)
+@pytest.mark.parametrize("num_seqs", [127, 128, 129])       # 129: the 3-D grid
+@pytest.mark.parametrize("partition,R", [(128, 1), (256, 2), (0, 0)])
+def test_decode_compact_grid_mixed_lengths(span, num_seqs, partition, R):
+    """Batches around the compact-grid limit with zero-length, one-token and
+    long sequences in the middle of the batch: every output."""
+    if R:
+        span(R)
+    case = Case(workloads.make_plan("qwen", num_seqs=num_seqs))
+    case.gpu_writes(0)
+    lens = case.lay.seq_lens.copy()
+    rng = np.random.default_rng(num_seqs)
+    pick = rng.choice(num_seqs, 12, replace=False)
+    lens[pick[:6]] = 0
+    lens[pick[6:9]] = 1
+    lens_t = torch.as_tensor(lens, device="cuda")
+    hk, hv = case.snapshot(0)
+    out = torch.full_like(case.vals.q, float("nan"))
+    api.decode(out, case.vals.q, case.vals.k_pools[0], case.vals.v_pools[0], case.tables,
+               lens_t, case.max_seq_len, case.plan.scale, partition_tokens=partition)
+    api.check_error()
+    ref = oracle.decode(bits(case.vals.q), hk, hv, case.lay.block_tables, lens, case.plan.scale,
+                        case.spec.dtype)
+    assert torch.all(out[torch.as_tensor(pick[:6], device="cuda")] == 0)
+    assert_close(out, ref, f"compact S={num_seqs} P={partition} R={R}")
