@@ -362,11 +362,17 @@ class GpuStep:
     def step_bytes(self):
         return self.spec.num_layers * (self.decode_bytes + self.write_bytes + self.copy_bytes)
 
-    def run(self, ev=None, q=None, k_new=None, v_new=None, stream=None):
+    def run(self, ev=None, q=None, k_new=None, v_new=None, stream=None, tables=None, lens=None,
+            slots=None, out=None):
         """One step.  ev: optional list collecting (start, end) events around
-        each decode call."""
+        each decode call.  q .. out: other input and output tensors of the
+        same shapes (the end-to-end run's second buffer set)."""
         api, v = self.api, self.vals
         q = v.q if q is None else q
+        tables = self.tables if tables is None else tables
+        lens = self.lens if lens is None else lens
+        slots = self.slots if slots is None else slots
+        outs = self.out if out is None else out
         for layer in range(self.spec.num_layers):
             kp, vp = v.k_pools[layer], v.v_pools[layer]
             if self.copies.numel():
@@ -377,25 +383,25 @@ class GpuStep:
                 a.record(stream)
             if self.fp8:
                 # E4M3 pools: quantised write of the new token and the decode, one launch
-                api.decode_fp8(self.out[layer], q, kp, vp, self.tables, self.lens,
+                api.decode_fp8(outs[layer], q, kp, vp, tables, lens,
                                self.max_seq_len, self.plan.scale, self.FP8_SCALE, self.FP8_SCALE,
                                partition_tokens=self.P,
                                k_new=v.k_new[layer] if k_new is None else k_new[layer],
                                v_new=v.v_new[layer] if v_new is None else v_new[layer],
-                               slot_mapping=self.slots, workspace=self.ws, stream=stream)
+                               slot_mapping=slots, workspace=self.ws, stream=stream)
             elif self.prefix_len:
                 # prefix pass, then the tails with the new token's write and the merge
-                api.decode_cascade(self.out[layer], q, kp, vp, self.tables, self.lens,
+                api.decode_cascade(outs[layer], q, kp, vp, tables, lens,
                                    self.max_seq_len, self.plan.scale, self.prefix_len,
                                    k_new=v.k_new[layer] if k_new is None else k_new[layer],
                                    v_new=v.v_new[layer] if v_new is None else v_new[layer],
-                                   slot_mapping=self.slots, workspace=self.ws, stream=stream)
+                                   slot_mapping=slots, workspace=self.ws, stream=stream)
             else:
                 # the new token's cache write and the decode, one launch
-                api.decode_step(self.out[layer], q,
+                api.decode_step(outs[layer], q,
                                 v.k_new[layer] if k_new is None else k_new[layer],
-                                v.v_new[layer] if v_new is None else v_new[layer], self.slots,
-                                kp, vp, self.tables, self.lens, self.max_seq_len,
+                                v.v_new[layer] if v_new is None else v_new[layer], slots,
+                                kp, vp, tables, lens, self.max_seq_len,
                                 self.plan.scale, partition_tokens=self.P, workspace=self.ws,
                                 stream=stream)
             if ev is not None:
@@ -502,35 +508,91 @@ def run_gpu(args, rank, world, local_rank):
                              ("_fp8" if st.fp8 else ""))
 
     # ------------------------------------------------ end to end (host buffers)
-    # Every step copies its inputs from pinned host memory into the step's
-    # device input tensors, runs the step, and reads every layer's output back.
+    # Every step copies its inputs from pinned host memory into device input
+    # tensors, runs the step, and reads every layer's output back.  Steps
+    # alternate between two device buffer sets, with the
+    # host-to-device copies on one side stream and the device-to-host copies
+    # on another: step i+1's inputs arrive while step i runs, and step i's
+    # output leaves while step i+1 runs.  A graph-replayed step gets a second
+    # graph, captured on the second buffer set.
     pin = lambda t: t.cpu().pin_memory()
     h_in = [pin(st.vals.q)] + [pin(t) for t in st.vals.k_new + st.vals.v_new] + \
         [pin(st.tables), pin(st.lens), pin(st.slots)]
-    d_in = [st.vals.q] + list(st.vals.k_new) + list(st.vals.v_new) + \
-        [st.tables, st.lens, st.slots]
     h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in st.out]
     h2d = sum(t.nbytes for t in h_in)
     d2h = sum(t.nbytes for t in h_out)
+    nl = spec.num_layers
+    d_in = [[st.vals.q] + list(st.vals.k_new) + list(st.vals.v_new) + [st.tables, st.lens, st.slots]]
+    d_out = [st.out]
+    d_in.append([t.clone() for t in d_in[0]])
+    d_out.append([o.clone() for o in st.out])
+
+    def run_set(b, stream=None):
+        ins = d_in[b]
+        st.run(q=ins[0], k_new=ins[1:1 + nl], v_new=ins[1 + nl:1 + 2 * nl], tables=ins[-3],
+               lens=ins[-2], slots=ins[-1], out=d_out[b], stream=stream)
+
+    graphs = None
+    if graph is not None:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            run_set(1)
+        torch.cuda.current_stream().wait_stream(side)
+        graph1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph1):
+            run_set(1)
+        torch.cuda.synchronize()
+        graphs = [graph, graph1]
+    main = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ready = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    read = [torch.cuda.Event(), torch.cuda.Event()]
+    k = [0]  # steps issued
 
     def e2e_step():
-        for d, h in zip(d_in, h_in):
-            d.copy_(h, non_blocking=True)
-        one_step()
-        for h, o in zip(h_out, st.out):
-            h.copy_(o, non_blocking=True)
+        b = k[0] % 2
+        with torch.cuda.stream(up):
+            if k[0] >= 2:
+                up.wait_event(done[b])  # step k-2 has read this set's inputs
+            for d, h in zip(d_in[b], h_in):
+                d.copy_(h, non_blocking=True)
+            ready[b].record(up)
+        main.wait_event(ready[b])
+        if k[0] >= 2:
+            main.wait_event(read[b])  # step k-2's output has left
+        if graphs is not None:
+            graphs[b].replay()
+        else:
+            run_set(b, stream=main)
+        done[b].record(main)
+        with torch.cuda.stream(down):
+            down.wait_event(done[b])
+            for h, o in zip(h_out, d_out[b]):
+                h.copy_(o, non_blocking=True)
+            read[b].record(down)
+        k[0] += 1
+
+    def e2e_drain():
+        main.wait_stream(up)
+        main.wait_stream(down)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
+    e2e_drain()
     torch.cuda.synchronize()
     e2e_steps = max(3, args.steps // 2)
     barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
+    t0.record(main)
+    up.wait_stream(main)    # no copy of the timed steps starts before t0
+    down.wait_stream(main)
     for _ in range(e2e_steps):
         e2e_step()
-    t1.record()
+    e2e_drain()
+    t1.record(main)
     torch.cuda.synchronize()
     e2e_s, e2e_bytes = reduce_over_ranks(t0.elapsed_time(t1) / 1e3,
                                          st.step_bytes() * e2e_steps, device)
@@ -581,7 +643,10 @@ def run_gpu(args, rank, world, local_rank):
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "e2e": {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": 1e3 * e2e_s / e2e_steps},
+                "ms_per_step": 1e3 * e2e_s / e2e_steps,
+                "copies": ("pinned host buffers; two device buffer sets (a graph each when "
+                           "replayed), copies on side streams overlapping the neighbouring "
+                           "steps")},
         "gpu_launches": st.launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
