@@ -43,10 +43,10 @@
 // buffer 0, odd ones with S buffer 1; P and O double-buffered per group),
 // each with its own running maximum, sum and accumulator; the groups merge
 // their states at the end of each split-KV partition the CTA computes.
-// Roles: 0 producer (K at d = 128), 1 TMEM owner and q.K^T issuer (all MMAs
-// at d = 64), 2..5 and 6..9 softmax / epilogue groups A and B (A also builds
-// Qs); at d = 128 also 10 the V producer and 11 the P.V issuer, at d = 64
-// 10..15 V converters.
+// Roles: 0 producer (K at d = 128), 1 TMEM owner and MMA issuer (of group
+// A's tiles at d = 128), 2..5 and 6..9 softmax / epilogue groups A and B (A
+// also builds Qs); at d = 128 also 10 the V producer and 11 the MMA issuer of
+// group B's tiles, at d = 64 10..15 V converters.
 #include <cuda.h>  // CUtensorMap and its enums only; the encoder comes from the driver at run time
 
 #include <cmath>
@@ -67,7 +67,7 @@ constexpr int kF8N = 16;           // MMA N of P.V in f16: the query heads of a 
 constexpr int kF8G = 8;            // largest group the kernel serves
 constexpr int kF8Conv0 = 10;       // first converter warp (f16 P.V only)
 constexpr int kF8VProd = 10;       // the V producer warp (E4M3 P.V only)
-constexpr int kF8PvWarp = 11;      // the P.V issuer (E4M3 P.V only)
+constexpr int kF8Issuer1 = 11;     // the odd tiles' MMA issuer (E4M3 P.V only)
 constexpr int kF8ConvWarps = 6;    // converter warps (V)
 
 constexpr int kF8MaxRing = 12;     // slots of a staging ring
@@ -97,7 +97,8 @@ struct F8Shape {
     static constexpr int QN = (3 * GM + 15) / 16 * 16;
     static constexpr int S0 = 0, O0 = 2 * QN;
     static constexpr int COLS = 6 * QN <= 128 ? 128 : 256;
-    // d = 128: producer K, q.K^T issuer, 8 softmax, producer V, P.V issuer;
+    // d = 128: producer K, even tiles' issuer, 8 softmax, producer V, odd
+    // tiles' issuer;
     // d = 64: producer, MMA issuer, 8 softmax, 6 converters (4 per
     // sub-partition, 128 registers)
     static constexpr int WARPS = DIRECT ? 12 : 16;
@@ -132,7 +133,8 @@ struct F8Shape {
     static constexpr int XCH_BYTES = kF8G * D * 4 + 4 * kF8G * 4;
     static constexpr int OFF_BAR = OFF_XCH + 2 * XCH_BYTES;
     static constexpr int OFF_MISC = OFF_BAR + kNumF8Bars * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
+    // MISC: TMEM address, abort flag, then the issuers' progress (d = 128)
+    static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
     static_assert(STG_BYTES % 1024 == 0, "TMA swizzle alignment");
     static_assert(NK <= kF8MaxRing && NV <= kF8MaxRing, "ring barriers");
@@ -252,6 +254,8 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::OFF_MISC + 8);
+    // d = 128: per softmax group, q.K^T and P.V MMAs issued so far
+    volatile int *progress = reinterpret_cast<volatile int *>(smem + S::OFF_MISC + 16);
     float *red = reinterpret_cast<float *>(smem + S::OFF_RED);
     float *qmul = reinterpret_cast<float *>(smem + S::OFF_QMUL);
 
@@ -322,6 +326,7 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
             mbar_init(&bar[kVEmpty0 + b], S::DIRECT ? 1 : kF8ConvWarps);
         }
         *abort_flag = 0;
+        for (int i = 0; i < 4; ++i) progress[i] = 0;
         mbar_init_fence();
     }
     if (warp == 1) {
@@ -468,10 +473,10 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
             *abort_flag = 1;
         }
       }
-    } else if (warp == 1 || (S::DIRECT && warp == kF8PvWarp)) {
+    } else if (warp == 1 || (S::DIRECT && warp == kF8Issuer1)) {
         // ---------------------------------------------------------- MMA issue
-        // (d = 128: q.K^T from warp 1 and P.V from warp kF8PvWarp, two
-        // independent streams; d = 64: both from warp 1)
+        // (d = 128: warp 1 for the even tiles and warp kF8Issuer1 for the odd
+        // ones; d = 64: every MMA from warp 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = e4m3_idesc(kF8Tile, S::QN, false);
             constexpr uint32_t idesc_pv = f16_idesc(false, true, false, 128, kF8N);
@@ -533,11 +538,36 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
             // thing it does with tile t), so a softmax group finds its next S
             // ready when it has written P of this tile.
             bool ok = true;
-            if (S::DIRECT && warp == kF8PvWarp) {
-                for (int t = 0; ok && t < ntiles; ++t) ok = issue_pv(t);
-            } else if (S::DIRECT) {
-                ok = mbar_wait(&bar[kQReady], 0);
-                for (int t = 0; ok && t < ntiles; ++t) ok = issue_qk(t);
+            if constexpr (S::DIRECT) {
+                // One issuer per softmax group (warp 1: even tiles, warp
+                // kF8Issuer1: odd ones), each in its tiles' order: q.K^T of
+                // the group's first tile, then q.K^T of tile t+2 and P.V of
+                // tile t.  The groups only share the staging rings, whose
+                // slots alternate between them: before q.K^T of tile t the
+                // other group must have issued q.K^T of every tile up to
+                // t - NK and P.V of every tile up to t - NV, so those tiles
+                // have landed and the parity tests on the slots of t can
+                // only mean t's copies.
+                const int g = warp == 1 ? 0 : 1, o = 1 - g;
+                auto other_covers = [&](int t) -> bool {
+                    const unsigned long long t0 = global_timer_ns();
+                    for (;;) {
+                        // the other group's next tile to issue, q.K^T and P.V
+                        const int nq = o + 2 * progress[2 * o], nv = o + 2 * progress[2 * o + 1];
+                        if (nq > t - S::NK && nv > t - S::NV) return true;
+                        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+                    }
+                };
+                auto qk = [&](int t) -> bool {
+                    if (!other_covers(t) || !issue_qk(t)) return false;
+                    progress[2 * g] = progress[2 * g] + 1;
+                    return true;
+                };
+                ok = mbar_wait(&bar[kQReady], 0) && (g >= ntiles || qk(g));
+                for (int t = g; ok && t < ntiles; t += 2) {
+                    ok = (t + 2 >= ntiles || qk(t + 2)) && issue_pv(t);
+                    if (ok) progress[2 * g + 1] = progress[2 * g + 1] + 1;
+                }
             } else {
                 ok = mbar_wait(&bar[kQReady], 0) && issue_qk(0) && (ntiles < 2 || issue_qk(1));
                 for (int t = 0; ok && t < ntiles; ++t)
