@@ -315,7 +315,7 @@ class GpuStep:
         self.P = spec.partition_tokens if partition_tokens is None else partition_tokens
         self.resolved_P = self.P if self.P else api.auto_partition(
             spec.num_seqs, spec.num_kv_heads, self.max_seq_len, spec.head_dim, spec.block_size,
-            spec.num_q_heads // spec.num_kv_heads, self.vals.q.dtype)
+            spec.num_q_heads // spec.num_kv_heads, self.vals.q.dtype, fp8=self.fp8)
         wsize = api.fp8_workspace_size if self.fp8 else api.workspace_size
         size = wsize(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                      spec.block_size, self.max_seq_len, self.P, self.vals.q.dtype)

@@ -277,6 +277,9 @@ size_t pa_decode_fp8_workspace_size(int num_seqs, int num_q_heads, int num_kv_he
  * (-1 means it will run single pass).  Needs the current CUDA device. */
 int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
                              int block_size, int group_size, pa_dtype dtype);
+/* The same for pa_decode_fp8 (E4M3 pools; coarser partitions). */
+int pa_decode_fp8_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
+                                 int block_size, int group_size, pa_dtype dtype);
 
 /* Decode kernel selection, process-wide, for every later call:
  *   0 automatic (default): the tensor-core kernel (tcgen05 MMAs, TMA tensor

@@ -111,9 +111,12 @@ def _decode_dims(q, k_pool, block_tables, seq_lens):
     return S, hq, hkv, d, nb, bs
 
 
-def auto_partition(num_seqs, num_kv_heads, max_seq_len, head_dim, block_size, group, dtype):
-    return _lib.load().pa_decode_auto_partition(num_seqs, num_kv_heads, max_seq_len, head_dim,
-                                                block_size, group, _DTYPES[dtype])
+def auto_partition(num_seqs, num_kv_heads, max_seq_len, head_dim, block_size, group, dtype,
+                   fp8=False):
+    """Partition size decode (fp8=False) or decode_fp8 (fp8=True) uses for
+    partition_tokens=0; -1 for single pass."""
+    fn = _lib.load().pa_decode_fp8_auto_partition if fp8 else _lib.load().pa_decode_auto_partition
+    return fn(num_seqs, num_kv_heads, max_seq_len, head_dim, block_size, group, _DTYPES[dtype])
 
 
 DECODE_IMPLS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}

@@ -721,14 +721,18 @@ static int decode_ctas_per_sm(const DecodeEntry &e) {
 }
 
 // Automatic partition size: aim for the largest work item to be at most
-// 1/32 of one CTA slot's share of the whole job (taking the average length
-// as half the maximum), in multiples of 256 positions and at least 512, and run single pass
-// when that would not split anything.
-static int auto_partition(int S, int Hkv, int max_seq_len, int ctas_per_sm, int block_size) {
+// 1/share_div of one CTA slot's share of the whole job (the share taken at
+// the maximum length), in multiples of 256 positions and at least 512, and
+// run single pass when that would not split anything.  share_div is 32 for
+// kernels that keep several CTAs an SM (another CTA streams while one is in
+// its prologue or epilogue) and 8 for the E4M3 kernel, one CTA an SM, whose
+// per-item prologue and ring fill weigh more.
+static int auto_partition(int S, int Hkv, int max_seq_len, int ctas_per_sm, int block_size,
+                          double share_div = 32.0) {
     if (max_seq_len <= 0) return -1;
     const int slots = sm_count() * ctas_per_sm;
     const double units = (double)S * Hkv;
-    double target = (double)max_seq_len * units / (32.0 * (slots > 0 ? slots : 1));
+    double target = (double)max_seq_len * units / (share_div * (slots > 0 ? slots : 1));
     int P = (int)std::ceil(target / 256.0) * 256;
     if (P < 512) P = 512;
     if (P % block_size) P = (P / block_size + 1) * block_size;
@@ -788,7 +792,8 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
         const int per_sm = r->fp8  ? fp8_ctas_per_sm(dtype == PA_BF16, head_dim, G)
                            : r->tc ? tc_ctas_per_sm(dtype == PA_BF16, head_dim)
                                    : decode_ctas_per_sm(r->entry);
-        P = auto_partition(num_seqs, num_kv_heads, max_seq_len, per_sm, block_size);
+        P = auto_partition(num_seqs, num_kv_heads, max_seq_len, per_sm, block_size,
+                           r->fp8 ? 8.0 : 32.0);
     }
     if (P < -1) return PA_ERR_INVALID;
     if (P > 0 && (P % block_size != 0 || P % kUnit != 0)) return PA_ERR_INVALID;
@@ -1016,6 +1021,15 @@ int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, in
     ResolvedDecode r;
     if (group_size < 1 || resolve(num_seqs, num_kv_heads * group_size, num_kv_heads, head_dim,
                                   block_size, max_seq_len, 0, dtype, &r) != PA_OK)
+        return -1;
+    return r.P;
+}
+
+int pa_decode_fp8_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
+                                 int block_size, int group_size, pa_dtype dtype) {
+    ResolvedDecode r;
+    if (group_size < 1 || resolve(num_seqs, num_kv_heads * group_size, num_kv_heads, head_dim,
+                                  block_size, max_seq_len, 0, dtype, &r, true) != PA_OK)
         return -1;
     return r.P;
 }
