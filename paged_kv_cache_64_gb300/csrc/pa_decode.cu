@@ -723,12 +723,13 @@ static int decode_ctas_per_sm(const DecodeEntry &e) {
 // Automatic partition size: aim for the largest work item to be at most
 // 1/share_div of one CTA slot's share of the whole job (the share taken at
 // the maximum length), in multiples of 256 positions and at least 512, and
-// run single pass when that would not split anything.  share_div is 32 for
-// kernels that keep several CTAs an SM (another CTA streams while one is in
-// its prologue or epilogue) and 8 for the E4M3 kernel, one CTA an SM, whose
-// per-item prologue and ring fill weigh more.
+// run single pass when that would not split anything.  share_div is 4 for
+// the 16-bit kernels and 8 for the E4M3 kernel (one CTA an SM, so twice the
+// slot share): coarse enough that a work item's prologue, ring fill and
+// partial writes stay small next to its tiles (the Llama-shaped batch runs
+// single pass), fine enough to split a few long sequences over the GPU.
 static int auto_partition(int S, int Hkv, int max_seq_len, int ctas_per_sm, int block_size,
-                          double share_div = 32.0) {
+                          double share_div) {
     if (max_seq_len <= 0) return -1;
     const int slots = sm_count() * ctas_per_sm;
     const double units = (double)S * Hkv;
@@ -793,7 +794,7 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
                            : r->tc ? tc_ctas_per_sm(dtype == PA_BF16, head_dim)
                                    : decode_ctas_per_sm(r->entry);
         P = auto_partition(num_seqs, num_kv_heads, max_seq_len, per_sm, block_size,
-                           r->fp8 ? 8.0 : 32.0);
+                           r->fp8 ? 8.0 : 4.0);
     }
     if (P < -1) return PA_ERR_INVALID;
     if (P > 0 && (P % block_size != 0 || P % kUnit != 0)) return PA_ERR_INVALID;
