@@ -32,7 +32,6 @@ Arrays of 16-bit elements are passed as numpy uint16 bit patterns; dtype is
 "f16" or "bf16".
 """
 import ctypes
-import os
 
 import numpy as np
 
