@@ -151,7 +151,8 @@ def stored_traffic(workload):
     path = os.path.join(ROOT, "profiles", f"pa_decode_{workload}.md")
     if not os.path.exists(path):
         return None
-    text = open(path).read()
+    with open(path) as fh:
+        text = fh.read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
     if not m or not s or s.group(1) != source_digest():

@@ -15,3 +15,10 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+def read_json(path):
+    """A golden fixture's contents (the file closed afterwards)."""
+    import json
+    with open(path) as fh:
+        return json.load(fh)

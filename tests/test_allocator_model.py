@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 
 from oracle.allocator import BlockAllocatorModel, OutOfBlocks
+from conftest import read_json
 
 
 def replay_hand_table(model, steps):
@@ -23,7 +24,7 @@ def replay_hand_table(model, steps):
 
 
 def test_hand_worked_table(golden_dir):
-    g = json.load(open(os.path.join(golden_dir, "p2_hand_worked_table.json")))
+    g = read_json(os.path.join(golden_dir, "p2_hand_worked_table.json"))
     model = BlockAllocatorModel(g["num_blocks"], g["block_size"])
     for st in replay_hand_table(model, g["steps"]):
         assert {s: model.table(s) for s in model.tables} == st["tables"], st
@@ -33,8 +34,8 @@ def test_hand_worked_table(golden_dir):
 
 
 def test_quiz4_new_request(golden_dir):
-    g = json.load(open(os.path.join(golden_dir, "p2_hand_worked_table.json")))
-    q = json.load(open(os.path.join(golden_dir, "p2_quiz4.json")))
+    g = read_json(os.path.join(golden_dir, "p2_hand_worked_table.json"))
+    q = read_json(os.path.join(golden_dir, "p2_quiz4.json"))
     model = BlockAllocatorModel(g["num_blocks"], g["block_size"])
     for _ in replay_hand_table(model, g["steps"]):
         pass
@@ -52,7 +53,7 @@ def test_quiz4_new_request(golden_dir):
 
 
 def test_prefix_sharing_copy_on_write(golden_dir):
-    g = json.load(open(os.path.join(golden_dir, "p2_prefix_sharing.json")))
+    g = read_json(os.path.join(golden_dir, "p2_prefix_sharing.json"))
     model = BlockAllocatorModel(g["num_blocks"], g["block_size"])
     for st in g["steps"]:
         ev = st["event"]

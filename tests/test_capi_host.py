@@ -12,6 +12,7 @@ import pytest
 
 from oracle.allocator import BlockAllocatorModel, OutOfBlocks as ModelOutOfBlocks
 from paged_kv_cache_64_gb300 import _lib, api, workloads
+from conftest import read_json
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -24,7 +25,8 @@ def lib():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    with open(os.path.join(ROOT, "include", "pa.h")) as fh:
+        text = fh.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
 
@@ -117,7 +119,7 @@ def replay(alloc, steps):
 
 
 def test_native_allocator_hand_worked_table(lib, golden_dir):
-    g = json.load(open(os.path.join(golden_dir, "p2_hand_worked_table.json")))
+    g = read_json(os.path.join(golden_dir, "p2_hand_worked_table.json"))
     ids = {"A": 1, "B": 2, "C": 3}
     alloc = api.BlockAllocator(g["num_blocks"], g["block_size"])
     for st in g["steps"]:
@@ -133,7 +135,7 @@ def test_native_allocator_hand_worked_table(lib, golden_dir):
 
 
 def test_native_allocator_prefix_sharing(lib, golden_dir):
-    g = json.load(open(os.path.join(golden_dir, "p2_prefix_sharing.json")))
+    g = read_json(os.path.join(golden_dir, "p2_prefix_sharing.json"))
     ids = {"S1": 1, "S2": 2}
     alloc = api.BlockAllocator(g["num_blocks"], g["block_size"])
     for st in g["steps"]:

@@ -14,6 +14,7 @@ import pytest
 from scipy.special import softmax
 
 import oracle
+from conftest import read_json
 
 RNG = np.random.default_rng(20261202)
 
@@ -37,7 +38,8 @@ def widen_lib(bits, dtype):
     """Library widening used as the independent side of the checks."""
     if dtype == "f16":
         return bits.view(np.float16).astype(np.float64)
-    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # NaN patterns stay NaN
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def scatter_into_pool(logical, table, num_blocks, block_size, fill):
@@ -315,7 +317,7 @@ def test_cache_write_and_copy_blocks_readback():
 
 # ------------------------------------------------------------- closed forms
 def test_kv_bytes_closed_forms(golden_dir):
-    g = json.load(open(os.path.join(golden_dir, "kv_sizes.json")))
+    g = read_json(os.path.join(golden_dir, "kv_sizes.json"))
     for c in g["per_token"]:
         assert oracle.kv_bytes_per_token(c["n_layers"], c["n_kv_heads"], c["head_dim"],
                                          c["bytes_per_elem"]) == c["bytes"], c["source"]
@@ -329,7 +331,7 @@ def test_kv_bytes_closed_forms(golden_dir):
 
 
 def test_address_translation(golden_dir):
-    g = json.load(open(os.path.join(golden_dir, "address_translation.json")))
+    g = read_json(os.path.join(golden_dir, "address_translation.json"))
     for c in g["cases"]:
         j, o, phys = oracle.translate(c["table"], c["t"], c["block_size"])
         assert (j, o, phys) == (c["j"], c["o"], c["phys"]), c["source"]

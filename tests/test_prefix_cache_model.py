@@ -11,6 +11,7 @@ import pytest
 
 from oracle.allocator import OutOfBlocks as ModelOutOfBlocks
 from oracle.prefix_cache import PrefixCachePoolModel, block_hash, fnv1a64
+from conftest import read_json
 
 
 @pytest.fixture(params=["model", "native"])
@@ -44,7 +45,7 @@ def test_block_hash_encoding():
 
 
 def test_pages_2407_token_prefix(Pool, golden_dir):
-    g = json.load(open(os.path.join(golden_dir, "p1_prefix_match.json")))
+    g = read_json(os.path.join(golden_dir, "p1_prefix_match.json"))
     B, n = g["block_size"], g["prompt_tokens"]
     rng = np.random.default_rng(0)
     prompt = rng.integers(0, 150000, n).tolist()
