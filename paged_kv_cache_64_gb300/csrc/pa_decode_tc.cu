@@ -430,15 +430,109 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
             }
         };
 
-        for (int i = 0; i < ntiles; ++i) {
-            const int b = i & 1;
-            bool drained = false;
-            if (SPAN && i > 0 && i % tpp == 0) {
-                // tile i opens the next partition of the span: the previous
-                // one's last O, its partial, then a fresh running state
-                if (!failed && !accumulate(i - 1)) failed = true;
-                drained = true;
-                emit_partial(part0 + i / tpp - 1);
+        // Partition by partition of the CTA's span (one partition without
+        // SPAN): the tiles of partition j, its last O folded in, then (for
+        // all but the last) its partial and a fresh running state.
+        const int nspan = SPAN ? part_end - part0 : 1;
+        for (int j = 0; j < nspan; ++j) {
+            const int t_lo = SPAN ? j * tpp : 0;
+            const int t_hi = SPAN ? ((j + 1) * tpp < ntiles ? (j + 1) * tpp : ntiles) : ntiles;
+            for (int i = t_lo; i < t_hi; ++i) {
+              const int b = i & 1;
+              const bool landed = !failed && mbar_wait(&bar[kSFull0 + b], (i >> 1) & 1);
+              const bool ok = __all_sync(kFullMask, landed);
+              float s[16];
+              if (ok) {
+                  tc_fence_after();
+                  tmem_load16(tmem + lane_addr + kSCol0 + 16 * b, s);
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(&bar[kSEmpty0 + b]);
+              } else {
+  #pragma unroll
+                  for (int g = 0; g < 16; ++g) s[g] = 0.f;
+              }
+              const int tile0 = start + i * kTcTile;
+              const int nvalid = (end - tile0 < kTcTile) ? end - tile0 : kTcTile;
+              const bool valid = r < nvalid;
+              // tile max of each head over the 128 positions
+              float *tmax = red + b * (4 * kTcN);
+  #pragma unroll
+              for (int g = 0; g < kTcG; ++g) {
+                  s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
+                  float v = s[g];
+  #pragma unroll
+                  for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
+                  if (lane == 0) tmax[sw * kTcN + g] = v;
+              }
+              if (lane == 0) tmax[sw * kTcN + kTcN - 1] = ok ? 1.f : 0.f;  // column 15: health flag
+              softmax_bar();
+              bool all_ok = true;
+  #pragma unroll
+              for (int w = 0; w < 4; ++w) all_ok &= tmax[w * kTcN + kTcN - 1] != 0.f;
+              if (!all_ok) {
+                  failed = true;
+                  break;
+              }
+              bool need = false;
+              float mx[kTcG];
+  #pragma unroll
+              for (int g = 0; g < kTcG; ++g) {
+                  mx[g] = fmaxf(fmaxf(tmax[g], tmax[kTcN + g]),
+                                fmaxf(tmax[2 * kTcN + g], tmax[3 * kTcN + g]));
+                  need |= (g < G) && (mx[g] > m_run[g] + kLazyRescale);
+              }
+              float alpha[kTcG];
+  #pragma unroll
+              for (int g = 0; g < kTcG; ++g) {
+                  alpha[g] = 1.f;
+                  if (need) {  // block-uniform
+                      const float mn = fmaxf(m_run[g], mx[g]);
+                      alpha[g] = fast_exp2(m_run[g] - mn);
+                      m_run[g] = mn;
+                      l_part[g] *= alpha[g];
+                  }
+                  m_true[g] = fmaxf(m_true[g], mx[g]);
+              }
+              // P^T (16 rows = heads, 128 positions) in the operand layout
+              uint8_t *pbuf = smem + S::OFF_P + b * S::P_BYTES;
+  #pragma unroll
+              for (int g = 0; g < kTcN; ++g) {
+                  float pv = 0.f;
+                  if (g < kTcG && g < G) {
+                      pv = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
+                      l_part[g] += pv;
+                  }
+                  *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kTcN * 128)) =
+                      narrow1<BF16>(pv);
+              }
+              if (!valid) {
+                  // Stale rows of the last tile: V must be finite there (0 * NaN
+                  // would poison the product), so zero the row once it has landed.
+                  // Tile i-1's V has been consumed (the MMA issuer holds back
+                  // q.K^T of the last tile until every earlier P.V is issued), so
+                  // the parity wait below can only mean tile i's phase.
+                  if (mbar_wait(&bar[kVFull], i & 1)) {
+  #pragma unroll
+                      for (int h = 0; h < S::KH; ++h) {
+                          uint4 *row = reinterpret_cast<uint4 *>(smem + S::OFF_V + h * S::SLAB + r * 128);
+  #pragma unroll
+                          for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                      }
+                  } else {
+                      failed = true;
+                  }
+              }
+              fence_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bar[kPFull0 + b]);
+              if (i > t_lo && !accumulate(i - 1)) failed = true;
+  #pragma unroll
+              for (int g = 0; g < kTcG; ++g) alpha_prev[g] = alpha[g];
+            }
+            if (!failed && !accumulate(t_hi - 1)) failed = true;
+            if (j + 1 < nspan) {
+                emit_partial(part0 + j);
 #pragma unroll
                 for (int g = 0; g < kTcG; ++g) {
                     m_run[g] = -INFINITY;
@@ -448,98 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
                     alpha_prev[g] = 1.f;
                 }
             }
-            const bool landed = !failed && mbar_wait(&bar[kSFull0 + b], (i >> 1) & 1);
-            const bool ok = __all_sync(kFullMask, landed);
-            float s[16];
-            if (ok) {
-                tc_fence_after();
-                tmem_load16(tmem + lane_addr + kSCol0 + 16 * b, s);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[kSEmpty0 + b]);
-            } else {
-#pragma unroll
-                for (int g = 0; g < 16; ++g) s[g] = 0.f;
-            }
-            const int tile0 = start + i * kTcTile;
-            const int nvalid = (end - tile0 < kTcTile) ? end - tile0 : kTcTile;
-            const bool valid = r < nvalid;
-            // tile max of each head over the 128 positions
-            float *tmax = red + b * (4 * kTcN);
-#pragma unroll
-            for (int g = 0; g < kTcG; ++g) {
-                s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
-                float v = s[g];
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
-                if (lane == 0) tmax[sw * kTcN + g] = v;
-            }
-            if (lane == 0) tmax[sw * kTcN + kTcN - 1] = ok ? 1.f : 0.f;  // column 15: health flag
-            softmax_bar();
-            bool all_ok = true;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) all_ok &= tmax[w * kTcN + kTcN - 1] != 0.f;
-            if (!all_ok) {
-                failed = true;
-                break;
-            }
-            bool need = false;
-            float mx[kTcG];
-#pragma unroll
-            for (int g = 0; g < kTcG; ++g) {
-                mx[g] = fmaxf(fmaxf(tmax[g], tmax[kTcN + g]),
-                              fmaxf(tmax[2 * kTcN + g], tmax[3 * kTcN + g]));
-                need |= (g < G) && (mx[g] > m_run[g] + kLazyRescale);
-            }
-            float alpha[kTcG];
-#pragma unroll
-            for (int g = 0; g < kTcG; ++g) {
-                alpha[g] = 1.f;
-                if (need) {  // block-uniform
-                    const float mn = fmaxf(m_run[g], mx[g]);
-                    alpha[g] = fast_exp2(m_run[g] - mn);
-                    m_run[g] = mn;
-                    l_part[g] *= alpha[g];
-                }
-                m_true[g] = fmaxf(m_true[g], mx[g]);
-            }
-            // P^T (16 rows = heads, 128 positions) in the operand layout
-            uint8_t *pbuf = smem + S::OFF_P + b * S::P_BYTES;
-#pragma unroll
-            for (int g = 0; g < kTcN; ++g) {
-                float pv = 0.f;
-                if (g < kTcG && g < G) {
-                    pv = fast_exp2(s[g] - m_run[g]);  // masked: 2^-inf = 0
-                    l_part[g] += pv;
-                }
-                *reinterpret_cast<uint16_t *>(pbuf + sw128_offset(g, r, kTcN * 128)) =
-                    narrow1<BF16>(pv);
-            }
-            if (!valid) {
-                // Stale rows of the last tile: V must be finite there (0 * NaN
-                // would poison the product), so zero the row once it has landed.
-                // Tile i-1's V has been consumed (the MMA issuer holds back
-                // q.K^T of the last tile until every earlier P.V is issued), so
-                // the parity wait below can only mean tile i's phase.
-                if (mbar_wait(&bar[kVFull], i & 1)) {
-#pragma unroll
-                    for (int h = 0; h < S::KH; ++h) {
-                        uint4 *row = reinterpret_cast<uint4 *>(smem + S::OFF_V + h * S::SLAB + r * 128);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
-                    }
-                } else {
-                    failed = true;
-                }
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kPFull0 + b]);
-            if (i >= 1 && !drained && !accumulate(i - 1)) failed = true;
-#pragma unroll
-            for (int g = 0; g < kTcG; ++g) alpha_prev[g] = alpha[g];
         }
-        if (!failed && !accumulate(ntiles - 1)) failed = true;
 
         // l over the 128 position-threads, per head
 #pragma unroll
