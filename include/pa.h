@@ -157,6 +157,8 @@ pa_status pa_copy_blocks(void *const *k_pools, void *const *v_pools, int num_lay
  *   max_seq_len            host int, an upper bound of every L_i (sizes the
  *                          launch); 0 is allowed
  *   head_dim in {64,128}; block_size in {16,32}; 1 <= G <= 8; scale finite.
+ *   num_seqs and num_kv_heads at most 65535 (PA_ERR_INVALID above: a larger
+ *   batch is split into several calls by the caller).
  *   q, out, pools and workspace 16-byte aligned.
  * ---------------------------------------------------------------------- */
 pa_status pa_decode(void *out, const void *q, const void *k_pool, const void *v_pool,

@@ -151,6 +151,30 @@ def make_plan(name, num_seqs=None, len_range=None, cow=False, seed=None, apc=Fal
     return Plan(spec, lens, nb, free_order, ops, pre, cow)
 
 
+def make_shape_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, dtype,
+                    len_range, seed):
+    """A plain decode batch of any supported head shape, for tests that sweep
+    shapes: num_seqs sequences with cached lengths uniform in len_range (both
+    ends included), each added and appended on its own, in a pool of 1.2x the
+    blocks the step needs (at least 8), block ids handed out in a seeded
+    permutation."""
+    spec = Spec("shape", int(num_seqs), int(num_q_heads), int(num_kv_heads), int(head_dim),
+                int(block_size), dtype, 1, int(seed), 0,
+                f"{num_seqs} seqs, {num_q_heads}q/{num_kv_heads}kv, d{head_dim}, {dtype}, "
+                f"B{block_size}, lengths U[{len_range[0]}, {len_range[1]}]")
+    rng = np.random.default_rng(spec.seed)
+    lo, hi = len_range
+    lens = rng.integers(lo, hi, spec.num_seqs, endpoint=True).astype(np.int64)
+    nb = max(8, int(math.ceil(1.2 * sum(_blocks(L + 1, spec.block_size) for L in lens))))
+    ops = []
+    for s in range(spec.num_seqs):
+        ops.append(("add", s))
+        if lens[s]:
+            ops.append(("append", s, int(lens[s])))
+    free_order = rng.permutation(nb).astype(np.int32)
+    return Plan(spec, lens, nb, free_order, ops)
+
+
 @dataclass
 class Layout:
     block_tables: np.ndarray   # int32 [S, max_blocks_per_seq] after the step

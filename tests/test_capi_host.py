@@ -242,6 +242,28 @@ def test_workload_layouts_agree(lib, name, cow):
         assert len(a.pre_copies) == 0   # full shared blocks are never written
 
 
+@pytest.mark.parametrize("shape", [(7, 28, 4, 128, 16, "f16", (0, 1500)),
+                                   (7, 6, 2, 64, 32, "f16", (0, 1500)),
+                                   (3000, 4, 1, 64, 16, "f16", (0, 24))])
+def test_shape_plan_layouts_agree(lib, shape):
+    """Shape-sweep batches: native allocator and model agree, every table
+    entry a sequence uses is a distinct block of the pool, and each new
+    token's slot is the one its table gives for position L - 1."""
+    plan = workloads.make_shape_plan(*shape, seed=5)
+    a = workloads.layout(plan, api.BlockAllocator)
+    b = workloads.layout(plan, BlockAllocatorModel)
+    for f in ("block_tables", "seq_lens", "slot_mapping", "pre_copies", "step_copies"):
+        assert np.array_equal(getattr(a, f), getattr(b, f)), f
+    B = plan.spec.block_size
+    assert np.array_equal(a.seq_lens, plan.cached_lens + 1)
+    used = [a.block_tables[s, :-(-int(L) // B)] for s, L in enumerate(a.seq_lens)]
+    flat = np.concatenate(used)
+    assert len(np.unique(flat)) == len(flat) and flat.min() >= 0 and flat.max() < plan.num_blocks
+    last = a.seq_lens.astype(np.int64) - 1
+    want = a.block_tables[np.arange(len(last)), last // B].astype(np.int64) * B + last % B
+    assert np.array_equal(a.slot_mapping, want)
+
+
 def test_shared_prefix_len():
     """Whole blocks that every sequence reaches through the same entries,
     capped by the shortest sequence."""

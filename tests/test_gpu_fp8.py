@@ -37,8 +37,8 @@ def np_codes(t):
 class Fp8Case:
     """A workload's layout with E4M3 pools of random codes."""
 
-    def __init__(self, name, seed=0, **kw):
-        self.plan = workloads.make_plan(name, **kw)
+    def __init__(self, name, seed=0, plan=None, **kw):
+        self.plan = plan if plan is not None else workloads.make_plan(name, **kw)
         self.spec = spec = self.plan.spec
         self.lay = workloads.layout(self.plan, workloads.native_allocator(self.plan))
         shape = (self.plan.num_blocks, spec.num_kv_heads, spec.block_size, spec.head_dim)
