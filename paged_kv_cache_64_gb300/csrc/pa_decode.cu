@@ -722,20 +722,22 @@ static int decode_ctas_per_sm(const DecodeEntry &e) {
 
 // Automatic partition size: aim for the largest work item to be at most
 // 1/share_div of one CTA slot's share of the whole job (the share taken at
-// the maximum length), in multiples of 256 positions and at least 512, and
-// run single pass when that would not split anything.  share_div is 4 for
-// the 16-bit kernels and 8 for the E4M3 kernel (one CTA an SM, so twice the
-// slot share): coarse enough that a work item's prologue, ring fill and
-// partial writes stay small next to its tiles (the Llama-shaped batch runs
-// single pass), fine enough to split a few long sequences over the GPU.
+// the maximum length), in multiples of 256 positions and at least min_tokens,
+// and run single pass when that would not split anything.  share_div is 4
+// for the 16-bit kernels and 8 for the E4M3 kernel (one CTA an SM, so twice
+// the slot share); min_tokens is 512 for 16-bit pools and 1,024 for E4M3
+// ones (the same bytes): coarse enough that a work item's prologue, ring
+// fill and partial writes stay small next to its tiles (the Llama-shaped
+// batch runs single pass), fine enough to split a few long sequences over
+// the GPU.
 static int auto_partition(int S, int Hkv, int max_seq_len, int ctas_per_sm, int block_size,
-                          double share_div) {
+                          double share_div, int min_tokens) {
     if (max_seq_len <= 0) return -1;
     const int slots = sm_count() * ctas_per_sm;
     const double units = (double)S * Hkv;
     double target = (double)max_seq_len * units / (share_div * (slots > 0 ? slots : 1));
     int P = (int)std::ceil(target / 256.0) * 256;
-    if (P < 512) P = 512;
+    if (P < min_tokens) P = min_tokens;
     if (P % block_size) P = (P / block_size + 1) * block_size;
     if (P >= max_seq_len) return -1;
     return P;
@@ -794,7 +796,7 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
                            : r->tc ? tc_ctas_per_sm(dtype == PA_BF16, head_dim)
                                    : decode_ctas_per_sm(r->entry);
         P = auto_partition(num_seqs, num_kv_heads, max_seq_len, per_sm, block_size,
-                           r->fp8 ? 8.0 : 4.0);
+                           r->fp8 ? 8.0 : 4.0, r->fp8 ? 1024 : 512);
     }
     if (P < -1) return PA_ERR_INVALID;
     if (P > 0 && (P % block_size != 0 || P % kUnit != 0)) return PA_ERR_INVALID;
@@ -807,12 +809,13 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
     if ((r->tc || r->fp8) && P > 0 && P % (r->fp8 ? 256 : 128) == 0) {
         // One CTA computes several consecutive partitions (each still its own
         // partial) when partitions are short: a CTA's prologue and pipeline
-        // fill are then paid once per ~2048 positions, as long as a CTA's
-        // span stays within a quarter of one CTA slot's share of the job (the
-        // share taken at the maximum length, an upper bound), so that short,
-        // latency-bound batches keep one partition a CTA.
+        // fill are then paid once per ~2048 positions (4,096 of E4M3 pools:
+        // the same bytes), as long as a CTA's span stays within a quarter of
+        // one CTA slot's share of the job (the share taken at the maximum
+        // length, an upper bound), so that short, latency-bound batches keep
+        // one partition a CTA.
         const int forced = g_decode_span.load(std::memory_order_relaxed);
-        int R = forced > 0 ? forced : 2048 / P;
+        int R = forced > 0 ? forced : (r->fp8 ? 4096 : 2048) / P;
         if (R > r->NP) R = r->NP;
         if (forced <= 0) {
             const int slots = sm_count() * (r->fp8 ? fp8_ctas_per_sm(dtype == PA_BF16, head_dim, G)
