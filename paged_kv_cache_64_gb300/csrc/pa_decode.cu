@@ -585,59 +585,104 @@ struct ReduceParams {
 
 constexpr int kReduceWarps = 4;
 
-// One warp per (sequence, query head); lane owns D/32 consecutive dims.
+// One block per (sequence, query head) row: the log-sum-exp merge of the
+// row's partials (Parallel Partitioning, step 3).  The block first takes
+// the largest m_k, then its warps take every kReduceWarps-th partial, four
+// at a time (the loads of four partials in flight per warp, sixteen per
+// row), and the warps' sums are added in shared memory.  A lane owns D/32
+// consecutive dims.
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kReduceWarps * 32) split_reduce_kernel(const ReduceParams p) {
-    constexpr int V = D / 32;
+    constexpr int V = D / 32, W = kReduceWarps, U = 4;
+    __shared__ float s_max[W];
+    __shared__ float s_acc[W][D];
+    __shared__ float s_l[W];
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * kReduceWarps + warp;
-    if (row >= (int64_t)p.num_seqs * p.num_q_heads) return;
+    const int64_t row = blockIdx.x;
     const int seq = (int)(row / p.num_q_heads);
     const int L = checked_len(p.seq_lens, seq, p.max_seq_len, p.max_seq_len, p.err, false);
     const int np = L == 0 ? 0 : (L - 1) / p.partition_tokens + 1;
     if (p.skip_single && np <= 1) return;
     uint16_t *out = static_cast<uint16_t *>(p.out) + row * D + lane * V;
     if (np == 0) {
+        if (warp == 0) {
 #pragma unroll
-        for (int k = 0; k < V; ++k) out[k] = 0;
+            for (int k = 0; k < V; ++k) out[k] = 0;
+        }
         return;
     }
     const float *m = p.part_m + row * p.num_partitions;
     const float *l = p.part_l + row * p.num_partitions;
     const float *o = p.part_o + row * p.num_partitions * D + lane * V;
     float M = -INFINITY;
-    for (int k = lane; k < np; k += 32) M = fmaxf(M, m[k]);
+    for (int k = threadIdx.x; k < np; k += W * 32) M = fmaxf(M, __ldcg(m + k));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
+    if (lane == 0) s_max[warp] = M;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, s_max[w]);
+
     float acc[V];
 #pragma unroll
-    for (int k = 0; k < V; ++k) acc[k] = 0.f;
+    for (int x = 0; x < V; ++x) acc[x] = 0.f;
     float lsum = 0.f;
-    for (int k = 0; k < np; ++k) {
-        const float mk = m[k];
-        const float w = (mk == -INFINITY) ? 0.f : l[k] * fast_exp2(mk - M);
-        lsum += w;
-        const float *ok = o + (int64_t)k * D;
+    auto fold = [&](float mk, float lk, const float *v) {
+        const float wk = (mk == -INFINITY) ? 0.f : lk * fast_exp2(mk - M);  // empty partial: 0
+        lsum += wk;
+#pragma unroll
+        for (int x = 0; x < V; ++x) acc[x] += wk * v[x];
+    };
+    auto load_o = [&](int k, float *v) {
+        const float *src = o + (int64_t)k * D;
         if constexpr (V == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(ok);
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
-            acc[2] += w * v.z;
-            acc[3] += w * v.w;
+            const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+            v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
         } else {
-            const float2 v = *reinterpret_cast<const float2 *>(ok);
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
+            const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+            v[0] = t.x; v[1] = t.y;
         }
+    };
+    int k = warp;
+    for (; k + (U - 1) * W < np; k += U * W) {
+        float mk[U], lk[U], v[U][V];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            mk[u] = __ldcg(m + k + u * W);
+            lk[u] = __ldcg(l + k + u * W);
+            load_o(k + u * W, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) fold(mk[u], lk[u], v[u]);
     }
-    const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+    for (; k < np; k += W) {
+        float v[V];
+        load_o(k, v);
+        fold(__ldcg(m + k), __ldcg(l + k), v);
+    }
+#pragma unroll
+    for (int x = 0; x < V; ++x) s_acc[warp][lane * V + x] = acc[x];
+    if (lane == 0) s_l[warp] = lsum;
+    __syncthreads();
+    if (warp != 0) return;
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) tot += s_l[w];
+    const float inv = tot > 0.f ? 1.0f / tot : 0.f;
+    float r[V];
+#pragma unroll
+    for (int x = 0; x < V; ++x) {
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) a += s_acc[w][lane * V + x];
+        r[x] = a * inv;
+    }
     if constexpr (V == 4) {
-        uint2 packed = make_uint2(narrow2<BF16>(acc[0] * inv, acc[1] * inv),
-                                  narrow2<BF16>(acc[2] * inv, acc[3] * inv));
-        *reinterpret_cast<uint2 *>(out) = packed;
+        *reinterpret_cast<uint2 *>(out) =
+            make_uint2(narrow2<BF16>(r[0], r[1]), narrow2<BF16>(r[2], r[3]));
     } else {
-        *reinterpret_cast<uint32_t *>(out) = narrow2<BF16>(acc[0] * inv, acc[1] * inv);
+        *reinterpret_cast<uint32_t *>(out) = narrow2<BF16>(r[0], r[1]);
     }
 }
 
@@ -983,8 +1028,8 @@ static pa_status decode_impl(void *out, const void *q, const void *k_new, const 
     rp.num_partitions = r.NP;
     rp.skip_single = 1;
     const int64_t rows = (int64_t)num_seqs * num_q_heads;
-    const unsigned blocks = (unsigned)((rows + kReduceWarps - 1) / kReduceWarps);
-    if (launch_pdl(pick_reduce(dtype, head_dim), dim3(blocks), dim3(kReduceWarps * 32), 0, s,
+    if (rows > 0x7fffffff) return PA_ERR_INVALID;
+    if (launch_pdl(pick_reduce(dtype, head_dim), dim3((unsigned)rows), dim3(kReduceWarps * 32), 0, s,
                    rp) != cudaSuccess)
         return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -1281,8 +1326,8 @@ pa_status pa_split_kv_reduce(void *out, const void *workspace, size_t workspace_
     rp.num_partitions = NP;
     rp.skip_single = 0;
     const int64_t rows = (int64_t)num_seqs * num_q_heads;
-    const unsigned blocks = (unsigned)((rows + kReduceWarps - 1) / kReduceWarps);
-    pick_reduce(dtype, head_dim)<<<blocks, kReduceWarps * 32, 0, as_stream(stream)>>>(rp);
+    if (rows > 0x7fffffff) return PA_ERR_INVALID;
+    pick_reduce(dtype, head_dim)<<<(unsigned)rows, kReduceWarps * 32, 0, as_stream(stream)>>>(rp);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

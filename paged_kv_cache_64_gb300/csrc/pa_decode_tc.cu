@@ -74,7 +74,12 @@ struct TcShape {
     // cascade tail: the shared prefix's partials merged per head (O, then m, l)
     static constexpr int OFF_PRE = OFF_RED + RED_BYTES;
     static constexpr int PRE_BYTES = kTcG * D * 4 + 2 * kTcG * 4;
-    static constexpr int OFF_BAR = OFF_PRE + PRE_BYTES;
+    // SPAN: a closed partition's per-warp sums and its maxima (m_run,
+    // m_true), kept until its partial is written; two buffers (partition
+    // parity)
+    static constexpr int PEND_FLOATS = 4 * kTcN + 2 * kTcG;
+    static constexpr int OFF_PEND = OFF_PRE + PRE_BYTES;
+    static constexpr int OFF_BAR = OFF_PEND + 2 * PEND_FLOATS * 4;
     static constexpr int OFF_MISC = OFF_BAR + kNumTcBars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
@@ -403,36 +408,61 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
             return true;
         };
 
-        // Partial of partition `slot` from the running state (all 128 threads).
         float *lsum = red + 2 * (4 * kTcN);
-        auto emit_partial = [&](int slot) {
+        float *pend = reinterpret_cast<float *>(smem + S::OFF_PEND);
+        // SPAN: close partition j without waiting for its last P.V: the
+        // per-warp sums and the maxima go to pending buffer j & 1, and the
+        // running state starts afresh (acc still takes the last O).
+        auto close_partition = [&](int j) {
+            float *pb = pend + (j & 1) * S::PEND_FLOATS;
 #pragma unroll
             for (int g = 0; g < kTcG; ++g) {
                 float v = l_part[g];
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
-                if (lane == 0) lsum[sw * kTcN + g] = v;
+                if (lane == 0) pb[sw * kTcN + g] = v;
             }
-            softmax_bar();
+            if (st == 0) {
+#pragma unroll
+                for (int g = 0; g < kTcG; ++g) {
+                    pb[4 * kTcN + g] = m_run[g];
+                    pb[4 * kTcN + kTcG + g] = m_true[g];
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < kTcG; ++g) {
+                m_run[g] = -INFINITY;
+                m_true[g] = -INFINITY;
+                l_part[g] = 0.f;
+            }
+        };
+        // Partial of closed partition j (acc complete), written to slot
+        // part0 + j; its pending buffer was filled before a softmax barrier
+        // that every thread has passed since.
+        auto emit_partial = [&](int j) {
+            const float *pb = pend + (j & 1) * S::PEND_FLOATS;
             if (!failed && r < D) {
 #pragma unroll
                 for (int g = 0; g < kTcG; ++g) {
                     if (g >= G) break;
-                    const float lt =
-                        lsum[g] + lsum[kTcN + g] + lsum[2 * kTcN + g] + lsum[3 * kTcN + g];
-                    const int64_t row = part_row(p, seq, kvh * G + g, slot);
+                    const float lt = pb[g] + pb[kTcN + g] + pb[2 * kTcN + g] + pb[3 * kTcN + g];
+                    const float mr = pb[4 * kTcN + g], mt = pb[4 * kTcN + kTcG + g];
+                    const int64_t row = part_row(p, seq, kvh * G + g, part0 + j);
                     p.part_o[row * D + r] = acc[g] / lt;
                     if (r == 0) {
-                        p.part_m[row] = m_true[g];
-                        p.part_l[row] = lt * fast_exp2(m_run[g] - m_true[g]);
+                        p.part_m[row] = mt;
+                        p.part_l[row] = lt * fast_exp2(mr - mt);
                     }
                 }
             }
         };
 
         // Partition by partition of the CTA's span (one partition without
-        // SPAN): the tiles of partition j, its last O folded in, then (for
-        // all but the last) its partial and a fresh running state.
+        // SPAN).  Partitions but the last are closed at their end; the last
+        // O of partition j is folded in, and its partial written, during
+        // the first tile of partition j+1 (after that tile's P is handed to
+        // the MMA), as any tile's O is during the next tile, so the pipeline
+        // does not drain at partition ends.
         const int nspan = SPAN ? part_end - part0 : 1;
         for (int j = 0; j < nspan; ++j) {
             const int t_lo = SPAN ? j * tpp : 0;
@@ -526,22 +556,22 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
               fence_async_smem();
               __syncwarp();
               if (lane == 0) mbar_arrive(&bar[kPFull0 + b]);
-              if (i > t_lo && !accumulate(i - 1)) failed = true;
+              if (i > t_lo) {
+                  if (!accumulate(i - 1)) failed = true;
+              } else if (SPAN && j > 0) {
+                  // partition j-1: its last O, its partial, a fresh acc
+                  if (!failed && !accumulate(i - 1)) failed = true;
+                  emit_partial(j - 1);
+  #pragma unroll
+                  for (int g = 0; g < kTcG; ++g) acc[g] = 0.f;
+              }
   #pragma unroll
               for (int g = 0; g < kTcG; ++g) alpha_prev[g] = alpha[g];
             }
-            if (!failed && !accumulate(t_hi - 1)) failed = true;
-            if (j + 1 < nspan) {
-                emit_partial(part0 + j);
-#pragma unroll
-                for (int g = 0; g < kTcG; ++g) {
-                    m_run[g] = -INFINITY;
-                    m_true[g] = -INFINITY;
-                    l_part[g] = 0.f;
-                    acc[g] = 0.f;
-                    alpha_prev[g] = 1.f;
-                }
-            }
+            if (SPAN && j + 1 < nspan)
+                close_partition(j);
+            else if (!failed && !accumulate(t_hi - 1))
+                failed = true;
         }
 
         // l over the 128 position-threads, per head
