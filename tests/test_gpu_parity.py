@@ -381,14 +381,21 @@ def test_partitions_match_oracle(name, kw, P):
     api.check_error()
 
 
-@pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_split_reduce_matches_oracle(dtype):
+@pytest.mark.parametrize("dtype,d,P,lens", [
+    ("f16", 128, 64, [0, 1, 64, 65, 200, 448, 129]),
+    ("bf16", 128, 64, [0, 1, 64, 65, 200, 448, 129]),
+    # hundreds of partials a row (313, 1 and 2): the four-at-a-time walk,
+    # its tail, and empty partials inside a row
+    ("bf16", 64, 16, [5000, 16, 17]),
+    ("f16", 128, 32, [2049, 4000, 33, 95]),
+])
+def test_split_reduce_matches_oracle(dtype, d, P, lens):
     """Split-KV step 3 on its own: oracle partials (converted to the
     workspace's fp32 base-2 layout) combined by the kernel against the
     oracle's combine."""
-    rng = np.random.default_rng(5)
-    S, Hq, d, P = 7, 6, 128, 64
-    lens = np.array([0, 1, 64, 65, 200, 448, 129], dtype=np.int32)
+    rng = np.random.default_rng(5 + len(lens))
+    lens = np.array(lens, dtype=np.int32)
+    S, Hq = len(lens), 6
     max_len = int(lens.max())
     NP = api.partition_count(max_len, P)
     m = rng.normal(0, 3, (S, Hq, NP))
@@ -397,6 +404,9 @@ def test_split_reduce_matches_oracle(dtype):
     for i, L in enumerate(lens):
         k = -(-int(L) // P)
         m[i, :, k:], l[i, :, k:], o[i, :, k:] = -np.inf, 0, 0
+        if k > 8:  # a few empty partials inside the row (all positions masked)
+            hole = rng.choice(k - 1, 3, replace=False)
+            m[i, :, hole], l[i, :, hole], o[i, :, hole] = -np.inf, 0, 0
     tdt = workloads.torch_dtype(dtype)
     size = api.workspace_size(S, Hq, 1, d, 16, max_len, P, tdt)
     ws = api.alloc_workspace(size, "cuda")
@@ -409,8 +419,10 @@ def test_split_reduce_matches_oracle(dtype):
     # oracle on the fp32-rounded partials the kernel actually read
     ref = oracle.reduce(gm.double().cpu().numpy() / LOG2E, gl.double().cpu().numpy(),
                         go.double().cpu().numpy())
-    assert torch.all(out[0] == 0)
-    assert_close(out, ref, "reduce")
+    for i, L in enumerate(lens):
+        if L == 0:
+            assert torch.all(out[i] == 0)
+    assert_close(out, ref, f"reduce d={d} P={P}")
     api.check_error()
 
 
