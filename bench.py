@@ -161,57 +161,78 @@ def stored_traffic(workload):
 
 
 # ----------------------------------------------------------------- oracle arm
-def oracle_sample(plan, budget_s, rng_seed=0):
-    """Time the fp64 oracle on as many of the workload's sequences as fit in
-    about budget_s seconds of host time.  Inputs are drawn on the host for
-    the sampled sequences only.  Returns (seconds, algorithmic bytes, tokens,
-    number of sequences, threads)."""
-    import torch
+def _bits16(x, dtype):
+    """float32 array -> uint16 bit patterns of f16 or bf16 (round to nearest
+    even), the host inputs' storage format."""
+    if dtype == "f16":
+        return x.astype(np.float16).view(np.uint16)
+    b = x.view(np.uint32)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
 
-    import oracle
+
+def oracle_inputs(plan, seed=0):
+    """Host inputs of the oracle arm: the plan's layout (the allocator
+    model's), q drawn N(0, 1), and K/V pools filled in every block a sequence
+    uses with N(0, 1) draws, taken as seeded slices of one seeded table of
+    2^24 draws (the oracle's time does not depend on the values; drawing
+    every element afresh would take the host longer than the oracle does).
+    Returns (layout, q, k, v)."""
     from oracle.allocator import BlockAllocatorModel
     from oracle.prefix_cache import PrefixCachePoolModel
     from paged_kv_cache_64_gb300 import workloads
 
     spec = plan.spec
     lay = workloads.layout(plan, PrefixCachePoolModel if plan.apc else BlockAllocatorModel)
+    rng = np.random.default_rng(spec.seed * 7919 + seed)
     B = spec.block_size
     shape = (plan.num_blocks, spec.num_kv_heads, B, spec.head_dim)
+    per_block = spec.num_kv_heads * B * spec.head_dim
     k = np.zeros(shape, dtype=np.uint16)  # pages are only touched where filled
     v = np.zeros(shape, dtype=np.uint16)
-    dt = workloads.torch_dtype(spec.dtype)
-    gen = torch.Generator().manual_seed(spec.seed + rng_seed)
-    q = torch.randn((spec.num_seqs, spec.num_q_heads, spec.head_dim), generator=gen,
-                    dtype=dt).view(torch.int16).numpy().view(np.uint16)
+    q = _bits16(rng.standard_normal((spec.num_seqs, spec.num_q_heads, spec.head_dim),
+                                    dtype=np.float32), spec.dtype)
+    T = 1 << 24
+    table = _bits16(rng.standard_normal(T, dtype=np.float32), spec.dtype)
+    chunk = (T // 2) // per_block  # blocks per slice
+    for s in range(spec.num_seqs):
+        ids = lay.block_tables[s, :-(-int(lay.seq_lens[s]) // B)]
+        for pool in (k, v):
+            for c in range(0, len(ids), chunk):
+                part = ids[c:c + chunk]
+                n = len(part) * per_block
+                off = int(rng.integers(0, T - n))
+                pool[part] = table[off:off + n].reshape((len(part),) + shape[1:])
+    return lay, q, k, v
 
-    def fill(seqs):
-        for s in seqs:
-            nb = -(-int(lay.seq_lens[s]) // B)
-            ids = lay.block_tables[s, :nb]
-            for pool in (k, v):
-                vals = torch.randn((nb,) + shape[1:], generator=gen, dtype=dt)
-                pool[ids] = vals.view(torch.int16).numpy().view(np.uint16)
 
-    order = list(range(spec.num_seqs))
-    done, seconds, nbytes, tokens = [], 0.0, 0, 0
+def oracle_sample(plan, inputs, budget_s, first=0):
+    """Time the fp64 oracle on as many of the workload's sequences as fit in
+    about budget_s seconds of host time, starting at sequence `first` and
+    going round the batch.  Returns (seconds, algorithmic bytes, tokens,
+    number of sequences, threads)."""
+    import oracle
+    from paged_kv_cache_64_gb300 import workloads
+
+    spec = plan.spec
+    lay, q, k, v = inputs
+    S = spec.num_seqs
+    order = [(first + i) % S for i in range(S)]
+    done, seconds, nbytes, tokens = 0, 0.0, 0, 0
     batch = 1
-    filled = set()
     while order and seconds < budget_s:
         take, order = order[:batch], order[batch:]
-        fill([s for s in take if s not in filled])
-        filled.update(take)
         if not order and seconds < 0.6 * budget_s:
-            order = list(range(spec.num_seqs))  # go round the batch again
+            order = list(range(S))  # go round the batch again
         t0 = time.perf_counter()
         oracle.decode(q, k, v, lay.block_tables, lay.seq_lens, plan.scale, spec.dtype, seqs=take)
         dt_s = time.perf_counter() - t0
         seconds += dt_s
-        done += take
+        done += len(take)
         nbytes += workloads.algorithmic_bytes(spec, lay.seq_lens[take])
         tokens += len(take)
         per_seq = dt_s / len(take)
         batch = max(1, min(len(order), int((budget_s - seconds) / max(per_seq, 1e-6) / 2) or 1))
-    return seconds, nbytes, tokens, len(done), oracle.num_threads()
+    return seconds, nbytes, tokens, done, oracle.num_threads()
 
 
 def sample_text(nseq, total):
@@ -226,11 +247,17 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs)
+    inputs = oracle_inputs(plan)
     per_step = []
     info = None
+    # each step a bounded sample: the whole run's oracle time stays near
+    # --ref-total-seconds whatever --steps and --warmup are
+    budget = min(args.ref_step_seconds,
+                 max(0.25, args.ref_total_seconds / (args.warmup + args.steps)))
+    first = 0
     for i in range(args.warmup + args.steps):
-        budget = args.ref_step_seconds
-        secs, nbytes, toks, nseq, threads = oracle_sample(plan, budget, rng_seed=i)
+        secs, nbytes, toks, nseq, threads = oracle_sample(plan, inputs, budget, first)
+        first = (first + nseq) % plan.spec.num_seqs
         if i >= args.warmup:
             per_step.append((secs, nbytes, toks, nseq))
         info = threads
@@ -247,7 +274,8 @@ def run_reference(args, rank, world):
         "config": {"workload": plan.spec.name + ": " + plan.spec.describe,
                    "layers_in_step": layers,
                    "sample": "each step decodes as many of the batch's sequences as fit in "
-                             f"~{args.ref_step_seconds:.0f} s (all heads of each)"},
+                             f"~{budget:.2g} s (all heads of each), the next step going on "
+                             "from there"},
         "tokens_per_s": toks / secs / layers,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": info, "kind": "oracle",
                          "sample": sample_text(per_step[0][3], plan.spec.num_seqs) + " per step"},
@@ -655,7 +683,8 @@ def run_gpu(args, rank, world, local_rank):
                                     "prefix-caching pool (pa_pcache)")
         line["host_allocator"] = host_pool_timing(plan)
     if world == 1 and not args.no_cpu_baseline:
-        secs_c, nbytes_c, toks_c, nseq_c, threads = oracle_sample(plan, args.cpu_seconds)
+        secs_c, nbytes_c, toks_c, nseq_c, threads = oracle_sample(plan, oracle_inputs(plan),
+                                                                  args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": nbytes_c / secs_c / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"fp64 oracle decode of {sample_text(nseq_c, spec.num_seqs)} (all "
@@ -692,7 +721,10 @@ def main(argv=None):
                     help="prefix workload as separate requests laid out by the prefix-caching "
                          "pool (automatic prefix caching) instead of forks")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-step-seconds", type=float, default=8.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=8.0,
+                    help="reference arm: at most this much oracle time a step")
+    ap.add_argument("--ref-total-seconds", type=float, default=120.0,
+                    help="reference arm: about this much oracle time over all steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -63,3 +63,41 @@ def test_reference_arm_runs_on_cpu(capsys):
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_step_budget_shrinks_with_steps(capsys):
+    """The oracle time of the whole reference run stays near
+    --ref-total-seconds: here 7 steps of 0.1 s are raised to the 0.25 s
+    floor."""
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "4", "--warmup", "3",
+                "--ref-total-seconds", "0.7"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert "~0.25 s" in line["config"]["sample"]
+    assert 0 < line["ms_per_step"] < 1000
+
+
+def test_oracle_inputs_fill_every_used_block():
+    """Host inputs of the oracle arm: every block a sequence reaches holds
+    drawn values (no all-zero block), blocks no sequence uses stay zero, and
+    the values look N(0, 1)."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    from paged_kv_cache_64_gb300 import workloads
+    plan = workloads.make_plan("qwen", num_seqs=16)
+    lay, q, k, v = bench.oracle_inputs(plan)
+    B = plan.spec.block_size
+    used = set()
+    for s, L in enumerate(lay.seq_lens):
+        used.update(lay.block_tables[s, :-(-int(L) // B)].tolist())
+    used = np.array(sorted(used))
+    unused = np.setdiff1d(np.arange(plan.num_blocks), used)
+    for pool in (k, v):
+        assert (pool[used].reshape(len(used), -1) != 0).any(axis=1).all()
+        assert not pool[unused[:1000]].any()
+    vals = k[used].view(np.float16).astype(np.float64)  # qwen pools are fp16
+    assert abs(vals.mean()) < 0.01 and abs(vals.std() - 1) < 0.01
+    assert q.shape == (16, 14, 64) and q.dtype == np.uint16
