@@ -824,6 +824,8 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
                          ResolvedDecode *r, bool fp8 = false) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0)
         return PA_ERR_INVALID;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_INVALID;  // grid y and z
+    if ((int64_t)num_seqs * num_q_heads > 0x7fffffff) return PA_ERR_INVALID;  // combine grid
     if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_INVALID;
     if (num_q_heads % num_kv_heads) return PA_ERR_INVALID;
     const int G = num_q_heads / num_kv_heads;
