@@ -391,10 +391,11 @@ class GpuStep:
         return self.spec.num_layers * (self.decode_bytes + self.write_bytes + self.copy_bytes)
 
     def run(self, ev=None, q=None, k_new=None, v_new=None, stream=None, tables=None, lens=None,
-            slots=None, out=None):
-        """One step.  ev: optional list collecting (start, end) events around
-        each decode call.  q .. out: other input and output tensors of the
-        same shapes (the end-to-end run's second buffer set)."""
+            slots=None, out=None, cev=None):
+        """One step.  ev / cev: optional lists collecting (start, end) events
+        around each decode call / each block-copy call.  q .. out: other
+        input and output tensors of the same shapes (the end-to-end run's
+        second buffer set)."""
         api, v = self.api, self.vals
         q = v.q if q is None else q
         tables = self.tables if tables is None else tables
@@ -404,7 +405,14 @@ class GpuStep:
         for layer in range(self.spec.num_layers):
             kp, vp = v.k_pools[layer], v.v_pools[layer]
             if self.copies.numel():
+                if cev is not None:
+                    c0 = self.torch.cuda.Event(enable_timing=True)
+                    c1 = self.torch.cuda.Event(enable_timing=True)
+                    c0.record(stream)
                 api.copy_blocks([kp], [vp], self.copies, stream=stream)
+                if cev is not None:
+                    c1.record(stream)
+                    cev.append((c0, c1))
             if ev is not None:
                 a = self.torch.cuda.Event(enable_timing=True)
                 b = self.torch.cuda.Event(enable_timing=True)
@@ -446,7 +454,8 @@ def run_gpu(args, rank, world, local_rank):
     api.set_decode_impl(args.decode_impl)
     base = workloads.SPECS[args.workload]
     plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs,
-                               seed=base.seed + 1000 * rank if rank else None, apc=args.apc)
+                               seed=base.seed + 1000 * rank if rank else None, apc=args.apc,
+                               cow=args.cow)
     if args.layers:
         plan.spec = dataclasses.replace(plan.spec, num_layers=int(args.layers))
     st = GpuStep(plan, device, args.partition_tokens, cascade=args.cascade, kv=args.kv)
@@ -481,10 +490,11 @@ def run_gpu(args, rank, world, local_rank):
         if graph is not None:
             graph.replay()
         else:
-            st.run(ev)
+            st.run(ev, cev=cev)
 
     # ------------------------------------------------ timed region (device)
     ev = []
+    cev = []  # block-copy launches (copy-on-write workloads)
     step_ev = []
     barrier()
     torch.cuda.synchronize()
@@ -532,8 +542,8 @@ def run_gpu(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     launch_bytes = st.decode_bytes + st.write_bytes  # what one decode_step launch must move
     achieved = launch_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = stored_traffic(args.workload + ("_cascade" if st.prefix_len else "") +
-                             ("_fp8" if st.fp8 else ""))
+    traffic = stored_traffic(args.workload + ("_cow" if args.cow else "") +
+                             ("_cascade" if st.prefix_len else "") + ("_fp8" if st.fp8 else ""))
 
     # ------------------------------------------------ end to end (host buffers)
     # Every step copies its inputs from pinned host memory into device input
@@ -678,6 +688,19 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": st.launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    if cev:
+        copy_s = statistics.mean(a.elapsed_time(b) for a, b in cev) / 1e3
+        per_launch = st.copy_bytes  # K and V blocks read and written, one layer
+        line["copy_blocks"] = {
+            "pairs": int(len(st.lay.pre_copies)), "launches": len(cev),
+            "bytes_per_launch": int(per_launch), "avg_us": 1e6 * copy_s,
+            "achieved_gbs": per_launch / copy_s / 1e9,
+            "note": ("pa_copy_blocks of the layout's copy-on-write pairs (K and V), re-run "
+                     "every step as its timing stand-in, CUDA events")}
+    if args.cow:
+        line["config"]["copy_on_write"] = (
+            "shared prompt of 4,112 positions: its last block half full and shared, so the "
+            "first tail token of 63 of the 64 sequences copies it")
     if plan.apc:
         line["config"]["layout"] = ("separate requests with one prompt, shared by the "
                                     "prefix-caching pool (pa_pcache)")
@@ -717,6 +740,9 @@ def main(argv=None):
     ap.add_argument("--kv", default="16bit", choices=["16bit", "fp8"],
                     help="K/V pool format: the workload's 16-bit type, or E4M3 codes with one "
                          "scale per pool (q and out stay 16-bit)")
+    ap.add_argument("--cow", action="store_true",
+                    help="prefix workload, copy-on-write reading: a 4,112-position shared "
+                         "prompt whose half-full last block is copied 63 times, every step")
     ap.add_argument("--apc", action="store_true",
                     help="prefix workload as separate requests laid out by the prefix-caching "
                          "pool (automatic prefix caching) instead of forks")
@@ -731,6 +757,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.apc and args.workload != "prefix":
         ap.error("--apc applies to the prefix workload")
+    if args.cow and (args.workload != "prefix" or args.apc):
+        ap.error("--cow applies to the prefix workload laid out by forks")
     if args.kv == "fp8" and args.cascade:
         ap.error("--cascade reads 16-bit pools")
     rank, world, local_rank = dist_env()
