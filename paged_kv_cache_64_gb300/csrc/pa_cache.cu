@@ -150,6 +150,8 @@ __global__ void cache_write_fp8_kernel(const uint4 *__restrict__ k_new,
     }
 }
 
+constexpr int kCopyPer = 4;  // 16-byte pieces a thread copies per round
+
 __global__ void copy_blocks_kernel(const PoolPtrs pools, const int64_t *__restrict__ mapping,
                                    int num_blocks, int64_t pieces, int *err) {
     const int pair = blockIdx.y;
@@ -163,9 +165,24 @@ __global__ void copy_blocks_kernel(const PoolPtrs pools, const int64_t *__restri
     uint4 *pool = (blockIdx.z & 1) ? pools.v[layer] : pools.k[layer];
     const uint4 *s = pool + src * pieces;
     uint4 *d = pool + dst * pieces;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < pieces;
-         i += (int64_t)gridDim.x * blockDim.x)
-        d[i] = s[i];
+    // kCopyPer pieces a thread, all loaded before any is stored (the pairs
+    // are independent, so no store of this launch feeds one of its loads):
+    // one memory round trip instead of one per piece
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x * kCopyPer;
+    for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x * kCopyPer + threadIdx.x; i0 < pieces;
+         i0 += stride) {
+        uint4 v[kCopyPer];
+#pragma unroll
+        for (int k = 0; k < kCopyPer; ++k) {
+            const int64_t i = i0 + (int64_t)k * blockDim.x;
+            if (i < pieces) v[k] = s[i];
+        }
+#pragma unroll
+        for (int k = 0; k < kCopyPer; ++k) {
+            const int64_t i = i0 + (int64_t)k * blockDim.x;
+            if (i < pieces) d[i] = v[k];
+        }
+    }
 }
 
 // Waits on a barrier that never completes; the bounded wait must give up.
@@ -275,7 +292,7 @@ pa_status pa_copy_blocks(void *const *k_pools, void *const *v_pools, int num_lay
     if (!err) return PA_ERR_CUDA;
     const int64_t pieces = (int64_t)(block_bytes / 16);
     const int threads = 256;
-    int64_t bx = (pieces + threads * 4 - 1) / (threads * 4);
+    int64_t bx = (pieces + threads * kCopyPer - 1) / (threads * kCopyPer);
     if (bx < 1) bx = 1;
     if (bx > 65535) bx = 65535;
     for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
