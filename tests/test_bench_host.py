@@ -101,3 +101,14 @@ def test_oracle_inputs_fill_every_used_block():
     vals = k[used].view(np.float16).astype(np.float64)  # qwen pools are fp16
     assert abs(vals.mean()) < 0.01 and abs(vals.std() - 1) < 0.01
     assert q.shape == (16, 14, 64) and q.dtype == np.uint16
+
+
+def test_cow_and_apc_arguments_are_checked():
+    """--cow is the prefix workload's copy-on-write reading (forks only)."""
+    sys.path.insert(0, ROOT)
+    import pytest
+    import bench
+    for argv in (["--workload", "llama", "--cow"], ["--workload", "prefix", "--cow", "--apc"],
+                 ["--workload", "qwen", "--apc"], ["--warmup", "2"]):
+        with pytest.raises(SystemExit):
+            bench.main(argv)
