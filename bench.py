@@ -235,6 +235,40 @@ def oracle_sample(plan, inputs, budget_s, first=0):
     return seconds, nbytes, tokens, done, oracle.num_threads()
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def single_thread_gbs(plan, inputs, budget_s):
+    """The oracle on one host thread: GB/s equivalent on a sample of about
+    budget_s seconds (the thread count is restored afterwards)."""
+    import oracle
+    n = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        secs, nbytes, _, _, _ = oracle_sample(plan, inputs, budget_s)
+    finally:
+        oracle.set_num_threads(n)
+    return nbytes / secs / 1e9
+
+
 def sample_text(nseq, total):
     if nseq <= total:
         return f"{nseq} of {total} sequences"
@@ -278,7 +312,8 @@ def run_reference(args, rank, world):
                              "from there"},
         "tokens_per_s": toks / secs / layers,
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": info, "kind": "oracle",
-                         "sample": sample_text(per_step[0][3], plan.spec.num_seqs) + " per step"},
+                         "sample": sample_text(per_step[0][3], plan.spec.num_seqs) + " per step",
+                         "cpu_model": cpu_model()},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -706,12 +741,14 @@ def run_gpu(args, rank, world, local_rank):
                                     "prefix-caching pool (pa_pcache)")
         line["host_allocator"] = host_pool_timing(plan)
     if world == 1 and not args.no_cpu_baseline:
-        secs_c, nbytes_c, toks_c, nseq_c, threads = oracle_sample(plan, oracle_inputs(plan),
-                                                                  args.cpu_seconds)
+        inputs = oracle_inputs(plan)
+        secs_c, nbytes_c, toks_c, nseq_c, threads = oracle_sample(plan, inputs, args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": nbytes_c / secs_c / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"fp64 oracle decode of {sample_text(nseq_c, spec.num_seqs)} (all "
-                      f"heads), {secs_c:.1f} s on host cores"}
+                      f"heads), {secs_c:.1f} s on host cores",
+            "cpu_model": cpu_model(),
+            "single_thread_value": single_thread_gbs(plan, inputs, 3.0)}
     print(json.dumps(line), flush=True)
 
 

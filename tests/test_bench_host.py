@@ -61,7 +61,7 @@ def test_reference_arm_runs_on_cpu(capsys):
                 "--ref-step-seconds", "0.2"])
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cpu_model"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
