@@ -163,7 +163,10 @@ def alloc_workspace(nbytes, device):
 def decode(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale,
            partition_tokens=0, workspace=None, stream=None):
     """Paged decode attention into out [S, Hq, d].  partition_tokens: -1
-    single pass, 0 automatic, >0 split-KV partition size."""
+    single pass, 0 automatic, >0 split-KV partition size.  workspace: a
+    device buffer of at least workspace_size(...) bytes (alloc_workspace);
+    when it is missing or too small one is allocated here, so a decode loop
+    passes its own.  Returns the workspace used."""
     S, hq, hkv, d, nb, bs = _decode_dims(q, k_pool, block_tables, seq_lens)
     if out.shape != q.shape or out.dtype != q.dtype or k_pool.dtype != q.dtype:
         raise ValueError("out/q/pool shapes or types differ")
@@ -185,7 +188,8 @@ def decode_step(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables
                 max_seq_len, scale, partition_tokens=0, workspace=None, stream=None):
     """One fused decode step: write each sequence's newest token (k_new /
     v_new [S, Hkv, d] at slot_mapping [S], the slot of position seq_lens-1)
-    and attend over seq_lens positions, in one launch."""
+    and attend over seq_lens positions, in one launch.  workspace as for
+    decode."""
     S, hq, hkv, d, nb, bs = _decode_dims(q, k_pool, block_tables, seq_lens)
     if out.shape != q.shape or out.dtype != q.dtype or k_pool.dtype != q.dtype:
         raise ValueError("out/q/pool shapes or types differ")
