@@ -79,6 +79,41 @@ def test_quantize_uses_fp32_product():
     assert oracle.e4m3_decode(got)[1] == 1.0       # 3 * fl32(1/3) rounds to 1
 
 
+def test_cache_write_fp8_read_back():
+    """The quantising cache write puts token t's K codes (K scale) and V codes
+    (V scale) at (slot // B, head, slot % B); a negative slot writes nothing;
+    every other byte of the pools is untouched.  Read back through the E4M3
+    definition: |code value * scale - x| stays within half an E4M3 step."""
+    rng = np.random.default_rng(9)
+    NB, H, B, d, T = 6, 2, 16, 64, 5
+    kp = rng.integers(0, 0x7f, (NB, H, B, d), dtype=np.uint8)
+    vp = rng.integers(0, 0x7f, (NB, H, B, d), dtype=np.uint8)
+    k0, v0 = kp.copy(), vp.copy()
+    xk = rng.normal(0, 1, (T, H, d)).astype(np.float32)
+    xv = rng.normal(0, 3, (T, H, d)).astype(np.float32)
+    bf = lambda x: (x.view(np.uint32) >> 16).astype(np.uint16)  # truncation: exact bf16 values
+    kb, vb = bf(xk), bf(xv)
+    slots = np.array([17, 0, -1, 95, 40], dtype=np.int64)
+    ks, vs = 0.0625, 0.5
+    oracle.cache_write_fp8(kp, vp, kb, vb, slots, "bf16", ks, vs)
+    touched = np.zeros((NB, B), bool)
+    for t, slot in enumerate(slots):
+        if slot < 0:
+            continue
+        blk, off = slot // B, slot % B
+        touched[blk, off] = True
+        for pool, x, sc in ((kp, oracle.widen(kb[t], "bf16"), ks), (vp, oracle.widen(vb[t], "bf16"), vs)):
+            got = oracle.e4m3_decode(pool[blk, :, off, :]) * sc
+            # E4M3 has 3 mantissa bits: error <= 2^-4 relative, or half the
+            # subnormal step (2^-10) times the scale near zero
+            assert np.all(np.abs(got - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * sc))
+    for pool, p0 in ((kp, k0), (vp, v0)):
+        mask = np.broadcast_to(touched[:, None, :, None], pool.shape)
+        assert np.array_equal(pool[~mask], p0[~mask])
+    # K and V are not swapped: the V codes carry the V scale
+    assert not np.array_equal(kp[1, :, 1, :], vp[1, :, 1, :])
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_fp8_decode_reduces_to_16bit_decode(dtype):
     """Pools whose values E4M3 and the 16-bit type both hold exactly: the FP8
