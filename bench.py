@@ -521,11 +521,28 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
         api.check_error()
 
-    def one_step(ev=None):
+    def one_step(ev=None, cev=None):
         if graph is not None:
             graph.replay()
         else:
             st.run(ev, cev=cev)
+
+    # The timed region runs the K steps `repeats` times, enough for at least
+    # --min-timed-seconds (so the clock sampler sees the GPU under load for a
+    # while); the count comes from one untimed pass of K steps, the largest
+    # over the ranks so that every rank times the same steps.
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for _ in range(args.steps):
+        if flush is not None:
+            flush.fill_(1)
+        one_step()
+    c1.record()
+    torch.cuda.synchronize()
+    repeats = max(1, int(np.ceil(args.min_timed_seconds * 1e3 / max(c0.elapsed_time(c1), 1e-3))))
+    repeats = int(reduce_over_ranks(float(repeats), 0.0, device)[0])
+    n_timed = repeats * args.steps
 
     # ------------------------------------------------ timed region (device)
     ev = []
@@ -538,26 +555,26 @@ def run_gpu(args, rank, world, local_rank):
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record()
-            for _ in range(args.steps):
-                one_step(ev)
+            for _ in range(n_timed):
+                one_step(ev, cev)
             t1.record()
             torch.cuda.synchronize()
             total_ms = t0.elapsed_time(t1)
         else:
-            for _ in range(args.steps):
+            for _ in range(n_timed):
                 if flush is not None:
                     flush.fill_(1)
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record()
-                one_step(ev)
+                one_step(ev, cev)
                 b.record()
                 step_ev.append((a, b))
             torch.cuda.synchronize()
             total_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     barrier()
     api.check_error()
-    secs, all_bytes = reduce_over_ranks(total_ms / 1e3, st.step_bytes() * args.steps, device)
+    secs, all_bytes = reduce_over_ranks(total_ms / 1e3, st.step_bytes() * n_timed, device)
     value = all_bytes / secs / 1e9
     if ev:
         dec_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
@@ -675,7 +692,8 @@ def run_gpu(args, rank, world, local_rank):
         return
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / n_timed,
+        "repeats": repeats, "timed_steps": n_timed, "timed_seconds": total_ms / 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": (f"e4m3 K/V ({spec.dtype} q/out, f16 products, fp32 accumulate)" if st.fp8
                   else spec.dtype), "data": "synthetic",
@@ -697,7 +715,8 @@ def run_gpu(args, rank, world, local_rank):
             "launch": "CUDA graph replay" if graph is not None else "eager",
             "kv_format": ("E4M3 codes, scale 1/64 per pool, quantised from the same N(0,1) "
                           "values" if st.fp8 else spec.dtype),
-            "decode_kernel": "tensor cores, E4M3 widened to f16 in shared memory" if st.fp8 else
+            "decode_kernel": ("tensor cores (tcgen05 kind::f8f6f4 on the E4M3 codes, q and P as "
+                              "E5M2 terms; at d=64 V widened to f16)") if st.fp8 else
                              ("CUDA cores" if args.decode_impl == "cuda_cores"
                               else "tensor cores (tcgen05)"),
             "l2": ("inputs larger than L2 (%.2f GB per step)" % (st.step_bytes() / 1e9))
@@ -707,7 +726,7 @@ def run_gpu(args, rank, world, local_rank):
         # bytes plain paged decode would read for the same attention, per second
         "logical_gbs": value * (st.logical_bytes + st.write_bytes + st.copy_bytes) /
         (st.decode_bytes + st.write_bytes + st.copy_bytes),
-        "tokens_per_s": spec.num_seqs * world / (secs / args.steps),
+        "tokens_per_s": spec.num_seqs * world / (secs / n_timed),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": kernel_note,
@@ -720,7 +739,7 @@ def run_gpu(args, rank, world, local_rank):
                 "copies": ("pinned host buffers; two device buffer sets (a graph each when "
                            "replayed), copies on side streams overlapping the neighbouring "
                            "steps")},
-        "gpu_launches": st.launches_per_step * args.steps,
+        "gpu_launches": st.launches_per_step * n_timed,
         "clocks": clocks.summary(),
     }
     if cev:
@@ -789,16 +808,25 @@ def main(argv=None):
     ap.add_argument("--ref-total-seconds", type=float, default=120.0,
                     help="reference arm: about this much oracle time over all steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-timed-seconds", type=float, default=2.0,
+                    help="repeat the K timed steps until the timed region lasts at least this "
+                         "long (the count is reported as `repeats`)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+    rank, world, local_rank = dist_env()
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} needs {args.gpus} ranks, one per GPU: launch with "
+                 f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py "
+                 f"--gpus {args.gpus} (this process sees WORLD_SIZE={world})")
     if args.apc and args.workload != "prefix":
         ap.error("--apc applies to the prefix workload")
     if args.cow and (args.workload != "prefix" or args.apc):
         ap.error("--cow applies to the prefix workload laid out by forks")
     if args.kv == "fp8" and args.cascade:
         ap.error("--cascade reads 16-bit pools")
-    rank, world, local_rank = dist_env()
     if world > 1:
         import torch.distributed as dist
         backend = "gloo" if args.impl == "reference" else "nccl"

@@ -229,6 +229,24 @@ pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, const v
                             float scale, int prefix_len, void *workspace, size_t workspace_bytes,
                             pa_dtype dtype, void *stream);
 
+/* ------------------------------------------------------------------------
+ * pa_shared_prefix_len: the prefix_len pa_decode_cascade can be given for a
+ * batch (host-side planning; no device work).  Counts the leading block-table
+ * entries b that every sequence holds in common (block_tables[i][b] ==
+ * block_tables[0][b] for all i: forks of one prompt, [P2] "Sharing a prefix
+ * with copy-on-write"), capped by the shortest sequence's whole blocks
+ * (min seq_lens / block_size) and by max_blocks_per_seq, and writes that
+ * count times block_size to *prefix_len_out.  An empty batch gives 0.
+ *   block_tables: int32 [num_seqs][max_blocks_per_seq], HOST memory;
+ *   seq_lens: int32 [num_seqs], HOST memory; neither is modified.
+ * Errors: PA_ERR_INVALID (nothing written) for num_seqs < 0,
+ * max_blocks_per_seq < 0, block_size < 1, a null prefix_len_out, null
+ * arrays with num_seqs > 0, or a negative length.
+ * ---------------------------------------------------------------------- */
+pa_status pa_shared_prefix_len(const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *seq_lens, int num_seqs, int block_size,
+                               int *prefix_len_out);
+
 /* Bytes of workspace pa_decode_cascade needs for these shapes on the current
  * CUDA device (the prefix chunking follows its SM count); 0 for invalid
  * arguments. */
@@ -376,7 +394,10 @@ pa_status pa_split_kv_reduce(void *out, const void *workspace, size_t workspace_
  *    partition_tokens (fewer partials) or -1 (single pass, no scratch).
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process (as is the error word's, for every entry point): after a
+ *    cudaDeviceReset it would be stale, so resetting a device while this
+ *    library is loaded is not supported.
  *  - Every call on a device shares the one array, and it keeps whatever the
  *    last call left there.  Nothing in it needs to start at zero: every
  *    partial the combine step reads is written earlier in the same call.

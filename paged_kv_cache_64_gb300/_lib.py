@@ -86,6 +86,7 @@ SIGNATURES = {
     "pa_decode_static_scratch": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _vp, _c_int,
                                           _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int,
                                           _c_int, _vp]),
+    "pa_shared_prefix_len": (_c_int, [_i32p, _c_int, _i32p, _c_int, _c_int, _intp]),
     "pa_check_error": (_c_int, [_vp]),
     "pa_selftest_wait_timeout": (_c_int, [_vp]),
     "pa_alloc_create": (_c_int, [_c_int, _c_int, _i32p, ctypes.POINTER(_vp)]),

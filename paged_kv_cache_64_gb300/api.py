@@ -214,15 +214,19 @@ def decode_step(out, q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables
 def shared_prefix_len(block_tables, seq_lens, block_size):
     """Longest whole-block prefix that every sequence reaches through the
     same block-table entries (host arrays), capped by the shortest sequence:
-    the prefix_len decode_cascade can be given for this batch."""
-    t = np.asarray(block_tables)
-    lens = np.asarray(seq_lens)
-    if t.shape[0] == 0:
-        return 0
-    nb = int(lens.min()) // block_size
-    same = np.all(t[:, :nb] == t[:1, :nb], axis=0)
-    n = nb if same.all() else int(np.argmin(same))
-    return n * block_size
+    the prefix_len decode_cascade can be given for this batch
+    (pa_shared_prefix_len)."""
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    if t.ndim != 2 or lens.shape != (t.shape[0],):
+        raise ValueError("block_tables must be [S, max_blocks], seq_lens [S]")
+    out = ctypes.c_int(0)
+    rc = _lib.load().pa_shared_prefix_len(
+        t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), t.shape[1],
+        lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), t.shape[0], int(block_size),
+        ctypes.byref(out))
+    _lib.check("pa_shared_prefix_len", rc)
+    return out.value
 
 
 def cache_write_fp8(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale, v_scale, stream=None):

@@ -1,8 +1,9 @@
 """Build the CUDA library libpa.so (sm_103a) in-tree.
 
-Three translation units are compiled in parallel (nvcc for the two .cu files,
-g++ for the host allocator) and linked by nvcc into
-paged_kv_cache_64_gb300/_build/libpa.so.  The CUDA runtime is linked
+Every translation unit under csrc/ is compiled in parallel (nvcc for the .cu
+files: decode, tensor-core decode, E4M3 decode, cascade, cache write and block
+copy; g++ for the .cpp files: the block allocator and the prefix-caching
+pool) and linked by nvcc into paged_kv_cache_64_gb300/_build/libpa.so.  The CUDA runtime is linked
 statically, so the library only needs the driver at run time.
 """
 import os

@@ -13,6 +13,7 @@
 // Data layout: the free list is a ring buffer of block ids (FIFO); tables are
 // std::vector<int32_t> keyed by a 64-bit sequence id.  Every operation checks
 // first and then mutates, so a failing call changes nothing.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -213,6 +214,36 @@ pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n_ou
 int pa_block_refcount(const pa_alloc *a, int block) {
     if (!a || block < 0 || block >= a->num_blocks) return -1;
     return a->refs[block];
+}
+
+// Whole blocks every sequence reaches through the same table entries (the
+// cascade's shared prefix), capped by the shortest sequence.
+pa_status pa_shared_prefix_len(const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *seq_lens, int num_seqs, int block_size,
+                               int *prefix_len_out) {
+    if (num_seqs < 0 || max_blocks_per_seq < 0 || block_size < 1 || !prefix_len_out)
+        return PA_ERR_INVALID;
+    if (num_seqs == 0) {
+        *prefix_len_out = 0;
+        return PA_OK;
+    }
+    if (!block_tables || !seq_lens) return PA_ERR_INVALID;
+    int min_len = seq_lens[0];
+    for (int i = 0; i < num_seqs; ++i) {
+        if (seq_lens[i] < 0) return PA_ERR_INVALID;
+        min_len = seq_lens[i] < min_len ? seq_lens[i] : min_len;
+    }
+    const int nb = std::min(min_len / block_size, max_blocks_per_seq);
+    int n = 0;
+    for (; n < nb; ++n) {
+        const int32_t b0 = block_tables[n];
+        bool same = true;
+        for (int i = 1; i < num_seqs && same; ++i)
+            same = block_tables[(int64_t)i * max_blocks_per_seq + n] == b0;
+        if (!same) break;
+    }
+    *prefix_len_out = n * block_size;
+    return PA_OK;
 }
 
 }  // extern "C"

@@ -9,26 +9,30 @@
 // describes the products, the roles and the online softmax), with half the
 // K/V bytes moved.  Per tile of 128 positions:
 //
-//   S^T[128 pos x N] = K_codes[128 x d] . Qs^T[d x N]       kind::f8f6f4, E4M3 x E4M3
-//   d = 128: O^T[128 x N] = V_codes^T[128 x 128 pos] . Ps^T  kind::f8f6f4, E4M3 x E4M3
+//   S^T[128 pos x N] = K_codes[128 x d] . Qs^T[d x N]       kind::f8f6f4, E4M3 x E5M2
+//   d = 128: O^T[128 x N] = V_codes^T[128 x 128 pos] . Ps^T  kind::f8f6f4, E4M3 x E5M2
 //   d = 64:  O^T[128 x 16] = V16^T[128 x 128 pos] . P16^T    kind::f16 (rows 64.. zero)
 //
-// with N = 16 for groups of up to 4 query heads, 32 for up to 8 (three
-// E4M3 terms a head, zero-padded).
+// with N = 16 for groups of up to 4 query heads, 32 for up to 8 (four E5M2
+// terms a head).
 // q.K^T reads the E4M3 K tile exactly as the TMA copy lands it (K-major,
 // swizzled), so K is never converted.  Its other operand, Qs, holds each query
-// head as three E4M3 terms: with 2^e_g the power of two that brings head g's
-// largest |q| into [128, 256), q_g * 2^e_g = t1 + t2 + t3, t1 the nearest
-// E4M3 value, t2 that of the remainder, t3 that of the next remainder (each
-// remainder is exact in fp32).  A 16-bit q has at most 11 significant bits
-// and the three terms carry 12, so the sum equals q * 2^e_g except for
-// elements below 2^-17 of the head's largest (E4M3's subnormal floor), and
-// the three S columns of a head add up, times 2^-e_g, to q.K^T within fp32
-// rounding.
+// head as four E5M2 terms: with 2^e_g the power of two that brings head g's
+// largest |q| into [2^14, 2^15), q_g * 2^e_g = t1 + t2 + t3 + t4, t1 the
+// nearest E5M2 value, t2 that of the remainder, and so on (each remainder is
+// exact in fp32).  A 16-bit q has at most 11 significant bits and the four
+// terms carry 12, so the sum equals q * 2^e_g except for the part of an
+// element below E5M2's subnormal quantum 2^-16 (under 2^-31 of the head's
+// largest), and the four S columns of a head add up, times 2^-e_g, to q.K^T
+// within fp32 rounding.  E5M2 rather than E4M3 terms: the same bits per term
+// but a floor 2^14 times lower, so a q row whose elements span more than
+// 2^17 keeps its small elements (three E4M3 terms lose everything under
+// 2^-17 of the largest, which moves scores measurably when those elements
+// meet large keys).
 // At d = 128 P.V reads V the same way: the staged V tile (128-byte swizzle)
-// is V^T as an MN-major operand, and P is split like q (Ps: three E4M3 terms
+// is V^T as an MN-major operand, and P is split like q (Ps: four E5M2 terms
 // per head of P times 2^k, the power of two that brings the tile's largest P
-// into [128, 256), rounded to f16 first; the tile's O is scaled back by
+// into [2^14, 2^15), rounded to f16 first; the tile's O is scaled back by
 // 2^-k), so nothing is converted and the tensor cores run 8 instructions a
 // tile.  Stale V rows of the last tile are zeroed in the staged tile before
 // P.V (0 * NaN would poison the product).  At d = 64 a V row is 64 bytes,
@@ -88,13 +92,15 @@ enum F8Bar {
 template <int D, int GM>
 struct F8Shape {
     // d = 128: P.V on E4M3 codes too (V^T straight from the staged tile, P as
-    // three E4M3 terms); d = 64: V widened to f16 by converter warps
+    // four E5M2 terms); d = 64: V widened to f16 by converter warps
     static constexpr bool DIRECT = D == 128;
-    // GM (4 or 8): the heads a KV head's group may have.  E4M3 operands hold
-    // three terms per head in rows t * GM + g, zero-padded to QN rows (the
-    // MMA N).  TMEM: S of each softmax group at 0 and QN, O of tile t at
+    // GM (4 or 8): the heads a KV head's group may have.  The E5M2 operands
+    // hold four terms per head in rows t * GM + g: QN rows (the MMA N).
+    // TMEM: S of each softmax group at 0 and QN, O of tile t at
     // 2 * QN + QN * (2 * (t & 1) + ((t >> 1) & 1)) (two per group).
-    static constexpr int QN = (3 * GM + 15) / 16 * 16;
+    static constexpr int NTERM = 4;  // E5M2 terms of a q or P value
+    static constexpr int QN = NTERM * GM;
+    static_assert(QN == 16 || QN == 32, "MMA N");
     static constexpr int S0 = 0, O0 = 2 * QN;
     static constexpr int COLS = 6 * QN <= 128 ? 128 : 256;
     // d = 128: producer K, even tiles' issuer, 8 softmax, producer V, odd
@@ -106,10 +112,10 @@ struct F8Shape {
     static constexpr int SLAB = kF8Tile * 128;        // one 64-dim f16 slab of a tile: 16 KiB
     static constexpr int V_BYTES = 2 * SLAB;          // V^T is M = 128 dims; d = 64 pads with zeros
     static constexpr int STG_BYTES = kF8Tile * D;     // E4M3 tile of K (or V): 128 rows of d bytes
-    // K tiles and Qs: K-major E4M3 operands of d-byte rows, in atoms of 8 rows
+    // K tiles and Qs: K-major 8-bit operands of d-byte rows, in atoms of 8 rows
     // (128-byte swizzle for d = 128, 64-byte for d = 64)
     static constexpr int Q_BYTES = QN * D;
-    // P^T: 16 rows of 128 f16 positions, or 32 rows of 128 E4M3 positions
+    // P^T: 16 rows of 128 f16 positions, or up to 32 rows of 128 E5M2 positions
     static constexpr int P_BYTES = 4096;
     // Staging rings of E4M3 tiles: a K slot is free once q.K^T has read it,
     // a V slot only once P.V (d = 128) or the converters (d = 64) have, so
@@ -158,11 +164,26 @@ __device__ __forceinline__ uint64_t e4m3_operand_desc(uint32_t saddr) {
     return D == 128 ? sw128_desc(saddr, 16, 8 * D) : sw64_desc(saddr, 16, 8 * D);
 }
 
-// Two f16 values (low half first) to two E4M3 codes (low byte first),
-// nearest with ties to even, saturating (PTX cvt.rn.satfinite.e4m3x2.f16x2).
-__device__ __forceinline__ uint32_t e4m3x2_from_f16x2(uint32_t h) {
+// Two fp32 values to two E5M2 codes (the first in the low byte), nearest
+// with ties to even, saturating at +-57344 (PTX cvt.rn.satfinite.e5m2x2.f32).
+__device__ __forceinline__ uint32_t e5m2x2_from_f32(float lo, float hi) {
     uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The same from two f16 values (low half first; PTX cvt.rn.satfinite.e5m2x2.f16x2).
+__device__ __forceinline__ uint32_t e5m2x2_from_f16x2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e5m2x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    return r;
+}
+
+// Two E5M2 codes (low byte first) to two f16 values, exactly (PTX
+// cvt.rn.f16x2.e5m2x2: every E5M2 value is an f16 value).
+__device__ __forceinline__ uint32_t f16x2_from_e5m2x2(uint16_t c) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(c));
     return r;
 }
 
@@ -176,9 +197,9 @@ __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
 // 2^e for e in [-126, 127], exactly.
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
-// E4M3 code (low byte) back to fp32, exactly.
-__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t codes) {
-    const uint32_t h = f16x2_from_e4m3x2((uint16_t)codes);
+// Two E5M2 codes (low byte first) back to fp32, exactly.
+__device__ __forceinline__ float2 e5m2x2_to_f32(uint32_t codes) {
+    const uint32_t h = f16x2_from_e5m2x2((uint16_t)codes);
     __half2 hh;
     memcpy(&hh, &h, 4);
     return __half22float2(hh);
@@ -333,16 +354,7 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
         tmem_alloc(tmem_slot, S::COLS);
         tmem_relinquish();
     }
-    if constexpr (S::DIRECT) {
-        // rows 3 * GM .. QN-1 of the four E4M3 P^T buffers (whole 128-byte
-        // rows, contiguous): zero once, never written again
-        constexpr int Z0 = (3 * GM / 8) * 1024 + (3 * GM % 8) * 128, ZN = (S::QN * 128 - Z0) / 16;
-        for (int i = threadIdx.x; i < 4 * ZN; i += S::THREADS) {
-            uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_P + (i / ZN) * S::P_BYTES + Z0);
-            z[i % ZN] = make_uint4(0, 0, 0, 0);
-        }
-        fence_async_smem();
-    } else {
+    if constexpr (!S::DIRECT) {
         // rows 64..127 of both V^T operand buffers: zero once, never written again
         for (int vb = 0; vb < S::NVB; ++vb) {
             uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_V + vb * S::V_BYTES + S::SLAB);
@@ -478,9 +490,9 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
         // (d = 128: warp 1 for the even tiles and warp kF8Issuer1 for the odd
         // ones; d = 64: every MMA from warp 1)
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = e4m3_idesc(kF8Tile, S::QN, false);
+            constexpr uint32_t idesc_qk = e4m3_e5m2_idesc(kF8Tile, S::QN, false);
             constexpr uint32_t idesc_pv = f16_idesc(false, true, false, 128, kF8N);
-            constexpr uint32_t idesc_pv8 = e4m3_idesc(128, S::QN, true);  // V^T MN-major
+            constexpr uint32_t idesc_pv8 = e4m3_e5m2_idesc(128, S::QN, true);  // V^T MN-major
             const uint32_t sbase = smem_addr(smem);
             // q.K^T of tile t (its K landed, its S buffer read by the softmax)
             auto issue_qk = [&](int t) -> bool {
@@ -590,9 +602,9 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
         float *xch = reinterpret_cast<float *>(smem + S::OFF_XCH);
 
         if (grp == 0) {
-            // Qs: head g's q times 2^e_g as three E4M3 terms in rows g, GM + g
-            // and 2 GM + g of a QN-row K-major operand (the rows of absent
-            // heads and rows 3 GM.. zero).  Thread (g, j) takes EPT elements.
+            // Qs: head g's q times 2^e_g as four E5M2 terms in rows t * GM + g
+            // (t = 0..3) of a QN-row K-major operand (the rows of absent heads
+            // zero).  Thread (g, j) takes EPT elements.
             constexpr int TPH = 128 / GM, EPT = D / TPH;  // threads per head, elements each
             const int g = st / TPH, j = st % TPH;
             float x[EPT];
@@ -624,42 +636,41 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
 #pragma unroll
             for (int off = TPH / 2; off >= 1; off >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
-            // 2^e_g brings amax into [128, 256): e_g = 7 - floor(log2 amax)
+            // 2^e_g brings amax into [2^14, 2^15): e_g = 14 - floor(log2 amax)
             int eg = 0;
             if (amax > 0.f) {
                 const int ex = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
-                eg = 7 - (ex < -126 ? -126 : ex);
+                eg = 14 - (ex < -126 ? -126 : ex);
                 eg = eg < -120 ? -120 : (eg > 120 ? 120 : eg);
             }
             const float up = exp2i(eg);
-            uint32_t code[3][(EPT + 3) / 4];  // EPT codes per term, 4 per word
+            uint32_t code[S::NTERM][(EPT + 3) / 4];  // EPT codes per term, 4 per word
 #pragma unroll
-            for (int t = 0; t < 3; ++t)
+            for (int t = 0; t < S::NTERM; ++t)
 #pragma unroll
                 for (int w4 = 0; w4 < (EPT + 3) / 4; ++w4) code[t][w4] = 0u;
 #pragma unroll
             for (int e2 = 0; e2 < EPT / 2; ++e2) {  // element pairs
                 float a = x[2 * e2] * up, b = x[2 * e2 + 1] * up;
 #pragma unroll
-                for (int t = 0; t < 3; ++t) {
-                    const uint32_t c = e4m3x2_from_f32(a, b);
-                    const float2 back = e4m3x2_to_f32(c);
+                for (int t = 0; t < S::NTERM; ++t) {
+                    const uint32_t c = e5m2x2_from_f32(a, b);
+                    const float2 back = e5m2x2_to_f32(c);
                     a -= back.x;  // exact: the remainder is representable
                     b -= back.y;
                     code[t][e2 >> 1] |= c << (16 * (e2 & 1));
                 }
             }
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {  // term rows, then a zero row (3 GM + g)
+            for (int t = 0; t < S::NTERM; ++t) {
                 const int row = GM * t + g;
                 uint8_t *dst = smem + S::OFF_Q + e4m3_operand_offset<D>(row, j * EPT);
                 if constexpr (EPT == 8) {
-                    *reinterpret_cast<uint2 *>(dst) =
-                        t < 3 ? make_uint2(code[t][0], code[t][1]) : make_uint2(0u, 0u);
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(code[t][0], code[t][1]);
                 } else if constexpr (EPT == 4) {
-                    *reinterpret_cast<uint32_t *>(dst) = t < 3 ? code[t][0] : 0u;
+                    *reinterpret_cast<uint32_t *>(dst) = code[t][0];
                 } else {
-                    *reinterpret_cast<uint16_t *>(dst) = (uint16_t)(t < 3 ? code[t][0] : 0u);
+                    *reinterpret_cast<uint16_t *>(dst) = (uint16_t)code[t][0];
                 }
             }
             if (j == 0) qmul[g] = g < G ? p.scale_log2 * exp2i(-eg) : 0.f;
@@ -694,13 +705,15 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
             float o[16];
             tmem_load16(tmem + lane_addr + S::O0 + S::QN * ob, o);
             if constexpr (S::DIRECT) {
-                // a head's three P terms are three columns: add them, undo the
+                // a head's four P terms are four columns: add them, undo the
                 // tile's power-of-two P scale
-                float o3[8];
-                if constexpr (GM == 8) tmem_load8(tmem + lane_addr + S::O0 + S::QN * ob + 16, o3);
+                float o34[16];
+                if constexpr (GM == 8) tmem_load16(tmem + lane_addr + S::O0 + S::QN * ob + 16, o34);
 #pragma unroll
                 for (int g = 0; g < GM; ++g)
-                    o[g] = ((o[g] + o[GM + g]) + (GM == 8 ? o3[g] : o[2 * GM + g])) * kinv_prev[g];
+                    o[g] = (GM == 8 ? (o[g] + o[GM + g]) + (o34[g] + o34[GM + g])
+                                    : (o[g] + o[GM + g]) + (o[2 * GM + g] + o[3 * GM + g])) *
+                           kinv_prev[g];
             }
             tc_fence_before();
             __syncwarp();
@@ -724,15 +737,16 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
               float s[GM];
               if (ok) {
                   tc_fence_after();
-                  float t12[16], t3[8];
+                  float t12[16], t34[16];
                   tmem_load16(tmem + lane_addr + S::S0 + S::QN * grp, t12);
-                  if constexpr (GM == 8) tmem_load8(tmem + lane_addr + S::S0 + S::QN * grp + 16, t3);
+                  if constexpr (GM == 8) tmem_load16(tmem + lane_addr + S::S0 + S::QN * grp + 16, t34);
                   tc_fence_before();
                   __syncwarp();
                   if (lane == 0) mbar_arrive(&bar[kSEmpty0 + grp]);
   #pragma unroll
                   for (int g = 0; g < GM; ++g)
-                      s[g] = (t12[g] + t12[GM + g]) + (GM == 8 ? t3[g] : t12[2 * GM + g]);
+                      s[g] = GM == 8 ? (t12[g] + t12[GM + g]) + (t34[g] + t34[GM + g])
+                                     : (t12[g] + t12[GM + g]) + (t12[2 * GM + g] + t12[3 * GM + g]);
               } else {
   #pragma unroll
                   for (int g = 0; g < GM; ++g) s[g] = 0.f;
@@ -800,10 +814,11 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
                   }
                   m_true[g] = fmaxf(m_true[g], mx[g]);
               }
-              // E4M3 P: each head's P is taken times 2^k, the power of two that
-              // brings the tile's largest P into [128, 256), so that its three
-              // E4M3 terms keep 12 bits of every value down to 2^-17 of that
-              // largest (the sum l keeps the unscaled values)
+              // E5M2 P: each head's P is taken times 2^k, the power of two that
+              // brings the tile's largest P into [2^14, 2^15), so that its four
+              // E5M2 terms keep 12 bits of every value down to 2^-21 of that
+              // largest, and lose less than 2^-31 of it below (the sum l keeps
+              // the unscaled values)
               float pv[GM], kinv[GM];
   #pragma unroll
               for (int g = 0; g < GM; ++g) {
@@ -816,11 +831,11 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
                           const float dm = mx[g] - m_run[g];  // <= lazy-rescale threshold
                           int k = 0;
                           if (dm > -INFINITY) {
-                              k = 7 - __float2int_rd(dm);
+                              k = 14 - __float2int_rd(dm);
                               k = k > 126 ? 126 : k;
                           }
                           kinv[g] = exp2i(-k);
-                          pg *= exp2i(k);  // exact: a power of two, k >= -1
+                          pg *= exp2i(k);  // exact: a power of two, k >= 6
                       }
                       pv[g] = pg;
                   }
@@ -829,18 +844,18 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
               // group accumulated (after waiting for it) two tiles ago
               uint8_t *pbuf = smem + S::OFF_P + (2 * grp + ((i >> 1) & 1)) * S::P_BYTES;
               if constexpr (S::DIRECT) {
-                  // P^T as three E4M3 terms of P rounded to f16 (11 significant
-                  // bits: the terms hold it exactly down to E4M3's subnormal
-                  // floor), split in packed f16 pairs: rows t*8 + g (t = term,
+                  // P^T as four E5M2 terms of P rounded to f16 (11 significant
+                  // bits: the terms hold it exactly down to E5M2's subnormal
+                  // range), split in packed f16 pairs: rows t*GM + g (t = term,
                   // g = head), 128 positions of one byte, K-major with 128-byte
                   // swizzle
   #pragma unroll
                   for (int g = 0; g < GM; g += 2) {
                       uint32_t h = narrow2<false>(pv[g], pv[g + 1]);
   #pragma unroll
-                      for (int t = 0; t < 3; ++t) {
-                          const uint32_t c = e4m3x2_from_f16x2(h);
-                          h = hsub2_bits(h, f16x2_from_e4m3x2((uint16_t)c));  // exact
+                      for (int t = 0; t < S::NTERM; ++t) {
+                          const uint32_t c = e5m2x2_from_f16x2(h);
+                          h = hsub2_bits(h, f16x2_from_e5m2x2((uint16_t)c));  // exact
                           pbuf[e4m3_operand_offset<128>(GM * t + g, r)] = (uint8_t)(c & 0xffu);
                           pbuf[e4m3_operand_offset<128>(GM * t + g + 1, r)] = (uint8_t)(c >> 8);
                       }

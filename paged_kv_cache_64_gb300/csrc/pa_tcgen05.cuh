@@ -134,10 +134,12 @@ __host__ __device__ constexpr uint32_t f16_idesc(bool bf16, bool a_mn, bool b_mn
            ((uint32_t)(M >> 4) << 24);
 }
 
-// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0
-// in both fields), f32 accumulator, B K-major, A K-major or MN-major.
-__host__ __device__ constexpr uint32_t e4m3_idesc(int M, int N, bool a_mn) {
-    return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) |
+// Instruction descriptor of kind::f8f6f4 with an E4M3 A (format code 0 in
+// bits 7-9) and an E5M2 B (format code 1 in bits 10-12; the kind takes the
+// two operand formats independently), f32 accumulator, B K-major, A K-major
+// or MN-major.
+__host__ __device__ constexpr uint32_t e4m3_e5m2_idesc(int M, int N, bool a_mn) {
+    return (1u << 4) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
 

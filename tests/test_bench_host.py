@@ -104,11 +104,14 @@ def test_oracle_inputs_fill_every_used_block():
 
 
 def test_cow_and_apc_arguments_are_checked():
-    """--cow is the prefix workload's copy-on-write reading (forks only)."""
+    """--cow is the prefix workload's copy-on-write reading (forks only);
+    --gpus N must match the ranks the launcher started (one process here)."""
     sys.path.insert(0, ROOT)
     import pytest
     import bench
+    assert "WORLD_SIZE" not in os.environ
     for argv in (["--workload", "llama", "--cow"], ["--workload", "prefix", "--cow", "--apc"],
-                 ["--workload", "qwen", "--apc"], ["--warmup", "2"]):
+                 ["--workload", "qwen", "--apc"], ["--warmup", "2"], ["--gpus", "2"],
+                 ["--impl", "reference", "--gpus", "4"], ["--steps", "0"]):
         with pytest.raises(SystemExit):
             bench.main(argv)

@@ -280,6 +280,28 @@ def test_shared_prefix_len():
         assert api.shared_prefix_len(lay.block_tables, lay.seq_lens, 32) == 4096
 
 
+def test_shared_prefix_len_brute_force_and_errors():
+    """pa_shared_prefix_len against a direct count on random tables; bad
+    arguments are refused."""
+    rng = np.random.default_rng(3)
+    for _ in range(300):
+        S, nb, B = int(rng.integers(1, 6)), int(rng.integers(0, 9)), int(rng.choice([1, 4, 16]))
+        t = rng.integers(0, 4, (S, nb)).astype(np.int32)
+        share = int(rng.integers(0, nb + 1))
+        t[:, :share] = t[0, :share]
+        lens = rng.integers(0, nb * B + 3, S)
+        want = 0
+        while (want < min(int(lens.min()) // B, nb)
+               and all(t[i, want] == t[0, want] for i in range(S))):
+            want += 1
+        assert api.shared_prefix_len(t, lens, B) == want * B
+    t = np.zeros((2, 3), np.int32)
+    for lens, B in (([5, -1], 16), ([5, 5], 0)):
+        with pytest.raises(_lib.PagedAttentionError) as e:
+            api.shared_prefix_len(t, lens, B)
+        assert e.value.code == 1
+
+
 def test_prefix_caching_layout_agrees(lib):
     """The prefix workload as 64 separate requests laid out by the
     prefix-caching pool: native pool and model agree, and the prompt's 128

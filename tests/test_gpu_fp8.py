@@ -34,16 +34,28 @@ def np_codes(t):
     return t.cpu().numpy().astype(np.uint8)
 
 
-class Fp8Case:
-    """A workload's layout with E4M3 pools of random codes."""
+# Every finite E4M3 code: 0x00..0x7E and 0x80..0xFE (0x7F and 0xFF are NaN):
+# zeros, the subnormals 0x01..0x07 (2^-9 .. 7 * 2^-9), normals up to 0x7E = 448.
+FINITE_CODES = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
 
-    def __init__(self, name, seed=0, plan=None, **kw):
+
+def full_range_codes(shape, seed):
+    """Codes drawn uniformly from every finite E4M3 code."""
+    rng = np.random.default_rng(seed)
+    return torch.as_tensor(rng.choice(FINITE_CODES, shape), device="cuda")
+
+
+class Fp8Case:
+    """A workload's layout with E4M3 pools of random codes.  `codes(shape,
+    seed)` draws the pools' codes; `scales` are (k_scale, v_scale)."""
+
+    def __init__(self, name, seed=0, plan=None, codes=codes_like, scales=(1.0 / 16, 0.37), **kw):
         self.plan = plan if plan is not None else workloads.make_plan(name, **kw)
         self.spec = spec = self.plan.spec
         self.lay = workloads.layout(self.plan, workloads.native_allocator(self.plan))
         shape = (self.plan.num_blocks, spec.num_kv_heads, spec.block_size, spec.head_dim)
-        self.kp = codes_like(shape, 100 + seed)
-        self.vp = codes_like(shape, 200 + seed)
+        self.kp = codes(shape, 100 + seed)
+        self.vp = codes(shape, 200 + seed)
         dt = workloads.torch_dtype(spec.dtype)
         self.q = workloads.normal((spec.num_seqs, spec.num_q_heads, spec.head_dim), dt, "cuda", 300 + seed)
         self.k_new = workloads.normal((spec.num_seqs, spec.num_kv_heads, spec.head_dim), dt, "cuda", 400 + seed)
@@ -52,7 +64,7 @@ class Fp8Case:
         self.lens = torch.as_tensor(self.lay.seq_lens, device="cuda")
         self.slots = torch.as_tensor(self.lay.slot_mapping, device="cuda")
         self.max_seq_len = int(self.lay.max_seq_len)
-        self.k_scale, self.v_scale = 1.0 / 16, 0.37
+        self.k_scale, self.v_scale = scales
 
     def gpu(self, partition=0, step=False, workspace=None):
         out = torch.full_like(self.q, float("nan"))
@@ -242,3 +254,147 @@ def test_decode_fp8_partitions_per_cta_stale_slots_poisoned(span):
     out = c.gpu(256)
     assert torch.isfinite(out).all()
     assert_close(out, c.oracle(kc, vc), "fp8 span poison")
+
+
+# ------------------------------------------- the whole E4M3 format
+# Pools of codes drawn from every finite E4M3 code (subnormals, zeros, +-448)
+# with the scales a cache of values up to about 7 in magnitude would use
+# (amax / 448 = 1/64), through single pass, the fused combine, the combine
+# kernel, several partitions a CTA and the fused cache write; head dims 64 and
+# 128, groups padded to 4 and to 8 query heads.
+FULL_SCALES = (1.0 / 64, 1.0 / 64)
+# (q heads, KV heads, head_dim, block_size, dtype): G = 4 and 8 at d = 64 and 128
+FULL_SHAPES = {
+    "g4_d64": (16, 4, 64, 16, "f16"),
+    "g8_d64": (16, 2, 64, 32, "bf16"),
+    "g4_d128": (8, 2, 128, 16, "bf16"),
+    "g8_d128": (16, 2, 128, 16, "f16"),
+}
+
+
+def full_plan(name, seed=0, lens=(0, 1500), num_seqs=5):
+    hq, hkv, d, B, dt = FULL_SHAPES[name]
+    return workloads.make_shape_plan(num_seqs, hq, hkv, d, B, dt, lens, seed=41 + seed)
+
+
+def used_codes(c):
+    """The set of codes the sequences' valid positions hold (K and V)."""
+    B = c.spec.block_size
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    seen = set()
+    for s, L in enumerate(c.lay.seq_lens):
+        for p in range(int(L)):
+            blk = c.lay.block_tables[s, p // B]
+            seen.update(np.unique(kc[blk, :, p % B]).tolist())
+            seen.update(np.unique(vc[blk, :, p % B]).tolist())
+    return seen
+
+
+@pytest.mark.parametrize("name", sorted(FULL_SHAPES))
+@pytest.mark.parametrize("partition,fused,R", [
+    (-1, False, 1),    # single pass
+    (512, True, 1),    # fused cache write, partials combined inside the launch
+    (128, False, 1),   # > 8 partitions: the combine kernel
+    (256, False, 2),   # two partitions a CTA
+])
+def test_decode_fp8_every_finite_code(span, name, partition, fused, R):
+    span(R)
+    c = Fp8Case("shape", seed=1, plan=full_plan(name), codes=full_range_codes, scales=FULL_SCALES)
+    assert used_codes(c) >= set(FINITE_CODES.tolist())  # every finite code is read
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    out = c.gpu(partition, step=fused)
+    api.check_error()
+    assert_close(out, c.oracle(kc, vc, step=fused), f"fp8 all codes {name} P={partition} R={R}")
+
+
+def log_uniform_q(shape, dtype, seed, span_log2=25):
+    """Random signs, magnitudes 2^U(-22, 3): a row spans about 2^25."""
+    rng = np.random.default_rng(seed)
+    x = rng.choice([-1.0, 1.0], shape) * 2.0 ** rng.uniform(-22, 3, shape)
+    return torch.as_tensor(x, dtype=workloads.torch_dtype(dtype), device="cuda")
+
+
+@pytest.mark.parametrize("name", sorted(FULL_SHAPES))
+@pytest.mark.parametrize("partition", [-1, 256])
+def test_decode_fp8_q_rows_spanning_2_25(name, partition):
+    """q elements from 2^-22 to 2^3 in one row: the small ones sit far below
+    the row's largest, where a split of q into terms with one scale a head
+    loses them unless its floor is low enough."""
+    c = Fp8Case("shape", seed=2, plan=full_plan(name, seed=2), codes=full_range_codes,
+                scales=FULL_SCALES)
+    c.q = log_uniform_q(tuple(c.q.shape), c.spec.dtype, 5)
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    out = c.gpu(partition)
+    api.check_error()
+    assert_close(out, c.oracle(kc, vc), f"fp8 q spanning 2^25 {name} P={partition}")
+
+
+def fill_pools(c, k, v):
+    """Overwrite the pools with host code arrays of the pools' shape."""
+    c.kp.copy_(torch.as_tensor(k, device="cuda"))
+    c.vp.copy_(torch.as_tensor(v, device="cuda"))
+
+
+@pytest.mark.parametrize("name", sorted(FULL_SHAPES))
+@pytest.mark.parametrize("partition", [-1, 512])
+def test_decode_fp8_small_q_elements_against_large_keys(name, partition):
+    """Each head: one q element of about 1000 whose key column holds
+    subnormal codes, every other element about 2^-17.6 of it, their key
+    columns all +448 or all -448 (by position).  The scores' differences then
+    come entirely from the small elements (about +-0.4 after scaling)."""
+    c = Fp8Case("shape", seed=3, plan=full_plan(name, seed=3), codes=full_range_codes,
+                scales=FULL_SCALES)
+    rng = np.random.default_rng(11)
+    shape = tuple(c.kp.shape)
+    k = np.empty(shape, np.uint8)
+    k[..., 0] = rng.integers(1, 8, shape[:-1]) | (rng.integers(0, 2, shape[:-1]) << 7)
+    k[..., 1:] = np.where(rng.random(shape[:-1] + (1,)) < 0.5, 0x7E, 0xFE)
+    fill_pools(c, k, np_codes(c.vp))
+    S, Hq, d = c.q.shape
+    big = 1000.0 * rng.uniform(0.7, 1.4, (S, Hq))
+    q = np.empty((S, Hq, d))
+    q[..., 0] = big
+    q[..., 1:] = (big * 2.0 ** -17.6)[..., None] * rng.uniform(0.8, 1.2, (S, Hq, d - 1))
+    c.q = torch.as_tensor(q, dtype=workloads.torch_dtype(c.spec.dtype), device="cuda")
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    out = c.gpu(partition)
+    api.check_error()
+    assert_close(out, c.oracle(kc, vc), f"fp8 small q elements {name} P={partition}")
+
+
+@pytest.mark.parametrize("name", sorted(FULL_SHAPES))
+@pytest.mark.parametrize("partition", [-1, 256])
+def test_decode_fp8_output_from_weights_near_2_minus_17(name, partition):
+    """The first position of every 128-position tile has a score about 17.5
+    (log2 units) above the rest and a value row of zeros; the other
+    positions' values are +448 codes (56 with the V scale 1/8).  The output
+    is then made only of weights 2^-16.5 .. 2^-18.5 of the largest, the range
+    where a split of P into terms meets its floor."""
+    c = Fp8Case("shape", seed=4, plan=full_plan(name, seed=4), codes=full_range_codes,
+                scales=(FULL_SCALES[0], 1.0 / 8))
+    rng = np.random.default_rng(13)
+    shape = tuple(c.kp.shape)
+    d, B = shape[-1], c.spec.block_size
+    top = np.zeros(shape[:-1], bool)
+    for s, L in enumerate(c.lay.seq_lens):
+        for p in range(0, int(L), 128):
+            top[c.lay.block_tables[s, p // B], :, p % B] = True
+    k = np.zeros(shape, np.uint8)
+    # 448 at the top positions, 160 / 176 / 192 at the others (score gaps of
+    # 18.5 / 17.5 / 16.5 in log2 units with q0 below)
+    low = oracle.e4m3_encode(rng.choice([160.0, 176.0, 192.0], shape[:-1]))
+    k[..., 0] = np.where(top, 0x7E, low)
+    v = np.where(top[..., None], 0x00, 0x7E).astype(np.uint8) * np.ones((1, 1, 1, d), np.uint8)
+    fill_pools(c, k, v)
+    S, Hq, _ = c.q.shape
+    q0 = 17.5 * np.log(2) / (c.plan.scale * FULL_SCALES[0] * (448 - 176))
+    q = np.zeros((S, Hq, d))
+    q[..., 0] = q0
+    c.q = torch.as_tensor(q, dtype=workloads.torch_dtype(c.spec.dtype), device="cuda")
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    ref = c.oracle(kc, vc)
+    # the outputs (about 0.045) come from the tiny weights only
+    assert 0.02 < np.abs(ref).max() < 0.1
+    out = c.gpu(partition)
+    api.check_error()
+    assert_close(out, ref, f"fp8 tiny weights {name} P={partition}")
