@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
         // tail: the output is the prefix's partials combined.
         if (p.prefix_parts > 0) {
             if (nparts_seq == 0 && part == 0)
-                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem));
+                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem), S::RING_BYTES);
         } else if (p.mode == 0) {
             if (part == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
         }
     }
     if (!direct && (p.counters != nullptr || p.prefix_parts > 0))
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem));
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem), S::RING_BYTES);
 }
 
 // ------------------------------------------------------------------ reduce

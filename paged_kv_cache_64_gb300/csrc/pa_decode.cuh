@@ -118,22 +118,30 @@ constexpr int kCompactMaxSeqs = 128;
 // Work item of CTA `c` of a compact grid.  Items are, sequence by sequence,
 // the chunks of span * P positions of each sequence (at least one, so a
 // zero-length sequence still has its CTA), each split over the KV heads:
-// c = item * Hkv + kvh.  Every thread of a warp calls it (converged); it
-// scans the sequence lengths 32 at a time (an inclusive warp prefix sum)
-// and returns false for c past the last item.
+// c = item * Hkv + kvh.  Every thread of a warp calls it (converged).  Lane
+// j loads the lengths of sequences j, 32 + j, 64 + j, 96 + j together (one
+// memory round trip for the at most kCompactMaxSeqs sequences of a compact
+// launch), then scans them 32 at a time (an inclusive warp prefix sum); it
+// returns false for c past the last item.
 __device__ __forceinline__ bool compact_item(const DecodeParams &p, int c, int *seq, int *chunk,
                                              int *kvh) {
     const int lane = threadIdx.x & 31;
     const int item = c / p.num_kv_heads;
     const int chunk_tok = p.partition_tokens * (p.span > 1 ? p.span : 1);
+    constexpr int kGroups = kCompactMaxSeqs / 32;
+    int len[kGroups];
+#pragma unroll
+    for (int k = 0; k < kGroups; ++k) {
+        const int s = 32 * k + lane;
+        len[k] = s < p.num_seqs ? item_len(p, s, false) : -1;
+    }
     int base = 0;  // items of the sequences before this group of 32
-    for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
-        const int s = s0 + lane;
-        int n = 0;
-        if (s < p.num_seqs) {
-            const int L = item_len(p, s, false);
-            n = L == 0 ? 1 : (L - 1) / chunk_tok + 1;
-        }
+#pragma unroll
+    for (int k = 0; k < kGroups; ++k) {
+        const int s0 = 32 * k;
+        if (s0 >= p.num_seqs) break;
+        const int L = len[k];
+        const int n = L < 0 ? 0 : (L == 0 ? 1 : (L - 1) / chunk_tok + 1);
         int incl = n;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -183,6 +191,13 @@ __device__ __forceinline__ void fused_cache_write(const DecodeParams &p, int seq
     const int t = threadIdx.x;
     if (t >= 2 * pieces) return;
     const int pos = L - 1;
+    const bool is_v = t >= pieces;
+    const int c = t % pieces;
+    // the table entry, the slot and the token's piece are loaded together
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+                           (is_v ? p.v_new : p.k_new) + ((int64_t)seq * p.num_kv_heads + kvh) * D) +
+                       c;
+    const uint4 val = *src;
     const int phys = seq_table(p, seq)[pos >> p.log2_block];
     const int off = pos & (p.block_size - 1);
     const int64_t slot = p.slot_mapping[seq];
@@ -190,16 +205,11 @@ __device__ __forceinline__ void fused_cache_write(const DecodeParams &p, int seq
         if (t == 0) record_error(p.err, PA_ERR_BAD_INDEX);
         return;
     }
-    const bool is_v = t >= pieces;
-    const int c = t % pieces;
-    const uint4 *src = reinterpret_cast<const uint4 *>(
-                           (is_v ? p.v_new : p.k_new) + ((int64_t)seq * p.num_kv_heads + kvh) * D) +
-                       c;
     uint4 *dst = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(is_v ? p.v_pool : p.k_pool) +
                                            (((int64_t)phys * p.num_kv_heads + kvh) * p.block_size +
                                             off) * D) +
                  c;
-    *dst = *src;
+    *dst = val;
     // make the generic-proxy store visible to the bulk-copy (async) proxy
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -207,27 +217,38 @@ __device__ __forceinline__ void fused_cache_write(const DecodeParams &p, int seq
 constexpr int kFuseMaxParts = 8;  // combine inside the decode kernel up to this many partitions
 
 // Epoch-tagged arrival counter of the fused combine: true in exactly one CTA,
-// the last of `expected` to arrive in this call.  The count is kept under the
-// call's epoch (a stale or garbage word reads as zero) and is reset by the
-// last arrival, so graph replays of one call start from zero again.
+// the last of `expected` to arrive in this call.  The word holds the call's
+// epoch (high half) and its count (low half); a stale or garbage word counts
+// as zero.  The last arrival swaps in the reset value (epoch, 0), so graph
+// replays of one call start from zero again.  Every arrival first tries the
+// swap a last arrival would make (the word then holds (epoch, expected - 1)):
+// the last CTA, the one on the critical path, usually needs one round trip;
+// the others learn the word's value from the failed swap and retry.
 __device__ __forceinline__ bool arrive_last(unsigned long long *ctr, unsigned int epoch,
                                             int expected, int *err) {
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(ctr);
+    const unsigned long long tag = (unsigned long long)epoch << 32;
+    unsigned long long old = tag | (unsigned long long)(expected - 1);
     for (int it = 0; it < (1 << 16); ++it) {
         const unsigned long long cnt = ((old >> 32) == epoch) ? (old & 0xffffffffull) : 0ull;
-        const unsigned long long nv = ((unsigned long long)epoch << 32) | (cnt + 1);
-        const unsigned long long prev = atomicCAS(ctr, old, nv);
-        if (prev == old) {
-            if (cnt + 1 == (unsigned long long)expected) {
-                atomicExch(ctr, (unsigned long long)epoch << 32);
-                return true;
-            }
-            return false;
-        }
+        const bool last = cnt + 1 == (unsigned long long)expected;
+        const unsigned long long prev = atomicCAS(ctr, old, last ? tag : (tag | (cnt + 1)));
+        if (prev == old) return last;
         old = prev;
     }
     record_error(err, PA_ERR_DEVICE_TIMEOUT);
     return false;
+}
+
+// 16-byte global -> shared copy through L2 only (cp.async.cg), and the wait
+// for every copy this thread has committed.
+__device__ __forceinline__ void cp_async16_cg(void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gmem_src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 
 // Most partials one combine merges (the cascade's prefix chunks plus the
@@ -237,22 +258,38 @@ constexpr int kCombineMaxParts = 256;
 // Split-KV step 3 inside the CTA that finishes (seq, kvh): for each of its
 // G heads, over the slots [0, np) of the row, M = max_k m_k,
 // w_k = l_k 2^(m_k - M) / sum_j l_j 2^(m_j - M), out = sum_k w_k O_k.  All
-// `nthreads` threads of the CTA call it.  `scratch` is shared memory the CTA
-// no longer needs, 2 * G * np floats.  Partials are read through L2 (other
-// CTAs wrote them), every (m, l) pair at once and four O rows in flight per
-// thread, so the merge costs a few L2 round trips rather than one per partial.
+// `nthreads` threads of the CTA call it.  `scratch` is 16-byte aligned
+// shared memory the CTA no longer needs, `scratch_bytes` of it, at least
+// 2 * G * np floats.  Partials are read through L2 (other CTAs wrote them).
+// When every O row fits in the scratch after the (m, l) pairs, the rows are
+// copied in (cp.async) together with the (m, l) loads, so the merge costs
+// one round of loads; otherwise four O rows per thread are kept in flight
+// after the weights are known.
 template <bool BF16, int D>
 __device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, float *scratch,
-                              int nthreads) {
+                              int scratch_bytes, int nthreads) {
     const int G = p.group;
     const int tid = threadIdx.x;
     const int64_t row0 = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * p.ws_parts;
     float *ms = scratch, *ws = scratch + G * np;
+    const int buf_off = (2 * G * np + 3) & ~3;  // floats; rows [k][g][D] after (m, l)
+    float *buf = scratch + buf_off;
+    const bool staged = (int64_t)(buf_off + np * G * D) * 4 <= (int64_t)scratch_bytes;
+    if (staged) {
+        const int n16 = np * G * (D / 4);
+        for (int i = tid; i < n16; i += nthreads) {
+            const int x4 = i % (D / 4), r = i / (D / 4);  // r = k * G + g
+            const int k = r / G, g = r - k * G;
+            cp_async16_cg(buf + r * D + x4 * 4,
+                          p.part_o + (row0 + (int64_t)g * p.ws_parts + k) * D + x4 * 4);
+        }
+    }
     for (int i = tid; i < G * np; i += nthreads) {
         const int g = i / np, k = i - g * np;
         ms[i] = __ldcg(p.part_m + row0 + (int64_t)g * p.ws_parts + k);
         ws[i] = __ldcg(p.part_l + row0 + (int64_t)g * p.ws_parts + k);
     }
+    if (staged) cp_async_commit_wait_all();
     __syncthreads();
     if (tid < G) {
         float M = -INFINITY;
@@ -268,6 +305,27 @@ __device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, f
         for (int k = 0; k < np; ++k) ws[tid * np + k] *= inv;
     }
     __syncthreads();
+    if (staged) {
+        for (int item = tid; item < G * (D / 8); item += nthreads) {
+            const int g = item / (D / 8);
+            const int x0 = (item % (D / 8)) * 8;
+            const float *w = ws + g * np;
+            float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < np; ++k) {
+                const float4 *src = reinterpret_cast<const float4 *>(buf + (k * G + g) * D + x0);
+                const float4 a = src[0], b = src[1];
+                const float wk = w[k];
+                o[0] += wk * a.x; o[1] += wk * a.y; o[2] += wk * a.z; o[3] += wk * a.w;
+                o[4] += wk * b.x; o[5] += wk * b.y; o[6] += wk * b.z; o[7] += wk * b.w;
+            }
+            uint16_t *out = static_cast<uint16_t *>(p.out) +
+                            ((int64_t)seq * p.num_q_heads + kvh * G + g) * D + x0;
+            *reinterpret_cast<uint4 *>(out) =
+                make_uint4(narrow2<BF16>(o[0], o[1]), narrow2<BF16>(o[2], o[3]),
+                           narrow2<BF16>(o[4], o[5]), narrow2<BF16>(o[6], o[7]));
+        }
+        return;
+    }
     for (int item = tid; item < G * (D / 8); item += nthreads) {
         const int g = item / (D / 8);
         const int x0 = (item % (D / 8)) * 8;
@@ -308,10 +366,11 @@ __device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, f
 // combines; a cascade tail of a single
 // partition (no counters), or an empty one, combines at once.  The combined
 // slots are the prefix's and the item's: [0, prefix_parts + nparts_seq).
-// Called by every thread of the CTA; scratch as in fused_combine.
+// Called by every thread of the CTA; scratch and scratch_bytes as in
+// fused_combine.
 template <bool BF16, int D>
 __device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_seq,
-                            float *scratch, int arrivals = -1) {
+                            float *scratch, int scratch_bytes, int arrivals = -1) {
     __shared__ int last_flag;
     __threadfence();
     __syncthreads();
@@ -323,7 +382,8 @@ __device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_
     __syncthreads();
     if (last_flag) {
         __threadfence();
-        fused_combine<BF16, D>(p, seq, kvh, p.prefix_parts + nparts_seq, scratch, blockDim.x);
+        fused_combine<BF16, D>(p, seq, kvh, p.prefix_parts + nparts_seq, scratch, scratch_bytes,
+                               blockDim.x);
     }
 }
 

@@ -996,6 +996,7 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
     }
     if (!direct && !*abort_flag && p.counters != nullptr)
         finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_STG),
+                             (S::NK + S::NV) * S::STG_BYTES,
                              (nparts_seq + R - 1) / R);
 }
 

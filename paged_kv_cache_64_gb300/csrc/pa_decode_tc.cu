@@ -51,23 +51,44 @@ constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcCols = 64;        // TMEM columns: S x2 and O x2, 16 fp32 columns each
 constexpr int kSCol0 = 0, kOCol0 = 32;
 
+constexpr int kTcMaxStages = 3;    // most K (or V) tiles in flight a CTA
+
 enum TcBar {
-    kKFull = 0, kVFull, kKEmpty, kVEmpty, kQReady,
+    kQReady = 0,
     kSFull0, kSFull1, kSEmpty0, kSEmpty1, kPFull0, kPFull1, kOFull0, kOFull1, kOEmpty0, kOEmpty1,
-    kPreReady, kNumTcBars
+    kPreReady,
+    // the K and V staging rings, kTcMaxStages of each
+    kKFull0, kKEmpty0 = kKFull0 + kTcMaxStages, kVFull0 = kKEmpty0 + kTcMaxStages,
+    kVEmpty0 = kVFull0 + kTcMaxStages, kNumTcBars = kVEmpty0 + kTcMaxStages
 };
 
 template <int D>
 struct TcShape {
     static constexpr int KH = D / 64;                 // 64-dim (128-byte) slabs of K along d
     static constexpr int SLAB = kTcTile * 128;        // one slab of a tile: 16 KiB
-    static constexpr int K_BYTES = KH * SLAB;
-    static constexpr int V_BYTES = 2 * SLAB;          // V^T is M = 128 dims; d = 64 pads with zeros
+    static constexpr int K_STAGE = KH * SLAB;
+    // Staging rings: three K and three V tiles at d = 64, so a CTA has its
+    // next tiles in flight while it computes one (short work items, such as
+    // a small model's decode step, are bound by that latency; two CTAs an
+    // SM); one of each at d = 128 (two CTAs an SM already keep enough copies
+    // in flight for long items, and a second stage would leave one CTA an
+    // SM).  P.V reads V^T as an M = 128 (dims) MN-major operand whose two
+    // 64-dim slabs are SLAB bytes apart.  At d = 64 only the first slab is
+    // real: rows 64..127 of the operand are read from the next SLAB bytes
+    // (the next V stage or the first K stage), and only reach TMEM lanes
+    // 64..127 of O, which no thread ever writes out.  So the V stages come
+    // first at d = 64, K after them, and nothing is zero-padded.
+    static constexpr int NK = D == 64 ? 3 : 1;
+    static constexpr int NV = D == 64 ? 3 : 1;
+    static_assert(NK <= kTcMaxStages && NV <= kTcMaxStages, "ring barriers");
+    static constexpr int V_STAGE = KH * SLAB;
+    static constexpr int V_BYTES = NV * V_STAGE;
+    static constexpr int K_BYTES = NK * K_STAGE;
     static constexpr int Q_BYTES = KH * kTcN * 128;   // q as a 16-row K-major operand
     static constexpr int P_BYTES = 2 * kTcN * 128;    // P^T: 16 rows x 128 positions (two atoms)
-    static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = OFF_K + K_BYTES;
-    static constexpr int OFF_Q = OFF_V + V_BYTES;
+    static constexpr int OFF_V = D == 64 ? 0 : K_BYTES;
+    static constexpr int OFF_K = D == 64 ? V_BYTES : 0;
+    static constexpr int OFF_Q = (D == 64 ? OFF_K + K_BYTES : OFF_V + V_BYTES);
     static constexpr int OFF_P = OFF_Q + Q_BYTES;     // two buffers
     static constexpr int OFF_RED = OFF_P + 2 * P_BYTES;
     static constexpr int RED_BYTES = 3 * 4 * kTcN * 4;  // two tile-max buffers + the final sums
@@ -82,15 +103,20 @@ struct TcShape {
     static constexpr int OFF_BAR = OFF_PEND + 2 * PEND_FLOATS * 4;
     static constexpr int OFF_MISC = OFF_BAR + kNumTcBars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
-    static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "atom alignment");
-    static_assert(K_BYTES >= 2 * kTcG * kCombineMaxParts * 4, "combine scratch in the K tile");
+    static_assert(OFF_V % 1024 == 0 && OFF_K % 1024 == 0 && OFF_Q % 1024 == 0 &&
+                  OFF_P % 1024 == 0, "atom alignment");
+    static_assert(OFF_V + (NV - 1) * V_STAGE + 2 * SLAB <= OFF_BAR, "V^T operand rows in bounds");
+    // the combine's scratch: the staging rings, [0, OFF_Q)
+    static_assert(OFF_Q >= 2 * kTcG * kCombineMaxParts * 4, "combine scratch in the rings");
 };
 
-// SPAN: a CTA may compute several consecutive partitions (p.span > 1); the
-// variant without it keeps to 96 registers (three CTAs an SM).  COMPACT: the
-// launch uses a compact grid (p.compact).
+
+// SPAN: a CTA may compute several consecutive partitions (p.span > 1).
+// COMPACT: the launch uses a compact grid (p.compact).  Every variant runs
+// two CTAs an SM (shared memory allows no more), so registers are capped
+// for two.
 template <bool BF16, int D, bool SPAN, bool COMPACT>
-__global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
+__global__ void __launch_bounds__(kTcThreads, 2)
     paged_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v) {
     using S = TcShape<D>;
@@ -128,7 +154,7 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
         if (p.prefix_parts > 0) {
             // empty cascade tail: the output is the prefix's partials combined
             if (nparts_seq == 0 && part == 0)
-                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem + S::OFF_K));
+                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem), S::OFF_Q);
         } else if (p.mode == 0) {
             if (part == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
@@ -161,22 +187,35 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
     const bool merge_prefix = direct && p.prefix_parts > 0;
     float *pre = reinterpret_cast<float *>(smem + S::OFF_PRE);
 
+    // Loads needed after the set-up below are issued first, so they travel
+    // while it runs: the producer's first 32 block-table entries (lane j:
+    // unit j) and the softmax warps' pieces of q.
+    const int32_t *table = seq_table(p, seq);
+    int phys_first = 0;
+    if (warp == 0 && lane < nunits) phys_first = table[(start + lane * kUnit) >> p.log2_block];
+    constexpr int kQPieces = kTcN * (D / 8) / 128;  // 16-byte pieces of q per softmax thread
+    uint4 qv[kQPieces];
+#pragma unroll
+    for (int j = 0; j < kQPieces; ++j) {
+        qv[j] = make_uint4(0, 0, 0, 0);
+        const int ci = threadIdx.x - 64 + 128 * j;  // softmax threads: 0..127
+        const int g = ci / (D / 8), c = ci % (D / 8);
+        if (warp >= 2 && g < G)
+            qv[j] = *reinterpret_cast<const uint4 *>(
+                p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * 8);
+    }
     if (p.k_new != nullptr && part_end == nparts_seq) fused_cache_write<D>(p, seq, kvh, L);
     if (threadIdx.x == 0) {
-        const int counts[kNumTcBars] = {1, 1, 1, 1, 4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4, 1};
-        for (int b = 0; b < kNumTcBars; ++b) mbar_init(&bar[b], counts[b]);
+        // kQReady, kSEmpty, kPFull, kOEmpty: the 4 softmax warps; the rest one
+        // arrival (the producer's expect-tx, an MMA commit, the prefix merge)
+        const int counts[kKFull0] = {4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4, 1};
+        for (int b = 0; b < kNumTcBars; ++b) mbar_init(&bar[b], b < kKFull0 ? counts[b] : 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTcCols);
         tmem_relinquish();
-    }
-    if constexpr (D == 64) {
-        // rows 64..127 of the V^T operand: zero once, never loaded
-        uint4 *z = reinterpret_cast<uint4 *>(smem + S::OFF_V + S::SLAB);
-        for (int i = threadIdx.x; i < S::SLAB / 16; i += kTcThreads) z[i] = make_uint4(0, 0, 0, 0);
-        fence_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -185,15 +224,19 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        const int32_t *table = seq_table(p, seq);
+        // Windows of 32 units (4 tiles), lane j holding unit j of the window;
+        // the next window's table entries are loaded when a window opens.
         const int rows_per_block = p.block_size;
         bool ok = true;
+        int phys_cur = phys_first;
         for (int u0 = 0; u0 < nunits && ok; u0 += 32) {  // 32 units = 4 tiles
             const int u = u0 + lane;
+            const int phys_next =
+                (u + 32 < nunits) ? table[(start + (u + 32) * kUnit) >> p.log2_block] : 0;
             int row0 = 0;  // first row of the unit in the 2-D view [NB*Hkv*B, d]
             if (u < nunits) {
                 const int pos = start + u * kUnit;
-                int phys = table[pos >> p.log2_block];
+                int phys = phys_cur;
                 if ((unsigned)phys >= (unsigned)p.num_blocks) {
                     record_error(p.err, PA_ERR_BAD_INDEX);
                     phys = 0;
@@ -203,16 +246,19 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
             for (int t = u0 / 8; t < ntiles && t < (u0 + 32) / 8 && ok; ++t) {
                 const int nu = (nunits - 8 * t < 8) ? nunits - 8 * t : 8;
                 for (int kv = 0; kv < 2 && ok; ++kv) {
-                    if (t >= 1) {
-                        const bool done = mbar_wait(&bar[kv ? kVEmpty : kKEmpty], (t - 1) & 1);
+                    const int n = kv ? S::NV : S::NK;  // stages of this ring
+                    const int slot = t % n;
+                    if (t >= n) {
+                        const bool done =
+                            mbar_wait(&bar[(kv ? kVEmpty0 : kKEmpty0) + slot], ((t / n) - 1) & 1);
                         if (!__all_sync(kFullMask, done)) {
                             ok = false;
                             break;
                         }
                     }
-                    const int base_off = kv ? S::OFF_V : S::OFF_K;
+                    const int base_off = kv ? S::OFF_V + slot * S::V_STAGE : S::OFF_K + slot * S::K_STAGE;
                     const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
-                    uint64_t *full = &bar[kv ? kVFull : kKFull];
+                    uint64_t *full = &bar[(kv ? kVFull0 : kKFull0) + slot];
                     if (lane == 0) mbar_arrive_expect_tx(full, nu * S::KH * 2048);
                     // lane j < nu copies unit j of the tile: one instruction issues
                     // the tile's copies
@@ -226,6 +272,7 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
                     __syncwarp();
                 }
             }
+            phys_cur = phys_next;
         }
         if (!ok && lane == 0) {
             record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
@@ -316,7 +363,7 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
                 // (q.K^T of the last tile only once P.V of every earlier tile
                 // is issued: see the stale-row zeroing in the softmax)
                 if (nq < ntiles && (nq + 1 < ntiles || nv == nq) &&
-                    mbar_test_wait(&bar[kKFull], nq & 1) &&
+                    mbar_test_wait(&bar[kKFull0 + nq % S::NK], (nq / S::NK) & 1) &&
                     (nq < 2 || mbar_test_wait(&bar[kSEmpty0 + (nq & 1)], ((nq >> 1) - 1) & 1))) {
                     const int b = nq & 1;
                     tc_fence_after();
@@ -324,15 +371,16 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
                         const uint32_t qoff = (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
-                        tc_mma(tmem + kSCol0 + 16 * b, sw128_desc(sbase + S::OFF_K + koff, 16, 1024),
+                        tc_mma(tmem + kSCol0 + 16 * b,
+                               sw128_desc(sbase + S::OFF_K + (nq % S::NK) * S::K_STAGE + koff, 16, 1024),
                                sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
                     }
                     tc_commit(&bar[kSFull0 + b]);
-                    tc_commit(&bar[kKEmpty]);
+                    tc_commit(&bar[kKEmpty0 + nq % S::NK]);
                     ++nq;
                     moved = true;
                 }
-                if (nv < nq && mbar_test_wait(&bar[kVFull], nv & 1) &&
+                if (nv < nq && mbar_test_wait(&bar[kVFull0 + nv % S::NV], (nv / S::NV) & 1) &&
                     mbar_test_wait(&bar[kPFull0 + (nv & 1)], (nv >> 1) & 1) &&
                     (nv < 2 || mbar_test_wait(&bar[kOEmpty0 + (nv & 1)], ((nv >> 1) - 1) & 1))) {
                     const int b = nv & 1;
@@ -342,11 +390,12 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
                         const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
                         const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
                         tc_mma(tmem + kOCol0 + 16 * b,
-                               sw128_desc(sbase + S::OFF_V + voff, S::SLAB, 1024),
+                               sw128_desc(sbase + S::OFF_V + (nv % S::NV) * S::V_STAGE + voff,
+                                          S::SLAB, 1024),
                                sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
                     }
                     tc_commit(&bar[kOFull0 + b]);
-                    tc_commit(&bar[kVEmpty]);
+                    tc_commit(&bar[kVEmpty0 + nv % S::NV]);
                     ++nv;
                     moved = true;
                 }
@@ -370,14 +419,13 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
 
         // q of the group as the K-major B operand (16 rows, 128-byte swizzle),
-        // rows >= G zero.  Unscaled: the scale is applied to S in fp32.
-        for (int ci = st; ci < kTcN * (D / 8); ci += 128) {
+        // rows >= G zero (loaded before the set-up).  Unscaled: the scale is
+        // applied to S in fp32.
+#pragma unroll
+        for (int j = 0; j < kQPieces; ++j) {
+            const int ci = st + 128 * j;
             const int g = ci / (D / 8), c = ci % (D / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (g < G)
-                v = *reinterpret_cast<const uint4 *>(
-                    p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * 8);
-            *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(g, c * 8, kTcN * 128)) = v;
+            *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(g, c * 8, kTcN * 128)) = qv[j];
         }
         fence_async_smem();
         __syncwarp();
@@ -539,13 +587,17 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
               if (!valid) {
                   // Stale rows of the last tile: V must be finite there (0 * NaN
                   // would poison the product), so zero the row once it has landed.
-                  // Tile i-1's V has been consumed (the MMA issuer holds back
-                  // q.K^T of the last tile until every earlier P.V is issued), so
-                  // the parity wait below can only mean tile i's phase.
-                  if (mbar_wait(&bar[kVFull], i & 1)) {
+                  // The V stage's previous tile (i - NV) has been consumed
+                  // (the MMA issuer holds back q.K^T of the last tile until every
+                  // earlier P.V is issued, and tile i's copy waited for that
+                  // P.V to finish), so the parity wait below can only mean tile
+                  // i's phase.
+                  const int vs = i % S::NV;
+                  if (mbar_wait(&bar[kVFull0 + vs], (i / S::NV) & 1)) {
   #pragma unroll
                       for (int h = 0; h < S::KH; ++h) {
-                          uint4 *row = reinterpret_cast<uint4 *>(smem + S::OFF_V + h * S::SLAB + r * 128);
+                          uint4 *row = reinterpret_cast<uint4 *>(smem + S::OFF_V + vs * S::V_STAGE +
+                                                                 h * S::SLAB + r * 128);
   #pragma unroll
                           for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
                       }
@@ -629,9 +681,15 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
     if (*abort_flag && threadIdx.x == 0) {
         // let copies and MMAs still in flight finish before shared memory and
         // TMEM are released (each wait is bounded)
-        (void)mbar_wait(&bar[kKFull], (ntiles - 1) & 1);
-        (void)mbar_wait(&bar[kVFull], (ntiles - 1) & 1);
-        (void)mbar_wait(&bar[kVEmpty], (ntiles - 1) & 1);
+        for (int ks = 0; ks < S::NK && ks < ntiles; ++ks) {
+            const int tl = ks + S::NK * ((ntiles - 1 - ks) / S::NK);  // last tile of stage ks
+            (void)mbar_wait(&bar[kKFull0 + ks], (tl / S::NK) & 1);
+        }
+        for (int vs = 0; vs < S::NV && vs < ntiles; ++vs) {
+            const int tl = vs + S::NV * ((ntiles - 1 - vs) / S::NV);  // last tile of stage vs
+            (void)mbar_wait(&bar[kVFull0 + vs], (tl / S::NV) & 1);
+            (void)mbar_wait(&bar[kVEmpty0 + vs], (tl / S::NV) & 1);
+        }
     }
     if (warp == 1) {
         __syncwarp();
@@ -639,7 +697,7 @@ __global__ void __launch_bounds__(kTcThreads, SPAN ? 2 : 3)
         tmem_dealloc(tmem, kTcCols);
     }
     if (!direct && !*abort_flag && (p.counters != nullptr || p.prefix_parts > 0))
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_K),
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem), S::OFF_Q,
                               (nparts_seq + R - 1) / R);
 }
 
