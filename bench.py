@@ -489,6 +489,7 @@ def run_gpu(args, rank, world, local_rank):
     api.set_decode_impl(args.decode_impl)
     base = workloads.SPECS[args.workload]
     plan = workloads.make_plan(args.workload, num_seqs=args.num_seqs,
+                               len_range=tuple(args.len_range) if args.len_range else None,
                                seed=base.seed + 1000 * rank if rank else None, apc=args.apc,
                                cow=args.cow)
     if args.layers:
@@ -780,6 +781,8 @@ def main(argv=None):
                     choices=["tiny", "qwen", "llama", "prefix", "long"])
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="shrink the batch (profiling of small cases only)")
+    ap.add_argument("--len-range", type=int, nargs=2, default=None, metavar=("LO", "HI"),
+                    help="cached lengths uniform in [LO, HI] (profiling of small cases only)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (profiling of small cases only)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])

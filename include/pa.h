@@ -347,6 +347,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  *   l  float [num_seqs][num_q_heads][NP]
  *   O  float [num_seqs][num_q_heads][NP][head_dim]
  *   arrival counters  uint64 [num_seqs][num_kv_heads]  (pa_decode only)
+ *   ready flags  uint32 [num_seqs][num_kv_heads][NP]  (pa_decode only)
  *   [P3] section 4, "Parallel Partitioning Across GPU Warps", step 2.
  * partition_tokens must be > 0 here.  Other arguments as pa_decode.
  * ---------------------------------------------------------------------- */

@@ -189,7 +189,8 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
         // tail: the output is the prefix's partials combined.
         if (p.prefix_parts > 0) {
             if (nparts_seq == 0 && part == 0)
-                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem), S::RING_BYTES);
+                finish_item<BF16, D>(p, seq, kvh, 0, 0, 1, false, reinterpret_cast<float *>(smem),
+                                     S::RING_BYTES);
         } else if (p.mode == 0) {
             if (part == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
@@ -564,7 +565,8 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<GP
         }
     }
     if (!direct && (p.counters != nullptr || p.prefix_parts > 0))
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem), S::RING_BYTES);
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, part, nparts_seq, false,
+                             reinterpret_cast<float *>(smem), S::RING_BYTES);
 }
 
 // ------------------------------------------------------------------ reduce
@@ -731,11 +733,12 @@ static int ilog2_exact(int x) {
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WorkspaceLayout {
-    size_t m_off, l_off, o_off, c_off, bytes;
+    size_t m_off, l_off, o_off, c_off, f_off, bytes;
 };
 
-// m, l, O partials, then one 64-bit arrival counter per (sequence, KV head)
-// for the fused combine.
+// m, l, O partials, then the fused combine's arrival counters (one 64-bit
+// word per (sequence, KV head)) and ready flags (one 32-bit word per
+// (sequence, KV head, slot)).
 static WorkspaceLayout workspace_layout(int S, int Hq, int D, int NP, int Hkv) {
     const size_t rows = (size_t)S * Hq * NP;
     WorkspaceLayout w;
@@ -743,15 +746,19 @@ static WorkspaceLayout workspace_layout(int S, int Hq, int D, int NP, int Hkv) {
     w.l_off = align256(rows * sizeof(float));
     w.o_off = w.l_off + align256(rows * sizeof(float));
     w.c_off = w.o_off + align256(rows * D * sizeof(float));
-    w.bytes = w.c_off + align256((size_t)S * Hkv * sizeof(unsigned long long));
+    w.f_off = w.c_off + align256((size_t)S * Hkv * sizeof(unsigned long long));
+    w.bytes = w.f_off + align256((size_t)S * Hkv * NP * sizeof(unsigned int));
     return w;
 }
 
-// Tag of a decode call in the fused-combine counters (never 0 twice in a row).
+// Tag of a decode call in the fused-combine flags: never 0 (a cleared flag)
+// nor all ones (a workspace filled with 0xFF bytes).
 static unsigned int next_epoch() {
     static std::atomic<unsigned int> epoch{0x9e3779b9u};
-    unsigned int e = epoch.fetch_add(1) + 1;
-    return e ? e : epoch.fetch_add(1) + 1;
+    for (;;) {
+        const unsigned int e = epoch.fetch_add(1) + 1;
+        if (e != 0u && e != 0xffffffffu) return e;
+    }
 }
 
 
@@ -887,6 +894,15 @@ static pa_status launch_decode(const ResolvedDecode &r, DecodeParams prm, int nu
     prm.compact = prm.mode == 0 && prm.prefix_parts == 0 && num_seqs <= kCompactMaxSeqs &&
                   (int64_t)chunks * num_kv_heads * num_seqs < (1ll << 31);
     if (!prm.out && (prm.mode == 0 || prm.counters || prm.prefix_parts)) return PA_ERR_INVALID;
+    if (prm.counters) {
+        // ready flags only when every CTA is resident at once (a waiting
+        // combiner must never hold a slot a partner needs)
+        const int per_sm = r.fp8 ? fp8_ctas_per_sm(r.bf16, r.head_dim, prm.group)
+                           : r.tc ? tc_ctas_per_sm(r.bf16, r.head_dim)
+                                  : 0;
+        prm.one_wave = (r.tc || r.fp8) &&
+                       (int64_t)chunks * num_kv_heads * num_seqs <= (int64_t)sm_count() * per_sm;
+    }
     if (r.fp8) {
         if (prm.prefix_parts) return PA_ERR_UNSUPPORTED;  // no cascade over E4M3 pools
         prm.span = span;
@@ -1008,8 +1024,9 @@ static pa_status decode_impl(void *out, const void *q, const void *k_new, const 
     prm.num_partitions = r.NP;
     const bool fuse = r.NP <= kFuseMaxParts;
     if (fuse) {
-        // the last CTA of each (sequence, KV head) combines its partials
+        // one CTA of each (sequence, KV head) combines its partials
         prm.counters = reinterpret_cast<unsigned long long *>(ws + w.c_off);
+        prm.flags = reinterpret_cast<unsigned int *>(ws + w.f_off);
         prm.epoch = next_epoch();
     }
     st = launch_decode(r, prm, num_seqs, num_kv_heads, s);
@@ -1261,6 +1278,7 @@ pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, const v
     prm.num_partitions = c.tail.NP;
     if (c.tail.NP > 1) {
         prm.counters = reinterpret_cast<unsigned long long *>(ws + w.c_off);
+        prm.flags = reinterpret_cast<unsigned int *>(ws + w.f_off);
         prm.epoch = next_epoch();
     }
     return launch_decode(c.tail, prm, num_seqs, num_kv_heads, s);

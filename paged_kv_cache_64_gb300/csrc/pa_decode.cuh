@@ -51,9 +51,15 @@ struct DecodeParams {
     const uint16_t *k_new;       // [S][Hkv][D]
     const uint16_t *v_new;
     const int64_t *slot_mapping; // [S]
-    // Fused split-KV combine: one arrival counter per (sequence, KV head), or nullptr.
+    // Fused split-KV combine (nullptr when the launch does not combine):
+    // arrival counters [S][Hkv] (the last chunk to arrive combines) and ready
+    // flags [S][Hkv][ws_parts] (the last chunk waits for the others' flags;
+    // only when every CTA of the launch is resident, see finish_item).  A
+    // flag holds the call's epoch once its chunk's partials are published.
     unsigned long long *counters;
-    unsigned int epoch;          // tag of this call in the counters
+    unsigned int *flags;
+    unsigned int epoch;          // tag of this call (never 0)
+    int one_wave;                // 3-D grid: every CTA of the launch fits on the GPU at once
     // Sub-range of each sequence (the tail of a cascade step): positions
     // [len_offset, seq_lens[i]) read through block-table entries from
     // table_offset on; partials go to slot part_base + part of a workspace laid
@@ -115,29 +121,36 @@ __device__ __forceinline__ int item_len(const DecodeParams &p, int seq, bool rep
 
 constexpr int kCompactMaxSeqs = 128;
 
-// Work item of CTA `c` of a compact grid.  Items are, sequence by sequence,
-// the chunks of span * P positions of each sequence (at least one, so a
-// zero-length sequence still has its CTA), each split over the KV heads:
-// c = item * Hkv + kvh.  Every thread of a warp calls it (converged).  Lane
-// j loads the lengths of sequences j, 32 + j, 64 + j, 96 + j together (one
-// memory round trip for the at most kCompactMaxSeqs sequences of a compact
-// launch), then scans them 32 at a time (an inclusive warp prefix sum); it
-// returns false for c past the last item.
-__device__ __forceinline__ bool compact_item(const DecodeParams &p, int c, int *seq, int *chunk,
-                                             int *kvh) {
+constexpr int kCompactGroups = kCompactMaxSeqs / 32;
+
+// Lengths of the sequences of a compact launch (at most kCompactMaxSeqs):
+// lane j loads those of sequences j, 32 + j, 64 + j, 96 + j together (one
+// memory round trip), -1 past the batch.
+__device__ __forceinline__ void compact_lens(const DecodeParams &p, int *len) {
     const int lane = threadIdx.x & 31;
-    const int item = c / p.num_kv_heads;
-    const int chunk_tok = p.partition_tokens * (p.span > 1 ? p.span : 1);
-    constexpr int kGroups = kCompactMaxSeqs / 32;
-    int len[kGroups];
 #pragma unroll
-    for (int k = 0; k < kGroups; ++k) {
+    for (int k = 0; k < kCompactGroups; ++k) {
         const int s = 32 * k + lane;
         len[k] = s < p.num_seqs ? item_len(p, s, false) : -1;
     }
+}
+
+// Work item `c` of a compact grid, from the lengths compact_lens loaded.
+// Items are, sequence by sequence, the chunks of span * P positions of each
+// sequence (at least one, so a zero-length sequence still has its CTA), each
+// split over the KV heads: c = item * Hkv + kvh.  *total is set to the number
+// of items times Hkv (the launch's work, whatever c is).  Every thread of a
+// warp calls it (converged); it scans the lengths 32 at a time (an inclusive
+// warp prefix sum) and returns false for c past the last item.
+__device__ __forceinline__ bool compact_find(const DecodeParams &p, const int *len, int c, int *seq,
+                                             int *chunk, int *kvh, int *total) {
+    const int lane = threadIdx.x & 31;
+    const int item = c / p.num_kv_heads;
+    const int chunk_tok = p.partition_tokens * (p.span > 1 ? p.span : 1);
     int base = 0;  // items of the sequences before this group of 32
+    bool found = false;
 #pragma unroll
-    for (int k = 0; k < kGroups; ++k) {
+    for (int k = 0; k < kCompactGroups; ++k) {
         const int s0 = 32 * k;
         if (s0 >= p.num_seqs) break;
         const int L = len[k];
@@ -148,18 +161,28 @@ __device__ __forceinline__ bool compact_item(const DecodeParams &p, int c, int *
             const int t = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += t;
         }
-        const int total = base + __shfl_sync(0xffffffffu, incl, 31);
-        if (item < total) {
+        const int group_total = base + __shfl_sync(0xffffffffu, incl, 31);
+        if (!found && item < group_total) {
             const unsigned m = __ballot_sync(0xffffffffu, base + incl > item);
             const int l = __ffs(m) - 1;
             *seq = s0 + l;
             *chunk = item - (base + __shfl_sync(0xffffffffu, incl - n, l));
             *kvh = c - item * p.num_kv_heads;
-            return true;
+            found = true;
         }
-        base = total;
+        base = group_total;
     }
-    return false;
+    *total = base * p.num_kv_heads;
+    return found;
+}
+
+// Work item of CTA `c` of a compact grid (lengths loaded here).
+__device__ __forceinline__ bool compact_item(const DecodeParams &p, int c, int *seq, int *chunk,
+                                             int *kvh) {
+    int len[kCompactGroups];
+    compact_lens(p, len);
+    int total;
+    return compact_find(p, len, c, seq, chunk, kvh, &total);
 }
 
 // Grid of a decode launch: chunks x KV heads x sequences, or the same count
@@ -216,14 +239,29 @@ __device__ __forceinline__ void fused_cache_write(const DecodeParams &p, int seq
 
 constexpr int kFuseMaxParts = 8;  // combine inside the decode kernel up to this many partitions
 
+// Compare-and-swap with acquire-release semantics at GPU scope: the
+// caller's earlier writes (and those its CTA barrier ordered before it) are
+// visible to whoever reads the swapped value, and the caller's later reads
+// see what the writers of earlier values published.
+__device__ __forceinline__ unsigned long long atom_cas_acq_rel(unsigned long long *p,
+                                                               unsigned long long cmp,
+                                                               unsigned long long val) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+                 : "=l"(old)
+                 : "l"(p), "l"(cmp), "l"(val)
+                 : "memory");
+    return old;
+}
+
 // Epoch-tagged arrival counter of the fused combine: true in exactly one CTA,
 // the last of `expected` to arrive in this call.  The word holds the call's
 // epoch (high half) and its count (low half); a stale or garbage word counts
 // as zero.  The last arrival swaps in the reset value (epoch, 0), so graph
 // replays of one call start from zero again.  Every arrival first tries the
-// swap a last arrival would make (the word then holds (epoch, expected - 1)):
-// the last CTA, the one on the critical path, usually needs one round trip;
-// the others learn the word's value from the failed swap and retry.
+// swap a last arrival would make (the word then holds (epoch, expected - 1)),
+// so the last CTA usually needs one round trip; the others learn the word's
+// value from the failed swap and retry.
 __device__ __forceinline__ bool arrive_last(unsigned long long *ctr, unsigned int epoch,
                                             int expected, int *err) {
     const unsigned long long tag = (unsigned long long)epoch << 32;
@@ -231,12 +269,34 @@ __device__ __forceinline__ bool arrive_last(unsigned long long *ctr, unsigned in
     for (int it = 0; it < (1 << 16); ++it) {
         const unsigned long long cnt = ((old >> 32) == epoch) ? (old & 0xffffffffull) : 0ull;
         const bool last = cnt + 1 == (unsigned long long)expected;
-        const unsigned long long prev = atomicCAS(ctr, old, last ? tag : (tag | (cnt + 1)));
+        const unsigned long long prev = atom_cas_acq_rel(ctr, old, last ? tag : (tag | (cnt + 1)));
         if (prev == old) return last;
         old = prev;
     }
     record_error(err, PA_ERR_DEVICE_TIMEOUT);
     return false;
+}
+
+// Ready flags of the fused combine: a release store (the writer's earlier
+// stores, and those its CTA barrier ordered before it, are visible to whoever
+// acquires the value), and a bounded acquire wait for a value.
+__device__ __forceinline__ void flag_release(unsigned int *f, unsigned int v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int flag_acquire(const unsigned int *f) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+__device__ __forceinline__ bool flag_wait(const unsigned int *f, unsigned int v) {
+    if (flag_acquire(f) == v) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (flag_acquire(f) == v) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // 16-byte global -> shared copy through L2 only (cp.async.cg), and the wait
@@ -361,30 +421,61 @@ __device__ void fused_combine(const DecodeParams &p, int seq, int kvh, int np, f
     }
 }
 
-// End of a CTA that wrote partials of (seq, kvh): with arrival counters,
-// the last of the item's CTAs (`arrivals` of them, nparts_seq by default)
-// combines; a cascade tail of a single
-// partition (no counters), or an empty one, combines at once.  The combined
-// slots are the prefix's and the item's: [0, prefix_parts + nparts_seq).
-// Called by every thread of the CTA; scratch and scratch_bytes as in
-// fused_combine.
+// End of a CTA that wrote the partials of chunk `chunk` of (seq, kvh), an
+// item of `nchunks` chunks; one CTA of the item combines them.
+//  - use_flags (every CTA of the launch is resident at once): every chunk
+//    but the last publishes its partials by a release store of the call's
+//    epoch into its flag and is done; the last chunk's CTA, which has the
+//    item's highest block index, waits for the other flags (acquire;
+//    bounded), clears them for the next call on this workspace (a graph
+//    replay repeats the epoch), and combines.  The waiting CTA holds its
+//    slot, which is why this needs the whole launch resident.
+//  - otherwise, with counters (p.counters): the last chunk to arrive
+//    combines (arrive_last).
+//  - a cascade tail of one partition (neither), or an empty tail: combine at
+//    once.
+// The combined slots are the prefix's and the item's: [0, prefix_parts +
+// nparts_seq).  Called by every thread of the CTA; scratch and scratch_bytes
+// as in fused_combine.  Ordering: the CTA barrier puts every thread's
+// partial stores before thread 0's release (flag store or counter swap);
+// the combiner acquires, and the next barrier orders its CTA's reads of the
+// partials after that.
 template <bool BF16, int D>
-__device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_seq,
-                            float *scratch, int scratch_bytes, int arrivals = -1) {
-    __shared__ int last_flag;
-    __threadfence();
+__device__ void finish_item(const DecodeParams &p, int seq, int kvh, int nparts_seq, int chunk,
+                            int nchunks, bool use_flags, float *scratch, int scratch_bytes) {
+    __shared__ int all_ready;
     __syncthreads();
-    if (threadIdx.x == 0)
-        last_flag = (p.counters == nullptr || nparts_seq == 0)
-                        ? 1
-                        : arrive_last(p.counters + (int64_t)seq * p.num_kv_heads + kvh, p.epoch,
-                                      arrivals < 0 ? nparts_seq : arrivals, p.err);
-    __syncthreads();
-    if (last_flag) {
-        __threadfence();
-        fused_combine<BF16, D>(p, seq, kvh, p.prefix_parts + nparts_seq, scratch, scratch_bytes,
-                               blockDim.x);
+    if (nparts_seq > 0 && p.counters != nullptr && !use_flags) {
+        if (threadIdx.x == 0)
+            all_ready = arrive_last(p.counters + (int64_t)seq * p.num_kv_heads + kvh, p.epoch,
+                                    nchunks, p.err);
+        __syncthreads();
+        if (!all_ready) return;
+    } else if (nparts_seq > 0 && p.flags != nullptr) {
+        unsigned int *flag = p.flags + ((int64_t)seq * p.num_kv_heads + kvh) * p.ws_parts;
+        if (chunk + 1 < nchunks) {
+            if (threadIdx.x == 0) flag_release(flag + chunk, p.epoch);
+            return;
+        }
+        if (threadIdx.x < 32) {
+            bool ok = true;
+            for (int k = threadIdx.x; k < nchunks - 1; k += 32) {
+                if (flag_wait(flag + k, p.epoch))
+                    flag[k] = 0u;
+                else
+                    ok = false;
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            if (threadIdx.x == 0) {
+                all_ready = ok;
+                if (!ok) record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+            }
+        }
+        __syncthreads();
+        if (!all_ready) return;
     }
+    fused_combine<BF16, D>(p, seq, kvh, p.prefix_parts + nparts_seq, scratch, scratch_bytes,
+                           blockDim.x);
 }
 
 // Kernel launch with programmatic stream serialization allowed (PDL).

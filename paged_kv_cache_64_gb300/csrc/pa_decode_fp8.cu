@@ -995,9 +995,9 @@ __global__ void __launch_bounds__(F8Shape<D, GM>::THREADS, 1)
         tmem_dealloc(tmem, S::COLS);
     }
     if (!direct && !*abort_flag && p.counters != nullptr)
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem + S::OFF_STG),
-                             (S::NK + S::NV) * S::STG_BYTES,
-                             (nparts_seq + R - 1) / R);
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, part, (nparts_seq + R - 1) / R, p.one_wave,
+                             reinterpret_cast<float *>(smem + S::OFF_STG),
+                             (S::NK + S::NV) * S::STG_BYTES);
 }
 
 using F8Kernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);

@@ -18,14 +18,21 @@
 // MN-major A operand); the softmax warps read S^T and O^T out of TMEM one
 // row (position, or dimension) per thread.
 //
-// Roles (6 warps):
+// Roles (7 warps; 6 in the variant with several partitions a CTA, whose
+// warp 1 issues both products, so that its larger register state still
+// fits two CTAs an SM):
 //   warp 0      producer: block-table lookups and TMA tensor copies of 16-row
 //               boxes (one per 16 positions and 64 dims) into the K and V tiles;
-//   warp 1      allocates the 64 TMEM columns; lane 0 issues every MMA and
-//               commits its completion to mbarriers;
+//   warp 1      allocates the 64 TMEM columns; lane 0 issues the q.K^T MMAs
+//               and commits their completion to mbarriers;
 //   warps 2..5  softmax / epilogue: thread r owns TMEM lane r (position r of a
 //               tile for S, dimension r for O); they also write q and P^T into
-//               shared memory in the operand layout (K-major, 128-byte swizzle).
+//               shared memory in the operand layout (K-major, 128-byte swizzle);
+//   warp 6      lane 0 issues the P.V MMAs.
+// A small tcgen05.mma takes tens of nanoseconds to issue from one thread and
+// a tile needs 4 to 8 q.K^T and 8 P.V instructions, so the two products are
+// issued from different warps: q.K^T of the next tile never queues behind
+// P.V of this one.
 // Online softmax with the same lazy rescale as the CUDA-core kernel; the
 // accumulator lives in registers (thread = dimension) and takes each tile's
 // O^T from a double-buffered TMEM slot.
@@ -46,8 +53,12 @@ namespace pa {
 constexpr int kTcTile = 128;       // positions per tile (MMA M of q.K^T)
 constexpr int kTcN = 16;           // MMA N: the query heads of a group, zero-padded
 constexpr int kTcG = 8;            // largest group the kernel serves
-constexpr int kTcWarps = 6;
-constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcPvWarp = 6;       // issuer of the P.V MMAs (variants without SPAN)
+// Warps of a variant: the P.V issuer's warp is left out of the SPAN one.
+template <bool SPAN>
+constexpr int tc_warps() {
+    return SPAN ? 6 : 7;
+}
 constexpr int kTcCols = 64;        // TMEM columns: S x2 and O x2, 16 fp32 columns each
 constexpr int kSCol0 = 0, kOCol0 = 32;
 
@@ -113,10 +124,10 @@ struct TcShape {
 
 // SPAN: a CTA may compute several consecutive partitions (p.span > 1).
 // COMPACT: the launch uses a compact grid (p.compact).  Every variant runs
-// two CTAs an SM (shared memory allows no more), so registers are capped
-// for two.
+// two CTAs an SM (shared memory allows no more), so registers are capped for
+// two.
 template <bool BF16, int D, bool SPAN, bool COMPACT>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
     paged_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v) {
     using S = TcShape<D>;
@@ -126,6 +137,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::OFF_MISC + 8);
+    // P.V MMAs issued so far (written by the P.V issuer, read by the q.K^T one)
+    volatile int *pv_issued = reinterpret_cast<volatile int *>(smem + S::OFF_MISC + 12);
     float *red = reinterpret_cast<float *>(smem + S::OFF_RED);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,15 +148,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
-    pdl_wait();  // inputs may come from the previous kernel on the stream
-    int part, kvh, seq;  // split-KV chunk (span of partitions), KV head, sequence
-    if constexpr (COMPACT) {
-        if (!compact_item(p, blockIdx.x, &seq, &part, &kvh)) return;  // past the last item
-    } else {
-        part = blockIdx.x;
-        kvh = blockIdx.y;
-        seq = blockIdx.z;
+    // The CTA's TMEM columns, for all its items (allocated while an earlier
+    // kernel on the stream may still be finishing: it touches no input)
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTcCols);
+        tmem_relinquish();
     }
+    pdl_wait();  // inputs may come from the previous kernel on the stream
+
+    // One work item: split-KV chunk `part` (a span of partitions) of KV head
+    // kvh of sequence seq; `another` when the CTA has a next item.  false when
+    // the CTA aborted (a bounded wait gave up).
+    auto process = [&](const int seq, const int part, const int kvh, const bool use_flags,
+                       const bool another) -> bool {
     const int L = item_len(p, seq, threadIdx.x == 0 && part == 0 && kvh == 0);
     const int nparts_seq = L == 0 ? 0 : (L - 1) / P + 1;
     // partitions [part0, part0 + R) of the sequence: this CTA's span
@@ -154,7 +171,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (p.prefix_parts > 0) {
             // empty cascade tail: the output is the prefix's partials combined
             if (nparts_seq == 0 && part == 0)
-                finish_item<BF16, D>(p, seq, kvh, 0, reinterpret_cast<float *>(smem), S::OFF_Q);
+                finish_item<BF16, D>(p, seq, kvh, 0, 0, 1, false, reinterpret_cast<float *>(smem),
+                                     S::OFF_Q);
         } else if (p.mode == 0) {
             if (part == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
@@ -172,7 +190,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
                 }
         }
-        return;
+        return true;
     }
     const int part_end = (part0 + R < nparts_seq) ? part0 + R : nparts_seq;  // past the last
     const int end = (part_end * P < L) ? part_end * P : L;
@@ -200,7 +218,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         qv[j] = make_uint4(0, 0, 0, 0);
         const int ci = threadIdx.x - 64 + 128 * j;  // softmax threads: 0..127
         const int g = ci / (D / 8), c = ci % (D / 8);
-        if (warp >= 2 && g < G)
+        if (warp >= 2 && warp < kTcPvWarp && g < G)
             qv[j] = *reinterpret_cast<const uint4 *>(
                 p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * 8);
     }
@@ -211,11 +229,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const int counts[kKFull0] = {4, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4, 1};
         for (int b = 0; b < kNumTcBars; ++b) mbar_init(&bar[b], b < kKFull0 ? counts[b] : 1);
         *abort_flag = 0;
+        *pv_issued = 0;
         mbar_init_fence();
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, kTcCols);
-        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -344,7 +359,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kPreReady]);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && SPAN) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
             constexpr uint32_t idesc_qk = f16_idesc(BF16, false, false, kTcTile, kTcN);
@@ -404,6 +419,79 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                 } else if ((++spins & 31) == 0 && global_timer_ns() - since > kWaitLimitNs) {
                     ok = false;
                 }
+            }
+            if (!ok) {
+                record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- q.K^T issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = f16_idesc(BF16, false, false, kTcTile, kTcN);
+            const uint32_t sbase = smem_addr(smem);
+            bool ok = mbar_wait(&bar[kQReady], 0);
+            for (int nq = 0; ok && nq < ntiles; ++nq) {
+                // tile nq's K has landed and its S buffer has been read
+                ok = mbar_wait(&bar[kKFull0 + nq % S::NK], (nq / S::NK) & 1) &&
+                     (nq < 2 || mbar_wait(&bar[kSEmpty0 + (nq & 1)], ((nq >> 1) - 1) & 1));
+                if (ok && nq > 0 && nq + 1 == ntiles) {
+                    // q.K^T of the last tile only once P.V of every earlier tile
+                    // is issued (see the stale-row zeroing in the softmax)
+                    const unsigned long long t0 = global_timer_ns();
+                    while (*pv_issued < nq) {
+                        if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (!ok) break;
+                const int b = nq & 1;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = (ks >> 2) * S::SLAB + (ks & 3) * 32;
+                    const uint32_t qoff = (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
+                    tc_mma(tmem + kSCol0 + 16 * b,
+                           sw128_desc(sbase + S::OFF_K + (nq % S::NK) * S::K_STAGE + koff, 16, 1024),
+                           sw128_desc(sbase + S::OFF_Q + qoff, 16, 1024), idesc_qk, ks > 0);
+                }
+                tc_commit(&bar[kSFull0 + b]);
+                tc_commit(&bar[kKEmpty0 + nq % S::NK]);
+            }
+            if (!ok) {
+                record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+    } else if (!SPAN && warp == kTcPvWarp) {
+        // ---------------------------------------------------------- P.V issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_pv = f16_idesc(BF16, true, false, 128, kTcN);
+            const uint32_t sbase = smem_addr(smem);
+            bool ok = true;
+            for (int nv = 0; ok && nv < ntiles; ++nv) {
+                // tile nv's V has landed, its P is written, its O buffer has
+                // been accumulated from tile nv - 2
+                const int b = nv & 1;
+                ok = mbar_wait(&bar[kVFull0 + nv % S::NV], (nv / S::NV) & 1) &&
+                     mbar_wait(&bar[kPFull0 + b], (nv >> 1) & 1) &&
+                     (nv < 2 || mbar_wait(&bar[kOEmpty0 + b], ((nv >> 1) - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kTcTile / 16; ++ks) {
+                    const uint32_t voff = ks * 2048;  // 16 positions = two 8-row groups
+                    const uint32_t poff = b * S::P_BYTES + (ks >> 2) * (kTcN * 128) + (ks & 3) * 32;
+                    tc_mma(tmem + kOCol0 + 16 * b,
+                           sw128_desc(sbase + S::OFF_V + (nv % S::NV) * S::V_STAGE + voff, S::SLAB,
+                                      1024),
+                           sw128_desc(sbase + S::OFF_P + poff, 16, 1024), idesc_pv, ks > 0);
+                }
+                tc_commit(&bar[kOFull0 + b]);
+                tc_commit(&bar[kVEmpty0 + nv % S::NV]);
+                *pv_issued = nv + 1;
             }
             if (!ok) {
                 record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
@@ -678,7 +766,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     pdl_trigger();
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) {
+    const bool aborted = *abort_flag != 0;
+    if (aborted && threadIdx.x == 0) {
         // let copies and MMAs still in flight finish before shared memory and
         // TMEM are released (each wait is bounded)
         for (int ks = 0; ks < S::NK && ks < ntiles; ++ks) {
@@ -691,14 +780,49 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             (void)mbar_wait(&bar[kVEmpty0 + vs], (tl / S::NV) & 1);
         }
     }
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, kTcCols);
+    if (aborted) return false;
+    if (!direct && (p.counters != nullptr || p.prefix_parts > 0))
+        finish_item<BF16, D>(p, seq, kvh, nparts_seq, part, (nparts_seq + R - 1) / R, use_flags,
+                             reinterpret_cast<float *>(smem), S::OFF_Q);
+    if (another && threadIdx.x == 0) {
+        // the last stages' release arrivals (MMA commits nobody waited for)
+        // land before the barriers are set up again for the CTA's next item
+        for (int ks = 0; ks < S::NK && ks < ntiles; ++ks) {
+            const int tl = ks + S::NK * ((ntiles - 1 - ks) / S::NK);
+            (void)mbar_wait(&bar[kKEmpty0 + ks], (tl / S::NK) & 1);
+        }
+        for (int vs = 0; vs < S::NV && vs < ntiles; ++vs) {
+            const int tl = vs + S::NV * ((ntiles - 1 - vs) / S::NV);
+            (void)mbar_wait(&bar[kVEmpty0 + vs], (tl / S::NV) & 1);
+        }
     }
-    if (!direct && !*abort_flag && (p.counters != nullptr || p.prefix_parts > 0))
-        finish_item<BF16, D>(p, seq, kvh, nparts_seq, reinterpret_cast<float *>(smem), S::OFF_Q,
-                              (nparts_seq + R - 1) / R);
+    return true;
+    };  // process
+
+    if constexpr (COMPACT) {
+        // Compact grid: CTA b takes items b, b + gridDim.x, ... in order
+        // (more than one when the grid was capped at the resident slots).
+        // When the grid is resident at once (p.one_wave) and every item has
+        // its own CTA, the combine may use ready flags.
+        int len[kCompactGroups];
+        compact_lens(p, len);
+        int seq = 0, part = 0, kvh = 0, total = 0;
+        int c = blockIdx.x;
+        bool more = compact_find(p, len, c, &seq, &part, &kvh, &total);
+        const bool use_flags = p.one_wave && total <= (int)gridDim.x;
+        while (more && process(seq, part, kvh, use_flags, c + (int)gridDim.x < total)) {
+            c += gridDim.x;
+            more = c < total && compact_find(p, len, c, &seq, &part, &kvh, &total);
+        }
+    } else {
+        (void)process(blockIdx.z, blockIdx.x, blockIdx.y, p.one_wave != 0, false);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(*tmem_slot, kTcCols);
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -794,7 +918,7 @@ int tc_ctas_per_sm(bool bf16, int head_dim) {
     const int by_smem = smem_sm / (smem + reserved);
     const int regs = (a.numRegs + 7) / 8 * 8;
     const int warps_per_subpartition = 16384 / (regs * 32);
-    const int by_regs = 4 * warps_per_subpartition / kTcWarps;
+    const int by_regs = 4 * warps_per_subpartition / tc_warps<false>();
     const int by_tmem = 512 / kTcCols;
     int n = by_smem < by_regs ? by_smem : by_regs;
     n = n < by_tmem ? n : by_tmem;
@@ -812,8 +936,21 @@ pa_status launch_decode_tc(const DecodeParams &prm, bool bf16, int head_dim, int
     if (!pool_tensor_map(&mk, prm.k_pool, rows, head_dim, bf16) ||
         !pool_tensor_map(&mv, prm.v_pool, rows, head_dim, bf16))
         return PA_ERR_CUDA;
-    const dim3 grid = decode_grid(prm, num_partitions, num_kv_heads, num_seqs);
-    if (launch_pdl(k, grid, dim3(kTcThreads), (size_t)smem, stream, prm, mk, mv) != cudaSuccess)
+    dim3 grid = decode_grid(prm, num_partitions, num_kv_heads, num_seqs);
+    DecodeParams p = prm;
+    if (p.compact) {
+        // Compact grids whose upper bound (every sequence at the longest
+        // length) is within four waves: one CTA a resident slot, each taking
+        // every gridDim.x-th item, so that the CTAs a short batch does not
+        // need are never launched (each would hold a slot for a memory round
+        // trip only to find nothing to do, at the end of the launch).  Larger
+        // grids keep one item a CTA, balanced by the hardware scheduler.
+        const unsigned slots = (unsigned)(sm_count() * tc_ctas_per_sm(bf16, head_dim));
+        if (slots > 0 && grid.x > slots && grid.x <= 4 * slots) grid.x = slots;
+        p.one_wave = slots > 0 && grid.x <= slots;
+    }
+    const int threads = 32 * (prm.span > 1 ? tc_warps<true>() : tc_warps<false>());
+    if (launch_pdl(k, grid, dim3(threads), (size_t)smem, stream, p, mk, mv) != cudaSuccess)
         return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

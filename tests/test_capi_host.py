@@ -99,7 +99,8 @@ def test_workspace_size_layout(lib):
     NP = 4
     rows = S * hq * NP
     a = lambda x: (x + 255) // 256 * 256
-    want = a(rows * 4) * 2 + a(rows * d * 4) + a(S * hkv * 8)  # + one counter per (seq, kv head)
+    # + the fused combine: a 64-bit counter per (seq, kv head), a 32-bit flag per partition
+    want = a(rows * 4) * 2 + a(rows * d * 4) + a(S * hkv * 8) + a(S * hkv * NP * 4)
     assert lib.pa_decode_workspace_size(S, hq, hkv, d, 16, maxlen, P, 1) == want
     assert lib.pa_decode_workspace_size(S, hq, 2, d, 16, maxlen, -1, 1) == 0
 

@@ -149,7 +149,7 @@ SHAPES = {
     # 1,008 = 7 full tiles of 128 and one of 112; 280 query rows = 3 row tiles, the last ragged;
     # tails from 0 (the sequence is all prefix) upwards
     "qwen_g7_partial_tile": (40, 14, 2, 64, 16, "f16", 1008, (0, 300), False),
-    # long tails: the tail pass splits into partitions (arrival counters)
+    # long tails: the tail pass splits into partitions (ready flags)
     "g8_long_tails": (5, 64, 8, 128, 16, "bf16", 2048, (1000, 3000), True),
     # one query head per KV head; 130 rows = 2 row tiles
     "mha_b32": (130, 4, 4, 128, 32, "bf16", 512, (1, 64), True),
@@ -229,7 +229,7 @@ def test_invalid_prefix_len_rejected_on_host():
 
 def test_graph_replay():
     """Captured once, replayed: the same output each time (the workspace is
-    scratch and its counters carry over between replays)."""
+    scratch and its ready flags carry over between replays)."""
     c = SharedPrefix(5, 64, 8, 128, 16, "bf16", 2048, np.array([1200, 2900, 5, 2000, 1700]),
                      seed=11, step=False)
     hk, hv = bits(c.kp), bits(c.vp)

@@ -296,9 +296,9 @@ def test_decode_step_fused_matches_oracle(name, kw, partition):
 
 
 def test_fused_combine_garbage_workspace_and_graph_replay():
-    """The fused combine's counters need no initialisation (garbage
+    """The fused combine's ready flags need no initialisation (garbage
     workspace), and a CUDA graph of the step replays correctly (each replay
-    reuses the captured epoch; the last CTA resets the count)."""
+    reuses the captured epoch; the combining CTA clears the flags it read)."""
     case = Case(workloads.make_plan("llama", num_seqs=6, len_range=(900, 2100)))
     spec, P = case.spec, 512
     size = api.workspace_size(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
@@ -570,3 +570,28 @@ def test_decode_compact_grid_mixed_lengths(span, num_seqs, partition, R):
                         case.spec.dtype)
     assert torch.all(out[torch.as_tensor(pick[:6], device="cuda")] == 0)
     assert_close(out, ref, f"compact S={num_seqs} P={partition} R={R}")
+
+
+# ------------------------- compact grid capped at the resident slots
+@pytest.mark.parametrize("hq,hkv,d,dtype,num_seqs,lens,partition,R,fused", [
+    (14, 2, 64, "f16", 100, (2000, 3000), 512, 1, False),   # ~1,000 items, 304 CTAs
+    (14, 2, 64, "f16", 100, (2000, 3000), 256, 2, True),    # the same with two partitions a CTA
+    (32, 8, 128, "bf16", 40, (1100, 1500), 512, 1, True),   # d = 128: 960 items
+])
+def test_decode_compact_several_items_per_cta(span, hq, hkv, d, dtype, num_seqs, lens, partition,
+                                              R, fused):
+    """A compact launch whose upper bound (every sequence at the longest
+    length) is within four waves runs one CTA a resident slot; when the
+    batch has more items than that, each CTA computes several in turn and the
+    arrival counters pick the combining CTA.  Every output."""
+    span(R)
+    case = Case(workloads.make_shape_plan(num_seqs, hq, hkv, d, 16, dtype, lens, seed=71 + d))
+    hk, hv = case.snapshot(0)
+    if fused:
+        out = case.gpu_step_fused(0, partition)
+    else:
+        case.gpu_writes(0)
+        out = case.gpu_decode(0, partition)
+    api.check_error()
+    ref = case.oracle_step(0, hk, hv)
+    assert_close(out, ref, f"several items a CTA S={num_seqs} d={d} P={partition} R={R}")
