@@ -113,7 +113,9 @@ struct TcShape {
     static constexpr int OFF_PEND = OFF_PRE + PRE_BYTES;
     static constexpr int OFF_BAR = OFF_PEND + 2 * PEND_FLOATS * 4;
     static constexpr int OFF_MISC = OFF_BAR + kNumTcBars * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
+    // compact grids: the batch's lengths, kept for the CTA's later items
+    static constexpr int OFF_LENS = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = OFF_LENS + kCompactMaxSeqs * 4 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_V % 1024 == 0 && OFF_K % 1024 == 0 && OFF_Q % 1024 == 0 &&
                   OFF_P % 1024 == 0, "atom alignment");
     static_assert(OFF_V + (NV - 1) * V_STAGE + 2 * SLAB <= OFF_BAR, "V^T operand rows in bounds");
@@ -799,20 +801,42 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
     return true;
     };  // process
 
-    if constexpr (COMPACT) {
+    if constexpr (COMPACT && SPAN) {
+        // (several partitions a CTA serve long batches, whose compact grids
+        // are never capped: one item a CTA)
+        int seq = 0, part = 0, kvh = 0;
+        if (compact_item(p, blockIdx.x, &seq, &part, &kvh))
+            (void)process(seq, part, kvh, false, false);
+    } else if constexpr (COMPACT) {
         // Compact grid: CTA b takes items b, b + gridDim.x, ... in order
         // (more than one when the grid was capped at the resident slots).
         // When the grid is resident at once (p.one_wave) and every item has
         // its own CTA, the combine may use ready flags.
-        int len[kCompactGroups];
-        compact_lens(p, len);
+        // (the lengths wait in shared memory while an item runs: no registers
+        // held across it)
+        int *lens_smem = reinterpret_cast<int *>(smem + S::OFF_LENS);
         int seq = 0, part = 0, kvh = 0, total = 0;
-        int c = blockIdx.x;
-        bool more = compact_find(p, len, c, &seq, &part, &kvh, &total);
+        bool more;
+        {
+            int len[kCompactGroups];
+            compact_lens(p, len);
+            more = compact_find(p, len, blockIdx.x, &seq, &part, &kvh, &total);
+            if (warp == 0) {
+#pragma unroll
+                for (int k = 0; k < kCompactGroups; ++k) lens_smem[32 * k + lane] = len[k];
+            }
+        }
         const bool use_flags = p.one_wave && total <= (int)gridDim.x;
-        while (more && process(seq, part, kvh, use_flags, c + (int)gridDim.x < total)) {
+        for (int c = blockIdx.x;
+             more && process(seq, part, kvh, use_flags, c + (int)gridDim.x < total);) {
             c += gridDim.x;
-            more = c < total && compact_find(p, len, c, &seq, &part, &kvh, &total);
+            more = c < total;
+            if (more) {
+                int len[kCompactGroups];
+#pragma unroll
+                for (int k = 0; k < kCompactGroups; ++k) len[k] = lens_smem[32 * k + lane];
+                more = compact_find(p, len, c, &seq, &part, &kvh, &total);
+            }
         }
     } else {
         (void)process(blockIdx.z, blockIdx.x, blockIdx.y, p.one_wave != 0, false);
@@ -946,8 +970,8 @@ pa_status launch_decode_tc(const DecodeParams &prm, bool bf16, int head_dim, int
         // trip only to find nothing to do, at the end of the launch).  Larger
         // grids keep one item a CTA, balanced by the hardware scheduler.
         const unsigned slots = (unsigned)(sm_count() * tc_ctas_per_sm(bf16, head_dim));
-        if (slots > 0 && grid.x > slots && grid.x <= 4 * slots) grid.x = slots;
-        p.one_wave = slots > 0 && grid.x <= slots;
+        if (p.span <= 1 && slots > 0 && grid.x > slots && grid.x <= 4 * slots) grid.x = slots;
+        p.one_wave = p.span <= 1 && slots > 0 && grid.x <= slots;
     }
     const int threads = 32 * (prm.span > 1 ? tc_warps<true>() : tc_warps<false>());
     if (launch_pdl(k, grid, dim3(threads), (size_t)smem, stream, p, mk, mv) != cudaSuccess)

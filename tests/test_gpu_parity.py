@@ -575,15 +575,16 @@ def test_decode_compact_grid_mixed_lengths(span, num_seqs, partition, R):
 # ------------------------- compact grid capped at the resident slots
 @pytest.mark.parametrize("hq,hkv,d,dtype,num_seqs,lens,partition,R,fused", [
     (14, 2, 64, "f16", 100, (2000, 3000), 512, 1, False),   # ~1,000 items, 304 CTAs
-    (14, 2, 64, "f16", 100, (2000, 3000), 256, 2, True),    # the same with two partitions a CTA
+    (14, 2, 64, "f16", 100, (2000, 3000), 512, 1, True),    # the same, fused cache write
     (32, 8, 128, "bf16", 40, (1100, 1500), 512, 1, True),   # d = 128: 960 items
 ])
 def test_decode_compact_several_items_per_cta(span, hq, hkv, d, dtype, num_seqs, lens, partition,
                                               R, fused):
-    """A compact launch whose upper bound (every sequence at the longest
-    length) is within four waves runs one CTA a resident slot; when the
-    batch has more items than that, each CTA computes several in turn and the
-    arrival counters pick the combining CTA.  Every output."""
+    """A compact launch (one partition a CTA) whose upper bound (every
+    sequence at the longest length) is within four waves runs one CTA a
+    resident slot; when the batch has more items than that, each CTA
+    computes several in turn and the arrival counters pick the combining
+    CTA.  Every output."""
     span(R)
     case = Case(workloads.make_shape_plan(num_seqs, hq, hkv, d, 16, dtype, lens, seed=71 + d))
     hk, hv = case.snapshot(0)
