@@ -400,7 +400,12 @@ class GpuStep:
         self.write_bytes = workloads.cache_write_bytes(spec, spec.num_seqs, kvb)
         self.copy_bytes = 2 * 2 * len(self.lay.pre_copies) * spec.num_kv_heads * \
             spec.block_size * spec.head_dim * (kvb or workloads.DTYPE_BYTES[spec.dtype])
-        NP = -(-self.max_seq_len // self.resolved_P) if self.resolved_P and self.resolved_P > 0 else 1
+        # positions a partial covers (the partition times the partitions a
+        # CTA merges), hence the partials per row and the launches
+        self.partial_tokens = api.partial_tokens(
+            spec.num_seqs, spec.num_kv_heads, self.max_seq_len, spec.head_dim, spec.block_size,
+            spec.num_q_heads // spec.num_kv_heads, self.vals.q.dtype, self.P, fp8=self.fp8)
+        NP = -(-self.max_seq_len // self.partial_tokens) if self.partial_tokens > 0 else 1
         # fused write + decode (+ combine) launch, a separate combine above 8
         # partitions, and the copy-on-write copies when there are any
         per_layer = 1 + (1 if NP > 8 else 0) + (1 if len(self.lay.pre_copies) else 0)
@@ -705,6 +710,7 @@ def run_gpu(args, rank, world, local_rank):
             "block_size": spec.block_size, "layers": spec.num_layers,
             "mean_seq_len": float(np.mean(st.lay.seq_lens)),
             "partition_tokens": st.resolved_P,
+            "partial_tokens": st.partial_tokens,
             "decode_ctas_per_sm": api.ctas_per_sm(spec.head_dim,
                                                   spec.num_q_heads // spec.num_kv_heads,
                                                   st.vals.q.dtype),

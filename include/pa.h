@@ -140,10 +140,13 @@ pa_status pa_copy_blocks(void *const *k_pools, void *const *v_pools, int num_lay
  * pa_decode_workspace_size(...) bytes (device memory, 256-byte aligned); it
  * is scratch, overwritten on every call, and may be NULL when the size is 0.
  * It needs no initialisation: besides the partials it holds one arrival
- * counter per (sequence, KV head), tagged with a per-call epoch so that
- * stale contents read as zero; when a sequence has at most 8 partitions the
- * last CTA to finish combines them (one launch), otherwise a separate
- * combine kernel runs.  Launches use programmatic dependent launch: each
+ * counter per (sequence, KV head) and one ready flag per partial, tagged
+ * with a per-call epoch so that stale contents read as zero; when a
+ * sequence has at most 8 partials one CTA of the launch combines them (one
+ * launch), otherwise a separate combine kernel runs.  When a CTA computes
+ * several consecutive partitions (see pa_set_decode_span), it combines them
+ * as it goes (the online softmax's rescale is the combine formula) and
+ * leaves one partial for its span.  Launches use programmatic dependent launch: each
  * kernel waits for the previous work on the stream before reading memory.
  *
  * Arguments (device pointers unless stated):
@@ -297,6 +300,16 @@ size_t pa_decode_fp8_workspace_size(int num_seqs, int num_q_heads, int num_kv_he
  * (-1 means it will run single pass).  Needs the current CUDA device. */
 int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
                              int block_size, int group_size, pa_dtype dtype);
+/* Positions each split-KV partial of pa_decode (fp8 = 0) or pa_decode_fp8
+ * (fp8 = 1) covers for these shapes and partition_tokens (0 = automatic):
+ * the partition size times the partitions one CTA merges (see
+ * pa_set_decode_span), or -1 for single pass.  The decode writes
+ * ceil(max_seq_len / this) partials per (sequence, query head) and combines
+ * them inside the launch when there are at most 8.  -2 for unsupported or
+ * invalid shapes.  Needs the current CUDA device. */
+int pa_decode_partial_tokens(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
+                             int block_size, int group_size, int partition_tokens, pa_dtype dtype,
+                             int fp8);
 /* The same for pa_decode_fp8 (E4M3 pools; coarser partitions). */
 int pa_decode_fp8_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
                                  int block_size, int group_size, pa_dtype dtype);
@@ -316,8 +329,10 @@ int pa_get_decode_impl(void);
  * later call: 0 automatic (default: several consecutive partitions a CTA
  * when partitions are short and the grid keeps at least two waves of CTAs),
  * n >= 1 that many wherever partitions are a multiple of 128 positions (256
- * over E4M3 pools; 1 elsewhere).  Each partition still gets its own (m, l, O) partial, so the
- * result is the same for any setting (within the output tolerance).  Returns
+ * over E4M3 pools; 1 elsewhere).  pa_decode_partitions writes each
+ * partition's own (m, l, O) partial; the decode entry points merge a CTA's
+ * partitions into one partial.  The result is the same for any setting
+ * (within the output tolerance).  Returns
  * the previous setting, or -1 (nothing changed) for a negative value.  Not
  * synchronised with decode calls running on other host threads. */
 int pa_set_decode_span(int span);

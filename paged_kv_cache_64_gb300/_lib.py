@@ -72,6 +72,8 @@ SIGNATURES = {
                                           _c_int]),
     "pa_decode_fp8_auto_partition": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                           _c_int]),
+    "pa_decode_partial_tokens": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                          _c_int, _c_int]),
     "pa_decode_ctas_per_sm": (_c_int, [_c_int, _c_int, _c_int]),
     "pa_set_decode_impl": (_c_int, [_c_int]),
     "pa_get_decode_impl": (_c_int, []),

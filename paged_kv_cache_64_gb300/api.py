@@ -119,6 +119,15 @@ def auto_partition(num_seqs, num_kv_heads, max_seq_len, head_dim, block_size, gr
     return fn(num_seqs, num_kv_heads, max_seq_len, head_dim, block_size, group, _DTYPES[dtype])
 
 
+def partial_tokens(num_seqs, num_kv_heads, max_seq_len, head_dim, block_size, group, dtype,
+                   partition_tokens=0, fp8=False):
+    """Positions each split-KV partial of decode (or decode_fp8) covers: the
+    partition size times the partitions one CTA merges; -1 for single pass."""
+    return _lib.load().pa_decode_partial_tokens(num_seqs, num_kv_heads, max_seq_len, head_dim,
+                                                block_size, group, int(partition_tokens),
+                                                _DTYPES[dtype], int(bool(fp8)))
+
+
 DECODE_IMPLS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
 
 

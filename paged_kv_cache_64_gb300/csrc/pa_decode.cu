@@ -800,8 +800,9 @@ struct ResolvedDecode {
     bool tc;  // tensor-core kernel (pa_decode_tc.cu) instead of the CUDA-core one
     bool bf16;
     int head_dim;
-    int P;    // -1 single pass, else partition size
-    int NP;   // partitions (partial slots per row)
+    int P;    // -1 single pass, else the positions of a partial (a chunk, see resolve)
+    int NP;   // partials per row
+    int part_tokens;  // the partition size asked for (or chosen when automatic)
     bool fp8 = false;  // E4M3 pools: the FP8 tensor-core kernel (pa_decode_fp8.cu)
     int span = 1;      // partitions per CTA (tensor-core kernel); grid.x = ceil(NP / span)
 };
@@ -828,7 +829,7 @@ static bool use_tensor_cores(int head_dim, int group) {
 
 static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                          int block_size, int max_seq_len, int partition_tokens, pa_dtype dtype,
-                         ResolvedDecode *r, bool fp8 = false) {
+                         ResolvedDecode *r, bool fp8 = false, bool merge_span = true) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0)
         return PA_ERR_INVALID;
     if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_INVALID;  // grid y and z
@@ -879,6 +880,20 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
             while (R > 1 && 4.0 * R * P > share) --R;
         }
         r->span = R > 1 ? R : 1;
+    }
+    r->part_tokens = P;
+    if (merge_span && r->span > 1) {
+        // Decode (the output, not the partials, is the result): a CTA's span
+        // of consecutive partitions reaches HBM as one partial.  The online
+        // softmax runs on across their boundaries; its rescale is the
+        // cross-partition combine ([P3] section 4, step 3) applied as each
+        // partition arrives, so the CTA leaves the combine of its span, and
+        // the launch sees chunks of span * P positions with one partial each
+        // (pa_decode_partitions keeps one partial per partition).
+        r->P = P * r->span;
+        r->NP = (max_seq_len + r->P - 1) / r->P;
+        if (r->NP < 1) r->NP = 1;
+        r->span = 1;
     }
     return PA_OK;
 }
@@ -1090,7 +1105,18 @@ int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, in
     if (group_size < 1 || resolve(num_seqs, num_kv_heads * group_size, num_kv_heads, head_dim,
                                   block_size, max_seq_len, 0, dtype, &r) != PA_OK)
         return -1;
-    return r.P;
+    return r.part_tokens;
+}
+
+int pa_decode_partial_tokens(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
+                             int block_size, int group_size, int partition_tokens, pa_dtype dtype,
+                             int fp8) {
+    ResolvedDecode r;
+    if (group_size < 1 || resolve(num_seqs, num_kv_heads * group_size, num_kv_heads, head_dim,
+                                  block_size, max_seq_len, partition_tokens, dtype, &r,
+                                  fp8 != 0) != PA_OK)
+        return -2;
+    return r.P > 0 ? r.P : -1;
 }
 
 int pa_decode_fp8_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
@@ -1099,7 +1125,7 @@ int pa_decode_fp8_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len
     if (group_size < 1 || resolve(num_seqs, num_kv_heads * group_size, num_kv_heads, head_dim,
                                   block_size, max_seq_len, 0, dtype, &r, true) != PA_OK)
         return -1;
-    return r.P;
+    return r.part_tokens;
 }
 
 int pa_set_decode_impl(int impl) {
@@ -1127,7 +1153,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                 pa_dtype dtype) {
     ResolvedDecode r;
     if (resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
-                partition_tokens, dtype, &r) != PA_OK)
+                partition_tokens, dtype, &r, false, false) != PA_OK)
         return 0;
     if (r.P <= 0) return 0;
     return workspace_layout(num_seqs, num_q_heads, head_dim, r.NP, num_kv_heads).bytes;
@@ -1294,7 +1320,7 @@ pa_status pa_decode_partitions(const void *q, const void *k_pool, const void *v_
     if (partition_tokens <= 0) return PA_ERR_INVALID;
     ResolvedDecode r;
     pa_status st = resolve(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                           max_seq_len, partition_tokens, dtype, &r);
+                           max_seq_len, partition_tokens, dtype, &r, false, false);
     if (st != PA_OK) return st;
     DecodeParams prm;
     st = fill_common(&prm, q, k_pool, v_pool, num_blocks, block_tables, max_blocks_per_seq,

@@ -765,6 +765,19 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
         }
     }
 
+    if (SPAN && p.mode == 1) {
+        // split-KV partitions on their own: the span's partitions past the
+        // sequence's end hold the empty partial (-inf, 0, 0)
+        for (int j = part_end; j < part0 + R && j < p.num_partitions; ++j)
+            for (int g = 0; g < G; ++g) {
+                const int64_t row = part_row(p, seq, kvh * G + g, j);
+                if (threadIdx.x == 0) {
+                    p.part_m[row] = -INFINITY;
+                    p.part_l[row] = 0.f;
+                }
+                for (int x = threadIdx.x; x < D; x += blockDim.x) p.part_o[row * D + x] = 0.f;
+            }
+    }
     pdl_trigger();
     tc_fence_before();
     __syncthreads();

@@ -94,9 +94,10 @@ def test_cascade_validation_before_launch(lib):
 
 
 def test_workspace_size_layout(lib):
-    # explicit partition: m, l (256-aligned) then O
-    S, hq, hkv, d, maxlen, P = 3, 8, 2, 128, 1000, 256
-    NP = 4
+    # explicit partition: m, l (256-aligned) then O (64 positions: never
+    # several partitions a CTA, so one partial per partition)
+    S, hq, hkv, d, maxlen, P = 3, 8, 2, 128, 1000, 64
+    NP = 16
     rows = S * hq * NP
     a = lambda x: (x + 255) // 256 * 256
     # + the fused combine: a 64-bit counter per (seq, kv head), a 32-bit flag per partition

@@ -344,12 +344,20 @@ def test_decode_step_rejects_a_slot_off_the_table():
 
 
 # -------------------------------------------------------- split-KV steps
-@pytest.mark.parametrize("name,kw,P", [("long", {"num_seqs": 2, "len_range": (1500, 2600)}, 512),
-                                       ("tiny", {}, 16),
-                                       ("qwen", {"num_seqs": 8}, 64)])
-def test_partitions_match_oracle(name, kw, P):
+@pytest.mark.parametrize("name,kw,P,R", [
+    ("long", {"num_seqs": 2, "len_range": (1500, 2600)}, 512, 0),
+    ("tiny", {}, 16, 0),
+    ("qwen", {"num_seqs": 8}, 64, 0),
+    ("long", {"num_seqs": 2, "len_range": (1500, 2600)}, 512, 2),   # two partitions a CTA
+    ("long", {"num_seqs": 2, "len_range": (1500, 2600)}, 512, 4),   # ragged last span
+    ("llama", {"num_seqs": 4, "len_range": (300, 1200)}, 256, 4),
+])
+def test_partitions_match_oracle(span, name, kw, P, R):
     """Split-KV step 2 on its own: (m, l, O) per partition against the
-    oracle's partials; empty partitions hold (-inf, 0, 0)."""
+    oracle's partials; empty partitions hold (-inf, 0, 0).  With R > 0 a CTA
+    computes R consecutive partitions and still writes each one's partial."""
+    if R:
+        span(R)
     case = Case(workloads.make_plan(name, **kw))
     case.gpu_writes(0)
     spec = case.spec
