@@ -623,15 +623,39 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
               const int tile0 = start + i * kTcTile;
               const int nvalid = (end - tile0 < kTcTile) ? end - tile0 : kTcTile;
               const bool valid = r < nvalid;
-              // tile max of each head over the 128 positions
+              // tile max of each head over the 128 positions: a halving
+              // butterfly over the warp (each exchange hands the partner the
+              // heads it keeps; 9 shuffles for 8 heads), after which lane L
+              // holds the warp's maximum of head (L >> 2) & 7.  The d = 128
+              // 3-D-grid variant reduces each head on its own (40 shuffles):
+              // the butterfly's extra live registers spill at its cap.
               float *tmax = red + b * (4 * kTcN);
   #pragma unroll
-              for (int g = 0; g < kTcG; ++g) {
-                  s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
-                  float v = s[g];
+              for (int g = 0; g < kTcG; ++g) s[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
+              if constexpr (D == 128 && !SPAN && !COMPACT) {
   #pragma unroll
-                  for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
-                  if (lane == 0) tmax[sw * kTcN + g] = v;
+                  for (int g = 0; g < kTcG; ++g) {
+                      float v = s[g];
+  #pragma unroll
+                      for (int off = 16; off >= 1; off >>= 1)
+                          v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
+                      if (lane == 0) tmax[sw * kTcN + g] = v;
+                  }
+              } else {
+                  const bool b4 = lane & 16, c2 = lane & 8, c1 = lane & 4;
+                  float v4[4], v2[2];
+  #pragma unroll
+                  for (int j = 0; j < 4; ++j)
+                      v4[j] = fmaxf(b4 ? s[4 + j] : s[j],
+                                    __shfl_xor_sync(kFullMask, b4 ? s[j] : s[4 + j], 16));
+  #pragma unroll
+                  for (int j = 0; j < 2; ++j)
+                      v2[j] = fmaxf(c2 ? v4[2 + j] : v4[j],
+                                    __shfl_xor_sync(kFullMask, c2 ? v4[j] : v4[2 + j], 8));
+                  float v = fmaxf(c1 ? v2[1] : v2[0], __shfl_xor_sync(kFullMask, c1 ? v2[0] : v2[1], 4));
+                  v = fmaxf(v, __shfl_xor_sync(kFullMask, v, 2));
+                  v = fmaxf(v, __shfl_xor_sync(kFullMask, v, 1));
+                  if ((lane & 3) == 0) tmax[sw * kTcN + ((lane >> 2) & 7)] = v;
               }
               if (lane == 0) tmax[sw * kTcN + kTcN - 1] = ok ? 1.f : 0.f;  // column 15: health flag
               softmax_bar();
