@@ -138,8 +138,8 @@ def source_digest():
     """Hash of the decode kernel source, to tell whether a stored ncu traffic
     figure still describes the kernel being timed."""
     h = hashlib.sha256()
-    for f in ("pa_decode.cu", "pa_decode_tc.cu", "pa_decode.cuh", "pa_common.cuh",
-              "pa_tcgen05.cuh", "pa_cascade.cu", "pa_decode_fp8.cu"):
+    for f in ("pa_decode.cu", "pa_decode_tc.cu", "pa_decode_tc.cuh", "pa_decode_tc_fp8.cu",
+              "pa_decode.cuh", "pa_common.cuh", "pa_fp8.cuh", "pa_tcgen05.cuh", "pa_cascade.cu"):
         with open(os.path.join(ROOT, "paged_kv_cache_64_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -701,7 +701,8 @@ def run_gpu(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / n_timed,
         "repeats": repeats, "timed_steps": n_timed, "timed_seconds": total_ms / 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": (f"e4m3 K/V ({spec.dtype} q/out, f16 products, fp32 accumulate)" if st.fp8
+        "dtype": (f"e4m3 K/V ({spec.dtype} q/out, E4M3 x E5M2 products, fp32 accumulate)"
+                  if st.fp8
                   else spec.dtype), "data": "synthetic",
         "config": {
             "workload": f"{spec.name}: {spec.describe}",
@@ -723,7 +724,7 @@ def run_gpu(args, rank, world, local_rank):
             "kv_format": ("E4M3 codes, scale 1/64 per pool, quantised from the same N(0,1) "
                           "values" if st.fp8 else spec.dtype),
             "decode_kernel": ("tensor cores (tcgen05 kind::f8f6f4 on the E4M3 codes, q and P as "
-                              "E5M2 terms; at d=64 V widened to f16)") if st.fp8 else
+                              "E5M2 terms)") if st.fp8 else
                              ("CUDA cores" if args.decode_impl == "cuda_cores"
                               else "tensor cores (tcgen05)"),
             "l2": ("inputs larger than L2 (%.2f GB per step)" % (st.step_bytes() / 1e9))

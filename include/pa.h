@@ -280,8 +280,9 @@ pa_status pa_cache_write_fp8(const void *k_new, const void *v_new, const int64_t
  * with s_p = scale * dot(q[i][h], k_scale * K_i[p]) (code values).  q and out
  * are 16-bit (dtype).  With k_new != NULL, each sequence's newest token is
  * first quantised and written as pa_cache_write_fp8 would (the fused step of
- * pa_decode_step).  The tensor-core kernel widens the codes to f16 (exactly)
- * in shared memory and runs its products in f16 with fp32 accumulation.
+ * pa_decode_step).  The tensor-core kernel takes the codes as they are as
+ * E4M3 operands of q.K^T and P.V, with q and P as sums of four E5M2 terms
+ * each and fp32 accumulation.
  * head_dim in {64, 128}, G <= 8, block_size in {16, 32}; partition_tokens
  * and workspace as pa_decode (size from pa_decode_fp8_workspace_size). */
 pa_status pa_decode_fp8(void *out, const void *q, const void *k_new, const void *v_new,
@@ -310,7 +311,7 @@ int pa_decode_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, in
 int pa_decode_partial_tokens(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
                              int block_size, int group_size, int partition_tokens, pa_dtype dtype,
                              int fp8);
-/* The same for pa_decode_fp8 (E4M3 pools; coarser partitions). */
+/* The same for pa_decode_fp8 (E4M3 pools; the same choice as pa_decode). */
 int pa_decode_fp8_auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int head_dim,
                                  int block_size, int group_size, pa_dtype dtype);
 
@@ -328,13 +329,13 @@ int pa_get_decode_impl(void);
 /* Split-KV partitions one tensor-core CTA computes, process-wide, for every
  * later call: 0 automatic (default: several consecutive partitions a CTA
  * when partitions are short and the grid keeps at least two waves of CTAs),
- * n >= 1 that many wherever partitions are a multiple of 128 positions (256
- * over E4M3 pools; 1 elsewhere).  pa_decode_partitions writes each
- * partition's own (m, l, O) partial; the decode entry points merge a CTA's
- * partitions into one partial.  The result is the same for any setting
- * (within the output tolerance).  Returns
- * the previous setting, or -1 (nothing changed) for a negative value.  Not
- * synchronised with decode calls running on other host threads. */
+ * n >= 1 that many wherever partitions are a multiple of 128 positions (1
+ * elsewhere).  pa_decode_partitions writes each partition's own (m, l, O)
+ * partial; the decode entry points merge a CTA's partitions into one
+ * partial.  The result is the same for any setting (within the output
+ * tolerance).  Returns the previous setting, or -1 (nothing changed) for a
+ * negative value.  Not synchronised with decode calls running on other host
+ * threads. */
 int pa_set_decode_span(int span);
 
 /* Resident CTAs per SM of the decode kernel that these shapes select

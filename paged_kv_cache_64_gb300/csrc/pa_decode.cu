@@ -774,14 +774,13 @@ static int decode_ctas_per_sm(const DecodeEntry &e) {
 
 // Automatic partition size: aim for the largest work item to be at most
 // 1/share_div of one CTA slot's share of the whole job (the share taken at
-// the maximum length), in multiples of 256 positions and at least min_tokens,
-// and run single pass when that would not split anything.  share_div is 4
-// for the 16-bit kernels and 8 for the E4M3 kernel (one CTA an SM, so twice
-// the slot share); min_tokens is 512 for 16-bit pools and 1,024 for E4M3
-// ones (the same bytes): coarse enough that a work item's prologue, ring
-// fill and partial writes stay small next to its tiles (the Llama-shaped
-// batch runs single pass), fine enough to split a few long sequences over
-// the GPU.
+// the maximum length), in multiples of 256 positions and at least
+// min_tokens, and run single pass when that would not split anything.
+// share_div is 4 and min_tokens 512, for 16-bit and E4M3 pools alike (a
+// tile's softmax, not its bytes, sets the pace of a short item): coarse
+// enough that a work item's prologue, ring fill and partial writes stay
+// small next to its tiles (the Llama-shaped batch runs single pass), fine
+// enough to split a few long sequences over the GPU.
 static int auto_partition(int S, int Hkv, int max_seq_len, int ctas_per_sm, int block_size,
                           double share_div, int min_tokens) {
     if (max_seq_len <= 0) return -1;
@@ -803,7 +802,7 @@ struct ResolvedDecode {
     int P;    // -1 single pass, else the positions of a partial (a chunk, see resolve)
     int NP;   // partials per row
     int part_tokens;  // the partition size asked for (or chosen when automatic)
-    bool fp8 = false;  // E4M3 pools: the FP8 tensor-core kernel (pa_decode_fp8.cu)
+    bool fp8 = false;  // E4M3 pools: the E4M3 variants of the tensor-core kernel
     int span = 1;      // partitions per CTA (tensor-core kernel); grid.x = ceil(NP / span)
 };
 
@@ -850,8 +849,7 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
         const int per_sm = r->fp8  ? fp8_ctas_per_sm(dtype == PA_BF16, head_dim, G)
                            : r->tc ? tc_ctas_per_sm(dtype == PA_BF16, head_dim)
                                    : decode_ctas_per_sm(r->entry);
-        P = auto_partition(num_seqs, num_kv_heads, max_seq_len, per_sm, block_size,
-                           r->fp8 ? 8.0 : 4.0, r->fp8 ? 1024 : 512);
+        P = auto_partition(num_seqs, num_kv_heads, max_seq_len, per_sm, block_size, 4.0, 512);
     }
     if (P < -1) return PA_ERR_INVALID;
     if (P > 0 && (P % block_size != 0 || P % kUnit != 0)) return PA_ERR_INVALID;
@@ -859,18 +857,15 @@ static pa_status resolve(int num_seqs, int num_q_heads, int num_kv_heads, int he
     r->NP = (P > 0) ? (max_seq_len + P - 1) / P : 1;
     if (r->NP < 1) r->NP = 1;
     r->span = 1;
-    // (E4M3 pools: partitions of an even number of tiles, so that the two
-    // softmax groups meet at each partition's end)
-    if ((r->tc || r->fp8) && P > 0 && P % (r->fp8 ? 256 : 128) == 0) {
+    if ((r->tc || r->fp8) && P > 0 && P % 128 == 0) {
         // One CTA computes several consecutive partitions (each still its own
         // partial) when partitions are short: a CTA's prologue and pipeline
-        // fill are then paid once per ~2048 positions (4,096 of E4M3 pools:
-        // the same bytes), as long as a CTA's span stays within a quarter of
-        // one CTA slot's share of the job (the share taken at the maximum
-        // length, an upper bound), so that short, latency-bound batches keep
-        // one partition a CTA.
+        // fill are then paid once per ~2048 positions, as long as a CTA's
+        // span stays within a quarter of one CTA slot's share of the job (the
+        // share taken at the maximum length, an upper bound), so that short,
+        // latency-bound batches keep one partition a CTA.
         const int forced = g_decode_span.load(std::memory_order_relaxed);
-        int R = forced > 0 ? forced : (r->fp8 ? 4096 : 2048) / P;
+        int R = forced > 0 ? forced : 2048 / P;
         if (R > r->NP) R = r->NP;
         if (forced <= 0) {
             const int slots = sm_count() * (r->fp8 ? fp8_ctas_per_sm(dtype == PA_BF16, head_dim, G)

@@ -501,7 +501,7 @@ int tc_ctas_per_sm(bool bf16, int head_dim);
 pa_status launch_decode_tc(const DecodeParams &prm, bool bf16, int head_dim, int num_partitions,
                            int num_kv_heads, int num_seqs, cudaStream_t stream);
 
-// Tensor-core decode over E4M3 pools (pa_decode_fp8.cu).
+// Tensor-core decode over E4M3 pools (pa_decode_tc_fp8.cu).
 bool fp8_supported(int head_dim, int group);
 int fp8_ctas_per_sm(bool bf16, int head_dim, int group);
 pa_status launch_decode_fp8(const DecodeParams &prm, bool bf16, int head_dim, int num_partitions,

@@ -218,6 +218,8 @@ def span():
     ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, 256, 4),   # 2 tiles a partition
     ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, 512, 4),
     ("llama", {"num_seqs": 6, "len_range": (100, 900)}, 256, 8),
+    ("long", {"num_seqs": 2, "len_range": (3000, 5000)}, 128, 3),   # one tile a partition
+    ("llama", {"num_seqs": 6, "len_range": (512, 2100)}, 128, 5),
 ])
 def test_decode_fp8_partitions_per_cta_every_output(span, name, kw, partition, R):
     span(R)
@@ -398,3 +400,39 @@ def test_decode_fp8_output_from_weights_near_2_minus_17(name, partition):
     out = c.gpu(partition)
     api.check_error()
     assert_close(out, ref, f"fp8 tiny weights {name} P={partition}")
+
+
+# ------------------------------------------- group sizes and compact grids
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 6, 7])
+@pytest.mark.parametrize("partition", [-1, 256])
+def test_decode_fp8_group_sizes(G, d, partition):
+    """Groups of 1..7 query heads a KV head (8 and 4 are covered above): the
+    q and P terms of the absent heads of an 8-head operand must not reach
+    the present heads' outputs.  Every finite code, every output."""
+    plan = workloads.make_shape_plan(4, 2 * G, 2, d, 16, "bf16" if G % 2 else "f16", (1, 700),
+                                     seed=90 + G + d)
+    c = Fp8Case("shape", seed=G, plan=plan, codes=full_range_codes, scales=FULL_SCALES)
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    out = c.gpu(partition)
+    api.check_error()
+    assert_close(out, c.oracle(kc, vc), f"fp8 G={G} d={d} P={partition}")
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype,num_seqs,lens,partition,fused", [
+    (14, 2, 64, "f16", 100, (2000, 3000), 512, False),   # ~1,000 items over the resident slots
+    (14, 2, 64, "f16", 100, (2000, 3000), 512, True),    # the same, fused cache write
+    (32, 8, 128, "bf16", 40, (1100, 1500), 512, True),   # d = 128: 960 items
+])
+def test_decode_fp8_compact_several_items_per_cta(span, hq, hkv, d, dtype, num_seqs, lens,
+                                                   partition, fused):
+    """A compact launch over E4M3 pools with more items than resident CTA
+    slots but within four waves: each CTA computes several items in turn.
+    Every output."""
+    span(1)
+    plan = workloads.make_shape_plan(num_seqs, hq, hkv, d, 16, dtype, lens, seed=81 + d)
+    c = Fp8Case("shape", seed=9, plan=plan, codes=full_range_codes, scales=FULL_SCALES)
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    out = c.gpu(partition, step=fused)
+    api.check_error()
+    assert_close(out, c.oracle(kc, vc, step=fused), f"fp8 several items a CTA d={d} fused={fused}")
