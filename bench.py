@@ -139,7 +139,8 @@ def source_digest():
     figure still describes the kernel being timed."""
     h = hashlib.sha256()
     for f in ("pa_decode.cu", "pa_decode_tc.cu", "pa_decode_tc.cuh", "pa_decode_tc_fp8.cu",
-              "pa_decode.cuh", "pa_common.cuh", "pa_fp8.cuh", "pa_tcgen05.cuh", "pa_cascade.cu"):
+              "pa_decode_tc_fp8_g4.cu", "pa_decode.cuh", "pa_common.cuh", "pa_fp8.cuh",
+              "pa_tcgen05.cuh", "pa_cascade.cu"):
         with open(os.path.join(ROOT, "paged_kv_cache_64_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

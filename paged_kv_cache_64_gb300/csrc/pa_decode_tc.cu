@@ -63,12 +63,12 @@ bool pool_tensor_map_fp8(CUtensorMap *map, const void *pool, int64_t rows, int D
 
 template <int D, bool SPAN, bool COMPACT>
 static TcKernel tc_variant(bool bf16) {
-    return bf16 ? paged_decode_tc_kernel<true, D, SPAN, COMPACT, false>
-                : paged_decode_tc_kernel<false, D, SPAN, COMPACT, false>;
+    return bf16 ? paged_decode_tc_kernel<true, D, SPAN, COMPACT, 0>
+                : paged_decode_tc_kernel<false, D, SPAN, COMPACT, 0>;
 }
 
 static TcKernel pick_tc(bool bf16, int D, int *smem, bool span = false, bool compact = false) {
-    *smem = D == 128 ? TcShape<128, false>::SMEM_BYTES : TcShape<64, false>::SMEM_BYTES;
+    *smem = D == 128 ? TcShape<128, 0>::SMEM_BYTES : TcShape<64, 0>::SMEM_BYTES;
     if (D == 128)
         return span ? (compact ? tc_variant<128, true, true>(bf16) : tc_variant<128, true, false>(bf16))
                     : (compact ? tc_variant<128, false, true>(bf16) : tc_variant<128, false, false>(bf16));
@@ -109,7 +109,7 @@ int tc_occupancy(TcKernel k, int smem, int tmem_cols) {
 int tc_ctas_per_sm(bool bf16, int head_dim) {
     int smem = 0;
     TcKernel k = pick_tc(bf16, head_dim, &smem);
-    return tc_occupancy(k, smem, TcShape<64, false>::COLS);
+    return tc_occupancy(k, smem, TcShape<64, 0>::COLS);
 }
 
 pa_status launch_tc_kernel(TcKernel k, int smem, int ctas_per_sm, const DecodeParams &prm,

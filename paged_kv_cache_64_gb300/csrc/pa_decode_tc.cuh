@@ -42,6 +42,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "pa_common.cuh"
 #include "pa_decode.cuh"
@@ -67,18 +68,20 @@ enum TcBar {
     kRingBars  // then the staging rings' full and empty barriers (TcShape)
 };
 
-// F8: E4M3 pools (one byte an element).
-template <int D, bool F8>
+// F8G: 0 for 16-bit pools; 4 or 8 for E4M3 pools (one byte an element),
+// groups of up to F8G query heads.
+template <int D, int F8G>
 struct TcShape {
+    static constexpr bool F8 = F8G != 0;
     static constexpr int RB = F8 ? D : 2 * D;         // bytes of a K or V row
     static constexpr int KH = D / 64;                 // 16-bit: 64-dim (128-byte) slabs along d
     static constexpr int SLAB = kTcTile * 128;        // 16-bit: one slab of a tile, 16 KiB
     static constexpr int STAGE = kTcTile * RB;        // one staged K or V tile
     // MMA N of both products: the heads zero-padded to 16 (16-bit), or four
-    // E5M2 terms of each of 8 heads, rows t * 8 + g (E4M3)
-    static constexpr int QN = F8 ? 4 * kTcG : kTcN;
+    // E5M2 terms of each of F8G heads, rows t * F8G + g (E4M3)
+    static constexpr int QN = F8 ? 4 * F8G : kTcN;
     // TMEM: S x2 at column 0, O x2 at 2 * QN, QN fp32 columns each
-    static constexpr int COLS = F8 ? 128 : 64;
+    static constexpr int COLS = F8 ? 4 * QN : 64;
     static constexpr int S_COL = 0, O_COL = 2 * QN;
     static_assert(4 * QN <= COLS, "TMEM columns");
     // Staging rings (K and V tiles in flight), sized to the shared memory of
@@ -87,13 +90,14 @@ struct TcShape {
     // items, such as a small model's decode step, are bound by that
     // latency), one of each at d = 128 (two CTAs an SM already keep enough
     // copies in flight for long items, and a second stage would leave one
-    // CTA an SM); E4M3 pools the same bytes or more in twice the tiles.
+    // CTA an SM); E4M3 pools, whose tiles take the softmax as long for half
+    // the bytes, three K and three V tiles at d = 128, six of each at d = 64.
     // P.V reads V^T as an M = 128 (dims) MN-major operand.  At d = 64 only
     // its first 64 rows are real: rows 64..127 are read from the next STAGE
     // bytes (the next V stage or the first K stage), and only reach TMEM
     // lanes 64..127 of O, which no thread ever writes out.  So the V stages
     // come first at d = 64, K after them, and nothing is zero-padded.
-    static constexpr int NK = F8 ? (D == 64 ? 6 : 2) : (D == 64 ? 3 : 1);
+    static constexpr int NK = F8 ? (D == 64 ? 6 : 3) : (D == 64 ? 3 : 1);
     static constexpr int NV = F8 ? (D == 64 ? 6 : 3) : (D == 64 ? 3 : 1);
     // barriers: those of TcBar, then K full, K empty, V full and V empty, CAP
     // of each (CAP >= NK, NV; 3 unless a ring has more slots)
@@ -106,8 +110,7 @@ struct TcShape {
     static constexpr int Q_BYTES = F8 ? QN * D : KH * kTcN * 128;
     // P^T: QN rows x 128 positions, K-major, 128-byte swizzle (16-bit: two
     // atoms of 64 positions; E4M3: one of 128)
-    static constexpr int P_BYTES = 4096;
-    static_assert(P_BYTES == (F8 ? QN * 128 : 2 * kTcN * 128), "P operand");
+    static constexpr int P_BYTES = F8 ? QN * 128 : 2 * kTcN * 128;
     static constexpr int OFF_V = D == 64 ? 0 : K_BYTES;
     static constexpr int OFF_K = D == 64 ? V_BYTES : 0;
     static constexpr int OFF_Q = (D == 64 ? OFF_K + K_BYTES : OFF_V + V_BYTES);
@@ -119,9 +122,10 @@ struct TcShape {
     // and its online-softmax rescale factors
     static constexpr int OFF_F8 = OFF_RED + RED_BYTES;
     static constexpr int F8_BYTES = 5 * kTcG * 4;
-    // cascade tail: the shared prefix's partials merged per head (O, then m, l)
+    // cascade tail: the shared prefix's partials merged per head (O, then m,
+    // l); none over E4M3 pools (no cascade there)
     static constexpr int OFF_PRE = OFF_F8 + F8_BYTES;
-    static constexpr int PRE_BYTES = kTcG * D * 4 + 2 * kTcG * 4;
+    static constexpr int PRE_BYTES = F8 ? 0 : kTcG * D * 4 + 2 * kTcG * 4;
     // SPAN: a closed partition's per-warp sums and its maxima (m_run,
     // m_true), kept until its partial is written; two buffers (partition
     // parity)
@@ -146,10 +150,10 @@ struct TcShape {
 
 // q.K^T of one tile into the S buffer at TMEM address s_tmem: K (kaddr) as
 // the K-major A operand, q (qaddr) as the K-major B operand.
-template <bool BF16, int D, bool F8>
+template <bool BF16, int D, int F8G>
 __device__ __forceinline__ void tc_issue_qk(uint32_t s_tmem, uint32_t kaddr, uint32_t qaddr) {
-    using S = TcShape<D, F8>;
-    if constexpr (F8) {
+    using S = TcShape<D, F8G>;
+    if constexpr (S::F8) {
         // E4M3 K times the E5M2 terms of q, 32 bytes of d an instruction
         constexpr uint32_t idesc = e4m3_e5m2_idesc(kTcTile, S::QN, false);
 #pragma unroll
@@ -171,10 +175,10 @@ __device__ __forceinline__ void tc_issue_qk(uint32_t s_tmem, uint32_t kaddr, uin
 // P.V of one tile into the O buffer at o_tmem: the staged V tile (vaddr) as
 // V^T, an MN-major A operand of M = 128 dims; P^T (paddr) as the K-major B
 // operand.
-template <bool BF16, int D, bool F8>
+template <bool BF16, int D, int F8G>
 __device__ __forceinline__ void tc_issue_pv(uint32_t o_tmem, uint32_t vaddr, uint32_t paddr) {
-    using S = TcShape<D, F8>;
-    if constexpr (F8) {
+    using S = TcShape<D, F8G>;
+    if constexpr (S::F8) {
         // 32 positions an instruction: d = 128, one 128-byte atom across M,
         // 8-position groups 1,024 bytes apart; d = 64, two 64-byte atoms
         // across M (the second STAGE bytes on), groups 512 bytes apart
@@ -201,11 +205,14 @@ __device__ __forceinline__ void tc_issue_pv(uint32_t o_tmem, uint32_t vaddr, uin
 // COMPACT: the launch uses a compact grid (p.compact).  Every variant runs
 // two CTAs an SM (shared memory allows no more), so registers are capped for
 // two.
-template <bool BF16, int D, bool SPAN, bool COMPACT, bool F8>
+template <bool BF16, int D, bool SPAN, bool COMPACT, int F8G>
 __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
     paged_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v) {
-    using S = TcShape<D, F8>;
+    using S = TcShape<D, F8G>;
+    constexpr bool F8 = S::F8;
+    // heads the softmax keeps state for: 8, or the E4M3 operand's F8G
+    constexpr int NH = F8 ? F8G : kTcG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -288,24 +295,27 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
     int phys_first = 0;
     if (warp == 0 && lane < nunits) phys_first = table[(start + lane * kUnit) >> p.log2_block];
     // 16-byte pieces of q per softmax thread (E4M3 pools: thread st takes
-    // D / 16 elements of head st / 16, 16 or 8 bytes)
+    // kQEpt elements of head st / kQTph, 16, 8 or 4 bytes)
     constexpr int kQPieces = F8 ? 1 : kTcN * (D / 8) / 128;
+    constexpr int kQTph = F8 ? 128 / F8G : 1, kQEpt = F8 ? D / kQTph : 8;
     uint4 qv[kQPieces];
 #pragma unroll
     for (int j = 0; j < kQPieces; ++j) {
         qv[j] = make_uint4(0, 0, 0, 0);
         const int ci = threadIdx.x - 64 + 128 * j;  // softmax threads: 0..127
         if constexpr (F8) {
-            const int g = ci >> 4, c = ci & 15;
+            const int g = ci / kQTph, c = ci % kQTph;
             if (warp >= 2 && warp < kTcPvWarp && g < G) {
                 const uint16_t *src =
-                    p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * (D / 16);
-                if constexpr (D == 128) {
+                    p.q + ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G + g) * D + c * kQEpt;
+                if constexpr (kQEpt == 8) {
                     qv[j] = *reinterpret_cast<const uint4 *>(src);
-                } else {
+                } else if constexpr (kQEpt == 4) {
                     const uint2 v = *reinterpret_cast<const uint2 *>(src);
                     qv[j].x = v.x;
                     qv[j].y = v.y;
+                } else {
+                    qv[j].x = *reinterpret_cast<const uint32_t *>(src);
                 }
             }
         } else {
@@ -483,7 +493,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                     (nq < 2 || mbar_test_wait(&bar[kSEmpty0 + (nq & 1)], ((nq >> 1) - 1) & 1))) {
                     const int b = nq & 1;
                     tc_fence_after();
-                    tc_issue_qk<BF16, D, F8>(tmem + S::S_COL + S::QN * b,
+                    tc_issue_qk<BF16, D, F8G>(tmem + S::S_COL + S::QN * b,
                                              sbase + S::OFF_K + (nq % S::NK) * S::STAGE,
                                              sbase + S::OFF_Q);
                     tc_commit(&bar[kSFull0 + b]);
@@ -496,7 +506,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                     (nv < 2 || mbar_test_wait(&bar[kOEmpty0 + (nv & 1)], ((nv >> 1) - 1) & 1))) {
                     const int b = nv & 1;
                     tc_fence_after();
-                    tc_issue_pv<BF16, D, F8>(tmem + S::O_COL + S::QN * b,
+                    tc_issue_pv<BF16, D, F8G>(tmem + S::O_COL + S::QN * b,
                                              sbase + S::OFF_V + (nv % S::NV) * S::STAGE,
                                              sbase + S::OFF_P + b * S::P_BYTES);
                     tc_commit(&bar[kOFull0 + b]);
@@ -538,7 +548,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                 if (!ok) break;
                 const int b = nq & 1;
                 tc_fence_after();
-                tc_issue_qk<BF16, D, F8>(tmem + S::S_COL + S::QN * b,
+                tc_issue_qk<BF16, D, F8G>(tmem + S::S_COL + S::QN * b,
                                          sbase + S::OFF_K + (nq % S::NK) * S::STAGE,
                                          sbase + S::OFF_Q);
                 tc_commit(&bar[kSFull0 + b]);
@@ -563,7 +573,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                      (nv < 2 || mbar_wait(&bar[kOEmpty0 + b], ((nv >> 1) - 1) & 1));
                 if (!ok) break;
                 tc_fence_after();
-                tc_issue_pv<BF16, D, F8>(tmem + S::O_COL + S::QN * b,
+                tc_issue_pv<BF16, D, F8G>(tmem + S::O_COL + S::QN * b,
                                          sbase + S::OFF_V + (nv % S::NV) * S::STAGE,
                                          sbase + S::OFF_P + b * S::P_BYTES);
                 tc_commit(&bar[kOFull0 + b]);
@@ -584,16 +594,16 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
 
         if constexpr (F8) {
-            // Qs: head g's q times 2^e_g as four E5M2 terms in rows t * 8 + g
-            // (t = 0..3) of a 32-row K-major operand, rows of absent heads
-            // zero.  2^e_g brings the head's largest |q| into [2^14, 2^15);
+            // Qs: head g's q times 2^e_g as four E5M2 terms in rows t * F8G + g
+            // (t = 0..3) of a 4 * F8G-row K-major operand, rows of absent
+            // heads zero.  2^e_g brings the head's largest |q| into [2^14, 2^15);
             // each term is the nearest E5M2 value of what the earlier ones
             // left (an exact remainder in fp32).  A 16-bit q has at most 11
             // significant bits and the terms carry 12, so they add up to
             // q * 2^e_g except for the part of an element below E5M2's
             // subnormal quantum (under 2^-31 of the head's largest).
-            constexpr int EPT = D / 16;  // elements a thread (16 threads a head)
-            const int g = st >> 4, c = st & 15;
+            constexpr int EPT = kQEpt;  // elements a thread (kQTph threads a head)
+            const int g = st / kQTph, c = st % kQTph;
             float x[EPT];
             {
                 const uint32_t w[4] = {qv[0].x, qv[0].y, qv[0].z, qv[0].w};
@@ -608,7 +618,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
 #pragma unroll
             for (int e = 0; e < EPT; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
-            for (int off = 8; off >= 1; off >>= 1)
+            for (int off = kQTph / 2; off >= 1; off >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
             int eg = 0;  // 14 - floor(log2 amax), from amax's exponent field
             if (amax > 0.f) {
@@ -617,11 +627,12 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                 eg = eg < -120 ? -120 : (eg > 120 ? 120 : eg);
             }
             const float up = exp2i(eg);
-            uint32_t code[4][EPT / 4];  // per term, 4 codes a word
+            constexpr int NW = EPT >= 4 ? EPT / 4 : 1;
+            uint32_t code[4][NW];  // per term, 4 codes a word
 #pragma unroll
             for (int t = 0; t < 4; ++t)
 #pragma unroll
-                for (int w4 = 0; w4 < EPT / 4; ++w4) code[t][w4] = 0u;
+                for (int w4 = 0; w4 < NW; ++w4) code[t][w4] = 0u;
 #pragma unroll
             for (int e2 = 0; e2 < EPT / 2; ++e2) {  // element pairs
                 float a = x[2 * e2] * up, b = x[2 * e2 + 1] * up;
@@ -636,11 +647,13 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
             }
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                uint8_t *dst = smem + S::OFF_Q + e4m3_operand_offset<D>(8 * t + g, c * EPT);
+                uint8_t *dst = smem + S::OFF_Q + e4m3_operand_offset<D>(F8G * t + g, c * EPT);
                 if constexpr (EPT == 8)
                     *reinterpret_cast<uint2 *>(dst) = make_uint2(code[t][0], code[t][1]);
-                else
+                else if constexpr (EPT == 4)
                     *reinterpret_cast<uint32_t *>(dst) = code[t][0];
+                else
+                    *reinterpret_cast<uint16_t *>(dst) = (uint16_t)code[t][0];
             }
             // the score factor of head g: softmax scale (log2 units, K scale
             // included) times 2^-e_g
@@ -664,7 +677,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
 
         float m_run[kTcG], m_true[kTcG], l_part[kTcG], acc[kTcG], alpha_prev[kTcG];
 #pragma unroll
-        for (int g = 0; g < kTcG; ++g) {
+        for (int g = 0; g < NH; ++g) {
             m_run[g] = -INFINITY;
             m_true[g] = -INFINITY;
             l_part[g] = 0.f;
@@ -681,20 +694,25 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
             if constexpr (F8) {
                 // a head's four P terms are four columns: add them, undo the
                 // tile's power-of-two P scale
-                // (16 columns at a time: terms 0 and 1, then 2 and 3)
+                // (16 columns at a time: F8G = 8, terms 0 and 1, then 2 and 3)
                 float t[16];
                 tmem_load16(tmem + lane_addr + S::O_COL + S::QN * b, t);
 #pragma unroll
-                for (int g = 0; g < kTcG; ++g) o[g] = t[g] + t[8 + g];
-                tmem_load16(tmem + lane_addr + S::O_COL + S::QN * b + 16, t);
+                for (int g = 0; g < NH; ++g)
+                    o[g] = F8G == 8 ? t[g] + t[8 + g] : (t[g] + t[4 + g]) + (t[8 + g] + t[12 + g]);
+                if constexpr (F8G == 8) {
+                    tmem_load16(tmem + lane_addr + S::O_COL + S::QN * b + 16, t);
+#pragma unroll
+                    for (int g = 0; g < NH; ++g) o[g] += t[g] + t[8 + g];
+                }
                 const float *kinv = f8s + kTcG + 2 * kTcG * b;
 #pragma unroll
-                for (int g = 0; g < kTcG; ++g) o[g] = (o[g] + (t[g] + t[8 + g])) * kinv[g];
+                for (int g = 0; g < NH; ++g) o[g] *= kinv[g];
             } else {
                 float t[16];
                 tmem_load16(tmem + lane_addr + S::O_COL + 16 * b, t);
 #pragma unroll
-                for (int g = 0; g < kTcG; ++g) o[g] = t[g];
+                for (int g = 0; g < NH; ++g) o[g] = t[g];
             }
             tc_fence_before();
             __syncwarp();
@@ -704,10 +722,10 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                 // registers)
                 const float *alpha_k = f8s + 2 * kTcG + 2 * kTcG * b;
 #pragma unroll
-                for (int g = 0; g < kTcG; ++g) acc[g] = acc[g] * alpha_k[g] + o[g];
+                for (int g = 0; g < NH; ++g) acc[g] = acc[g] * alpha_k[g] + o[g];
             } else {
 #pragma unroll
-                for (int g = 0; g < kTcG; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
+                for (int g = 0; g < NH; ++g) acc[g] = acc[g] * alpha_prev[g] + o[g];
             }
             return true;
         };
@@ -720,7 +738,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
         auto close_partition = [&](int j) {
             float *pb = pend + (j & 1) * S::PEND_FLOATS;
 #pragma unroll
-            for (int g = 0; g < kTcG; ++g) {
+            for (int g = 0; g < NH; ++g) {
                 float v = l_part[g];
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
@@ -728,13 +746,13 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
             }
             if (st == 0) {
 #pragma unroll
-                for (int g = 0; g < kTcG; ++g) {
+                for (int g = 0; g < NH; ++g) {
                     pb[4 * kTcN + g] = m_run[g];
                     pb[4 * kTcN + kTcG + g] = m_true[g];
                 }
             }
 #pragma unroll
-            for (int g = 0; g < kTcG; ++g) {
+            for (int g = 0; g < NH; ++g) {
                 m_run[g] = -INFINITY;
                 m_true[g] = -INFINITY;
                 l_part[g] = 0.f;
@@ -747,7 +765,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
             const float *pb = pend + (j & 1) * S::PEND_FLOATS;
             if (!failed && r < D) {
 #pragma unroll
-                for (int g = 0; g < kTcG; ++g) {
+                for (int g = 0; g < NH; ++g) {
                     if (g >= G) break;
                     const float lt = pb[g] + pb[kTcN + g] + pb[2 * kTcN + g] + pb[3 * kTcN + g];
                     const float mr = pb[4 * kTcN + g], mt = pb[4 * kTcN + kTcG + g];
@@ -781,17 +799,19 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                   tc_fence_after();
                   if constexpr (F8) {
                       // a head's score is the sum of its four q-term columns
-                      // (16 columns at a time: terms 0 and 1, then 2 and 3)
+                      // (16 columns at a time: F8G = 8, terms 0 and 1, then 2 and 3)
                       float t[16];
                       tmem_load16(tmem + lane_addr + S::S_COL + S::QN * b, t);
   #pragma unroll
-                      for (int g = 0; g < kTcG; ++g) s[g] = t[g] + t[8 + g];
-                      tmem_load16(tmem + lane_addr + S::S_COL + S::QN * b + 16, t);
+                      for (int g = 0; g < NH; ++g)
+                          s[g] = F8G == 8 ? t[g] + t[8 + g] : (t[g] + t[4 + g]) + (t[8 + g] + t[12 + g]);
+                      if constexpr (F8G == 8) {
+                          tmem_load16(tmem + lane_addr + S::S_COL + S::QN * b + 16, t);
   #pragma unroll
-                      for (int g = 0; g < kTcG; ++g) {
-                          s[g] += t[g] + t[8 + g];
-                          s[kTcG + g] = 0.f;
+                          for (int g = 0; g < NH; ++g) s[g] += t[g] + t[8 + g];
                       }
+  #pragma unroll
+                      for (int g = NH; g < 16; ++g) s[g] = 0.f;
                   } else {
                       tmem_load16(tmem + lane_addr + S::S_COL + 16 * b, s);
                   }
@@ -814,17 +834,30 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
               // cap.
               float *tmax = red + b * (4 * kTcN);
   #pragma unroll
-              for (int g = 0; g < kTcG; ++g)
+              for (int g = 0; g < NH; ++g)
                   s[g] = valid ? s[g] * (F8 ? f8s[g] : p.scale_log2) : -INFINITY;
               if constexpr (!F8 && D == 128 && !SPAN && !COMPACT) {
   #pragma unroll
-                  for (int g = 0; g < kTcG; ++g) {
+                  for (int g = 0; g < NH; ++g) {
                       float v = s[g];
   #pragma unroll
                       for (int off = 16; off >= 1; off >>= 1)
                           v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
                       if (lane == 0) tmax[sw * kTcN + g] = v;
                   }
+              } else if constexpr (NH == 4) {
+                  // four heads: lane L ends with head (L >> 3) & 3 (5 shuffles)
+                  const bool c2 = lane & 16, c1 = lane & 8;
+                  float v2[2];
+  #pragma unroll
+                  for (int j = 0; j < 2; ++j)
+                      v2[j] = fmaxf(c2 ? s[2 + j] : s[j],
+                                    __shfl_xor_sync(kFullMask, c2 ? s[j] : s[2 + j], 16));
+                  float v = fmaxf(c1 ? v2[1] : v2[0], __shfl_xor_sync(kFullMask, c1 ? v2[0] : v2[1], 8));
+                  v = fmaxf(v, __shfl_xor_sync(kFullMask, v, 4));
+                  v = fmaxf(v, __shfl_xor_sync(kFullMask, v, 2));
+                  v = fmaxf(v, __shfl_xor_sync(kFullMask, v, 1));
+                  if ((lane & 7) == 0) tmax[sw * kTcN + ((lane >> 3) & 3)] = v;
               } else {
                   const bool b4 = lane & 16, c2 = lane & 8, c1 = lane & 4;
                   float v4[4], v2[2];
@@ -853,14 +886,14 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
               bool need = false;
               float mx[kTcG];
   #pragma unroll
-              for (int g = 0; g < kTcG; ++g) {
+              for (int g = 0; g < NH; ++g) {
                   mx[g] = fmaxf(fmaxf(tmax[g], tmax[kTcN + g]),
                                 fmaxf(tmax[2 * kTcN + g], tmax[3 * kTcN + g]));
                   need |= (g < G) && (mx[g] > m_run[g] + kLazyRescale);
               }
               float alpha[kTcG];
   #pragma unroll
-              for (int g = 0; g < kTcG; ++g) {
+              for (int g = 0; g < NH; ++g) {
                   alpha[g] = 1.f;
                   if (need) {  // block-uniform
                       const float mn = fmaxf(m_run[g], mx[g]);
@@ -875,7 +908,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                   // P^T as E5M2 terms: head g's P times 2^k_g, the power of
                   // two that brings the head's largest P of the tile into
                   // [2^14, 2^15), rounded to f16 (11 significant bits), then
-                  // split like q into four terms, rows t * 8 + g, 128
+                  // split like q into four terms, rows t * F8G + g, 128
                   // positions of one byte (K-major, 128-byte swizzle).  The
                   // terms keep every value down to E5M2's subnormal range
                   // (2^-30 of the tile's largest) exactly; the sum l takes the
@@ -884,9 +917,9 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                   // only reach O columns that are never read.
                   float *kinv = f8s + kTcG + 2 * kTcG * b;
   #pragma unroll
-                  for (int g = 0; g < kTcG; ++g) kinv[kTcG + g] = alpha[g];  // (same remark)
+                  for (int g = 0; g < NH; ++g) kinv[kTcG + g] = alpha[g];  // (same remark)
   #pragma unroll
-                  for (int g = 0; g < kTcG; g += 2) {
+                  for (int g = 0; g < NH; g += 2) {
                       if (g >= G) break;
                       float pp[2];
   #pragma unroll
@@ -914,8 +947,8 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                       for (int t = 0; t < 4; ++t) {
                           const uint32_t cd = e5m2x2_from_f16x2(hv);
                           hv = hsub2_bits(hv, f16x2_from_e5m2x2((uint16_t)cd));  // exact
-                          pbuf[e4m3_operand_offset<128>(8 * t + g, r)] = (uint8_t)(cd & 0xffu);
-                          pbuf[e4m3_operand_offset<128>(8 * t + g + 1, r)] = (uint8_t)(cd >> 8);
+                          pbuf[e4m3_operand_offset<128>(F8G * t + g, r)] = (uint8_t)(cd & 0xffu);
+                          pbuf[e4m3_operand_offset<128>(F8G * t + g + 1, r)] = (uint8_t)(cd >> 8);
                       }
                   }
               } else {
@@ -970,10 +1003,10 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
                   if (!failed && !accumulate(i - 1)) failed = true;
                   emit_partial(j - 1);
   #pragma unroll
-                  for (int g = 0; g < kTcG; ++g) acc[g] = 0.f;
+                  for (int g = 0; g < NH; ++g) acc[g] = 0.f;
               }
   #pragma unroll
-              for (int g = 0; g < kTcG; ++g) alpha_prev[g] = alpha[g];
+              for (int g = 0; g < NH; ++g) alpha_prev[g] = alpha[g];
             }
             if (SPAN && j + 1 < nspan)
                 close_partition(j);
@@ -983,7 +1016,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
 
         // l over the 128 position-threads, per head
 #pragma unroll
-        for (int g = 0; g < kTcG; ++g) {
+        for (int g = 0; g < NH; ++g) {
             float v = l_part[g];
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
@@ -1001,7 +1034,7 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
             }
         } else if (r < D) {
 #pragma unroll
-            for (int g = 0; g < kTcG; ++g) {
+            for (int g = 0; g < NH; ++g) {
                 if (g >= G) break;
                 const float lt =
                     lsum[g] + lsum[kTcN + g] + lsum[2 * kTcN + g] + lsum[3 * kTcN + g];
@@ -1132,6 +1165,30 @@ using TcKernel = void (*)(const DecodeParams, const CUtensorMap, const CUtensorM
 
 // Resident CTAs per SM of a variant (shared memory, registers, TMEM columns).
 int tc_occupancy(TcKernel k, int smem, int tmem_cols);
+
+// The E4M3 variant for head size D (64 or 128) and E4M3 operands of F8G
+// heads (4 or 8): its kernel, shared memory and TMEM columns.  Each F8G's
+// variants are instantiated in their own translation unit.
+template <int F8G>
+TcKernel tc8_pick(bool bf16, int D, bool span, bool compact, int *smem, int *cols) {
+    auto v = [&](auto d_const) -> TcKernel {
+        constexpr int DD = decltype(d_const)::value;
+        *smem = TcShape<DD, F8G>::SMEM_BYTES;
+        *cols = TcShape<DD, F8G>::COLS;
+        if (span)
+            return compact ? (bf16 ? paged_decode_tc_kernel<true, DD, true, true, F8G>
+                                   : paged_decode_tc_kernel<false, DD, true, true, F8G>)
+                           : (bf16 ? paged_decode_tc_kernel<true, DD, true, false, F8G>
+                                   : paged_decode_tc_kernel<false, DD, true, false, F8G>);
+        return compact ? (bf16 ? paged_decode_tc_kernel<true, DD, false, true, F8G>
+                               : paged_decode_tc_kernel<false, DD, false, true, F8G>)
+                       : (bf16 ? paged_decode_tc_kernel<true, DD, false, false, F8G>
+                               : paged_decode_tc_kernel<false, DD, false, false, F8G>);
+    };
+    return D == 128 ? v(std::integral_constant<int, 128>{}) : v(std::integral_constant<int, 64>{});
+}
+TcKernel tc8_pick4(bool bf16, int D, bool span, bool compact, int *smem, int *cols);
+TcKernel tc8_pick8(bool bf16, int D, bool span, bool compact, int *smem, int *cols);
 
 // Launch of a variant over the pools' tensor maps: the grid of decode_grid,
 // compact grids capped at the resident slots when that keeps them within
