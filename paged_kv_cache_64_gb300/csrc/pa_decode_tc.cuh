@@ -37,6 +37,18 @@
 // Online softmax with the same lazy rescale as the CUDA-core kernel; the
 // accumulator lives in registers (thread = dimension) and takes each tile's
 // O^T from a double-buffered TMEM slot.
+//
+// E4M3 pools (F8G = 4 or 8): the same roles and pipeline on 8-bit operands.
+// K and V tiles land as E4M3 codes (16 rows x d bytes a box; 128-byte
+// swizzle at d = 128, 64-byte at d = 64) and are the A operands of
+// tcgen05.mma kind::f8f6f4 as they are; q and P are the B operands as four
+// E5M2 terms of each of F8G heads (rows t * F8G + g, N = 4 * F8G), so a
+// head's score and output are the sums of four columns:
+//
+//   S^T[128 pos x 4*F8G] = K_codes[128 x d] . Qs^T[d x 4*F8G]
+//   O^T[d x 4*F8G]       = V_codes^T[d x 128 pos] . Ps^T[128 pos x 4*F8G]
+//
+// The K scale is folded into the score factor, the V scale into the output.
 #include <cuda.h>  // CUtensorMap and its enums only; the encoder comes from the driver at run time
 
 #include <cmath>
