@@ -436,3 +436,45 @@ def test_decode_fp8_compact_several_items_per_cta(span, hq, hkv, d, dtype, num_s
     out = c.gpu(partition, step=fused)
     api.check_error()
     assert_close(out, c.oracle(kc, vc, step=fused), f"fp8 several items a CTA d={d} fused={fused}")
+
+
+# ------------------------------------------- garbage workspace, graph replay
+@pytest.mark.parametrize("name,kw,partition", [
+    ("llama", {"num_seqs": 6, "len_range": (900, 2100)}, 512),   # ready flags (one wave)
+    ("qwen", {"num_seqs": 100}, 0),                             # compact grid, flags or counters
+])
+def test_decode_fp8_garbage_workspace_and_graph_replay(name, kw, partition):
+    """Over E4M3 pools: the fused combine needs no initialised workspace, and
+    a CUDA graph of the decode replays correctly (each replay reuses the
+    captured epoch; the combining CTA clears the flags it read)."""
+    c = Fp8Case(name, seed=21, codes=full_range_codes, scales=FULL_SCALES, **kw)
+    spec = c.spec
+    size = api.fp8_workspace_size(spec.num_seqs, spec.num_q_heads, spec.num_kv_heads,
+                                  spec.head_dim, spec.block_size, c.max_seq_len, partition,
+                                  c.q.dtype)
+    ws = api.alloc_workspace(size, "cuda")
+    ws.fill_(0xFF)
+    kc, vc = np_codes(c.kp), np_codes(c.vp)
+    ref = c.oracle(kc, vc)
+    out = torch.empty_like(c.q)
+
+    def run():
+        api.decode_fp8(out, c.q, c.kp, c.vp, c.tables, c.lens, c.max_seq_len, c.plan.scale,
+                       c.k_scale, c.v_scale, partition_tokens=partition, workspace=ws)
+
+    run()
+    api.check_error()
+    assert_close(out, ref, f"fp8 garbage workspace {name}")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g):
+            run()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(out, ref, f"fp8 graph replay {name}")
+    api.check_error()
