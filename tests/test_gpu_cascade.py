@@ -69,14 +69,19 @@ def test_prefix_workload_full_size_sampled(cow):
 
 
 def test_cascade_matches_plain_decode():
-    """Same inputs through pa_decode and pa_decode_cascade."""
+    """Same inputs through pa_decode and pa_decode_cascade: both match the
+    oracle, and each other, within the output tolerance."""
     case = Case(workloads.make_plan("prefix", num_seqs=20, cow=True))
+    hk, hv = case.snapshot(0)
     case.gpu_writes(0)
+    ref = case.oracle_step(0, hk, hv)
     plain = case.gpu_decode(0)
     out = torch.empty_like(plain)
     api.decode_cascade(out, case.vals.q, case.vals.k_pools[0], case.vals.v_pools[0], case.tables,
                        case.lens, case.max_seq_len, case.plan.scale, 4096)
     api.check_error()
+    assert_close(plain, ref, "plain vs oracle")
+    assert_close(out, ref, "cascade vs oracle")
     assert_close(out, plain.double().cpu().numpy(), "cascade vs plain")
 
 

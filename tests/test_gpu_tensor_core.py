@@ -160,11 +160,18 @@ def test_tc_decode_step_fused(name, kw, partition):
 
 
 def test_tc_matches_cuda_core_kernel():
-    """Both kernels on the same inputs agree within the output tolerance."""
+    """Both kernels on the same inputs match the oracle, and each other,
+    within the output tolerance."""
     case = Case(workloads.make_plan("long", num_seqs=4, len_range=(2000, 9000)))
+    hk, hv = case.snapshot(0)
     case.gpu_writes(0)
+    ref = case.oracle_step(0, hk, hv)
     a = case.gpu_decode(0)
     api.set_decode_impl("cuda_cores")
-    b = case.gpu_decode(0)
-    api.set_decode_impl("tensor_cores")
+    try:
+        b = case.gpu_decode(0)
+    finally:
+        api.set_decode_impl("tensor_cores")
+    assert_close(a, ref, "tensor cores vs oracle")
+    assert_close(b, ref, "CUDA cores vs oracle")
     assert_close(a, b.double().cpu().numpy(), "tensor vs CUDA cores")
