@@ -43,7 +43,8 @@ struct DecodeParams {
     // Compact grid (decode mode, no cascade, batches of up to
     // kCompactMaxSeqs): a 1-D grid whose CTAs map, in order, onto the work
     // items that exist (see compact_item), so CTAs with nothing to do come
-    // last and are dispatched after every CTA with work.
+    // last and are dispatched after every CTA with work.  0: 3-D grid; 1:
+    // items sequence by sequence; 2: full chunks first (see compact_find).
     int compact;
     float scale_log2;            // scale * log2(e)
     int mode;                    // 0: decode (direct output when 1 partition), 1: partials only
@@ -136,43 +137,94 @@ __device__ __forceinline__ void compact_lens(const DecodeParams &p, int *len) {
 }
 
 // Work item `c` of a compact grid, from the lengths compact_lens loaded.
-// Items are, sequence by sequence, the chunks of span * P positions of each
-// sequence (at least one, so a zero-length sequence still has its CTA), each
-// split over the KV heads: c = item * Hkv + kvh.  *total is set to the number
-// of items times Hkv (the launch's work, whatever c is).  Every thread of a
-// warp calls it (converged); it scans the lengths 32 at a time (an inclusive
-// warp prefix sum) and returns false for c past the last item.
+// The items are the chunks of span * P positions of each sequence (at least
+// one, so a zero-length sequence still has its CTA), each split over the KV
+// heads: c = item * Hkv + kvh, sequence by sequence (p.compact == 1), or
+// (p.compact == 2, grids the hardware schedules over several waves) every
+// full chunk first, sequence by sequence, then each sequence's last, shorter
+// chunk, so that the short items fill the end of the launch (longest first
+// is the better order for a greedy schedule; this is the part of it that
+// costs nothing).  A sequence's last chunk has the highest item index of its
+// chunks either way.  *total is set to the number of items times Hkv (the
+// launch's work, whatever c is).  Every thread of a warp calls it
+// (converged); it scans the lengths 32 at a time (inclusive warp prefix
+// sums) and returns false for c past the last item.
 __device__ __forceinline__ bool compact_find(const DecodeParams &p, const int *len, int c, int *seq,
                                              int *chunk, int *kvh, int *total) {
     const int lane = threadIdx.x & 31;
     const int item = c / p.num_kv_heads;
     const int chunk_tok = p.partition_tokens * (p.span > 1 ? p.span : 1);
-    int base = 0;  // items of the sequences before this group of 32
+    auto scan = [&](int n) -> int {  // inclusive prefix sum over the warp
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, n, off);
+            if (lane >= off) n += t;
+        }
+        return n;
+    };
     bool found = false;
+    if (p.compact != 2) {
+        int base = 0;  // items of the sequences before this group of 32
+#pragma unroll
+        for (int k = 0; k < kCompactGroups; ++k) {
+            const int s0 = 32 * k;
+            if (s0 >= p.num_seqs) break;
+            const int L = len[k];
+            const int n = L < 0 ? 0 : (L == 0 ? 1 : (L - 1) / chunk_tok + 1);
+            const int incl = scan(n);
+            const int group_total = base + __shfl_sync(0xffffffffu, incl, 31);
+            if (!found && item < group_total) {
+                const unsigned m = __ballot_sync(0xffffffffu, base + incl > item);
+                const int l = __ffs(m) - 1;
+                *seq = s0 + l;
+                *chunk = item - (base + __shfl_sync(0xffffffffu, incl - n, l));
+                *kvh = c - item * p.num_kv_heads;
+                found = true;
+            }
+            base = group_total;
+        }
+        *total = base * p.num_kv_heads;
+        return found;
+    }
+    // full chunks first, then each sequence's shorter last chunk
+    int nf_total = 0;  // full chunks of the sequences before this group of 32
+#pragma unroll
+    for (int k = 0; k < kCompactGroups; ++k) {
+        const int s0 = 32 * k;
+        if (s0 >= p.num_seqs) break;
+        const int n = len[k] < 0 ? 0 : len[k] / chunk_tok;
+        const int incl = scan(n);
+        const int group_total = nf_total + __shfl_sync(0xffffffffu, incl, 31);
+        if (!found && item < group_total) {
+            const unsigned m = __ballot_sync(0xffffffffu, nf_total + incl > item);
+            const int l = __ffs(m) - 1;
+            *seq = s0 + l;
+            *chunk = item - (nf_total + __shfl_sync(0xffffffffu, incl - n, l));
+            found = true;
+        }
+        nf_total = group_total;
+    }
+    int np_total = 0;  // last chunks of the sequences before this group of 32
 #pragma unroll
     for (int k = 0; k < kCompactGroups; ++k) {
         const int s0 = 32 * k;
         if (s0 >= p.num_seqs) break;
         const int L = len[k];
-        const int n = L < 0 ? 0 : (L == 0 ? 1 : (L - 1) / chunk_tok + 1);
-        int incl = n;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += t;
-        }
-        const int group_total = base + __shfl_sync(0xffffffffu, incl, 31);
-        if (!found && item < group_total) {
-            const unsigned m = __ballot_sync(0xffffffffu, base + incl > item);
+        const int n = (L == 0 || (L > 0 && L % chunk_tok != 0)) ? 1 : 0;
+        const int incl = scan(n);
+        const int group_total = np_total + __shfl_sync(0xffffffffu, incl, 31);
+        const int pi = item - nf_total;  // rank among the last chunks
+        if (!found && pi >= 0 && pi < group_total) {
+            const unsigned m = __ballot_sync(0xffffffffu, np_total + incl > pi);
             const int l = __ffs(m) - 1;
             *seq = s0 + l;
-            *chunk = item - (base + __shfl_sync(0xffffffffu, incl - n, l));
-            *kvh = c - item * p.num_kv_heads;
+            *chunk = __shfl_sync(0xffffffffu, L < 0 ? 0 : L / chunk_tok, l);  // after its full ones
             found = true;
         }
-        base = group_total;
+        np_total = group_total;
     }
-    *total = base * p.num_kv_heads;
+    *kvh = c - item * p.num_kv_heads;
+    *total = (nf_total + np_total) * p.num_kv_heads;
     return found;
 }
 

@@ -125,9 +125,13 @@ pa_status launch_tc_kernel(TcKernel k, int smem, int ctas_per_sm, const DecodePa
         // need are never launched (each would hold a slot for a memory round
         // trip only to find nothing to do, at the end of the launch).  Larger
         // grids keep one item a CTA, balanced by the hardware scheduler.
+        // Grids the hardware schedules over more than four waves take their
+        // full chunks first and the sequences' shorter last chunks at the end
+        // (compact_find), which evens out the last wave.
         const unsigned slots = (unsigned)(sm_count() * ctas_per_sm);
         if (p.span <= 1 && slots > 0 && grid.x > slots && grid.x <= 4 * slots) grid.x = slots;
         p.one_wave = p.span <= 1 && slots > 0 && grid.x <= slots;
+        p.compact = slots > 0 && grid.x > 4 * slots ? 2 : 1;
     }
     const int threads = 32 * (prm.span > 1 ? tc_warps<true>() : tc_warps<false>());
     if (launch_pdl(k, grid, dim3(threads), (size_t)smem, stream, p, mk, mv) != cudaSuccess)
