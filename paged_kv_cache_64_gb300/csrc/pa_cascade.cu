@@ -50,7 +50,7 @@ namespace pa {
 
 constexpr int kCsTile = 128;   // positions per tile: N of q.K^T, K of P.V
 constexpr int kCsRows = 128;   // query rows per CTA: M of both products
-constexpr int kCsWarps = 6;
+constexpr int kCsWarps = 10;   // producer, MMA issuer, two softmax warpgroups
 constexpr int kCsThreads = kCsWarps * 32;
 constexpr int kCsCols = 512;   // TMEM columns: S x2 (128 each) and O (d)
 constexpr int kCsS0 = 0, kCsO = 256;
@@ -70,7 +70,11 @@ struct CsShape {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;
     static constexpr int OFF_STAGE = OFF_P + P_BYTES;
-    static constexpr int OFF_BAR = OFF_STAGE + 2 * STAGE;
+    // the two softmax groups' row maxima (two buffers, by tile parity) and,
+    // at the end, their row sums
+    static constexpr int OFF_XCH = OFF_STAGE + 2 * STAGE;
+    static constexpr int XCH_FLOATS = 2 * 2 * kCsRows + 2 * kCsRows;
+    static constexpr int OFF_BAR = OFF_XCH + XCH_FLOATS * 4;
     static constexpr int OFF_MISC = OFF_BAR + kNumCsBars * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1 KiB
     static_assert(OFF_P % 1024 == 0 && OFF_STAGE % 1024 == 0 && STAGE % 1024 == 0, "atoms");
@@ -79,22 +83,39 @@ struct CsShape {
     static_assert(3 * kCsRows * 4 <= P_BYTES, "merge weights in the P tile");
 };
 
+// Named barrier 1 over the 256 softmax threads (warps 2-9); true on every
+// thread if any of them passed true.  Orders their shared-memory accesses
+// like bar.sync.
+__device__ __forceinline__ bool softmax_bar256_or(bool v) {
+    int any;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.s32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, 256, pi;\n\t"
+        "selp.s32 %0, 1, 0, po;\n\t}"
+        : "=r"(any)
+        : "r"((int)v)
+        : "memory");
+    return any != 0;
+}
+
 // Cluster merge, last step, in the CTA of rank `rank`: rows
 // [rank * R, rank * R + R) of the tile (R = 128 / CL) summed over the CL
 // chunks' weighted O rows that the cluster's CTAs pushed into this CTA's
 // shared memory (slot [c][row][D + 4]), with the weights already in
-// wts[R][CL]; written as one partial per row.  128 threads.
+// wts[R][CL]; written as one partial per row.  256 threads.
 template <int D, int CL>
 __device__ __forceinline__ void owner_sum(const CascadeParams &p, const float *ost,
                                           const float *wts, const float *rowM, const float *rowL,
                                           uint32_t rank, int t, int mt, int kvh, int slot) {
     constexpr int R = kCsRows / CL;
-    constexpr int ITEMS = R * (D / 4) / 128;  // float4 outputs per thread
+    constexpr int ITEMS = R * (D / 4) / 256;  // float4 outputs per thread
+    static_assert(R * (D / 4) % 256 == 0, "whole items per thread");
     const int G = p.group;
     const int rows_total = p.num_seqs * G;
 #pragma unroll 4
     for (int i = 0; i < ITEMS; ++i) {
-        const int idx = t + 128 * i;
+        const int idx = t + 256 * i;
         const int jl = idx / (D / 4), q4 = idx % (D / 4);
         const int gr = mt * kCsRows + (int)rank * R + jl;
         if (gr >= rows_total) continue;
@@ -142,8 +163,14 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         prefetch_tensormap(&tmap_v);
     }
     pdl_wait();  // inputs may come from the previous kernel on the stream
+    // The tail pass may start at once: it reads this launch's partials only
+    // after its own wait for the launch to complete, and everything else it
+    // reads or writes (the sequences' own blocks past the prefix, their
+    // newest tokens, its partial slots) is disjoint from what this launch
+    // touches.  Its CTAs take the SMs this grid leaves free.
+    pdl_trigger();
     if (threadIdx.x == 0) {
-        const int counts[kNumCsBars] = {1, 1, 1, 1, 4, 1, 1, 4, 4, 1};
+        const int counts[kNumCsBars] = {1, 1, 1, 1, 8, 1, 1, 8, 8, 1};
         for (int b = 0; b < kNumCsBars; ++b) mbar_init(&bar[b], counts[b]);
         *abort_flag = 0;
         mbar_init_fence();
@@ -327,19 +354,30 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         }
     } else {
         // ---------------------------------------------------------- softmax / epilogue
+        // Two warpgroups share the rows: thread r of each owns TMEM lane r
+        // (query row r of the tile); group sg takes positions [64 sg,
+        // 64 sg + 64) of each S row and dims [sg d/2, (sg + 1) d/2) of each O
+        // row.  The groups exchange their row maxima every tile and their row
+        // sums at the end, through shared memory at a named barrier that also
+        // ORs the threads' failures (so that all 256 take the same branches).
+        const int sg = (warp - 2) >> 2;          // softmax group
         const int quad = warp & 3;               // TMEM lane quadrant this warp may access
         const int r = quad * 32 + lane;          // query row of the tile = TMEM lane
-        const int st_id = threadIdx.x - 64;      // 0..127
+        const int st_id = threadIdx.x - 64;      // 0..255
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        float *xmax = reinterpret_cast<float *>(smem + S::OFF_XCH);  // [tile parity][group][row]
+        float *xsum = xmax + 4 * kCsRows;                            // [group][row]
+        constexpr int kHalf = kCsTile / 2;       // positions of a group
+        constexpr int kOHalf = D / 2;            // O dims of a group
 
         // Q tile (128 rows x d, K-major, 128-byte swizzle), rows past the last
         // sequence zero.  Unscaled: the scale is applied to S in fp32.
         // all of the thread's loads in flight before the first store
-        constexpr int kQPer = kCsRows * (D / 8) / 128;
+        constexpr int kQPer = kCsRows * (D / 8) / 256;
         uint4 qv[kQPer];
 #pragma unroll
         for (int i = 0; i < kQPer; ++i) {
-            const int ci = st_id + 128 * i;
+            const int ci = st_id + 256 * i;
             const int rr = ci / (D / 8), c = ci % (D / 8);
             const int gr = mt * kCsRows + rr;
             qv[i] = make_uint4(0, 0, 0, 0);
@@ -349,7 +387,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < kQPer; ++i) {
-            const int ci = st_id + 128 * i;
+            const int ci = st_id + 256 * i;
             const int rr = ci / (D / 8), c = ci % (D / 8);
             *reinterpret_cast<uint4 *>(smem + S::OFF_Q + sw128_offset(rr, c * 8, S::SLAB)) = qv[i];
         }
@@ -358,76 +396,87 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         if (lane == 0) mbar_arrive(&bar[kCsQReady]);
 
         float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
-        bool failed = false;
+        bool failed = false, fail_local = false;
         for (int t = 0; t < ntiles; ++t) {
             const int b = t & 1;
-            const bool landed = mbar_wait(&bar[kCsSFull0 + b], (t >> 1) & 1);
-            if (!__all_sync(kFullMask, landed)) {
-                failed = true;
-                break;
-            }
-            tc_fence_after();
-            float s[kCsTile];
+            const bool landed = __all_sync(kFullMask, mbar_wait(&bar[kCsSFull0 + b], (t >> 1) & 1));
+            float s[kHalf];
+            if (landed) {
+                tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < kCsTile / 32; ++c)
-                tmem_ld32(tmem + lane_addr + kCsS0 + 128 * b + 32 * c, s + 32 * c);
+                for (int c = 0; c < kHalf / 32; ++c)
+                    tmem_ld32(tmem + lane_addr + kCsS0 + 128 * b + kHalf * sg + 32 * c, s + 32 * c);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kHalf; ++j) s[j] = 0.f;
+            }
             const int nvalid = (cend - cstart - t * kCsTile < kCsTile) ? cend - cstart - t * kCsTile
                                                                         : kCsTile;
             float mx = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < kCsTile; ++j) {
-                s[j] = (j < nvalid) ? s[j] * p.scale_log2 : -INFINITY;  // select: NaN-safe
+            for (int j = 0; j < kHalf; ++j) {
+                s[j] = (kHalf * sg + j < nvalid) ? s[j] * p.scale_log2 : -INFINITY;  // NaN-safe select
                 mx = fmaxf(mx, s[j]);
             }
+            xmax[(2 * b + sg) * kCsRows + r] = mx;
+            if (softmax_bar256_or(!landed || fail_local)) {  // every thread breaks, or none
+                failed = true;
+                break;
+            }
+            mx = fmaxf(mx, xmax[(2 * b + 1 - sg) * kCsRows + r]);  // the row's tile maximum
             m_true = fmaxf(m_true, mx);
             float alpha = 1.f;
-            const bool need = mx > m_run + kLazyRescale;
+            const bool need = mx > m_run + kLazyRescale;  // the same in both groups' threads
             if (need) {  // first tile: alpha = 2^-inf = 0 on an empty sum
                 alpha = fast_exp2(m_run - mx);
                 m_run = mx;
                 l_run *= alpha;
             }
-            uint32_t pk[kCsTile / 2];
+            uint32_t pk[kHalf / 2];
 #pragma unroll
-            for (int j = 0; j < kCsTile / 2; ++j) {
+            for (int j = 0; j < kHalf / 2; ++j) {
                 const float a = fast_exp2(s[2 * j] - m_run), c = fast_exp2(s[2 * j + 1] - m_run);
                 l_run += a + c;
                 pk[j] = narrow2<BF16>(a, c);
             }
             if (t >= 1) {
                 // the previous tile's P.V must be done before P is rewritten or
-                // O rescaled
-                const bool done = mbar_wait(&bar[kCsODone], (t - 1) & 1);
-                if (!__all_sync(kFullMask, done)) {
-                    failed = true;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(kFullMask, need)) {
+                // O rescaled (a failure is everyone's at the next exchange)
+                const bool done = __all_sync(kFullMask, mbar_wait(&bar[kCsODone], (t - 1) & 1));
+                if (!done) {
+                    fail_local = true;
+                } else {
+                    tc_fence_after();
+                    if (__any_sync(kFullMask, need)) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tmem + lane_addr + kCsO + 32 * c, o);
-            #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(tmem + lane_addr + kCsO + 32 * c, o);
+                        for (int c = 0; c < kOHalf / 32; ++c) {
+                            float o[32];
+                            tmem_ld32(tmem + lane_addr + kCsO + kOHalf * sg + 32 * c, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                            tmem_st32(tmem + lane_addr + kCsO + kOHalf * sg + 32 * c, o);
+                        }
+                        tmem_wait_st();
                     }
-                    tmem_wait_st();
                 }
             }
-            // P row r (128 positions) in the K-major operand layout
+            // P row r, the group's 64 positions, in the K-major operand layout
 #pragma unroll
-            for (int c = 0; c < kCsTile / 8; ++c) {
-                const uint32_t off = (c >> 3) * S::SLAB + (r >> 3) * 1024 + (r & 7) * 128 +
-                                     (((c & 7) ^ (r & 7)) << 4);
+            for (int j = 0; j < kHalf / 8; ++j) {  // 16-byte chunk j of slab sg
+                const uint32_t off = sg * S::SLAB + (r >> 3) * 1024 + (r & 7) * 128 +
+                                     ((j ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4 *>(smem + S::OFF_P + off) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
             }
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kCsPReady0 + b]);
         }
+        // the row's sum over both groups' positions (and any failure, everyone's)
+        xsum[sg * kCsRows + r] = l_run;
+        failed |= softmax_bar256_or(failed || fail_local);
+        l_run += xsum[(1 - sg) * kCsRows + r];
         if (!failed && ntiles > 0) {
             const bool done = mbar_wait(&bar[kCsODone], (ntiles - 1) & 1);
             failed = !__all_sync(kFullMask, done);
@@ -442,11 +491,12 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         // A failed or empty chunk contributes l = 0.
         keep_have = !failed && ntiles > 0;  // warp-uniform
         keep_inv = keep_have ? 1.0f / l_run : 0.f;
-        cm[r] = keep_have ? m_true : -INFINITY;
-        cl[r] = keep_have ? l_run * fast_exp2(m_run - m_true) : 0.f;
+        if (sg == 0) {
+            cm[r] = keep_have ? m_true : -INFINITY;
+            cl[r] = keep_have ? l_run * fast_exp2(m_run - m_true) : 0.f;
+        }
     }
 
-    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0 && ntiles > 0) {
@@ -474,6 +524,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     __syncwarp();
     cluster_sync();  // every chunk's (m, l) is visible
     if (warp >= 2) {
+        const int sg = (warp - 2) >> 2;        // softmax group: pushes O dims [sg d/2, (sg + 1) d/2)
         const int r = (warp & 3) * 32 + lane;  // row of the tile = TMEM lane
         float mc[kCsMaxCluster], lc[kCsMaxCluster];
 #pragma unroll
@@ -501,7 +552,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             w[c] *= invL;
             if (c == (int)rank) w_self = w[c];
         }
-        if (r / R == (int)rank) {  // this CTA owns row r
+        if (sg == 0 && r / R == (int)rank) {  // this CTA owns row r
             const int jl = r % R;
 #pragma unroll
             for (int c = 0; c < kCsMaxCluster; ++c)
@@ -515,13 +566,14 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             const uint32_t dst = map_cluster(
                 smem_addr(ost + ((int)rank * R + r % R) * (D + 4)), (uint32_t)(r / R));
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 float o[32];
-                tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + kCsO + 32 * c, o);
+                const int col = (D / 2) * sg + 32 * c;
+                tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + kCsO + col, o);
                 if (w_self != 0.f) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        st_cluster_f4(dst + (32 * c + 4 * i) * 4,
+                        st_cluster_f4(dst + (col + 4 * i) * 4,
                                       make_float4(o[4 * i] * sc, o[4 * i + 1] * sc,
                                                   o[4 * i + 2] * sc, o[4 * i + 3] * sc));
                 }

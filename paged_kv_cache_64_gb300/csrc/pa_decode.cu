@@ -1295,6 +1295,7 @@ pa_status pa_decode_cascade(void *out, const void *q, const void *k_new, const v
     prm.ws_parts = c.ws_parts;
     prm.part_base = c.prefix_slots;
     prm.prefix_parts = c.prefix_slots;
+    prm.late_wait = cp.num_chunks > 0;  // the prefix pass was launched just before
     prm.partition_tokens = c.tail.P > 0 ? c.tail.P : kSinglePassTokens;
     prm.num_partitions = c.tail.NP;
     if (c.tail.NP > 1) {

@@ -74,6 +74,10 @@ struct DecodeParams {
     // partials follow at part_base == prefix_parts, and the CTA that finishes
     // the item combines all of them into the output.
     int prefix_parts;
+    // Cascade tail launched right after the prefix pass, which lets it start
+    // at once: its wait for the previous kernel is put off until it reads the
+    // prefix's partials (the prefix pass's only output).
+    int late_wait;
     // FP8 pools (E4M3 codes): fl32(1 / scale) of each pool for the fused
     // write, and the V scale applied to the output (the K scale is folded
     // into scale_log2).

@@ -249,7 +249,12 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
         tmem_alloc(tmem_slot, S::COLS);
         tmem_relinquish();
     }
-    pdl_wait();  // inputs may come from the previous kernel on the stream
+    // Inputs may come from the previous kernel on the stream.  A cascade
+    // tail's previous kernel is the prefix pass, whose only output is the
+    // prefix's partials: the wait for it is put off until they are read (the
+    // prefix pass lets this launch start only after its own wait, so the
+    // kernels before it are complete).
+    if (!p.late_wait) pdl_wait();
 
     // One work item: split-KV chunk `part` (a span of partitions) of KV head
     // kvh of sequence seq; `another` when the CTA has a next item.  false when
@@ -265,9 +270,11 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
     if (start >= L) {  // empty partitions: as in the CUDA-core kernel
         if (p.prefix_parts > 0) {
             // empty cascade tail: the output is the prefix's partials combined
-            if (nparts_seq == 0 && part == 0)
+            if (nparts_seq == 0 && part == 0) {
+                pdl_wait();
                 finish_item<BF16, D>(p, seq, kvh, 0, 0, 1, false, reinterpret_cast<float *>(smem),
                                      S::OFF_Q);
+            }
         } else if (p.mode == 0) {
             if (part == 0) {
                 uint32_t *o = reinterpret_cast<uint32_t *>(p.out);
@@ -420,9 +427,10 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
         }
         if (merge_prefix) {
             // The shared prefix's partials of the group's heads, merged with
-            // the online-softmax rescale while the tail is computed (they were
-            // complete before this launch); four heads per round of loads,
-            // lane owns D/32 dims.
+            // the online-softmax rescale while the tail is computed, once the
+            // prefix pass is complete; four heads per round of loads, lane
+            // owns D/32 dims.
+            pdl_wait();
             constexpr int V = D / 32;
             const int np = p.prefix_parts;
             const int64_t row0 = ((int64_t)seq * p.num_q_heads + (int64_t)kvh * G) * p.ws_parts;
@@ -1106,9 +1114,11 @@ __global__ void __launch_bounds__(tc_warps<SPAN>() * 32, 2)
         }
     }
     if (aborted) return false;
-    if (!direct && (p.counters != nullptr || p.prefix_parts > 0))
+    if (!direct && (p.counters != nullptr || p.prefix_parts > 0)) {
+        pdl_wait();  // a cascade tail's combine reads the prefix's partials
         finish_item<BF16, D>(p, seq, kvh, nparts_seq, part, (nparts_seq + R - 1) / R, use_flags,
                              reinterpret_cast<float *>(smem), S::OFF_Q);
+    }
     if (another && threadIdx.x == 0) {
         // the last stages' release arrivals (MMA commits nobody waited for)
         // land before the barriers are set up again for the CTA's next item

@@ -258,6 +258,42 @@ def test_graph_replay():
         assert_close(out, ref, "cascade graph replay")
 
 
+@pytest.mark.parametrize("name", ["mha_b32", "g8_long_tails"])
+def test_back_to_back_calls_chain_outputs(name):
+    """Layers run back to back on one stream, each call's q the previous
+    call's output, one workspace for all: the tail pass may start while the
+    prefix pass runs, and must still see every earlier write (the previous
+    layer's output) and leave the next prefix pass its workspace.  Every
+    output equals the same call made alone between device-wide synchronizes,
+    bit for bit; the first also matches the oracle."""
+    S, hq, hkv, d, B, dtype, P, (lo, hi), step = SHAPES[name]
+    tails = np.random.default_rng(5).integers(lo, hi, S, endpoint=True)
+    c = SharedPrefix(S, hq, hkv, d, B, dtype, P, tails, seed=17, step=step)
+    hk, hv = bits(c.kp), bits(c.vp)
+    kw = dict(k_new=c.k_new, v_new=c.v_new, slot_mapping=c.slots) if step else {}
+    ws = api.alloc_workspace(api.cascade_workspace_size(c.S, c.hq, c.hkv, c.d, c.B,
+                                                        c.max_seq_len, P, c.q.dtype), "cuda")
+    layers = 4
+    outs = [torch.full_like(c.q, float("nan")) for _ in range(layers)]
+    q = c.q
+    for layer in range(layers):
+        api.decode_cascade(outs[layer], q, c.kp, c.vp, c.tables, c.lens, c.max_seq_len, c.scale,
+                           P, workspace=ws, **kw)
+        q = outs[layer]
+    torch.cuda.synchronize()
+    api.check_error()
+    assert_close(outs[0], c.oracle(hk, hv), f"cascade {name} first layer")
+    q = c.q
+    for layer in range(layers):
+        alone = torch.full_like(c.q, float("nan"))
+        torch.cuda.synchronize()
+        api.decode_cascade(alone, q, c.kp, c.vp, c.tables, c.lens, c.max_seq_len, c.scale, P,
+                           workspace=ws, **kw)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(alone), bits(outs[layer])), f"layer {layer}"
+        q = outs[layer]
+
+
 # ------------------------------------------------------------ prefix caching layout
 @pytest.mark.parametrize("cascade", [False, True])
 def test_prefix_caching_layout_small(cascade):
