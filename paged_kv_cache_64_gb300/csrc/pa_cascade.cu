@@ -163,12 +163,6 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         prefetch_tensormap(&tmap_v);
     }
     pdl_wait();  // inputs may come from the previous kernel on the stream
-    // The tail pass may start at once: it reads this launch's partials only
-    // after its own wait for the launch to complete, and everything else it
-    // reads or writes (the sequences' own blocks past the prefix, their
-    // newest tokens, its partial slots) is disjoint from what this launch
-    // touches.  Its CTAs take the SMs this grid leaves free.
-    pdl_trigger();
     if (threadIdx.x == 0) {
         const int counts[kNumCsBars] = {1, 1, 1, 1, 8, 1, 1, 8, 8, 1};
         for (int b = 0; b < kNumCsBars; ++b) mbar_init(&bar[b], counts[b]);
@@ -183,6 +177,14 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The tail pass may start now: it reads this launch's partials only after
+    // its own wait for the launch to complete, and everything else it reads
+    // or writes (the sequences' own blocks past the prefix, their newest
+    // tokens, its partial slots) is disjoint from what this launch touches.
+    // Its CTAs take the SMs this grid leaves free.  Not before this CTA holds
+    // its TMEM: a tail CTA on the same SM could otherwise take columns first
+    // and then wait for this launch to complete.
+    pdl_trigger();
     // staging of the chunk's partial for the cluster merge, in the K/V ring
     float *ost = reinterpret_cast<float *>(smem + S::OFF_STAGE);  // [128][D + 4]
     float *cm = ost + kCsRows * (D + 4);
