@@ -23,13 +23,16 @@
 //
 // Q, K and P are K-major operands, V an MN-major one (its rows exactly as
 // the TMA copies land them); S (two buffers) and O live in TMEM.  Roles
-// (6 warps):
+// (10 warps):
 //   warp 0      producer: TMA copies of 16-row boxes through the prefix's
 //               block-table entries into a 2-stage K/V ring;
 //   warp 1      allocates TMEM; lane 0 issues every MMA and commits;
-//   warps 2..5  softmax / epilogue, one query row (TMEM lane) per thread:
-//               the whole 128-position score row is in the thread's
-//               registers, so row max and sum need no shuffles.
+//   warps 2..9  softmax / epilogue in two warpgroups; thread r of each owns
+//               query row r (TMEM lane r): group 0 positions 0..63 of every
+//               score tile and dims [0, d/2) of O, group 1 the rest.  Each
+//               half row is in the thread's registers; the two halves meet
+//               through shared memory, row maxima every tile and row sums at
+//               the end.
 // The CTAs of consecutive chunks form a thread-block cluster (up to 8); at
 // the end they merge their chunks' partials through distributed shared
 // memory, and the cluster leaves one (m, l, O) partial per row in workspace

@@ -100,9 +100,10 @@ __device__ __forceinline__ int checked_len(const int32_t *seq_lens, int i, int m
 }
 
 // Programmatic dependent launch: wait for the previous kernel on the stream
-// (and its memory) before touching global memory; let the next one start its
-// prologue once this one is past its main loop.  No-ops without the launch
-// attribute.
+// (and its memory) before touching global memory that it may write; let the
+// next one start its prologue once this one is past its main loop (the
+// cascade's prefix pass lets its tail pass start as soon as it holds its
+// TMEM).  No-ops without the launch attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
