@@ -219,7 +219,9 @@ pa_status pa_decode_step(void *out, const void *q, const void *k_new, const void
  * <= max_blocks_per_seq*block_size (else PA_ERR_INVALID); prefix_len = 0
  * is plain pa_decode / pa_decode_step with partition_tokens = 0.
  * k_new, v_new, slot_mapping: NULL for a plain decode, or the newest tokens
- * as in pa_decode_step (their positions lie in the tails).
+ * as in pa_decode_step; their positions must lie in the tails (the tail
+ * pass, which writes them, may run while the prefix pass is still reading
+ * the prefix).
  * workspace: pa_decode_cascade_workspace_size(...) bytes of device memory,
  * 256-byte aligned, scratch (no initialisation needed).  Other arguments as
  * pa_decode.
