@@ -148,14 +148,6 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
     return r;
 }
 
-// Two codes (low byte first) to two f16 values, exactly (PTX
-// cvt.rn.f16x2.e4m3x2: every E4M3 value is an f16 value).
-__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint16_t c) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
-    return r;
-}
-
 // 16 16-bit values (two uint4, low element first) times `inv` in fp32, as
 // 16 E4M3 codes.
 template <bool BF16>
